@@ -1,0 +1,213 @@
+"""fp64 CPU oracle for unified-max split-KV decode attention.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference legs of ``bench.py`` may import this package. The CUDA library shares
+no code with it.
+
+All arithmetic lives in ``oracle.c`` (plain C, double precision, pthreads over rows); this module
+only compiles it with gcc, loads it with ctypes and marshals numpy arrays. Each C function cites
+the passage of the pages it follows:
+
+* ``attention``        -- the plain definition softmax(scale * q K^T) V, max-shifted
+  (opt.ai.kr "FlashDecoding++ async softmax -- theory", section 3, first formula).
+* ``attention_shifted`` -- the same softmax shifted by a fixed value phi (same page, section 3,
+  second formula).
+* ``window_flags``     -- the per-(sequence, head, split) out-of-window decision (same page,
+  section 3: a score past the phi criterion sends its block back to online softmax).
+* ``split_method``     -- the method's steps in fp64: phi-frame partials per split, detect,
+  online recompute, max-rescaled (plain when nothing fell back) sum.
+* ``split_len`` / ``plan`` -- the split scheduler restated: n_b = ceil(L_b / S).
+
+Parity status: every function above is pinned by ``tests/test_oracle_pins.py``; phi calibration is
+not part of the oracle (parity unpinned: the pages give no calibration procedure).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+MODE_NORMAL, MODE_FORCE_FAST, MODE_FORCE_ONLINE = 0, 1, 2
+FLAG_OUT, FLAG_ABOVE, FLAG_BELOW, FLAG_NAN = 1, 2, 4, 8
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so with gcc (IEEE double, no contraction)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-Wno-unused-parameter",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int), ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("paged", ctypes.c_int),
+        ("max_seq_len", ctypes.c_int), ("block_size", ctypes.c_int),
+        ("max_blocks_per_seq", ctypes.c_int),
+        ("scale", ctypes.c_float), ("phi", ctypes.c_float), ("lo", ctypes.c_float),
+        ("hi", ctypes.c_float),
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.POINTER(Problem)
+            vp, ip = ctypes.c_void_p, ctypes.c_void_p
+            lib.or_attention.argtypes = [P, vp, vp, vp, ip, ip, ip, ctypes.c_int, vp, ctypes.c_int]
+            lib.or_attention.restype = ctypes.c_int
+            lib.or_attention_shifted.argtypes = [P, vp, vp, vp, ip, ip, ip, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_double, vp, ctypes.c_int]
+            lib.or_attention_shifted.restype = ctypes.c_int
+            lib.or_window_flags.argtypes = [P, vp, vp, ip, ip, ctypes.c_int, ctypes.c_int, vp, vp,
+                                            ctypes.c_int]
+            lib.or_window_flags.restype = ctypes.c_int
+            lib.or_split_method.argtypes = [P, vp, vp, vp, ip, ip, ip, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                                            ctypes.c_int]
+            lib.or_split_method.restype = ctypes.c_int
+            lib.or_split_len.argtypes = [ip] + [ctypes.c_int] * 8
+            lib.or_split_len.restype = ctypes.c_int
+            lib.or_plan.argtypes = [ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ip, ip]
+            lib.or_plan.restype = ctypes.c_longlong
+            lib.or_default_threads.argtypes = []
+            lib.or_default_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _kv_array(a, dtype):
+    """Inputs are uint16 bf16 bit patterns (dtype BF16) or float32 (dtype F32), C-contiguous."""
+    want = np.uint16 if dtype == BF16 else np.float32
+    a = np.ascontiguousarray(a)
+    if a.dtype != want:
+        raise TypeError(f"expected {want} array, got {a.dtype}")
+    return a
+
+
+def make_problem(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, scale, phi, lo, hi,
+                 max_seq_len=0, block_size=0, max_blocks_per_seq=0, paged=False) -> Problem:
+    if num_q_heads % num_kv_heads:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    return Problem(batch, num_q_heads, num_kv_heads, head_dim, dtype, 1 if paged else 0,
+                   max_seq_len, block_size, max_blocks_per_seq,
+                   np.float32(scale), np.float32(phi), np.float32(lo), np.float32(hi))
+
+
+def _rows_arg(prob, rows):
+    if rows is None:
+        return None, prob.batch * prob.num_q_heads
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+    return r, r.shape[0]
+
+
+def default_threads() -> int:
+    return _load().or_default_threads()
+
+
+def attention(prob, q, k, v, seq_lens, block_table=None, rows=None, n_threads=0):
+    """Exact attention rows in fp64. Returns (out [n_rows][d] float64, threads used)."""
+    lib = _load()
+    q, k, v = (_kv_array(x, prob.dtype) for x in (q, k, v))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    r, n = _rows_arg(prob, rows)
+    out = np.zeros((n, prob.head_dim), dtype=np.float64)
+    used = lib.or_attention(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
+                            _ptr(r), n, _ptr(out), n_threads)
+    return out, used
+
+
+def attention_shifted(prob, q, k, v, seq_lens, shift=None, block_table=None, rows=None,
+                      n_threads=0):
+    """exp(s - shift)-weighted attention (shift = prob.phi when None)."""
+    lib = _load()
+    q, k, v = (_kv_array(x, prob.dtype) for x in (q, k, v))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    r, n = _rows_arg(prob, rows)
+    out = np.zeros((n, prob.head_dim), dtype=np.float64)
+    lib.or_attention_shifted(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
+                             _ptr(r), n, 0 if shift is None else 1,
+                             0.0 if shift is None else float(shift), _ptr(out), n_threads)
+    return out
+
+
+def window_flags(prob, q, k, seq_lens, split_len, max_splits, block_table=None, n_threads=0):
+    """Returns (flags uint8 [B][Hq][max_splits], row_margin float64 [B][Hq])."""
+    lib = _load()
+    q, k = (_kv_array(x, prob.dtype) for x in (q, k))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    flags = np.zeros((prob.batch, prob.num_q_heads, max_splits), dtype=np.uint8)
+    margin = np.zeros((prob.batch, prob.num_q_heads), dtype=np.float64)
+    lib.or_window_flags(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), split_len,
+                        max_splits, _ptr(flags), _ptr(margin), n_threads)
+    return flags, margin
+
+
+def split_method(prob, q, k, v, seq_lens, split_len, max_splits, mode=MODE_NORMAL,
+                 block_table=None, rows=None, want_partials=False, n_threads=0):
+    """The method's steps in fp64. Returns dict(out, flags[, part_o, part_l, part_m])."""
+    lib = _load()
+    q, k, v = (_kv_array(x, prob.dtype) for x in (q, k, v))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    r, n = _rows_arg(prob, rows)
+    d = prob.head_dim
+    res = {"out": np.zeros((n, d), dtype=np.float64),
+           "flags": np.zeros((n, max_splits), dtype=np.uint8)}
+    if want_partials:
+        res["part_o"] = np.zeros((n, max_splits, d), dtype=np.float64)
+        res["part_l"] = np.zeros((n, max_splits), dtype=np.float64)
+        res["part_m"] = np.zeros((n, max_splits), dtype=np.float64)
+    lib.or_split_method(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
+                        _ptr(r), n, split_len, max_splits, mode, _ptr(res["out"]),
+                        _ptr(res.get("part_o")), _ptr(res.get("part_l")),
+                        _ptr(res.get("part_m")), _ptr(res["flags"]), n_threads)
+    return res
+
+
+def split_len(seq_lens, num_kv_heads, max_seq_len, split_len_req, num_sms, units_per_sm,
+              granule, min_split):
+    lib = _load()
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    return lib.or_split_len(_ptr(sl), sl.shape[0], num_kv_heads, max_seq_len, split_len_req,
+                            num_sms, units_per_sm, granule, min_split)
+
+
+def plan(seq_lens, num_kv_heads, max_seq_len, S):
+    """Returns (nsplit int32 [B], split_off int32 [B+1], n_units)."""
+    lib = _load()
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = sl.shape[0]
+    nsplit = np.zeros(B, dtype=np.int32)
+    off = np.zeros(B + 1, dtype=np.int32)
+    n_units = lib.or_plan(_ptr(sl), B, num_kv_heads, max_seq_len, S, _ptr(nsplit), _ptr(off))
+    return nsplit, off, int(n_units)

@@ -1,0 +1,481 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for unified-max split-KV decode attention.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE. Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py load this library. The CUDA path shares no code,
+ * header, table or helper with it, and neither side includes or links the other.
+ *
+ * What it follows (web pages, cited by title and section):
+ *   [theory]  opt.ai.kr, "FlashDecoding++ async softmax -- theory":
+ *             section 1: decode attention is one query token against a K/V cache that grows,
+ *                        so every step reads the whole cache; Flash-Decoding cuts that cache
+ *                        into splits that run in parallel.
+ *             section 3: the ordinary softmax shifted by the running max (first formula);
+ *                        the same softmax shifted by a unified max phi fixed in advance
+ *                        (second formula), so every block works alone and only a plain sum
+ *                        is left at the end; a block whose score crosses the phi criterion
+ *                        stops and is recomputed with the ordinary online softmax.
+ *   [export]  opt.ai.kr, "FlashDecoding++ export strategy", section 2: the KV cache is split
+ *             inside attention and each chunk carries its own partial sum and normaliser.
+ *   [3dgen]   hwan-h-heo.github.io, "Optimizing sparse 3D generation inference", section 2.2:
+ *             softmax rows sum to one, so value rows that are all equal to v0 give v0.
+ *
+ * Readings where the pages leave a step open (each is also listed in the design notes):
+ *   R1  The windowed quantity x is the scaled score s = scale * <q, k> (the softmax input of
+ *       [theory] s3), in the same units as phi.
+ *   R2  A score is in the window iff lo <= s - phi <= hi (closed). The pages name only the
+ *       upper (overflow) side; the lower side guards a split whose scores all lie far below
+ *       phi. NaN is outside.
+ *   R3  One decision per (sequence b, query head h, split j): each query head is its own
+ *       softmax row.
+ *   R4  A recomputed split is expressed in its own max frame m_j, so the final combine
+ *       rescales every split by exp(m_j - M), M = max_j m_j; when nothing fell back every
+ *       m_j = phi and this is exactly the plain sum of [theory] s3.
+ *   R5  Only tokens t < L_b take part. L_b == 0 gives an all-zero output row.
+ *   R6  scale, phi, lo and hi are the float32 values the caller passes, widened to double.
+ *
+ * Precision: every value is widened exactly to double (bf16 and fp32 both widen exactly);
+ * all arithmetic is double. Threads: rows are independent, and are spread over pthreads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ----------------------------------------------------------------------------------------- */
+/* problem description (the oracle's own struct; the CUDA side has a separate one)           */
+/* ----------------------------------------------------------------------------------------- */
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_MODE_NORMAL = 0, OR_MODE_FORCE_FAST = 1, OR_MODE_FORCE_ONLINE = 2 };
+
+/* flag bits of one (b, h, j) decision */
+enum { OR_FLAG_OUT = 1, OR_FLAG_ABOVE = 2, OR_FLAG_BELOW = 4, OR_FLAG_NAN = 8 };
+
+typedef struct {
+    int batch;            /* B */
+    int num_q_heads;      /* Hq */
+    int num_kv_heads;     /* Hkv, Hq % Hkv == 0, G = Hq / Hkv query heads share one kv head */
+    int head_dim;         /* d */
+    int dtype;            /* OR_F32 or OR_BF16 (bf16 given as raw uint16 bit patterns) */
+    int paged;            /* 0: K,V are [B][max_seq_len][Hkv][d]; 1: [blocks][block_size][Hkv][d] */
+    int max_seq_len;      /* contiguous: the token stride of the cache */
+    int block_size;       /* paged only */
+    int max_blocks_per_seq; /* paged only: row length of block_table */
+    float scale, phi, lo, hi;
+} or_problem;
+
+/* ----------------------------------------------------------------------------------------- */
+/* element access                                                                            */
+/* ----------------------------------------------------------------------------------------- */
+
+static double or_widen(const void* base, int dtype, size_t i)
+{
+    if (dtype == OR_BF16) {
+        /* bf16 is the upper half of an IEEE binary32 pattern */
+        uint32_t bits = ((uint32_t)((const uint16_t*)base)[i]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)base)[i];
+}
+
+/* Element offset of K/V row (b, t, g). Contiguous: token t of sequence b at [b][t][g][:].
+ * Paged: token t lives in slot t % block_size of physical block block_table[b][t / block_size]. */
+static size_t or_kv_offset(const or_problem* p, const int32_t* table, int b, int t, int g)
+{
+    size_t d = (size_t)p->head_dim, hkv = (size_t)p->num_kv_heads;
+    if (!p->paged)
+        return (((size_t)b * (size_t)p->max_seq_len + (size_t)t) * hkv + (size_t)g) * d;
+    int32_t blk = table[(size_t)b * (size_t)p->max_blocks_per_seq + (size_t)(t / p->block_size)];
+    size_t slot = (size_t)(t % p->block_size);
+    return (((size_t)blk * (size_t)p->block_size + slot) * hkv + (size_t)g) * d;
+}
+
+/* s_t = scale * sum_i q[b,h,i] * k[b,t,g(h),i]  for t < L, g(h) = floor(h / G)   ([theory] s1) */
+static void or_scores(const or_problem* p, const void* q, const void* k, const int32_t* table,
+                      int b, int h, int L, double* s)
+{
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
+    size_t qoff = ((size_t)b * (size_t)p->num_q_heads + (size_t)h) * (size_t)d;
+    double scale = (double)p->scale;
+    for (int t = 0; t < L; ++t) {
+        size_t koff = or_kv_offset(p, table, b, t, g);
+        double dot = 0.0;
+        for (int i = 0; i < d; ++i)
+            dot += or_widen(q, p->dtype, qoff + (size_t)i) * or_widen(k, p->dtype, koff + (size_t)i);
+        s[t] = scale * dot;
+    }
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* thread pool over rows                                                                      */
+/* ----------------------------------------------------------------------------------------- */
+
+typedef void (*or_row_fn)(void* ctx, int row_index);
+
+typedef struct {
+    or_row_fn fn;
+    void* ctx;
+    int n_rows;
+    int n_threads;
+    int tid;
+} or_job;
+
+static void* or_worker(void* arg)
+{
+    or_job* j = (or_job*)arg;
+    for (int r = j->tid; r < j->n_rows; r += j->n_threads)
+        j->fn(j->ctx, r);
+    return NULL;
+}
+
+static int or_resolve_threads(int n_threads, int n_rows)
+{
+    if (n_threads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = n > 0 ? (int)n : 1;
+    }
+    if (n_threads > n_rows) n_threads = n_rows > 0 ? n_rows : 1;
+    if (n_threads > 512) n_threads = 512;
+    return n_threads;
+}
+
+/* Runs fn over rows [0, n_rows) on n_threads threads; returns the thread count used. */
+static int or_parallel_rows(or_row_fn fn, void* ctx, int n_rows, int n_threads)
+{
+    n_threads = or_resolve_threads(n_threads, n_rows);
+    if (n_threads == 1) {
+        for (int r = 0; r < n_rows; ++r) fn(ctx, r);
+        return 1;
+    }
+    pthread_t th[512];
+    or_job jobs[512];
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+        jobs[t].fn = fn; jobs[t].ctx = ctx; jobs[t].n_rows = n_rows;
+        jobs[t].n_threads = n_threads; jobs[t].tid = t;
+        if (pthread_create(&th[t], NULL, or_worker, &jobs[t]) != 0) break;
+        ++started;
+    }
+    if (started < n_threads) {
+        /* a thread could not start: finish its share here */
+        for (int t = started; t < n_threads; ++t) or_worker(&jobs[t]);
+    }
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    return n_threads;
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 1. exact attention: the plain definition, max-shifted ([theory] s3, first formula)        */
+/* ----------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const or_problem* p;
+    const void *q, *k, *v;
+    const int32_t* table;
+    const int32_t* seq_lens;
+    const int32_t* rows;   /* pairs (b, h); NULL means row r = (r / Hq, r % Hq) */
+    double* out;           /* [n_rows][d] */
+    int use_phi;           /* 0: shift by max_t s_t ; 1: shift by phi ([theory] s3, second formula) */
+    double phi_override;   /* shift used when use_phi == 2 */
+} or_attn_ctx;
+
+static void or_row_bh(const or_problem* p, const int32_t* rows, int r, int* b, int* h)
+{
+    if (rows) { *b = rows[2 * r]; *h = rows[2 * r + 1]; }
+    else { *b = r / p->num_q_heads; *h = r % p->num_q_heads; }
+}
+
+static void or_attn_row(void* vctx, int r)
+{
+    or_attn_ctx* c = (or_attn_ctx*)vctx;
+    const or_problem* p = c->p;
+    int b, h;
+    or_row_bh(p, c->rows, r, &b, &h);
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
+    int L = c->seq_lens[b];
+    double* o = c->out + (size_t)r * (size_t)d;
+    for (int i = 0; i < d; ++i) o[i] = 0.0;
+    if (L <= 0) return;                                   /* R5 */
+
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+
+    double shift;
+    if (c->use_phi == 1) shift = (double)p->phi;
+    else if (c->use_phi == 2) shift = c->phi_override;
+    else {
+        shift = s[0];
+        for (int t = 1; t < L; ++t) if (s[t] > shift) shift = s[t];
+    }
+    double Z = 0.0;
+    for (int t = 0; t < L; ++t) {
+        double w = exp(s[t] - shift);
+        Z += w;
+        size_t voff = or_kv_offset(p, c->table, b, t, g);
+        for (int i = 0; i < d; ++i) o[i] += w * or_widen(c->v, p->dtype, voff + (size_t)i);
+    }
+    for (int i = 0; i < d; ++i) o[i] /= Z;
+    free(s);
+}
+
+/* out[r][:] = softmax(scale * q K^T) V for each requested row, shifted by the row max.
+ * Returns the number of threads used. */
+int or_attention(const or_problem* p, const void* q, const void* k, const void* v,
+                 const int32_t* block_table, const int32_t* seq_lens,
+                 const int32_t* rows, int n_rows, double* out, int n_threads)
+{
+    or_attn_ctx c = { p, q, k, v, block_table, seq_lens, rows, out, 0, 0.0 };
+    return or_parallel_rows(or_attn_row, &c, n_rows, n_threads);
+}
+
+/* Same definition with the shift fixed in advance ([theory] s3, second formula):
+ * w_t = exp(s_t - shift) / sum_u exp(s_u - shift). shift = p->phi when use_given == 0,
+ * else the value `shift`. Algebraically equal to or_attention wherever exp stays finite. */
+int or_attention_shifted(const or_problem* p, const void* q, const void* k, const void* v,
+                         const int32_t* block_table, const int32_t* seq_lens,
+                         const int32_t* rows, int n_rows, int use_given, double shift,
+                         double* out, int n_threads)
+{
+    or_attn_ctx c = { p, q, k, v, block_table, seq_lens, rows, out, use_given ? 2 : 1, shift };
+    return or_parallel_rows(or_attn_row, &c, n_rows, n_threads);
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 2. the split scheduler, restated                                                           */
+/* ----------------------------------------------------------------------------------------- */
+
+/* Split length actually used. split_len > 0 is taken as given. split_len == 0 asks for an
+ * automatic choice: spread sum_b L_b * Hkv (token, kv-head) pairs over units_per_sm * num_sms
+ * units, round the length up to a multiple of `granule`, then clamp it to
+ * [min_split, max(min_split, max_seq_len rounded up to granule)].
+ * (The pages give no sizing rule; this policy is the library's own and is restated here.) */
+int or_split_len(const int32_t* seq_lens, int batch, int num_kv_heads, int max_seq_len,
+                 int split_len, int num_sms, int units_per_sm, int granule, int min_split)
+{
+    if (split_len > 0) return split_len;
+    long long total = 0;
+    for (int b = 0; b < batch; ++b) {
+        long long L = seq_lens[b];
+        if (L < 0) L = 0;
+        if (L > max_seq_len) L = max_seq_len;
+        total += L;
+    }
+    long long units = (long long)units_per_sm * (long long)num_sms;
+    if (units < 1) units = 1;
+    long long pairs = total * (long long)num_kv_heads;
+    long long S = (pairs + units - 1) / units;
+    S = ((S + granule - 1) / granule) * granule;
+    long long hi = ((long long)max_seq_len + granule - 1) / granule * granule;
+    if (hi < min_split) hi = min_split;
+    if (S < min_split) S = min_split;
+    if (S > hi) S = hi;
+    return (int)S;
+}
+
+/* n_b = ceil(L_b / S) splits for sequence b; split_off[b] = sum of n_c for c < b
+ * (split_off has batch + 1 entries). Unit order is b-major, then kv head g, then split j, so
+ * the first unit of sequence b is num_kv_heads * split_off[b]. Returns the unit count. */
+long long or_plan(const int32_t* seq_lens, int batch, int num_kv_heads, int max_seq_len, int S,
+                  int32_t* nsplit, int32_t* split_off)
+{
+    long long off = 0;
+    for (int b = 0; b < batch; ++b) {
+        long long L = seq_lens[b];
+        if (L < 0) L = 0;
+        if (L > max_seq_len) L = max_seq_len;
+        int n = (int)((L + S - 1) / S);
+        nsplit[b] = n;
+        split_off[b] = (int32_t)off;
+        off += n;
+    }
+    split_off[batch] = (int32_t)off;
+    return off * (long long)num_kv_heads;
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 3. window decisions per (b, h, j)                                                          */
+/* ----------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const or_problem* p;
+    const void *q, *k;
+    const int32_t* table;
+    const int32_t* seq_lens;
+    int S, max_splits;
+    uint8_t* flags;         /* [B][Hq][max_splits] */
+    double* row_margin;     /* [B*Hq]: min over valid t of min(|x - lo|, |x - hi|), x = s - phi */
+} or_flag_ctx;
+
+static uint8_t or_classify(double x, double lo, double hi)
+{
+    if (x != x) return OR_FLAG_OUT | OR_FLAG_NAN;                      /* R2: NaN is outside */
+    if (x > hi) return OR_FLAG_OUT | OR_FLAG_ABOVE;                    /* [theory] s3 overflow side */
+    if (x < lo) return OR_FLAG_OUT | OR_FLAG_BELOW;                    /* R2 lower side */
+    return 0;
+}
+
+static void or_flag_row(void* vctx, int r)
+{
+    or_flag_ctx* c = (or_flag_ctx*)vctx;
+    const or_problem* p = c->p;
+    int b = r / p->num_q_heads, h = r % p->num_q_heads;
+    int L = c->seq_lens[b];
+    uint8_t* f = c->flags + (size_t)r * (size_t)c->max_splits;
+    for (int j = 0; j < c->max_splits; ++j) f[j] = 0;
+    double margin = INFINITY;
+    if (L > 0) {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        or_scores(p, c->q, c->k, c->table, b, h, L, s);
+        double phi = (double)p->phi, lo = (double)p->lo, hi = (double)p->hi;
+        for (int t = 0; t < L; ++t) {
+            double x = s[t] - phi;
+            int j = t / c->S;
+            if (j < c->max_splits) f[j] |= or_classify(x, lo, hi);
+            double m1 = fabs(x - lo), m2 = fabs(x - hi);
+            double m = m1 < m2 ? m1 : m2;
+            if (m < margin) margin = m;
+        }
+        free(s);
+    }
+    if (c->row_margin) c->row_margin[r] = margin;
+}
+
+/* flags[b][h][j] for every row; entries with j >= n_b stay 0. row_margin may be NULL. */
+int or_window_flags(const or_problem* p, const void* q, const void* k,
+                    const int32_t* block_table, const int32_t* seq_lens, int S, int max_splits,
+                    uint8_t* flags, double* row_margin, int n_threads)
+{
+    or_flag_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, flags, row_margin };
+    return or_parallel_rows(or_flag_row, &c, p->batch * p->num_q_heads, n_threads);
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 4. the method's own steps in fp64 (test-only restatement of the split decomposition)       */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * For each row (b, h) and split j covering tokens [jS, min((j+1)S, L_b)):
+ *   fast partial in the phi frame ([theory] s3, second formula; [export] s2 per-chunk sums):
+ *       o_j = sum_t exp(s_t - phi) v_t,  l_j = sum_t exp(s_t - phi),  m_j = phi
+ *   decision (R2, R3): flag_j = any t in the split with s_t - phi outside [lo, hi]
+ *   recompute when flagged (mode normal) or always (mode force_online), with the ordinary
+ *   online softmax ([theory] s3, first formula, max tracked while running):
+ *       m <- max(m, s_t); o, l scaled by exp(m_old - m); o += exp(s_t - m) v_t; l += exp(s_t - m)
+ *       giving (o_j, l_j, m_j = split max)
+ *   combine (R4): M = max_j m_j, out = sum_j exp(m_j - M) o_j / sum_j exp(m_j - M) l_j
+ *       (a plain sum whenever every m_j = phi).
+ * Partials are written when part_o / part_l / part_m are not NULL, indexed [row][j].
+ */
+
+typedef struct {
+    const or_problem* p;
+    const void *q, *k, *v;
+    const int32_t* table;
+    const int32_t* seq_lens;
+    const int32_t* rows;
+    int S, max_splits, mode;
+    double* out;       /* [n_rows][d] */
+    double* part_o;    /* [n_rows][max_splits][d] or NULL */
+    double* part_l;    /* [n_rows][max_splits] or NULL */
+    double* part_m;    /* [n_rows][max_splits] or NULL */
+    uint8_t* flags;    /* [n_rows][max_splits] or NULL */
+} or_split_ctx;
+
+static void or_split_row(void* vctx, int r)
+{
+    or_split_ctx* c = (or_split_ctx*)vctx;
+    const or_problem* p = c->p;
+    int b, h;
+    or_row_bh(p, c->rows, r, &b, &h);
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
+    int L = c->seq_lens[b];
+    double* out = c->out + (size_t)r * (size_t)d;
+    for (int i = 0; i < d; ++i) out[i] = 0.0;
+    int n = L > 0 ? (L + c->S - 1) / c->S : 0;
+    if (n > c->max_splits) n = c->max_splits;
+    if (n == 0) return;
+
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    double* o = (double*)calloc((size_t)n * (size_t)d, sizeof(double));
+    double* l = (double*)calloc((size_t)n, sizeof(double));
+    double* m = (double*)calloc((size_t)n, sizeof(double));
+    uint8_t* f = (uint8_t*)calloc((size_t)n, 1);
+    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+    double phi = (double)p->phi, lo = (double)p->lo, hi = (double)p->hi;
+
+    for (int j = 0; j < n; ++j) {
+        int t0 = j * c->S, t1 = t0 + c->S < L ? t0 + c->S : L;
+        double* oj = o + (size_t)j * (size_t)d;
+        /* fast partial against the unified max */
+        for (int t = t0; t < t1; ++t) {
+            double w = exp(s[t] - phi);
+            l[j] += w;
+            size_t voff = or_kv_offset(p, c->table, b, t, g);
+            for (int i = 0; i < d; ++i) oj[i] += w * or_widen(c->v, p->dtype, voff + (size_t)i);
+            f[j] |= or_classify(s[t] - phi, lo, hi);
+        }
+        m[j] = phi;
+        int redo = (c->mode == OR_MODE_FORCE_ONLINE) ||
+                   (c->mode == OR_MODE_NORMAL && (f[j] & OR_FLAG_OUT));
+        if (redo) {
+            /* ordinary online softmax over the same split */
+            double mm = -INFINITY, ll = 0.0;
+            for (int i = 0; i < d; ++i) oj[i] = 0.0;
+            for (int t = t0; t < t1; ++t) {
+                double mnew = s[t] > mm ? s[t] : mm;
+                double corr = exp(mm - mnew);           /* exp(-inf) = 0 on the first token */
+                ll *= corr;
+                for (int i = 0; i < d; ++i) oj[i] *= corr;
+                double w = exp(s[t] - mnew);
+                ll += w;
+                size_t voff = or_kv_offset(p, c->table, b, t, g);
+                for (int i = 0; i < d; ++i) oj[i] += w * or_widen(c->v, p->dtype, voff + (size_t)i);
+                mm = mnew;
+            }
+            l[j] = ll;
+            m[j] = mm;
+        }
+    }
+    /* combine: max-rescaled sum, a plain sum when every m_j == phi */
+    double M = m[0];
+    for (int j = 1; j < n; ++j) if (m[j] > M) M = m[j];
+    double lam = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double e = exp(m[j] - M);
+        lam += e * l[j];
+        for (int i = 0; i < d; ++i) out[i] += e * o[(size_t)j * (size_t)d + (size_t)i];
+    }
+    for (int i = 0; i < d; ++i) out[i] /= lam;
+
+    for (int j = 0; j < n; ++j) {
+        size_t pj = (size_t)r * (size_t)c->max_splits + (size_t)j;
+        if (c->part_o)
+            for (int i = 0; i < d; ++i) c->part_o[pj * (size_t)d + (size_t)i] = o[(size_t)j * (size_t)d + (size_t)i];
+        if (c->part_l) c->part_l[pj] = l[j];
+        if (c->part_m) c->part_m[pj] = m[j];
+        if (c->flags) c->flags[pj] = f[j];
+    }
+    free(s); free(o); free(l); free(m); free(f);
+}
+
+int or_split_method(const or_problem* p, const void* q, const void* k, const void* v,
+                    const int32_t* block_table, const int32_t* seq_lens,
+                    const int32_t* rows, int n_rows, int S, int max_splits, int mode,
+                    double* out, double* part_o, double* part_l, double* part_m, uint8_t* flags,
+                    int n_threads)
+{
+    or_split_ctx c = { p, q, k, v, block_table, seq_lens, rows, S, max_splits, mode,
+                       out, part_o, part_l, part_m, flags };
+    return or_parallel_rows(or_split_row, &c, n_rows, n_threads);
+}
+
+/* Number of threads or_* calls use for n_threads == 0 (the host's online CPUs). */
+int or_default_threads(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
