@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode-attention step (all of: split plan, phi-frame split partials, window
+test, fallback recompute, combine) through libfdpp's C ABI on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl fdpp|reference]
+
+Prints ONE JSON line (rank 0). The default workload is GQA decode: batch 8, 32 query / 8 kv heads,
+head_dim 128, 4096 tokens each, bf16, split 512, phi 0, window [-30, 10]. `--config` names one of
+workloads.ALL.
+
+  value      KV-read GB/s: algorithmic K+V bytes of all ranks' steps (tokens t < L_b only) over the
+             max-over-ranks device time of the K timed steps (CUDA events, inputs resident in HBM).
+             The steps rotate over R copies of K/V totalling >= 4x the L2 size, so no step reuses
+             the previous step's bytes from L2.
+  e2e        the same metric through the C ABI with HOST buffers: each step copies q, seq_lens
+             (and the block table) host->device from pinned memory, runs the step, copies the
+             output back and synchronises. The K/V cache is resident device state.
+  roofline   split kernel alone (CUDA events recorded around it by fdpp_decode_attn_timed):
+             algorithmic KV bytes per launch / mean launch time, against the measured HBM copy
+             bandwidth of MEASURED_PEAKS.json.
+  cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the same workload.
+
+With --gpus N > 1 (torchrun) every rank runs its own seeded batch (weak scaling, no collective on
+the data path); value sums all ranks' bytes over the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-read GB/s (% of ~8 TB/s HBM peak) and µs/step at 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_FALLBACK = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="gqa_decode")
+    ap.add_argument("--impl", default="fdpp", choices=["fdpp", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--kernel", type=int, default=0, help="fdpp_kernel (0 auto, 1 tensor, 2 simt)")
+    ap.add_argument("--mode", type=int, default=0, help="fdpp_mode (0 normal, 1 fast, 2 online)")
+    ap.add_argument("--tc-stages", type=int, default=0)
+    ap.add_argument("--tc-ctas", type=int, default=0)
+    ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier + max-over-ranks timing only)
+# ------------------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend)
+            self.pg = dist
+        if n_gpus != self.world and not (n_gpus >= 1 and self.world == 1 and n_gpus == 1):
+            if self.world == 1 and n_gpus > 1:
+                raise SystemExit("--gpus N > 1 must be launched with torchrun (one rank per GPU)")
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(per_rank_bytes: float, per_rank_seconds: float, dist: Dist):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    total = dist.sum(per_rank_bytes)
+    t = dist.max(per_rank_seconds)
+    return total, t, (total / t / 1e9 if t > 0 else 0.0)
+
+
+# ------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, enabled: bool):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        try:
+            out_dir = os.path.join(ROOT, "gpurun_out")
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), r[2:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def split_kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("split_tc.cu", "split_simt.cu", "device_common.cuh"):
+        with open(os.path.join(ROOT, "split_kv_async_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name: str, kernel_name: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, when it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(f"{config_name}/{kernel_name}")
+    if not e or e.get("source_hash") != split_kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def _dev_tensor(a, dev):
+    import numpy as np
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+# ------------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle, timed as it stands, on the host cores
+# ------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(inp, budget_s=None, max_groups=None):
+    """Times the oracle over whole (b, g) groups (all G query heads) until `budget_s` seconds
+    are spent or `max_groups` groups are done. Returns (GB/s of algorithmic KV bytes, threads
+    used, sample description, seconds, bytes)."""
+    import numpy as np
+
+    import oracle
+    wl = inp.wl
+    prob = oracle.make_problem(
+        batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+        head_dim=wl.head_dim, dtype=oracle.F32 if wl.dtype == "f32" else oracle.BF16,
+        scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi, max_seq_len=inp.max_seq_len,
+        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq)
+    es = 4 if wl.dtype == "f32" else 2
+    groups = [(b, g) for b in range(wl.batch) for g in range(wl.num_kv_heads)]
+    rng = np.random.default_rng(wl.seed ^ 0xC0FFEE)
+    order = rng.permutation(len(groups))
+    threads = oracle.default_threads()
+    done_bytes, done_s, n_groups, i = 0, 0.0, 0, 0
+    chunk = max(1, threads // max(1, wl.group))
+    while (budget_s is None or done_s < budget_s) and (max_groups is None or n_groups < max_groups):
+        c_n = chunk if max_groups is None else min(chunk, max_groups - n_groups)
+        sel = [groups[order[(i + c) % len(groups)]] for c in range(c_n)]
+        i += c_n
+        rows = np.array([(b, g * wl.group + h) for (b, g) in sel for h in range(wl.group)],
+                        np.int32)
+        t0 = time.perf_counter()
+        _, used = oracle.attention(prob, inp.q, inp.k, inp.v, inp.seq_lens,
+                                   block_table=inp.block_table, rows=rows, n_threads=threads)
+        done_s += time.perf_counter() - t0
+        threads = used if n_groups == 0 else threads
+        done_bytes += sum(int(inp.seq_lens[b]) * wl.head_dim * 2 * es for (b, g) in sel)
+        n_groups += len(sel)
+    gbs = done_bytes / done_s / 1e9 if done_s > 0 else 0.0
+    desc = (f"{n_groups} (sequence, kv-head) groups x {wl.group} query heads of {wl.name}, "
+            f"{done_s:.1f} s of fp64 oracle work on {threads} threads")
+    return gbs, threads, desc, done_s, done_bytes
+
+
+def run_reference(args, dist: Dist):
+    import workloads as W
+    if dist.rank != 0:
+        return None
+    wl = W.ALL[args.config]
+    inp = W.generate(wl)
+    # each step is a bounded sample: a fixed number of (b, g) groups sized so that
+    # warmup + steps fit in about args.cpu_budget_s * 10 seconds
+    gbs, threads, _, _, _ = oracle_sample_rate(inp, budget_s=1.0)
+    total_budget = 10.0 * args.cpu_budget_s
+    avg_group_bytes = inp.kv_bytes / (wl.batch * wl.num_kv_heads)
+    group_s = avg_group_bytes / (gbs * 1e9) if gbs > 0 else 1.0
+    groups_per_step = max(1, int(total_budget / (args.steps + args.warmup) / group_s))
+    groups_per_step = min(groups_per_step, wl.batch * wl.num_kv_heads)
+    for _ in range(args.warmup):
+        oracle_sample_rate(inp, max_groups=groups_per_step)
+    t_sum, b_sum = 0.0, 0
+    for _ in range(args.steps):
+        _, _, _, t, b = oracle_sample_rate(inp, max_groups=groups_per_step)
+        t_sum += t
+        b_sum += b
+    value = b_sum / t_sum / 1e9
+    sample = (f"each step: the fp64 oracle on {groups_per_step} (sequence, kv-head) groups x "
+              f"{wl.group} query heads of {wl.name} (of {wl.batch * wl.num_kv_heads}), "
+              f"{threads} host threads")
+    return {
+        "metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_sum / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "split_len": wl.split_len},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------------------------------
+# fdpp arm
+# ------------------------------------------------------------------------------------------
+
+def run_fdpp(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import split_kv_async_gb300 as F
+    import workloads as W
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.ALL[args.config]
+    if dist.world > 1:
+        wl = wl.replace(seed=wl.seed + 1000 * dist.rank)      # each rank its own batch
+    inp = W.generate(wl)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
+    kv_pool_bytes = inp.k.nbytes + inp.v.nbytes
+    R = max(1, min(8, math.ceil(4 * l2 / kv_pool_bytes)))
+
+    q = _dev_tensor(inp.q, dev)
+    ks = [_dev_tensor(inp.k, dev)]
+    vs = [_dev_tensor(inp.v, dev)]
+    for _ in range(R - 1):
+        ks.append(ks[0].clone())
+        vs.append(vs[0].clone())
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    bt = None if inp.block_table is None else torch.from_numpy(inp.block_table).to(dev)
+    out = torch.empty_like(q)
+    split_len = wl.split_len if args.split_len < 0 else args.split_len
+    kw = dict(batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+              head_dim=wl.head_dim, dtype=F.FDPP_F32 if wl.dtype == "f32" else F.FDPP_BF16,
+              max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
+              split_len=split_len, mode=args.mode, kernel=args.kernel, tc_stages=args.tc_stages,
+              tc_ctas_per_sm=args.tc_ctas)
+    if wl.paged:
+        kw.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
+                  num_kv_blocks=inp.num_kv_blocks,
+                  max_seq_len=inp.max_blocks_per_seq * wl.block_size)
+    p = F.make_params(**kw)
+    ws = F.alloc_workspace(p, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # raw C calls with pre-built arguments (the binding's per-call marshalling is not timed)
+    call = F.lib.fdpp_decode_attn_timed
+    pp = ctypes.byref(p)
+    ws_bytes = ws.numel()
+    argsets = [(q.data_ptr(), ks[i].data_ptr(), vs[i].data_ptr(),
+                None if bt is None else bt.data_ptr(), sl.data_ptr(), pp, ws.data_ptr(), ws_bytes,
+                out.data_ptr(), sh) for i in range(R)]
+
+    def step(i, eb=None, ee=None):
+        st = call(*argsets[i % R], eb, ee)
+        if st != 0:
+            raise F.FdppError(st, "fdpp_decode_attn_timed", F.fdpp_last_error())
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    diag, _, _ = F.fdpp_read_diag(ws, p)
+    kernel_name = {1: "tensor", 2: "simt"}.get(diag["kernel"], "?")
+
+    K = args.steps
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0,
+                           enabled=not args.no_clocks and dist.local_rank == 0)
+    time.sleep(0.25 if sampler.proc else 0.0)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        step(i, ev_b[i].cuda_event, ev_e[i].cuda_event)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    split_ms = [ev_b[i].elapsed_time(ev_e[i]) for i in range(K)]
+    diag, _, _ = F.fdpp_read_diag(ws, p)
+
+    kv_bytes = inp.kv_bytes
+    tot_bytes, t_max, value = aggregate(kv_bytes * K, total_ms / 1e3, dist)
+    ms_per_step = t_max * 1e3 / K
+    split_mean_ms = sum(split_ms) / K
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (split_mean_ms / 1e3) / 1e9
+
+    # end to end through the C ABI with host buffers (pinned), per step H2D + call + D2H + sync
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(inp.q.view(np.int16) if inp.q.dtype == np.uint16 else inp.q).pin_memory()
+        hsl = torch.from_numpy(inp.seq_lens).pin_memory()
+        hbt = None if bt is None else torch.from_numpy(inp.block_table).pin_memory()
+        hout = torch.empty(out.numel() * out.element_size(), dtype=torch.uint8).pin_memory()
+        qd = q.view(torch.int16) if q.dtype == torch.bfloat16 else q
+        h2d = hq.numel() * hq.element_size() + hsl.numel() * 4 + (0 if hbt is None else hbt.numel() * 4)
+        d2h = out.numel() * out.element_size()
+
+        def e2e_step(i):
+            qd.copy_(hq, non_blocking=True)
+            sl.copy_(hsl, non_blocking=True)
+            if hbt is not None:
+                bt.copy_(hbt, non_blocking=True)
+            step(i)
+            hout.copy_(out.view(-1).view(torch.uint8), non_blocking=True)
+            stream.synchronize()
+
+        for i in range(3):
+            e2e_step(i)
+        dist.barrier()
+        n = max(1, args.e2e_steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _, t_e2e, v_e2e = aggregate(kv_bytes * n, e0.elapsed_time(e1) / 1e3, dist)
+        e2e = {"value": v_e2e, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "us_per_step": t_e2e * 1e6 / n}
+
+    cpu = None
+    if not args.no_cpu and dist.rank == 0:
+        gbs, threads, desc, _, _ = oracle_sample_rate(inp, budget_s=args.cpu_budget_s)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if dist.rank != 0:
+        return None
+    traffic = recorded_traffic(wl.name, kernel_name)
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "pct_of_8TBps": 100.0 * value / dist.world / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * value / dist.world / peak,
+        "config": {"workload": wl.name, "batch": wl.batch, "num_q_heads": wl.num_q_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "seq_len": wl.seq_len if wl.seq_len else list(wl.seq_len_range),
+                   "paged": wl.paged, "block_size": wl.block_size if wl.paged else None,
+                   "split_len": diag["split_len"], "phi": wl.phi, "window": [wl.lo, wl.hi],
+                   "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
+                   "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "
+                                f"4x L2 {l2 / 2**20:.0f} MiB); no flush",
+                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": traffic, "kernel": f"split_{kernel_name}",
+                     "split_kernel_us": split_mean_ms * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "fallback": {"flagged_row_splits": diag["n_flagged_row_splits"],
+                     "flagged_units": diag["n_flagged_units"], "units": diag["n_units"],
+                     "unit_rate": diag["n_flagged_units"] / max(1, diag["n_units"])},
+        "clocks": clocks,
+        "error_bits": diag["error_bits"],
+    }
+    return res
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        else:
+            import __graft_entry__
+            if dist.rank == 0:
+                __graft_entry__.build()
+            dist.barrier()
+            __graft_entry__.build()
+            res = run_fdpp(args, dist)
+        if res is not None and dist.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

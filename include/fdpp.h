@@ -1,0 +1,188 @@
+/*
+ * fdpp.h -- C ABI of libfdpp: unified-max split-KV decode attention for GB300 (sm_103a).
+ *
+ * The operation. In the decode step, one query token per sequence attends to that sequence's
+ * K/V cache, which keeps growing (opt.ai.kr "FlashDecoding++ async softmax -- theory",
+ * section 1). For sequence b, query head h and kv head g = floor(h / G), G = Hq / Hkv:
+ *
+ *     s_t   = scale * <q[b,h,:], k[b,t,g,:]>                      for t < L_b = seq_lens[b]
+ *     out   = sum_t exp(s_t - mu) v[b,t,g,:] / sum_t exp(s_t - mu),  mu any finite shift
+ *
+ * How it is computed (same page, section 3). The cache of each sequence is cut into splits of
+ * S tokens. Every split works alone against a unified max phi fixed in advance: it forms
+ * o_j = sum exp(s_t - phi) v_t and l_j = sum exp(s_t - phi), with no communication between
+ * splits. A split in which some score leaves the safe window, i.e. NOT (lo <= s_t - phi <= hi),
+ * is computed again with the ordinary online softmax (running max m_j). The final combine is
+ * out = sum_j exp(m_j - M) o_j / sum_j exp(m_j - M) l_j with M = max_j m_j, which is the plain
+ * sum of the page whenever no split fell back (every m_j = phi).
+ *
+ * Conventions for every call below:
+ *   - Pointers marked DEVICE are device memory owned by the caller. The library allocates and
+ *     frees nothing, keeps no pointer after a call returns, and writes only `out` and the
+ *     caller's workspace.
+ *   - Calls that take a stream only enqueue work on it (no host synchronisation) and return
+ *     before the GPU runs it. Two calls that share one workspace must not overlap on the GPU.
+ *   - Argument errors are reported synchronously, before anything is enqueued, as a status code;
+ *     fdpp_last_error() then gives a one-line reason (thread-local). A CUDA launch error returns
+ *     FDPP_ERR_CUDA. Problems found on the device (a seq_len out of range, a bad block table
+ *     entry, a pipeline wait that ran out) never trap: they set sticky bits read by
+ *     fdpp_read_diag().
+ *   - Every kernel is bounded: each wait gives up after about two seconds, sets
+ *     FDPP_ERRBIT_TIMEOUT and lets the launch finish.
+ */
+#ifndef FDPP_H
+#define FDPP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* fdpp_stream;
+
+typedef enum {
+    FDPP_OK = 0,
+    FDPP_ERR_INVALID_ARG = 1,   /* a pointer, size or parameter violates the contract */
+    FDPP_ERR_UNSUPPORTED = 2,   /* valid, but no kernel here handles it (e.g. head_dim 96) */
+    FDPP_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or smaller than required */
+    FDPP_ERR_CUDA = 4           /* a CUDA runtime call or a launch failed */
+} fdpp_status;
+
+typedef enum { FDPP_F32 = 0, FDPP_BF16 = 1 } fdpp_dtype;
+
+typedef enum {
+    FDPP_MODE_NORMAL = 0,        /* phi frame, fallback recompute of out-of-window splits */
+    FDPP_MODE_FORCE_FAST = 1,    /* phi frame, never recompute (negative control: results of
+                                    flagged splits may be inf/NaN) */
+    FDPP_MODE_FORCE_ONLINE = 2   /* every split with the ordinary online softmax (the
+                                    running-max baseline the unified max replaces) */
+} fdpp_mode;
+
+typedef enum {
+    FDPP_KERNEL_AUTO = 0,        /* tensor-core kernel when it applies, else the SIMT kernel */
+    FDPP_KERNEL_TENSOR = 1,      /* TMA-fed kernel, q.K^T and P.V on tensor cores: bf16,
+                                    head_dim 64/128, G <= 8 */
+    FDPP_KERNEL_SIMT = 2         /* CUDA-core kernel with warp-shuffle reductions: f32 or bf16,
+                                    head_dim 64/128, G <= 16 */
+} fdpp_kernel;
+
+/* Flag byte per (b, h, j), readable through fdpp_read_diag. */
+enum {
+    FDPP_FLAG_OUT = 1,           /* some score of the split left the window */
+    FDPP_FLAG_ABOVE = 2,         /* ... above phi + hi (the overflow side) */
+    FDPP_FLAG_BELOW = 4,         /* ... below phi + lo */
+    FDPP_FLAG_NAN = 8,           /* ... was NaN */
+    FDPP_FLAG_RECOMPUTED = 16    /* the partial of this row-split came from online softmax */
+};
+
+/* Sticky device error bits (cleared by fdpp_workspace_init). */
+enum {
+    FDPP_ERRBIT_SEQ_LEN = 1,     /* a seq_lens entry was < 0 or > max_seq_len (clamped) */
+    FDPP_ERRBIT_BLOCK_TABLE = 2, /* a block table entry of a valid token was outside the pool
+                                    (that block was not read; its row is wrong) */
+    FDPP_ERRBIT_TIMEOUT = 4      /* a pipeline wait ran out; results of that call are invalid */
+};
+
+typedef struct fdpp_params {
+    int batch;               /* B >= 1 sequences, one query token each */
+    int num_q_heads;         /* Hq >= 1 */
+    int num_kv_heads;        /* Hkv >= 1, Hq % Hkv == 0 */
+    int head_dim;            /* d: 64 or 128 */
+    int dtype;               /* fdpp_dtype of q, k_cache, v_cache and out */
+    int max_seq_len;         /* contiguous cache: its token dimension Lmax. Paged cache: an
+                                upper bound on every seq_len, <= max_blocks_per_seq*block_size.
+                                Sizes the workspace. */
+    int block_size;          /* paged only: tokens per block, a power of two in [16, 256] */
+    int max_blocks_per_seq;  /* paged only: row length of block_table */
+    int num_kv_blocks;       /* paged only: number of blocks in the K (and V) pool */
+    float scale;             /* score scale, usually 1/sqrt(d) */
+    float phi;               /* unified max, in units of the scaled score s */
+    float lo, hi;            /* safe window: a score is inside iff lo <= s - phi <= hi */
+    int split_len;           /* S > 0: tokens per split (paged: a multiple of block_size).
+                                0: chosen per call from sum_b L_b, Hkv and the SM count */
+    int mode;                /* fdpp_mode */
+    int kernel;              /* fdpp_kernel */
+    int tc_stages;           /* tensor kernel: depth of the TMA ring (2..12), 0 = automatic */
+    int tc_ctas_per_sm;      /* tensor kernel: resident CTAs per SM (1..4), 0 = automatic */
+} fdpp_params;
+
+/* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over
+ * FDPP_AUTO_UNITS_PER_SM * num_sms units, round up to a multiple of FDPP_AUTO_GRANULE (or of
+ * block_size when larger), clamp to [FDPP_AUTO_MIN_SPLIT, max_seq_len rounded up]. */
+#define FDPP_AUTO_UNITS_PER_SM 4
+#define FDPP_AUTO_GRANULE 64
+#define FDPP_AUTO_MIN_SPLIT 256
+
+typedef struct fdpp_diag {
+    int32_t split_len;            /* S used by the last call on this workspace */
+    int32_t max_splits;           /* partial slots per (b, h) in this workspace */
+    int64_t n_units;              /* (b, g, j) units of the last call */
+    int64_t n_flagged_row_splits; /* (b, h, j) with FDPP_FLAG_OUT */
+    int64_t n_flagged_units;      /* (b, g, j) with at least one flagged head */
+    int64_t n_recomputed_row_splits; /* (b, h, j) with FDPP_FLAG_RECOMPUTED */
+    uint32_t error_bits;          /* FDPP_ERRBIT_* since the last fdpp_workspace_init */
+    int32_t kernel;               /* fdpp_kernel that ran last (1 tensor, 2 SIMT) */
+} fdpp_diag;
+
+/* Partial slots per (b, h) that a workspace for `p` holds: ceil(max_seq_len / S) for a fixed
+ * S, ceil(max_seq_len / FDPP_AUTO_MIN_SPLIT) for S == 0. Returns -1 on invalid params. */
+int fdpp_max_splits(const fdpp_params* p);
+
+/* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
+ * holds the split plan, the per-split partials (o: fp32 [B][Hq][max_splits][d]; l, m: fp32
+ * [B][Hq][max_splits]), the flag bytes [B][Hq][max_splits] and a small header. */
+fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
+
+/* Zeroes a workspace (stream-ordered). Call once after allocating it; it also clears the
+ * sticky error bits. workspace: DEVICE, 256-byte aligned. */
+fdpp_status fdpp_workspace_init(void* workspace, size_t workspace_bytes, fdpp_stream stream);
+
+/* One decode-attention step for B sequences (enqueued on `stream`).
+ *   q           DEVICE [B][Hq][d] of dtype, 16-byte aligned.
+ *   k_cache,    DEVICE, 16-byte aligned, dtype. Contiguous (block_table == NULL):
+ *   v_cache       [B][max_seq_len][Hkv][d]. Paged: pools [num_kv_blocks][block_size][Hkv][d];
+ *                 token t of sequence b is slot t % block_size of block
+ *                 block_table[b][t / block_size].
+ *   block_table DEVICE int32 [B][max_blocks_per_seq] or NULL (contiguous cache).
+ *   seq_lens    DEVICE int32 [B]: L_b, 0 <= L_b <= max_seq_len. L_b == 0 gives a zero row.
+ *   workspace   DEVICE, 256-byte aligned, >= fdpp_workspace_size bytes, zeroed once by
+ *               fdpp_workspace_init. Not shared by overlapping calls.
+ *   out         DEVICE [B][Hq][d] of dtype (rounded to nearest even from fp32).
+ * Tokens t >= L_b are never part of a score, a window test or a sum (they may hold anything,
+ * NaN included). */
+fdpp_status fdpp_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const fdpp_params* p, void* workspace, size_t workspace_bytes,
+                             void* out, fdpp_stream stream);
+
+/* fdpp_decode_attn, and also records two caller-owned CUDA events (cudaEvent_t, either may be
+ * NULL) on `stream`: ev_split_begin right before the split kernel (steps: split plan, phi-frame
+ * partials, window test, recompute) and ev_split_end right after it, before the combine kernel.
+ * Lets a caller time the dominant kernel alone; results are identical to fdpp_decode_attn. */
+fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const fdpp_params* p, void* workspace, size_t workspace_bytes,
+                                   void* out, fdpp_stream stream, void* ev_split_begin,
+                                   void* ev_split_end);
+
+/* Reads what the last call left in `workspace` (synchronous device-to-host copies; call after
+ * that call's stream has been synchronised). diag: HOST, required. flags_host: HOST uint8
+ * [B][Hq][max_splits] or NULL. nsplit_host: HOST int32 [B] (splits per sequence) or NULL.
+ * Entries with j >= nsplit[b] are stale. */
+fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const fdpp_params* p,
+                           fdpp_diag* diag, uint8_t* flags_host, int32_t* nsplit_host);
+
+/* Static name of a status code. */
+const char* fdpp_status_str(fdpp_status s);
+
+/* Reason for the last non-OK status returned on this thread ("" if none). */
+const char* fdpp_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FDPP_H */

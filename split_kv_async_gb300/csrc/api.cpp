@@ -1,0 +1,398 @@
+// api.cpp -- the C ABI of libfdpp: argument checks, workspace layout, kernel choice, TMA
+// descriptors and launches. Every entry point here is declared and documented in fdpp.h.
+//
+// A decode step is two stream-ordered launches:
+//   1. the split kernel (tensor-core or SIMT variant), persistent over the (b, g, j) units; each
+//      CTA plans the splits itself from seq_lens, so no plan launch and no host sync is needed;
+//   2. the combine kernel, one CTA per (b, h) row.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fdpp.h"
+#include "fdpp_internal.h"
+
+using namespace fdpp;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fdpp_status fail(fdpp_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int max_splits_of(const fdpp_params& p)
+{
+    const long long S = p.split_len > 0 ? p.split_len : FDPP_AUTO_MIN_SPLIT;
+    return (int)((p.max_seq_len + S - 1) / S);
+}
+
+// Host-only checks shared by every entry point (no CUDA call).
+fdpp_status check_params(const fdpp_params* p)
+{
+    if (!p) return fail(FDPP_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1) return fail(FDPP_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", p->batch);
+    if (p->num_q_heads < 1 || p->num_kv_heads < 1)
+        return fail(FDPP_ERR_INVALID_ARG, "head counts must be >= 1");
+    if (p->num_q_heads % p->num_kv_heads)
+        return fail(FDPP_ERR_INVALID_ARG, "num_q_heads (%d) is not a multiple of num_kv_heads (%d)",
+                    p->num_q_heads, p->num_kv_heads);
+    if (p->dtype != FDPP_F32 && p->dtype != FDPP_BF16)
+        return fail(FDPP_ERR_INVALID_ARG, "dtype must be FDPP_F32 or FDPP_BF16 (got %d)", p->dtype);
+    if (p->head_dim != 64 && p->head_dim != 128)
+        return fail(FDPP_ERR_UNSUPPORTED, "head_dim %d: only 64 and 128 are built", p->head_dim);
+    if (p->max_seq_len < 1) return fail(FDPP_ERR_INVALID_ARG, "max_seq_len must be >= 1");
+    if (p->split_len < 0) return fail(FDPP_ERR_INVALID_ARG, "split_len must be >= 0");
+    if (!std::isfinite(p->scale) || !std::isfinite(p->phi) || !std::isfinite(p->lo) ||
+        !std::isfinite(p->hi))
+        return fail(FDPP_ERR_INVALID_ARG, "scale, phi, lo and hi must be finite");
+    if (!(p->lo <= p->hi)) return fail(FDPP_ERR_INVALID_ARG, "window needs lo <= hi");
+    if (p->mode < FDPP_MODE_NORMAL || p->mode > FDPP_MODE_FORCE_ONLINE)
+        return fail(FDPP_ERR_INVALID_ARG, "unknown mode %d", p->mode);
+    if (p->kernel < FDPP_KERNEL_AUTO || p->kernel > FDPP_KERNEL_SIMT)
+        return fail(FDPP_ERR_INVALID_ARG, "unknown kernel %d", p->kernel);
+    if (p->tc_stages < 0 || p->tc_stages == 1 || p->tc_stages > 12)
+        return fail(FDPP_ERR_INVALID_ARG, "tc_stages must be 0 or in [2, 12]");
+    if (p->tc_ctas_per_sm < 0 || p->tc_ctas_per_sm > 4)
+        return fail(FDPP_ERR_INVALID_ARG, "tc_ctas_per_sm must be 0 or in [1, 4]");
+    const int G = p->num_q_heads / p->num_kv_heads;
+    if (G > SIMT_MAX_GROUP)
+        return fail(FDPP_ERR_UNSUPPORTED, "query heads per kv head %d > %d", G, SIMT_MAX_GROUP);
+    // sizes stay far from overflow: partials below 2^50 bytes, unit indices below 2^31
+    const long double o_bytes = (long double)p->batch * p->num_q_heads * max_splits_of(*p) *
+                                p->head_dim * 4.0L;
+    const long double units = (long double)p->batch * p->num_kv_heads * max_splits_of(*p);
+    if (o_bytes > 1e15L || units > 2e9L)
+        return fail(FDPP_ERR_INVALID_ARG, "problem too large for one workspace");
+    return FDPP_OK;
+}
+
+fdpp_status check_paged(const fdpp_params* p)
+{
+    if (!is_pow2(p->block_size) || p->block_size < 16 || p->block_size > 256)
+        return fail(FDPP_ERR_INVALID_ARG, "block_size must be a power of two in [16, 256] (got %d)",
+                    p->block_size);
+    if (p->max_blocks_per_seq < 1) return fail(FDPP_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+    if (p->num_kv_blocks < 1) return fail(FDPP_ERR_INVALID_ARG, "num_kv_blocks must be >= 1");
+    if ((long long)p->max_seq_len > (long long)p->max_blocks_per_seq * p->block_size)
+        return fail(FDPP_ERR_INVALID_ARG, "max_seq_len exceeds max_blocks_per_seq * block_size");
+    if (p->split_len > 0 && p->split_len % p->block_size)
+        return fail(FDPP_ERR_INVALID_ARG, "split_len (%d) must be a multiple of block_size (%d)",
+                    p->split_len, p->block_size);
+    return FDPP_OK;
+}
+
+WsLayout layout_of(const fdpp_params& p)
+{
+    WsLayout w{};
+    w.max_splits = max_splits_of(p);
+    const size_t rows = (size_t)p.batch * p.num_q_heads;
+    const size_t slots = rows * (size_t)w.max_splits;
+    size_t off = 0;
+    w.header = off;  off = align256(off + HDR_WORDS * 4);
+    w.nsplit = off;  off = align256(off + (size_t)p.batch * 4);
+    w.tickets = off; off = align256(off + (size_t)p.batch * p.num_kv_heads * 4);
+    w.flags = off;   off = align256(off + slots);
+    w.m_part = off;  off = align256(off + slots * 4);
+    w.l_part = off;  off = align256(off + slots * 4);
+    w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
+    w.total = off;
+    return w;
+}
+
+bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+struct DeviceInfo {
+    bool valid = false;
+    int sms = 0, smem_per_sm = 0, smem_per_block = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+fdpp_status device_info(DeviceInfo& out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return fail(FDPP_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.valid) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return fail(FDPP_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        if (major != 10 || minor != 3)
+            return fail(FDPP_ERR_UNSUPPORTED, "libfdpp is built for sm_103a only (device is sm_%d%d)",
+                        major, minor);
+        d.valid = true;
+    }
+    out = d;
+    return FDPP_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+fdpp_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000& fn)
+{
+    std::call_once(g_encode_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!g_encode) return fail(FDPP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    fn = g_encode;
+    return FDPP_OK;
+}
+
+// 3-D bf16 tensor map over a K or V cache with 128-byte swizzle and 64-element-wide boxes.
+//   contiguous: dims {Hkv*d, Lmax, B},          box {64, 64, 1}
+//   paged:      dims {Hkv*d, block_size, nblk}, box {64, min(block_size, 64), 1}
+fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params& p, bool paged)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    fdpp_status st = tensor_map_encoder(enc);
+    if (st != FDPP_OK) return st;
+    const cuuint64_t row = (cuuint64_t)p.num_kv_heads * p.head_dim;
+    const cuuint64_t d1 = paged ? (cuuint64_t)p.block_size : (cuuint64_t)p.max_seq_len;
+    const cuuint64_t d2 = paged ? (cuuint64_t)p.num_kv_blocks : (cuuint64_t)p.batch;
+    cuuint64_t dims[3] = {row, d1, d2};
+    cuuint64_t strides[2] = {row * 2, row * 2 * d1};
+    const cuuint32_t box_rows =
+        (cuuint32_t)(paged ? (p.block_size < TC_TILE_TOKENS ? p.block_size : TC_TILE_TOKENS)
+                           : TC_TILE_TOKENS);
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FDPP_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return FDPP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fdpp_status_str(fdpp_status s)
+{
+    switch (s) {
+    case FDPP_OK: return "FDPP_OK";
+    case FDPP_ERR_INVALID_ARG: return "FDPP_ERR_INVALID_ARG";
+    case FDPP_ERR_UNSUPPORTED: return "FDPP_ERR_UNSUPPORTED";
+    case FDPP_ERR_WORKSPACE: return "FDPP_ERR_WORKSPACE";
+    case FDPP_ERR_CUDA: return "FDPP_ERR_CUDA";
+    }
+    return "FDPP_UNKNOWN_STATUS";
+}
+
+const char* fdpp_last_error(void) { return g_last_error.c_str(); }
+
+int fdpp_max_splits(const fdpp_params* p)
+{
+    if (check_params(p) != FDPP_OK) return -1;
+    return max_splits_of(*p);
+}
+
+fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes)
+{
+    fdpp_status st = check_params(p);
+    if (st != FDPP_OK) return st;
+    if (!bytes) return fail(FDPP_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = layout_of(*p).total;
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_workspace_init(void* workspace, size_t workspace_bytes, fdpp_stream stream)
+{
+    if (!workspace) return fail(FDPP_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(FDPP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const fdpp_params* p, void* workspace, size_t workspace_bytes,
+                             void* out, fdpp_stream stream)
+{
+    return fdpp_decode_attn_timed(q, k_cache, v_cache, block_table, seq_lens, p, workspace,
+                                  workspace_bytes, out, stream, nullptr, nullptr);
+}
+
+fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const fdpp_params* p, void* workspace, size_t workspace_bytes,
+                                   void* out, fdpp_stream stream, void* ev_split_begin,
+                                   void* ev_split_end)
+{
+    fdpp_status st = check_params(p);
+    if (st != FDPP_OK) return st;
+    const bool paged = block_table != nullptr;
+    if (paged && (st = check_paged(p)) != FDPP_OK) return st;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out)
+        return fail(FDPP_ERR_INVALID_ARG, "q, k_cache, v_cache, seq_lens and out must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return fail(FDPP_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(seq_lens, 4) || (paged && !aligned(block_table, 4)))
+        return fail(FDPP_ERR_INVALID_ARG, "seq_lens and block_table must be 4-byte aligned");
+    if (!workspace) return fail(FDPP_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(FDPP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    const WsLayout w = layout_of(*p);
+    if (workspace_bytes < w.total)
+        return fail(FDPP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, w.total);
+
+    const int G = p->num_q_heads / p->num_kv_heads;
+    const bool tc_ok = p->dtype == FDPP_BF16 && G <= TC_MAX_GROUP;
+    int kernel = p->kernel;
+    if (kernel == FDPP_KERNEL_AUTO) kernel = tc_ok ? FDPP_KERNEL_TENSOR : FDPP_KERNEL_SIMT;
+    if (kernel == FDPP_KERNEL_TENSOR && !tc_ok)
+        return fail(FDPP_ERR_UNSUPPORTED, "tensor kernel needs bf16 and at most %d query heads per kv head",
+                    TC_MAX_GROUP);
+
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != FDPP_OK) return st;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    KernelArgs a{};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
+    a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
+    a.tickets = reinterpret_cast<int32_t*>(ws + w.tickets);
+    a.flags = ws + w.flags;
+    a.m_part = reinterpret_cast<float*>(ws + w.m_part);
+    a.l_part = reinterpret_cast<float*>(ws + w.l_part);
+    a.o_part = reinterpret_cast<float*>(ws + w.o_part);
+    a.B = p->batch;
+    a.Hq = p->num_q_heads;
+    a.Hkv = p->num_kv_heads;
+    a.G = G;
+    a.D = p->head_dim;
+    a.max_seq_len = p->max_seq_len;
+    a.block_size = paged ? p->block_size : 0;
+    a.max_blocks = paged ? p->max_blocks_per_seq : 0;
+    a.num_blocks = paged ? p->num_kv_blocks : 0;
+    a.split_req = p->split_len;
+    a.max_splits = w.max_splits;
+    a.num_sms = dev.sms;
+    a.scale = p->scale;
+    a.phi = p->phi;
+    a.lo = p->lo;
+    a.hi = p->hi;
+    a.mode = p->mode;
+    a.kernel_id = kernel;
+
+    const long long units_max = (long long)p->batch * p->num_kv_heads * w.max_splits;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+    if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
+        return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+    if (kernel == FDPP_KERNEL_TENSOR) {
+        const TcPlan plan = split_tc_plan(p->head_dim, G, p->tc_stages, p->tc_ctas_per_sm,
+                                          dev.smem_per_sm, dev.smem_per_block);
+        if (plan.nstage == 0)
+            return fail(FDPP_ERR_UNSUPPORTED, "no tensor-kernel geometry fits (stages %d, CTAs/SM %d)",
+                        p->tc_stages, p->tc_ctas_per_sm);
+        a.nstage = plan.nstage;
+        CUtensorMap tk, tv;
+        if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
+        if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;
+        long long grid = (long long)dev.sms * plan.ctas_per_sm;
+        if (grid > units_max) grid = units_max;
+        e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, s);
+    } else {
+        const int occ = split_simt_ctas_per_sm(a, p->dtype);
+        long long grid = (long long)dev.sms * (occ > 0 ? occ : 1);
+        if (grid > units_max) grid = units_max;
+        e = launch_split_simt(a, p->dtype, (int)grid, s);
+    }
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
+    if (ev_split_end && (e = cudaEventRecord((cudaEvent_t)ev_split_end, s)) != cudaSuccess)
+        return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+    e = launch_combine(a, p->dtype, s);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const fdpp_params* p,
+                           fdpp_diag* diag, uint8_t* flags_host, int32_t* nsplit_host)
+{
+    fdpp_status st = check_params(p);
+    if (st != FDPP_OK) return st;
+    if (!diag) return fail(FDPP_ERR_INVALID_ARG, "diag is NULL");
+    if (!workspace) return fail(FDPP_ERR_WORKSPACE, "workspace is NULL");
+    const WsLayout w = layout_of(*p);
+    if (workspace_bytes < w.total)
+        return fail(FDPP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, w.total);
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    int32_t hdr[HDR_WORDS];
+    cudaError_t e = cudaMemcpy(hdr, ws + w.header, sizeof hdr, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
+    const size_t B = (size_t)p->batch, Hq = (size_t)p->num_q_heads, ms = (size_t)w.max_splits;
+    std::string nsb(B * 4, '\0');
+    std::string flb(B * Hq * ms, '\0');
+    if ((e = cudaMemcpy(&nsb[0], ws + w.nsplit, nsb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(&flb[0], ws + w.flags, flb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
+    const int32_t* ns = reinterpret_cast<const int32_t*>(nsb.data());
+    const uint8_t* fl = reinterpret_cast<const uint8_t*>(flb.data());
+    std::memset(diag, 0, sizeof *diag);
+    diag->split_len = hdr[HDR_SPLIT];
+    diag->max_splits = w.max_splits;
+    diag->n_units = hdr[HDR_UNITS];
+    diag->error_bits = (uint32_t)hdr[HDR_ERR];
+    diag->kernel = hdr[HDR_KERNEL];
+    const size_t G = Hq / (size_t)p->num_kv_heads;
+    for (size_t b = 0; b < B; ++b) {
+        const int n = ns[b] < 0 ? 0 : (ns[b] > (int)ms ? (int)ms : ns[b]);
+        for (int j = 0; j < n; ++j) {
+            for (size_t g = 0; g < (size_t)p->num_kv_heads; ++g) {
+                bool any = false;
+                for (size_t hh = 0; hh < G; ++hh) {
+                    const uint8_t f = fl[((b * Hq) + g * G + hh) * ms + (size_t)j];
+                    if (f & FDPP_FLAG_OUT) { ++diag->n_flagged_row_splits; any = true; }
+                    if (f & FDPP_FLAG_RECOMPUTED) ++diag->n_recomputed_row_splits;
+                }
+                if (any) ++diag->n_flagged_units;
+            }
+        }
+    }
+    if (flags_host) std::memcpy(flags_host, fl, flb.size());
+    if (nsplit_host) std::memcpy(nsplit_host, ns, B * 4);
+    return FDPP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,278 @@
+// device_common.cuh -- device helpers shared by the kernels of libfdpp.
+//
+//  * the split scheduler (block-cooperative, run by every CTA so no plan launch is needed);
+//  * the unit cursor that maps a unit index to (sequence b, kv head g, split j);
+//  * inline-PTX wrappers for mbarrier, TMA (cp.async.bulk[.tensor]), ldmatrix and mma.sync;
+//  * bounded waits: every wait gives up after FDPP_WAIT_NS nanoseconds of global time.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fdpp_internal.h"
+
+namespace fdpp {
+
+#ifndef FDPP_WAIT_NS
+#define FDPP_WAIT_NS 2000000000ull   // 2 s of %globaltimer per wait
+#endif
+
+// ------------------------------------------------------------------------------------------
+// split scheduler
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// Split length: the caller's S when > 0, otherwise spread sum_b L_b * Hkv over
+// FDPP_AUTO_UNITS_PER_SM * num_sms units, rounded up to the granule and clamped to
+// [FDPP_AUTO_MIN_SPLIT, max_seq_len rounded up].
+__device__ __forceinline__ int auto_split_len(long long total_tokens, const KernelArgs& a)
+{
+    if (a.split_req > 0) return a.split_req;
+    long long units = (long long)FDPP_AUTO_UNITS_PER_SM * (long long)a.num_sms;
+    if (units < 1) units = 1;
+    long long gran = FDPP_AUTO_GRANULE;
+    if (a.block_table && a.block_size > gran) gran = a.block_size;
+    long long pairs = total_tokens * (long long)a.Hkv;
+    long long S = (pairs + units - 1) / units;
+    S = (S + gran - 1) / gran * gran;
+    long long hi = ((long long)a.max_seq_len + gran - 1) / gran * gran;
+    if (hi < FDPP_AUTO_MIN_SPLIT) hi = FDPP_AUTO_MIN_SPLIT;
+    if (S < FDPP_AUTO_MIN_SPLIT) S = FDPP_AUTO_MIN_SPLIT;
+    if (S > hi) S = hi;
+    return (int)S;
+}
+
+template <typename V>
+__device__ __forceinline__ V warp_sum(V x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Block-wide sum of a 64-bit value. `red` is shared scratch of >= 32 long longs. All threads of
+// the block call it; the result is returned to every thread.
+__device__ __forceinline__ long long block_sum_ll(long long x, long long* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    x = warp_sum(x);
+    __syncthreads();
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    long long t = 0;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    return t;
+}
+
+// Every CTA computes the same plan: S and the unit count. CTA 0 also publishes the plan
+// (nsplit[b] and the header) and reports out-of-range seq_lens. Called by all threads.
+__device__ __forceinline__ void block_plan(const KernelArgs& a, long long* red, int& S_out,
+                                           int& units_out)
+{
+    long long total = 0, bad = 0;
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+        int L = a.seq_lens[b];
+        bad += (L < 0 || L > a.max_seq_len) ? 1 : 0;
+        total += clamp_len(L, a.max_seq_len);
+    }
+    total = block_sum_ll(total, red);
+    const int S = auto_split_len(total, a);
+    long long n = 0;
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+        int nb = ceil_div_i(clamp_len(a.seq_lens[b], a.max_seq_len), S);
+        if (nb > a.max_splits) nb = a.max_splits;       // cannot happen for valid S; keeps writes in bounds
+        n += nb;
+        if (blockIdx.x == 0) a.nsplit[b] = nb;
+    }
+    n = block_sum_ll(n, red);
+    bad = block_sum_ll(bad, red);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.hdr[HDR_SPLIT] = S;
+        a.hdr[HDR_UNITS] = (int)(n * a.Hkv);
+        a.hdr[HDR_KERNEL] = a.kernel_id;
+        a.hdr[HDR_BATCH] = a.B;
+        a.hdr[HDR_MAXSPLITS] = a.max_splits;
+        if (bad) atomicOr((unsigned*)&a.hdr[HDR_ERR], (unsigned)FDPP_ERRBIT_SEQ_LEN);
+    }
+    S_out = S;
+    units_out = (int)(n * a.Hkv);
+}
+
+// Walks units in increasing order: unit u -> (b, g, j). Units are b-major, then kv head g,
+// then split j; sequence b owns Hkv * n_b consecutive units.
+struct UnitCursor {
+    int b;
+    int nb;
+    long long base;
+
+    __device__ __forceinline__ void reset() { b = -1; nb = 0; base = 0; }
+
+    __device__ __forceinline__ void seek(const KernelArgs& a, int S, long long u, int& ub, int& ug,
+                                         int& uj, int& L)
+    {
+        while (b < 0 || u >= base + (long long)a.Hkv * nb) {
+            if (b >= 0) base += (long long)a.Hkv * nb;
+            ++b;
+            int n = ceil_div_i(clamp_len(a.seq_lens[b], a.max_seq_len), S);
+            nb = n > a.max_splits ? a.max_splits : n;
+        }
+        long long r = u - base;
+        ub = b;
+        ug = (int)(r / nb);
+        uj = (int)(r % nb);
+        L = clamp_len(a.seq_lens[b], a.max_seq_len);
+    }
+};
+
+__device__ __forceinline__ void set_error(const KernelArgs& a, unsigned bit)
+{
+    atomicOr((unsigned*)&a.hdr[HDR_ERR], bit);
+}
+
+// ------------------------------------------------------------------------------------------
+// PTX wrappers
+// ------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete; false after FDPP_WAIT_NS without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_ns() - t0 > FDPP_WAIT_NS) return false;
+    }
+}
+
+// 3-D tiled TMA load into shared memory, completing `bytes` on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Plain bulk copy global -> shared (size and both addresses multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Window decision for x = s - phi (closed window; NaN is outside).
+__device__ __forceinline__ unsigned classify(float x, float lo, float hi)
+{
+    if (x >= lo && x <= hi) return 0u;
+    if (x != x) return FDPP_FLAG_OUT | FDPP_FLAG_NAN;
+    return x > hi ? (FDPP_FLAG_OUT | FDPP_FLAG_ABOVE) : (FDPP_FLAG_OUT | FDPP_FLAG_BELOW);
+}
+
+// exp(m_w - M) with the exact 1 when the frames agree (so phi-frame partials add plainly).
+__device__ __forceinline__ float frame_weight(float m, float M)
+{
+    return m == M ? 1.0f : __expf(m - M);
+}
+
+}  // namespace fdpp

@@ -1,0 +1,82 @@
+// fdpp_internal.h -- types shared by the host API and the kernels of libfdpp (not installed).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fdpp.h"
+
+namespace fdpp {
+
+// Workspace header words (int32 each).
+enum {
+    HDR_SPLIT = 0,      // S used by the last call
+    HDR_UNITS = 1,      // (b, g, j) units of the last call
+    HDR_KERNEL = 2,     // fdpp_kernel that ran
+    HDR_ERR = 3,        // sticky FDPP_ERRBIT_* (atomicOr)
+    HDR_BATCH = 4,      // B of the last call
+    HDR_MAXSPLITS = 5,  // partial slots per row
+    HDR_WORDS = 64
+};
+
+// Byte offsets of the workspace regions (each 256-byte aligned).
+struct WsLayout {
+    size_t header, nsplit, tickets, flags, m_part, l_part, o_part, total;
+    int max_splits;
+};
+
+// Everything a kernel of this library needs about one call. Plain pointers and sizes.
+struct KernelArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* block_table;   // nullptr: contiguous cache
+    const int32_t* seq_lens;
+    void* out;
+    int32_t* hdr;
+    int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
+    int32_t* tickets;             // [B][Hkv], zero at rest
+    uint8_t* flags;               // [B][Hq][max_splits]
+    float* m_part;                // [B][Hq][max_splits]
+    float* l_part;                // [B][Hq][max_splits]
+    float* o_part;                // [B][Hq][max_splits][D]
+    int B, Hq, Hkv, G, D;
+    int max_seq_len, block_size, max_blocks, num_blocks;
+    int split_req, max_splits, num_sms;
+    float scale, phi, lo, hi;
+    int mode;
+    int kernel_id;
+    int nstage;                   // tensor kernel: TMA ring depth
+};
+
+// Tensor-core kernel shape limits (bf16, G <= 8 so that the hi and lo halves of P fit the
+// 16 rows of one m16n8k16 A tile).
+constexpr int TC_MAX_GROUP = 8;
+constexpr int SIMT_MAX_GROUP = 16;
+
+// Launchers (each returns the launch status). `grid` is the persistent CTA count.
+cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                            int grid, int smem_bytes, cudaStream_t s);
+cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
+
+// Resident CTAs per SM of the SIMT split kernel for this shape (0 if it cannot launch).
+int split_simt_ctas_per_sm(const KernelArgs& a, int dtype);
+
+// Tensor-core kernel geometry for one call: ring depth, CTAs per SM and dynamic shared memory.
+struct TcPlan {
+    int nstage;
+    int ctas_per_sm;
+    int smem_bytes;
+};
+// Chooses the geometry (requested values when > 0) from the per-SM and per-block shared
+// memory limits of the device. nstage == 0 in the result means no geometry fits.
+TcPlan split_tc_plan(int head_dim, int group, int req_stages, int req_ctas, int smem_per_sm,
+                     int smem_per_block);
+// Tokens per TMA tile of the tensor-core kernel (box height of the contiguous tensor maps).
+constexpr int TC_TILE_TOKENS = 64;
+
+}  // namespace fdpp

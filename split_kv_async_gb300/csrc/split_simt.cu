@@ -1,0 +1,281 @@
+// split_simt.cu -- per-split kernel on CUDA cores (fp32 or bf16 K/V, head_dim 64/128, G <= 16).
+//
+// One CTA (4 warps) handles one unit (sequence b, kv head g, split j) at a time and loops over
+// the units of a persistent grid. For every token of the split a warp reads the K and V rows of
+// head g (32 lanes x E contiguous elements, coalesced), forms the G dot products with a
+// warp-shuffle butterfly, and accumulates in fp32 registers:
+//   fast pass  (opt.ai.kr "FlashDecoding++ async softmax -- theory", s3, unified max):
+//              p = exp(s - phi), l += p, o += p v; no running max, nothing shared between splits;
+//   detection  every valid score is tested against lo <= s - phi <= hi (same page, s3: a score
+//              past the phi criterion sends the block back to online softmax);
+//   recompute  when a head of the unit was flagged, the whole split is read again with the
+//              ordinary online softmax (running max m, rescale by exp(m_old - m)) and the
+//              partials of the flagged heads are replaced.
+// The 4 warps' partials are merged through shared memory (a plain sum in the phi frame).
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+
+namespace fdpp {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    // E consecutive fp32 values (E = 2 or 4) -> registers.
+    template <int E>
+    __device__ static __forceinline__ void load(const float* p, float (&x)[E])
+    {
+        if constexpr (E == 4) {
+            float4 v = __ldg(reinterpret_cast<const float4*>(p));
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        } else {
+            float2 v = __ldg(reinterpret_cast<const float2*>(p));
+            x[0] = v.x; x[1] = v.y;
+        }
+    }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    template <int E>
+    __device__ static __forceinline__ void load(const __nv_bfloat16* p, float (&x)[E])
+    {
+        if constexpr (E == 4) {
+            uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+            float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.x));
+            float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v.y));
+            x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+        } else {
+            unsigned v = __ldg(reinterpret_cast<const unsigned*>(p));
+            float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+            x[0] = a.x; x[1] = a.y;
+        }
+    }
+};
+
+template <int E, int GM>
+struct SimtShared {
+    long long red[32];
+    float o[kWarps][GM][E * 32];
+    float l[kWarps][GM];
+    float m[kWarps][GM];
+    unsigned f[kWarps][GM];
+    unsigned unit_flags[GM];
+    int flagged_any;
+};
+
+// Element offset of the K/V row (b, t, g), or -1 when the block table entry is outside the pool.
+__device__ __forceinline__ long long kv_row(const KernelArgs& a, int b, int t, int g)
+{
+    const long long hd = (long long)a.Hkv * a.D;
+    if (!a.block_table) return ((long long)b * a.max_seq_len + t) * hd + (long long)g * a.D;
+    int blk = a.block_table[(long long)b * a.max_blocks + t / a.block_size];
+    if (blk < 0 || blk >= a.num_blocks) return -1;
+    return ((long long)blk * a.block_size + (t % a.block_size)) * hd + (long long)g * a.D;
+}
+
+// One pass of one warp over its tokens of split [t0, t1). ONLINE selects the running-max
+// softmax; otherwise the phi frame. Results stay in the warp's registers.
+template <typename T, int E, int GM, bool ONLINE>
+__device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int t0, int t1,
+                                          const float (&qr)[GM][E], float (&o)[GM][E],
+                                          float (&l)[GM], float (&m)[GM], unsigned (&fl)[GM],
+                                          bool& bad_block)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const T* K = static_cast<const T*>(a.k);
+    const T* V = static_cast<const T*>(a.v);
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+        l[h] = 0.f;
+        m[h] = ONLINE ? -INFINITY : a.phi;
+        fl[h] = 0u;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+    }
+    for (int t = t0 + warp; t < t1; t += kWarps) {
+        const long long row = kv_row(a, b, t, g);
+        if (row < 0) { bad_block = true; continue; }
+        float kx[E], vx[E];
+        Elem<T>::template load<E>(K + row + lane * E, kx);
+        Elem<T>::template load<E>(V + row + lane * E, vx);
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+            if (h >= a.G) break;
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) part = fmaf(qr[h][e], kx[e], part);
+            part = warp_sum(part);
+            const float s = __fmul_rn(part, a.scale);
+            const float x = __fsub_rn(s, a.phi);
+            fl[h] |= classify(x, a.lo, a.hi);
+            if (ONLINE) {
+                const float mn = fmaxf(m[h], s);
+                const float corr = (m[h] == -INFINITY) ? 0.f : __expf(m[h] - mn);
+                const float p = __expf(s - mn);
+                l[h] = fmaf(l[h], corr, p);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[h][e] = fmaf(o[h][e], corr, p * vx[e]);
+                m[h] = mn;
+            } else {
+                const float p = __expf(x);
+                l[h] += p;
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[h][e] = fmaf(p, vx[e], o[h][e]);
+            }
+        }
+    }
+}
+
+// Merges the warps' partials of unit (b, g, j) and writes them. Heads are written when
+// `write_mask` has their bit; flags are OR-ed with `extra_flag` for written heads.
+template <int E, int GM>
+__device__ __forceinline__ void merge_and_store(const KernelArgs& a, SimtShared<E, GM>& sh, int b,
+                                                int g, int j, const float (&o)[GM][E],
+                                                const float (&l)[GM], const float (&m)[GM],
+                                                const unsigned (&fl)[GM], unsigned write_mask,
+                                                unsigned extra_flag, bool store_flags)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int D = a.D;
+    __syncthreads();   // previous readers of sh are done
+#pragma unroll
+    for (int h = 0; h < GM; ++h) {
+        if (h >= a.G) break;
+#pragma unroll
+        for (int e = 0; e < E; ++e) sh.o[warp][h][lane * E + e] = o[h][e];
+        if (lane == 0) { sh.l[warp][h] = l[h]; sh.m[warp][h] = m[h]; sh.f[warp][h] = fl[h]; }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < a.G * D; idx += kThreads) {
+        const int h = idx / D, d = idx - h * D;
+        if (!((write_mask >> h) & 1u)) continue;
+        float M = sh.m[0][h];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, sh.m[w][h]);
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) acc = fmaf(frame_weight(sh.m[w][h], M), sh.o[w][h][d], acc);
+        const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
+        a.o_part[r * D + d] = acc;
+    }
+    if (threadIdx.x < a.G && ((write_mask >> threadIdx.x) & 1u)) {
+        const int h = threadIdx.x;
+        float M = sh.m[0][h];
+        unsigned f = sh.f[0][h];
+        for (int w = 1; w < kWarps; ++w) { M = fmaxf(M, sh.m[w][h]); f |= sh.f[w][h]; }
+        float lsum = 0.f;
+        for (int w = 0; w < kWarps; ++w) lsum = fmaf(frame_weight(sh.m[w][h], M), sh.l[w][h], lsum);
+        const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
+        a.l_part[r] = lsum;
+        a.m_part[r] = M;
+        if (store_flags) a.flags[r] = (uint8_t)(f | extra_flag);
+        else a.flags[r] = (uint8_t)(a.flags[r] | extra_flag);
+        sh.unit_flags[h] = f;
+    }
+    __syncthreads();
+}
+
+template <typename T, int E, int GM>
+__global__ void __launch_bounds__(kThreads) split_simt_kernel(KernelArgs a)
+{
+    __shared__ SimtShared<E, GM> sh;
+    int S, n_units;
+    block_plan(a, sh.red, S, n_units);
+
+    const int lane = threadIdx.x & 31;
+    const T* Q = static_cast<const T*>(a.q);
+    UnitCursor cur;
+    cur.reset();
+    bool bad_block = false;
+    const unsigned all_heads = (a.G >= 32) ? 0xffffffffu : ((1u << a.G) - 1u);
+
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+        int b, g, j, L;
+        cur.seek(a, S, u, b, g, j, L);
+        const int t0 = j * S, t1 = min(t0 + S, L);
+
+        float qr[GM][E];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+            if (h < a.G) {
+                Elem<T>::template load<E>(Q + ((long long)b * a.Hq + (long long)g * a.G + h) * a.D + lane * E, qr[h]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) qr[h][e] = 0.f;
+            }
+        }
+        float o[GM][E], l[GM], m[GM];
+        unsigned fl[GM];
+        if (a.mode == FDPP_MODE_FORCE_ONLINE) {
+            warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+            merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, FDPP_FLAG_RECOMPUTED, true);
+            continue;
+        }
+        warp_pass<T, E, GM, false>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+        merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, 0u, true);
+        if (a.mode != FDPP_MODE_NORMAL) continue;
+        unsigned redo = 0u;
+        for (int h = 0; h < a.G; ++h)
+            if (sh.unit_flags[h] & FDPP_FLAG_OUT) redo |= 1u << h;
+        if (!redo) continue;
+        // the split left the safe window: read it again with the ordinary online softmax
+        warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+        merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, redo, FDPP_FLAG_RECOMPUTED, false);
+    }
+    if (bad_block) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
+}
+
+template <typename T, int E, int GM>
+cudaError_t launch_t(const KernelArgs& a, int grid, cudaStream_t s)
+{
+    split_simt_kernel<T, E, GM><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_dtype(const KernelArgs& a, int grid, cudaStream_t s)
+{
+    const bool e4 = (a.D == 128);
+    if (a.G <= 4) return e4 ? launch_t<T, 4, 4>(a, grid, s) : launch_t<T, 2, 4>(a, grid, s);
+    return e4 ? launch_t<T, 4, 16>(a, grid, s) : launch_t<T, 2, 16>(a, grid, s);
+}
+
+template <typename T, int E, int GM>
+int occ_t()
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, split_simt_kernel<T, E, GM>, kThreads, 0) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <typename T>
+int occ_dtype(const KernelArgs& a)
+{
+    const bool e4 = (a.D == 128);
+    if (a.G <= 4) return e4 ? occ_t<T, 4, 4>() : occ_t<T, 2, 4>();
+    return e4 ? occ_t<T, 4, 16>() : occ_t<T, 2, 16>();
+}
+
+}  // namespace
+
+cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStream_t s)
+{
+    return dtype == FDPP_F32 ? launch_dtype<float>(a, grid, s)
+                             : launch_dtype<__nv_bfloat16>(a, grid, s);
+}
+
+int split_simt_ctas_per_sm(const KernelArgs& a, int dtype)
+{
+    return dtype == FDPP_F32 ? occ_dtype<float>(a) : occ_dtype<__nv_bfloat16>(a);
+}
+
+}  // namespace fdpp

@@ -1,0 +1,103 @@
+"""Test harness: runs libfdpp through its C ABI (Python binding) and the fp64 oracle on the same
+seeded inputs, and compares them with the parity tolerance.
+
+Tolerance (bf16 K/V with fp32 accumulation; the same bar for the fp32 workload):
+    max |gpu - oracle| <= 2e-3   and   max |gpu - oracle| / max(|oracle|, 1e-3) <= 1e-2.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import workloads as W
+
+ABS_TOL = 2e-3
+REL_TOL = 1e-2
+REL_FLOOR = 1e-3
+
+
+def errors(got, ref):
+    err = np.abs(got - ref)
+    rel = err / np.maximum(np.abs(ref), REL_FLOOR)
+    return float(err.max(initial=0.0)), float(rel.max(initial=0.0))
+
+
+def assert_parity(got, ref, what=""):
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    a, r = errors(got, ref)
+    assert a <= ABS_TOL and r <= REL_TOL, f"{what}: max abs {a:.3e}, max rel {r:.3e}"
+
+
+def oracle_problem(inp: W.Inputs):
+    wl = inp.wl
+    return oracle.make_problem(
+        batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+        head_dim=wl.head_dim, dtype=oracle.F32 if wl.dtype == W.F32 else oracle.BF16,
+        scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi, max_seq_len=inp.max_seq_len,
+        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq)
+
+
+def oracle_out(inp: W.Inputs, rows=None):
+    out, _ = oracle.attention(oracle_problem(inp), inp.q, inp.k, inp.v, inp.seq_lens,
+                              block_table=inp.block_table, rows=rows)
+    return out
+
+
+def oracle_flags(inp: W.Inputs, split_len: int, max_splits: int):
+    return oracle.window_flags(oracle_problem(inp), inp.q, inp.k, inp.seq_lens, split_len,
+                               max_splits, block_table=inp.block_table)
+
+
+class DeviceInputs:
+    """The workload's arrays as contiguous torch tensors on cuda:0."""
+
+    def __init__(self, inp: W.Inputs, device="cuda:0"):
+        import torch
+        self.inp = inp
+        self.dev = torch.device(device)
+        self.tdt = torch.float32 if inp.wl.dtype == W.F32 else torch.bfloat16
+        self.q = self._t(inp.q)
+        self.k = self._t(inp.k)
+        self.v = self._t(inp.v)
+        self.seq_lens = torch.from_numpy(inp.seq_lens).to(self.dev)
+        self.block_table = (None if inp.block_table is None
+                            else torch.from_numpy(inp.block_table).to(self.dev))
+
+    def _t(self, a):
+        import torch
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(self.dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(self.dev)
+
+
+def params_for(inp: W.Inputs, **kw):
+    import split_kv_async_gb300 as F
+    wl = inp.wl
+    base = dict(batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                head_dim=wl.head_dim, dtype=F.FDPP_F32 if wl.dtype == W.F32 else F.FDPP_BF16,
+                max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
+                split_len=wl.split_len)
+    if wl.paged:
+        base.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
+                    num_kv_blocks=inp.num_kv_blocks,
+                    max_seq_len=inp.max_blocks_per_seq * wl.block_size)
+    base.update(kw)
+    return F.make_params(**base)
+
+
+def run(dinp: DeviceInputs, ws=None, out=None, **kw):
+    """One fdpp_decode_attn call. Returns (out float64 [B*Hq][d], diag, flags, nsplit, ws)."""
+    import torch
+
+    import split_kv_async_gb300 as F
+    p = params_for(dinp.inp, **kw)
+    if ws is None:
+        ws = F.alloc_workspace(p, dinp.dev)
+    if out is None:
+        out = torch.empty_like(dinp.q)
+    F.fdpp_decode_attn(dinp.q, dinp.k, dinp.v, dinp.block_table, dinp.seq_lens, p, ws, out)
+    torch.cuda.synchronize()
+    diag, flags, ns = F.fdpp_read_diag(ws, p, want_flags=True, want_nsplit=True)
+    got = out.float().cpu().numpy().reshape(-1, dinp.inp.wl.head_dim).astype(np.float64)
+    return got, diag, flags, ns, ws

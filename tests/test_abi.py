@@ -1,0 +1,151 @@
+"""The C ABI without a GPU: the library loads, exports every function fdpp.h declares, and every
+argument error is reported synchronously with the documented status before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import split_kv_async_gb300 as F
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "fdpp.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fdpp_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert _declared_functions() == sorted(F.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", F.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(F.lib, name)
+
+
+def test_params_struct_matches_header_field_order():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct fdpp_params \{(.*?)\} fdpp_params;", text, re.S).group(1)
+    names = re.findall(r"\b(\w+)\s*[;,]", body)
+    assert names == [n for n, _ in F.fdpp_params._fields_]
+    body = re.search(r"typedef struct fdpp_diag \{(.*?)\} fdpp_diag;", text, re.S).group(1)
+    names = re.findall(r"\b(\w+)\s*;", body)
+    assert names == [n for n, _ in F.fdpp_diag._fields_]
+
+
+def _gqa_params(**kw):
+    base = dict(batch=8, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=F.FDPP_BF16,
+                max_seq_len=4096, scale=float(np.float32(128 ** -0.5)), split_len=512)
+    base.update(kw)
+    return F.make_params(**base)
+
+
+def test_max_splits_and_workspace_size():
+    p = _gqa_params()
+    assert F.fdpp_max_splits(p) == 8
+    ws = F.fdpp_workspace_size(p)
+    slots = 8 * 32 * 8
+    # partials o (d floats), l, m and a flag byte per slot, plus header/plan/tickets
+    assert slots * (128 * 4 + 4 + 4 + 1) <= ws <= slots * (128 * 4 + 4 + 4 + 1) + 64 * 1024
+    assert ws % 256 == 0
+    p0 = _gqa_params(split_len=0)
+    assert F.fdpp_max_splits(p0) == 4096 // F.FDPP_AUTO_MIN_SPLIT
+    p1 = _gqa_params(split_len=1000, max_seq_len=4097)
+    assert F.fdpp_max_splits(p1) == 5
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, F.FDPP_ERR_INVALID_ARG),
+    ("num_q_heads", 30, F.FDPP_ERR_INVALID_ARG),        # not a multiple of 8 kv heads
+    ("num_kv_heads", 0, F.FDPP_ERR_INVALID_ARG),
+    ("head_dim", 96, F.FDPP_ERR_UNSUPPORTED),
+    ("dtype", 7, F.FDPP_ERR_INVALID_ARG),
+    ("max_seq_len", 0, F.FDPP_ERR_INVALID_ARG),
+    ("split_len", -1, F.FDPP_ERR_INVALID_ARG),
+    ("scale", float("nan"), F.FDPP_ERR_INVALID_ARG),
+    ("phi", float("inf"), F.FDPP_ERR_INVALID_ARG),
+    ("lo", 20.0, F.FDPP_ERR_INVALID_ARG),               # lo > hi
+    ("mode", 3, F.FDPP_ERR_INVALID_ARG),
+    ("kernel", 9, F.FDPP_ERR_INVALID_ARG),
+    ("tc_stages", 1, F.FDPP_ERR_INVALID_ARG),
+    ("tc_ctas_per_sm", 5, F.FDPP_ERR_INVALID_ARG),
+])
+def test_bad_params_are_rejected_on_the_host(field, value, status):
+    p = _gqa_params()
+    setattr(p, field, value)
+    n = ctypes.c_size_t(0)
+    assert F.lib.fdpp_workspace_size(ctypes.byref(p), ctypes.byref(n)) == status
+    assert F.fdpp_last_error()
+    fake = 1 << 20                                          # never dereferenced
+    st = F.lib.fdpp_decode_attn(fake, fake, fake, None, fake, ctypes.byref(p), fake * 256,
+                                1 << 30, fake, None)
+    assert st == status
+
+
+def test_group_too_large_is_unsupported():
+    p = _gqa_params(num_q_heads=64 * 8, num_kv_heads=8)     # G = 64
+    n = ctypes.c_size_t(0)
+    assert F.lib.fdpp_workspace_size(ctypes.byref(p), ctypes.byref(n)) == F.FDPP_ERR_UNSUPPORTED
+
+
+def _call(p, q=1 << 20, k=1 << 20, v=1 << 20, bt=None, sl=1 << 20, ws=1 << 28, ws_bytes=None,
+          out=1 << 20):
+    if ws_bytes is None:
+        ws_bytes = F.fdpp_workspace_size(p)
+    return F.lib.fdpp_decode_attn(q, k, v, bt, sl, ctypes.byref(p), ws, ws_bytes, out, None)
+
+
+def test_pointer_and_workspace_errors():
+    p = _gqa_params()
+    assert _call(p, q=None) == F.FDPP_ERR_INVALID_ARG
+    assert _call(p, out=None) == F.FDPP_ERR_INVALID_ARG
+    assert _call(p, sl=None) == F.FDPP_ERR_INVALID_ARG
+    assert _call(p, k=(1 << 20) + 8) == F.FDPP_ERR_INVALID_ARG       # 16-byte alignment
+    assert _call(p, sl=(1 << 20) + 2) == F.FDPP_ERR_INVALID_ARG      # 4-byte alignment
+    assert _call(p, ws=None) == F.FDPP_ERR_WORKSPACE
+    assert _call(p, ws=(1 << 28) + 128) == F.FDPP_ERR_WORKSPACE      # 256-byte alignment
+    assert _call(p, ws_bytes=F.fdpp_workspace_size(p) - 1) == F.FDPP_ERR_WORKSPACE
+    assert "needed" in F.fdpp_last_error()
+
+
+def test_paged_contract_errors():
+    base = dict(block_size=16, max_blocks_per_seq=256, num_kv_blocks=1000)
+    bt = 1 << 20
+    assert _call(_gqa_params(**dict(base, block_size=24)), bt=bt) == F.FDPP_ERR_INVALID_ARG
+    assert _call(_gqa_params(**dict(base, block_size=512)), bt=bt) == F.FDPP_ERR_INVALID_ARG
+    assert _call(_gqa_params(**dict(base, max_blocks_per_seq=100)), bt=bt) == F.FDPP_ERR_INVALID_ARG
+    assert _call(_gqa_params(**dict(base, num_kv_blocks=0)), bt=bt) == F.FDPP_ERR_INVALID_ARG
+    assert _call(_gqa_params(split_len=520, **base), bt=bt) == F.FDPP_ERR_INVALID_ARG
+    # the same parameters without a block table are a contiguous cache: block fields ignored
+    p = _gqa_params(**dict(base, block_size=24))
+    st = _call(p)
+    assert st in (F.FDPP_OK, F.FDPP_ERR_CUDA, F.FDPP_ERR_UNSUPPORTED) and st != F.FDPP_ERR_INVALID_ARG
+
+
+def test_tensor_kernel_limits():
+    fp32 = _gqa_params(dtype=F.FDPP_F32, kernel=F.FDPP_KERNEL_TENSOR)
+    assert _call(fp32) == F.FDPP_ERR_UNSUPPORTED
+    big_group = _gqa_params(num_q_heads=128, num_kv_heads=8, kernel=F.FDPP_KERNEL_TENSOR)
+    assert _call(big_group) == F.FDPP_ERR_UNSUPPORTED
+
+
+def test_status_strings():
+    for s, name in [(0, "FDPP_OK"), (1, "FDPP_ERR_INVALID_ARG"), (2, "FDPP_ERR_UNSUPPORTED"),
+                    (3, "FDPP_ERR_WORKSPACE"), (4, "FDPP_ERR_CUDA")]:
+        assert F.fdpp_status_str(s) == name
+
+
+def test_no_gpu_gives_cuda_error_not_a_crash():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _call(_gqa_params()) == F.FDPP_ERR_CUDA
