@@ -373,8 +373,13 @@ def run_fdpp(args, dist: Dist):
     kernel_name = {1: "tensor", 2: "simt"}.get(diag["kernel"], "?")
 
     K = args.steps
+    # torch creates an event's CUDA handle on its first record; record each once here so that
+    # the raw handles handed to fdpp_decode_attn_timed exist (the library records them again)
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for ev in ev_b + ev_e:
+        ev.record(stream)
+    torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0,

@@ -1,10 +1,10 @@
 // api.cpp -- the C ABI of libfdpp: argument checks, workspace layout, kernel choice, TMA
 // descriptors and launches. Every entry point here is declared and documented in fdpp.h.
 //
-// A decode step is two stream-ordered launches:
-//   1. the split kernel (tensor-core or SIMT variant), persistent over the (b, g, j) units; each
-//      CTA plans the splits itself from seq_lens, so no plan launch and no host sync is needed;
-//   2. the combine kernel, one CTA per (b, h) row.
+// A decode step is one launch on the tensor-core path (plan, phi-frame partials, window test,
+// fallback recompute and combine all inside the persistent kernel) and two on the SIMT path
+// (split kernel, then the combine kernel, one CTA per (b, h) row). Kernels plan the splits
+// themselves from seq_lens on the device, so no plan launch and no host sync is needed.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -111,6 +111,7 @@ WsLayout layout_of(const fdpp_params& p)
     w.header = off;  off = align256(off + HDR_WORDS * 4);
     w.nsplit = off;  off = align256(off + (size_t)p.batch * 4);
     w.tickets = off; off = align256(off + (size_t)p.batch * p.num_kv_heads * 4);
+    w.redo = off;    off = align256(off + (size_t)p.batch * p.num_kv_heads * w.max_splits * 8);
     w.flags = off;   off = align256(off + slots);
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
@@ -292,6 +293,7 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
     a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
     a.tickets = reinterpret_cast<int32_t*>(ws + w.tickets);
+    a.redo = reinterpret_cast<long long*>(ws + w.redo);
     a.flags = ws + w.flags;
     a.m_part = reinterpret_cast<float*>(ws + w.m_part);
     a.l_part = reinterpret_cast<float*>(ws + w.l_part);
@@ -321,8 +323,8 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     if (kernel == FDPP_KERNEL_TENSOR) {
-        const TcPlan plan = split_tc_plan(p->head_dim, G, p->tc_stages, p->tc_ctas_per_sm,
-                                          dev.smem_per_sm, dev.smem_per_block);
+        const TcPlan plan = split_tc_plan(p->head_dim, G, p->batch, p->tc_stages,
+                                          p->tc_ctas_per_sm, dev.smem_per_sm, dev.smem_per_block);
         if (plan.nstage == 0)
             return fail(FDPP_ERR_UNSUPPORTED, "no tensor-kernel geometry fits (stages %d, CTAs/SM %d)",
                         p->tc_stages, p->tc_ctas_per_sm);
@@ -330,9 +332,12 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         CUtensorMap tk, tv;
         if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
         if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;
-        long long grid = (long long)dev.sms * plan.ctas_per_sm;
-        if (grid > units_max) grid = units_max;
-        e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, s);
+        // persistent grid: at most SMs x resident CTAs, sized so every CTA owns the same number
+        // of units (the unit count is bounded by B * Hkv * max_splits; seq_lens stay on device)
+        const long long slots = (long long)dev.sms * plan.ctas_per_sm;
+        const long long per_cta = (units_max + slots - 1) / slots;
+        const long long grid = (units_max + per_cta - 1) / per_cta;
+        e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, plan.ctas_per_sm, s);
     } else {
         const int occ = split_simt_ctas_per_sm(a, p->dtype);
         long long grid = (long long)dev.sms * (occ > 0 ? occ : 1);
@@ -342,8 +347,10 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
     if (ev_split_end && (e = cudaEventRecord((cudaEvent_t)ev_split_end, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
-    e = launch_combine(a, p->dtype, s);
-    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
+    if (kernel == FDPP_KERNEL_SIMT) {   // the tensor-core kernel combines in place
+        e = launch_combine(a, p->dtype, s);
+        if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
+    }
     return FDPP_OK;
 }
 

@@ -19,12 +19,15 @@ enum {
     HDR_ERR = 3,        // sticky FDPP_ERRBIT_* (atomicOr)
     HDR_BATCH = 4,      // B of the last call
     HDR_MAXSPLITS = 5,  // partial slots per row
+    HDR_REDO_COUNT = 8, // fallback list: units pushed (zero at rest)
+    HDR_REDO_TAKEN = 9, // fallback list: units claimed (zero at rest)
+    HDR_DONE = 10,      // CTAs finished (zero at rest)
     HDR_WORDS = 64
 };
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-    size_t header, nsplit, tickets, flags, m_part, l_part, o_part, total;
+    size_t header, nsplit, tickets, redo, flags, m_part, l_part, o_part, total;
     int max_splits;
 };
 
@@ -39,6 +42,7 @@ struct KernelArgs {
     int32_t* hdr;
     int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
     int32_t* tickets;             // [B][Hkv], zero at rest
+    long long* redo;              // fallback list [B*Hkv*max_splits] of (b+1, g*max_splits+j)
     uint8_t* flags;               // [B][Hq][max_splits]
     float* m_part;                // [B][Hq][max_splits]
     float* l_part;                // [B][Hq][max_splits]
@@ -57,10 +61,12 @@ struct KernelArgs {
 constexpr int TC_MAX_GROUP = 8;
 constexpr int SIMT_MAX_GROUP = 16;
 
-// Launchers (each returns the launch status). `grid` is the persistent CTA count.
+// Launchers (each returns the launch status). `grid` is the persistent CTA count. The
+// tensor-core kernel also combines the splits (no combine launch follows it); the SIMT kernel is
+// followed by launch_combine.
 cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                            int grid, int smem_bytes, cudaStream_t s);
+                            int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s);
 cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
 
 // Resident CTAs per SM of the SIMT split kernel for this shape (0 if it cannot launch).
@@ -74,8 +80,8 @@ struct TcPlan {
 };
 // Chooses the geometry (requested values when > 0) from the per-SM and per-block shared
 // memory limits of the device. nstage == 0 in the result means no geometry fits.
-TcPlan split_tc_plan(int head_dim, int group, int req_stages, int req_ctas, int smem_per_sm,
-                     int smem_per_block);
+TcPlan split_tc_plan(int head_dim, int group, int batch, int req_stages, int req_ctas,
+                     int smem_per_sm, int smem_per_block);
 // Tokens per TMA tile of the tensor-core kernel (box height of the contiguous tensor maps).
 constexpr int TC_TILE_TOKENS = 64;
 

@@ -1,26 +1,35 @@
-// split_tc.cu -- per-split kernel for bf16 K/V: TMA-fed ring, tensor-core q.K^T and P.V.
+// split_tc.cu -- decode attention for bf16 K/V: TMA-fed ring, tensor-core q.K^T and P.V, fused
+// fallback and fused combine. One launch does the whole step.
 //
-// What it computes (opt.ai.kr "FlashDecoding++ async softmax -- theory", s1 and s3): for one
-// unit (sequence b, kv head g, split j) and the G query heads that share kv head g,
-//     s_t = scale <q_h, k_t>, p_t = exp(s_t - phi), l = sum p_t, o = sum p_t v_t   (fast pass)
+// What it computes (opt.ai.kr "FlashDecoding++ async softmax -- theory", s1 and s3). For one unit
+// (sequence b, kv head g, split j) and the G query heads that share kv head g:
+//     s_t = scale <q_h, k_t>, p_t = exp(s_t - phi), l = sum p_t, o = sum p_t v_t    (fast pass)
 // against the unified max phi, with no communication between splits; every score is tested
-// against lo <= s - phi <= hi; a unit with a head outside the window is streamed again at the
-// end of the CTA's work and recomputed with the ordinary online softmax (running max).
+// against lo <= s - phi <= hi. A unit with a head outside the window goes on a device-wide list
+// and is streamed again with the ordinary online softmax (running max) by whichever CTA is free
+// first. When the last unit of (b, g) is final, the CTA that finished it combines the n_b
+// partials of the G heads: out = sum_j w_j o_j / sum_j w_j l_j, w_j = exp(m_j - max m), which is
+// the plain sum of the page (w_j = 1 exactly) when no split of the row fell back.
 //
-// How. One CTA = 4 consumer warps + 1 producer warp, persistent over units. The producer streams
-// 64-token K and V tiles of head g with 3-D TMA loads (128-byte swizzle) into a ring of
-// `nstage` shared-memory stages guarded by mbarriers (full: TMA bytes landed; empty: 4 consumer
-// warps released the stage); for a paged cache it issues one box per 16..64-token block, using
-// the block table. Each consumer warp owns 16 tokens of a tile:
-//   S[16 x 16] = Q[16 x d] K^T        mma.m16n8k16 (bf16 in, fp32 accumulate); rows 0..G-1 are
-//                                     the G query heads (zero padded), so each K byte read from
-//                                     HBM feeds all G heads;
-//   P = exp(S - phi), detect window
-//   O[16 x d] += [P_hi ; P_lo] V      P is split into bf16 hi + lo parts stacked in the 16 rows
-//                                     of the A tile (G <= 8), so P.V keeps ~16 mantissa bits;
-//                                     row h + row h+8 is head h's output.
-// Warps merge their fp32 partials through shared memory (a plain sum in the phi frame) and
-// write o, l, m = phi and the flag byte of each head of the unit.
+// How. One CTA = 1 producer warp + 4 consumer warps, persistent over an equal share of units.
+//   producer  plans the splits in shared memory (prefix of n_b = ceil(L_b / S)), then for each
+//             unit writes a small header into a Q-ring slot and bulk-copies the unit's G query
+//             rows there (this slot is also how consumers learn which unit comes next), and
+//             streams 64-token K and V tiles of head g with 3-D TMA loads (128-byte swizzle)
+//             into a ring of `nstage` stages (mbarriers: full = bytes landed, empty = the four
+//             consumer warps released the stage). A paged cache is read one block per box,
+//             block-table entries fetched 32 at a time by the warp. After its own units it
+//             claims fallback units from the list until it is empty, then sends a sentinel.
+//   consumers each own 16 tokens of a tile:
+//             S[16 x 16] = Q K^T     mma.m16n8k16 bf16 -> fp32; rows 0..G-1 = the G heads, so
+//                                    each K byte read from HBM feeds all G heads once;
+//             P = exp(S - phi), window test;
+//             O += [P_hi ; P_lo] V   P split into bf16 hi + lo parts stacked in the 16 rows of
+//                                    the A tile (G <= 8): P.V keeps ~16 mantissa bits; head h's
+//                                    output is row h + row h+8.
+//             The four warps merge their fp32 partials through shared memory (a plain sum in
+//             the phi frame) and write o, l, m and the flag byte of each head.
+// Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT and the CTA stops.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -32,35 +41,45 @@ constexpr int NCW = 4;                  // consumer warps
 constexpr int TPW = 16;                 // tokens per consumer warp and tile
 constexpr int TILE = NCW * TPW;         // tokens per tile
 constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int NCT = NCW * 32;           // consumer threads
+constexpr int PLAN_SMEM_MAX_B = 1024;   // batches up to this size keep their plan in smem
+constexpr int QHDR_BYTES = 64;          // unit header at the start of each Q-ring slot
 static_assert(TILE == TC_TILE_TOKENS, "tile height is part of the tensor-map contract");
+
+// unit kinds carried in the Q-ring header
+enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
+// header words
+enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_NB, H_F0, H_F1, H_MASK, H_WORDS };
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base).
 struct TcLayout {
-    int stage_bytes, kv_bytes, q_bytes, scr_row;
-    int stages, qbuf, scr_o, scr_l, scr_m, scr_f, bars, misc, red, total;
+    int stage_bytes, kv_bytes, qslot_bytes, scr_row;
+    int stages, qring, scr_o, scr_l, scr_m, scr_f, plan, bars, misc, total;
 
     __host__ __device__ static constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-    __host__ __device__ TcLayout(int D, int G, int nstage)
-        : stage_bytes(2 * TILE * D * 2), kv_bytes(TILE * D * 2), q_bytes(round_up(G * D * 2, 128)),
-          scr_row(D + 8), stages(0), qbuf(0), scr_o(0), scr_l(0), scr_m(0), scr_f(0), bars(0),
-          misc(0), red(0), total(0)
+    __host__ __device__ TcLayout(int D, int G, int nstage, int B)
+        : stage_bytes(2 * TILE * D * 2), kv_bytes(TILE * D * 2),
+          qslot_bytes(round_up(QHDR_BYTES + G * D * 2, 128)), scr_row(D + 8), stages(0), qring(0),
+          scr_o(0), scr_l(0), scr_m(0), scr_f(0), plan(0), bars(0), misc(0), total(0)
     {
-        qbuf = stages + nstage * stage_bytes;
-        scr_o = qbuf + 2 * q_bytes;
+        qring = stages + nstage * stage_bytes;
+        scr_o = qring + 2 * qslot_bytes;
         scr_l = scr_o + NCW * G * scr_row * 4;
         scr_m = scr_l + NCW * G * 4;
         scr_f = scr_m + NCW * G * 4;
-        bars = round_up(scr_f + NCW * G * 4, 8);
-        misc = bars + (2 * nstage + 5) * 8;
-        red = round_up(misc + 16, 8);
-        total = red + 32 * 8;
+        plan = scr_f + NCW * G * 4;
+        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? B : 0) + 1;
+        bars = round_up(plan + plan_ints * 4, 8);
+        misc = bars + (2 * nstage + 6) * 8;
+        total = misc + 16;
     }
 };
 
 struct Ring {
     uint32_t full, empty, qfull, qempty;   // shared addresses of the barrier arrays
     uint32_t cbar;                         // consumer-warps barrier (128 arrivals per phase)
+    uint32_t own_done;                     // consumers finished the CTA's own units
     int nstage;
 };
 
@@ -68,13 +87,11 @@ struct Ring {
 __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatile int* misc,
                                           const KernelArgs& a)
 {
-    bool ok = (misc[1] == 0) && mbar_wait(bar, parity);
+    bool ok = (misc[0] == 0) && mbar_wait(bar, parity);
     ok = __all_sync(0xffffffffu, ok);
-    if (!ok) {
-        if ((threadIdx.x & 31) == 0) {
-            misc[1] = 1;
-            set_error(a, FDPP_ERRBIT_TIMEOUT);
-        }
+    if (!ok && (threadIdx.x & 31) == 0) {
+        misc[0] = 1;
+        set_error(a, FDPP_ERRBIT_TIMEOUT);
     }
     return ok;
 }
@@ -89,69 +106,138 @@ __device__ __forceinline__ bool consumer_sync(const Ring& rg, uint32_t& parity, 
     return ok;
 }
 
-// Heads of unit (b, g, j) whose fast pass left the window (bit h for head g*G + h).
-__device__ __forceinline__ unsigned unit_redo_mask(const KernelArgs& a, int b, int g, int j)
+__device__ __forceinline__ long long row_slot(const KernelArgs& a, int b, int h, int j)
 {
-    unsigned mask = 0u;
-    for (int h = 0; h < a.G; ++h) {
-        const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
-        if (a.flags[r] & FDPP_FLAG_OUT) mask |= 1u << h;
-    }
-    return mask;
+    return ((long long)b * a.Hq + h) * a.max_splits + j;
 }
 
 // ------------------------------------------------------------------------------------------
 // producer warp
 // ------------------------------------------------------------------------------------------
-template <int D, bool PAGED>
-__device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                        const KernelArgs& a, const TcLayout& lay, uint32_t sbase,
-                                        const Ring& rg, volatile int* misc, int S, int n_units,
-                                        bool recompute, uint32_t& p_stage, uint32_t& p_phase,
-                                        uint32_t& pq_iter)
-{
-    constexpr int HALVES = D / 64;
-    const int lane = threadIdx.x & 31;
-    const int bs = PAGED ? a.block_size : TILE;
-    const int rows_box = bs < TILE ? bs : TILE;
-    const uint32_t box_bytes = 128u * (uint32_t)rows_box;
-    UnitCursor cur;
-    cur.reset();
+struct Producer {
+    const CUtensorMap* tmK;
+    const CUtensorMap* tmV;
+    const KernelArgs* a;
+    const TcLayout* lay;
+    Ring rg;
+    uint32_t sbase;
+    uint8_t* smp;              // generic pointer to the same shared-memory base
+    volatile int* misc;
+    int* plan;                 // smem prefix of n_b (B <= PLAN_SMEM_MAX_B), else unused
+    int S;
+    uint32_t stage = 0, phase = 0, qiter = 0;
     bool bad_block = false;
 
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-        int b, g, j, L;
-        cur.seek(a, S, u, b, g, j, L);
-        if (recompute && unit_redo_mask(a, b, g, j) == 0u) continue;
-        const int t0 = j * S, t1 = min(t0 + S, L);
-        const int ntiles = ceil_div_i(t1 - t0, TILE);
-
-        // query rows of the unit's G heads: one bulk copy into the Q ring
-        {
-            const uint32_t qs = pq_iter & 1u, quse = pq_iter >> 1;
-            if (!ring_wait(rg.qempty + 8 * qs, (quse & 1u) ^ 1u, misc, a)) return;
-            if (lane == 0) {
-                const uint32_t bytes = (uint32_t)(a.G * D * 2);
-                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.q) +
-                                           ((long long)b * a.Hq + (long long)g * a.G) * D;
-                mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes);
-                bulk_load(sbase + lay.qbuf + qs * lay.q_bytes, src, bytes, rg.qfull + 8 * qs);
-            }
-            ++pq_iter;
+    // Split plan: S, n_b prefix in smem (or a global walk for large batches), unit count.
+    __device__ __forceinline__ int make_plan()
+    {
+        const KernelArgs& A = *a;
+        const int lane = threadIdx.x & 31;
+        const bool in_smem = A.B <= PLAN_SMEM_MAX_B;
+        long long sum = 0;
+        bool bad = false;
+        for (int b = lane; b < A.B; b += 32) {
+            const int L = A.seq_lens[b];
+            bad |= (L < 0 || L > A.max_seq_len);
+            const int Lc = clamp_len(L, A.max_seq_len);
+            sum += Lc;
+            if (in_smem) plan[b] = Lc;
         }
+        sum = warp_sum(sum);
+        bad = __any_sync(0xffffffffu, bad);
+        S = auto_split_len(sum, A);
+        int run = 0;
+        for (int base = 0; base < A.B; base += 32) {
+            const int b = base + lane;
+            int nb = 0;
+            if (b < A.B) {
+                const int Lc = in_smem ? plan[b] : clamp_len(A.seq_lens[b], A.max_seq_len);
+                nb = min(ceil_div_i(Lc, S), A.max_splits);
+            }
+            int incl = nb;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            __syncwarp();
+            if (b < A.B) {
+                if (in_smem) plan[b] = run + incl - nb;
+                if (blockIdx.x == 0) A.nsplit[b] = nb;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (in_smem && lane == 0) plan[A.B] = run;
+        __syncwarp();
+        const int n_units = run * A.Hkv;
+        if (blockIdx.x == 0) {
+            if (lane == 0) {
+                A.hdr[HDR_SPLIT] = S;
+                A.hdr[HDR_UNITS] = n_units;
+                A.hdr[HDR_KERNEL] = A.kernel_id;
+                A.hdr[HDR_BATCH] = A.B;
+                A.hdr[HDR_MAXSPLITS] = A.max_splits;
+                if (bad) set_error(A, FDPP_ERRBIT_SEQ_LEN);
+            }
+            // rows of empty sequences are zero (no unit will write them)
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(A.out);
+            for (int b = 0; b < A.B; ++b) {
+                const int nb = in_smem ? plan[b + 1] - plan[b]
+                                       : clamp_len(A.seq_lens[b], A.max_seq_len);
+                if (nb != 0) continue;
+                for (int i = lane; i < A.Hq * A.D; i += 32)
+                    out[(long long)b * A.Hq * A.D + i] = __float2bfloat16_rn(0.f);
+            }
+        }
+        return n_units;
+    }
 
-        int win_base = -(1 << 30), ent = -1;           // paged: 32 block-table entries per window
+    // Emits one unit: header + Q rows into the Q ring, then its K/V tiles into the stage ring.
+    template <int D, bool PAGED>
+    __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int nb, int L,
+                                         const int (&hw)[3])
+    {
+        constexpr int HALVES = D / 64;
+        const KernelArgs& A = *a;
+        const int lane = threadIdx.x & 31;
+        const int t0 = j * S, t1 = min(t0 + S, L);
+        const uint32_t qs = qiter & 1u;
+        if (!ring_wait(rg.qempty + 8 * qs, ((qiter >> 1) & 1u) ^ 1u, misc, A)) return false;
+        const uint32_t slot = sbase + lay->qring + qs * lay->qslot_bytes;
+        if (lane == 0) {
+            int* hdr = reinterpret_cast<int*>(smp + lay->qring + qs * lay->qslot_bytes);
+            hdr[H_KIND] = kind; hdr[H_B] = b; hdr[H_G] = g; hdr[H_J] = j;
+            hdr[H_T0] = t0; hdr[H_T1] = t1; hdr[H_NB] = nb;
+            hdr[H_F0] = hw[0]; hdr[H_F1] = hw[1]; hdr[H_MASK] = hw[2];
+            if (kind == KIND_END) {
+                mbar_arrive(rg.qfull + 8 * qs);
+            } else {
+                const uint32_t bytes = (uint32_t)(A.G * D * 2);
+                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(A.q) +
+                                           ((long long)b * A.Hq + (long long)g * A.G) * D;
+                mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes);
+                bulk_load(slot + QHDR_BYTES, src, bytes, rg.qfull + 8 * qs);
+            }
+        }
+        ++qiter;
+        if (kind == KIND_END) return true;
+
+        const int bs = PAGED ? A.block_size : TILE;
+        const int rows_box = bs < TILE ? bs : TILE;
+        const uint32_t box_bytes = 128u * (uint32_t)rows_box;
+        const int ntiles = ceil_div_i(t1 - t0, TILE);
+        int win_base = -(1 << 30), ent = -1;       // paged: 32 block-table entries per window
         const int nblk_seq = PAGED ? ceil_div_i(L, bs) : 0;
         for (int i = 0; i < ntiles; ++i) {
             const int tt = t0 + i * TILE;
             const int nvalid = min(TILE, t1 - tt);
-            if (!ring_wait(rg.empty + 8 * p_stage, p_phase ^ 1u, misc, a)) return;
-            const uint32_t kdst = sbase + lay.stages + p_stage * lay.stage_bytes;
-            const uint32_t vdst = kdst + lay.kv_bytes;
-            const uint32_t fb = rg.full + 8 * p_stage;
+            if (!ring_wait(rg.empty + 8 * stage, phase ^ 1u, misc, A)) return false;
+            const uint32_t kdst = sbase + lay->stages + stage * lay->stage_bytes;
+            const uint32_t vdst = kdst + lay->kv_bytes;
+            const uint32_t fb = rg.full + 8 * stage;
             if (!PAGED) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, (uint32_t)lay.stage_bytes);
+                    mbar_arrive_expect_tx(fb, (uint32_t)lay->stage_bytes);
 #pragma unroll
                     for (int hv = 0; hv < HALVES; ++hv) {
                         tma_load_3d(kdst + hv * TILE * 128, tmK, g * D + hv * 64, tt, b, fb);
@@ -159,23 +245,21 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
                     }
                 }
             } else {
-                // logical blocks touched by the valid tokens of this tile
                 const int lb0 = tt / bs;
-                const int nb = (bs <= TILE) ? ceil_div_i(nvalid, bs) : 1;
-                if (lb0 < win_base || lb0 + nb > win_base + 32) {
+                const int nbk = (bs <= TILE) ? ceil_div_i(nvalid, bs) : 1;
+                if (lb0 < win_base || lb0 + nbk > win_base + 32) {
                     win_base = lb0;
                     const int lb = lb0 + lane;
-                    ent = (lb < nblk_seq) ? __ldg(a.block_table + (long long)b * a.max_blocks + lb)
-                                          : -1;
+                    ent = (lb < nblk_seq) ? __ldg(A.block_table + (long long)b * A.max_blocks + lb) : -1;
                 }
                 int blk[TILE / 16];
                 uint32_t bytes = 0;
 #pragma unroll
                 for (int k = 0; k < TILE / 16; ++k) {
                     blk[k] = -1;
-                    if (k < nb) {
+                    if (k < nbk) {
                         const int e = __shfl_sync(0xffffffffu, ent, lb0 + k - win_base);
-                        if (e >= 0 && e < a.num_blocks) {
+                        if (e >= 0 && e < A.num_blocks) {
                             blk[k] = e;
                             bytes += 2u * HALVES * box_bytes;
                         } else {
@@ -198,20 +282,167 @@ __device__ __forceinline__ void produce(const CUtensorMap* tmK, const CUtensorMa
                     }
                 }
             }
-            if (++p_stage == (uint32_t)rg.nstage) { p_stage = 0; p_phase ^= 1u; }
+            if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
         }
+        return true;
     }
-    if (bad_block && lane == 0) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
-}
+
+    template <int D, bool PAGED>
+    __device__ __forceinline__ void run()
+    {
+        const KernelArgs& A = *a;
+        const int lane = threadIdx.x & 31;
+        const int n_units = make_plan();
+        const bool in_smem = A.B <= PLAN_SMEM_MAX_B;
+        const int zero3[3] = {0, 0, 0};
+
+        // own units: u = blockIdx.x + k * gridDim.x
+        UnitCursor cur;
+        cur.reset();
+        int b = 0;
+        bool had_own = false;
+        for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+            int g, j, nb, L;
+            if (in_smem) {
+                while ((long long)A.Hkv * plan[b + 1] <= u) ++b;
+                nb = plan[b + 1] - plan[b];
+                const long long r = u - (long long)A.Hkv * plan[b];
+                g = (int)(r / nb);
+                j = (int)(r % nb);
+                L = clamp_len(A.seq_lens[b], A.max_seq_len);
+            } else {
+                cur.seek(A, S, u, b, g, j, L);
+                nb = cur.nb;
+            }
+            const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
+            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3)) return;
+            had_own = true;
+        }
+
+        if (A.mode == FDPP_MODE_NORMAL) {
+            // the consumers push this CTA's flagged units before they report the own units done
+            if (had_own && !ring_wait(rg.own_done, 0u, misc, A)) return;
+            int* cnt = &A.hdr[HDR_REDO_COUNT];
+            int* taken = &A.hdr[HDR_REDO_TAKEN];
+            for (;;) {
+                int k = 0;
+                bool got = false, stop = false;
+                if (lane == 0) {
+                    for (;;) {
+                        const int t = atomicAdd(taken, 0);
+                        const int c = atomicAdd(cnt, 0);
+                        if (t >= c) { stop = true; break; }
+                        if (atomicCAS(taken, t, t + 1) == t) { k = t; got = true; break; }
+                    }
+                }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                if (stop) break;
+                got = __shfl_sync(0xffffffffu, got, 0);
+                k = __shfl_sync(0xffffffffu, k, 0);
+                if (!got) continue;
+                // the pusher reserved slot k before storing it: read it with a bounded wait
+                long long e = 0;
+                if (lane == 0) {
+                    volatile long long* slotp = reinterpret_cast<volatile long long*>(A.redo + k);
+                    const uint64_t t0 = global_ns();
+                    while ((e = *slotp) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
+                    }
+                    if (e != 0) *slotp = 0;            // leave the list zeroed for the next call
+                    __threadfence();
+                }
+                e = __shfl_sync(0xffffffffu, e, 0);
+                if (e == 0) {
+                    if (lane == 0) { misc[0] = 1; set_error(A, FDPP_ERRBIT_TIMEOUT); }
+                    return;
+                }
+                const int rb = (int)(e & 0xffffffffll) - 1;
+                const int gj = (int)(e >> 32);
+                const int rg_ = gj / A.max_splits, rj = gj % A.max_splits;
+                const int L = clamp_len(A.seq_lens[rb], A.max_seq_len);
+                const int nb = min(ceil_div_i(L, S), A.max_splits);
+                // flag bytes of the G heads (written by the pushing CTA before its push)
+                int hw[3] = {0, 0, 0};
+                if (lane < A.G) {
+                    const unsigned f = __ldcg(A.flags + row_slot(A, rb, rg_ * A.G + lane, rj));
+                    hw[0] = 0; hw[1] = 0;
+                    const unsigned sh = (unsigned)(lane & 3) * 8u;
+                    const unsigned w0 = lane < 4 ? (f << sh) : 0u;
+                    const unsigned w1 = lane >= 4 ? (f << sh) : 0u;
+                    const unsigned m = (f & FDPP_FLAG_OUT) ? (1u << lane) : 0u;
+                    hw[0] = (int)w0; hw[1] = (int)w1; hw[2] = (int)m;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    hw[0] |= __shfl_xor_sync(0xffffffffu, hw[0], o);
+                    hw[1] |= __shfl_xor_sync(0xffffffffu, hw[1], o);
+                    hw[2] |= __shfl_xor_sync(0xffffffffu, hw[2], o);
+                }
+                if (!emit<D, PAGED>(KIND_REDO, rb, rg_, rj, nb, L, hw)) return;
+            }
+        }
+        const int zeros[3] = {0, 0, 0};
+        emit<D, PAGED>(KIND_END, 0, 0, 0, 0, 0, zeros);
+    }
+};
 
 // ------------------------------------------------------------------------------------------
 // consumer warps
 // ------------------------------------------------------------------------------------------
 template <int D>
+__device__ __forceinline__ void combine_group(const KernelArgs& a, int b, int g, int nb, int ctid)
+{
+    constexpr int C4 = D / 4;
+    constexpr int U = 8;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    for (int it = ctid; it < a.G * C4; it += NCT) {
+        const int hh = it / C4, c4 = it - hh * C4;
+        const int h = g * a.G + hh;
+        const long long base = row_slot(a, b, h, 0);
+        float M = -INFINITY;
+        for (int j0 = 0; j0 < nb; j0 += U) {
+            float mv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) mv[u] = (j0 + u < nb) ? __ldcg(a.m_part + base + j0 + u) : -INFINITY;
+#pragma unroll
+            for (int u = 0; u < U; ++u) M = fmaxf(M, mv[u]);
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lam = 0.f;
+        for (int j0 = 0; j0 < nb; j0 += U) {
+            float mv[U], lv[U];
+            float4 ov[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (j0 + u < nb) {
+                    mv[u] = __ldcg(a.m_part + base + j0 + u);
+                    lv[u] = __ldcg(a.l_part + base + j0 + u);
+                    ov[u] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (base + j0 + u) * D) + c4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (j0 + u < nb) {
+                    const float w = frame_weight(mv[u], M);
+                    acc.x = fmaf(w, ov[u].x, acc.x);
+                    acc.y = fmaf(w, ov[u].y, acc.y);
+                    acc.z = fmaf(w, ov[u].z, acc.z);
+                    acc.w = fmaf(w, ov[u].w, acc.w);
+                    lam = fmaf(w, lv[u], lam);
+                }
+            }
+        }
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(__fdiv_rn(acc.x, lam), __fdiv_rn(acc.y, lam));
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(__fdiv_rn(acc.z, lam), __fdiv_rn(acc.w, lam));
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo2);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(out + ((long long)b * a.Hq + h) * D + 4 * c4) = pk;
+    }
+}
+
+template <int D>
 __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay, uint8_t* sm,
-                                        uint32_t sbase, const Ring& rg, volatile int* misc, int S,
-                                        int n_units, bool recompute, uint32_t& c_stage,
-                                        uint32_t& c_phase, uint32_t& cq_iter, uint32_t& cparity)
+                                        uint32_t sbase, const Ring& rg, volatile int* misc)
 {
     constexpr int KS = D / 16;           // k-steps of q.K^T, and column pairs of P.V
     constexpr int NT = D / 8;            // n-tiles of the output
@@ -219,7 +450,6 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const int h = lane >> 2, qd = lane & 3;       // head row and column pair of this lane
     const int mi = lane >> 3, r8 = lane & 7;      // ldmatrix: matrix and row of this lane
     const bool head_ok = h < a.G;
-    const bool online = recompute || (a.mode == FDPP_MODE_FORCE_ONLINE);
     const uint32_t k_row = warp * TPW + (mi >> 1) * 8 + r8;
     const uint32_t v_row = warp * TPW + (mi & 1) * 8 + r8;
     const int tok_lo = warp * TPW + 2 * qd;       // this lane's first token in n-tile 0
@@ -227,23 +457,27 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     float* scr_l = reinterpret_cast<float*>(sm + lay.scr_l);
     float* scr_m = reinterpret_cast<float*>(sm + lay.scr_m);
     unsigned* scr_f = reinterpret_cast<unsigned*>(sm + lay.scr_f);
-    UnitCursor cur;
-    cur.reset();
+    volatile int* s_last = misc + 1;
+    uint32_t stage = 0, phase = 0, qiter = 0, cpar = 0;
 
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-        int b, g, j, L;
-        cur.seek(a, S, u, b, g, j, L);
-        const unsigned redo = recompute ? unit_redo_mask(a, b, g, j) : 0u;
-        if (recompute && redo == 0u) continue;
-        const int t0 = j * S, t1 = min(t0 + S, L);
-        const int ntiles = ceil_div_i(t1 - t0, TILE);
+    for (;;) {
+        // ---- next unit from the producer ----
+        const uint32_t qs = qiter & 1u;
+        if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) return;
+        const uint8_t* slot = sm + lay.qring + qs * lay.qslot_bytes;
+        const int* hdr = reinterpret_cast<const int*>(slot);
+        const int kind = hdr[H_KIND];
+        if (kind == KIND_END) return;
+        const int b = hdr[H_B], g = hdr[H_G], j = hdr[H_J];
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], nb = hdr[H_NB];
+        const unsigned fw0 = (unsigned)hdr[H_F0], fw1 = (unsigned)hdr[H_F1];
+        const unsigned redo_mask = (unsigned)hdr[H_MASK];
+        const bool redo = kind == KIND_REDO;
+        const bool online = redo || (a.mode == FDPP_MODE_FORCE_ONLINE);
 
-        // Q fragments (A operand rows 0..7 = heads; rows 8..15 zero)
         uint32_t qa[KS][2];
         {
-            const uint32_t qs = cq_iter & 1u;
-            if (!ring_wait(rg.qfull + 8 * qs, (cq_iter >> 1) & 1u, misc, a)) return;
-            const uint8_t* qb = sm + lay.qbuf + qs * lay.q_bytes;
+            const uint8_t* qb = slot + QHDR_BYTES;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 qa[ks][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qb + (h * D + ks * 16 + 2 * qd) * 2) : 0u;
@@ -251,7 +485,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(rg.qempty + 8 * qs);
-            ++cq_iter;
+            ++qiter;
         }
 
         float o[NT][4];
@@ -260,11 +494,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         float lsum = 0.f;
         float mrun = online ? -INFINITY : a.phi;
         unsigned fl = 0u;
+        const int ntiles = ceil_div_i(t1 - t0, TILE);
 
         for (int i = 0; i < ntiles; ++i) {
             const int nvalid = min(TILE, t1 - (t0 + i * TILE));
-            if (!ring_wait(rg.full + 8 * c_stage, c_phase, misc, a)) return;
-            const uint32_t kb = sbase + lay.stages + c_stage * lay.stage_bytes;
+            if (!ring_wait(rg.full + 8 * stage, phase, misc, a)) return;
+            const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
             const uint32_t vb = kb + lay.kv_bytes;
 
             // S = Q K^T for this warp's 16 tokens (two n-tiles of 8 tokens), two chains each
@@ -283,7 +518,6 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 mma_16816(sa[ks & 1][1], qa[ks][0], 0u, qa[ks][1], 0u, k2, k3);
             }
 
-            // scores of head h at tokens tok_lo + 8*nt + e
             float s[2][2];
             bool valid[2][2];
 #pragma unroll
@@ -337,7 +571,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 pa[2 * nt + 1] = pack_bf16x2(p[nt][0] - hf.x, p[nt][1] - hf.y);
             }
 
-            // masks for V rows past the valid tokens (their shared-memory rows may hold NaN)
+            // V rows past the valid tokens may hold anything (NaN included): mask them to zero
             uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
             if (nvalid < TILE) {
                 vm_lo = (tok_lo < nvalid ? 0x0000ffffu : 0u) | (tok_lo + 1 < nvalid ? 0xffff0000u : 0u);
@@ -354,8 +588,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 mma_16816(o[2 * c2 + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(rg.empty + 8 * c_stage);
-            if (++c_stage == (uint32_t)rg.nstage) { c_stage = 0; c_phase ^= 1u; }
+            if (lane == 0) mbar_arrive(rg.empty + 8 * stage);
+            if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
         }
 
         // ---- merge the 4 warps' partials of this unit and write them ----
@@ -363,7 +597,6 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
         fl |= __shfl_xor_sync(0xffffffffu, fl, 1);
         fl |= __shfl_xor_sync(0xffffffffu, fl, 2);
-        if (!consumer_sync(rg, cparity, misc, a)) return;   // scratch of the previous unit is free
         if (head_ok) {
             float* row = scr_o + (warp * a.G + h) * lay.scr_row;
 #pragma unroll
@@ -375,9 +608,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 scr_f[warp * a.G + h] = fl;
             }
         }
-        if (!consumer_sync(rg, cparity, misc, a)) return;
-        const unsigned write_mask = recompute ? redo : 0xffffffffu;
-        for (int idx = ctid; idx < a.G * D; idx += NCW * 32) {
+        if (!consumer_sync(rg, cpar, misc, a)) return;
+        const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
+        for (int idx = ctid; idx < a.G * D; idx += NCT) {
             const int hh = idx / D, d = idx - hh * D;
             if (!((write_mask >> hh) & 1u)) continue;
             float M = scr_m[hh];
@@ -387,25 +620,51 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
             for (int w = 0; w < NCW; ++w)
                 acc = fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_o[(w * a.G + hh) * lay.scr_row + d], acc);
-            const long long r = ((long long)b * a.Hq + (long long)g * a.G + hh) * a.max_splits + j;
-            a.o_part[r * D + d] = acc;
+            a.o_part[row_slot(a, b, g * a.G + hh, j) * D + d] = acc;
         }
-        if (ctid < a.G && ((write_mask >> ctid) & 1u)) {
-            const int hh = ctid;
-            float M = scr_m[hh];
+        unsigned unit_out = 0u;                   // heads of this unit outside the window
+        for (int hh = 0; hh < a.G; ++hh) {
             unsigned f = scr_f[hh];
-            for (int w = 1; w < NCW; ++w) { M = fmaxf(M, scr_m[w * a.G + hh]); f |= scr_f[w * a.G + hh]; }
-            float lam = 0.f;
-            for (int w = 0; w < NCW; ++w) lam = fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_l[w * a.G + hh], lam);
-            const long long r = ((long long)b * a.Hq + (long long)g * a.G + hh) * a.max_splits + j;
-            a.l_part[r] = lam;
-            a.m_part[r] = M;
-            if (recompute) {
-                a.flags[r] = (uint8_t)(a.flags[r] | FDPP_FLAG_RECOMPUTED);
-            } else {
-                a.flags[r] = (uint8_t)(f | (online ? FDPP_FLAG_RECOMPUTED : 0u));
-                if ((f & FDPP_FLAG_OUT) && a.mode == FDPP_MODE_NORMAL) misc[0] = 1;
+            for (int w = 1; w < NCW; ++w) f |= scr_f[w * a.G + hh];
+            if (f & FDPP_FLAG_OUT) unit_out |= 1u << hh;
+            if (ctid == hh && ((write_mask >> hh) & 1u)) {
+                float M = scr_m[hh];
+                for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
+                float lam = 0.f;
+                for (int w = 0; w < NCW; ++w) lam = fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_l[w * a.G + hh], lam);
+                const long long r = row_slot(a, b, g * a.G + hh, j);
+                a.l_part[r] = lam;
+                a.m_part[r] = M;
+                if (redo) {
+                    const unsigned f0 = ((hh < 4 ? fw0 : fw1) >> ((hh & 3) * 8)) & 0xffu;
+                    a.flags[r] = (uint8_t)(f0 | FDPP_FLAG_RECOMPUTED);
+                } else {
+                    a.flags[r] = (uint8_t)(f | (online ? FDPP_FLAG_RECOMPUTED : 0u));
+                }
             }
+        }
+        __threadfence();
+        if (!consumer_sync(rg, cpar, misc, a)) return;
+        // ---- fallback push, or arrival on the (b, g) ticket ----
+        if (ctid == 0) {
+            int last = 0;
+            if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
+                const int k = atomicAdd(&a.hdr[HDR_REDO_COUNT], 1);
+                const long long e = ((long long)(g * a.max_splits + j) << 32) | (long long)(unsigned)(b + 1);
+                *reinterpret_cast<volatile long long*>(a.redo + k) = e;
+                __threadfence();
+            } else {
+                const int t = atomicAdd(&a.tickets[b * a.Hkv + g], 1);
+                last = (t == nb - 1);
+            }
+            *s_last = last;
+            if (kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
+        }
+        if (!consumer_sync(rg, cpar, misc, a)) return;
+        if (*s_last) {
+            __threadfence();
+            combine_group<D>(a, b, g, nb, ctid);
+            if (ctid == 0) a.tickets[b * a.Hkv + g] = 0;   // zero at rest for the next call
         }
     }
 }
@@ -413,17 +672,20 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 // ------------------------------------------------------------------------------------------
 // kernel
 // ------------------------------------------------------------------------------------------
-template <int D, bool PAGED>
-__global__ void __launch_bounds__(NTHREADS, 2)
+// MINB = CTAs per SM the build is register-limited for: 2 caps a thread at 168 registers (two
+// 5-warp CTAs, warps allocated in pairs), 1 leaves the compiler free (~240) and pairs with a
+// deeper TMA ring.
+template <int D, bool PAGED, int MINB>
+__global__ void __launch_bounds__(NTHREADS, MINB)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const KernelArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    const TcLayout lay(D, a.G, a.nstage);
+    const TcLayout lay(D, a.G, a.nstage, a.B);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    volatile int* misc = reinterpret_cast<volatile int*>(sm + lay.misc);   // [0] refetch needed, [1] abort
+    volatile int* misc = reinterpret_cast<volatile int*>(sm + lay.misc);   // [0] abort, [1] last
     Ring rg;
     rg.nstage = a.nstage;
     rg.full = sbase + lay.bars;
@@ -431,6 +693,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     rg.qfull = rg.empty + 8 * a.nstage;
     rg.qempty = rg.qfull + 16;
     rg.cbar = rg.qempty + 16;
+    rg.own_done = rg.cbar + 8;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.nstage; ++s) {
@@ -441,56 +704,58 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             mbar_init(rg.qfull + 8 * s, 1);
             mbar_init(rg.qempty + 8 * s, NCW);
         }
-        mbar_init(rg.cbar, NCW * 32);
+        mbar_init(rg.cbar, NCT);
+        mbar_init(rg.own_done, 1);
         misc[0] = 0;
         misc[1] = 0;
         fence_mbar_init();
     }
-    if (warp == NCW && lane == 0) {
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
-    }
-    int S, n_units;
-    block_plan(a, reinterpret_cast<long long*>(sm + lay.red), S, n_units);   // syncs the block
+    __syncthreads();
 
-    uint32_t stage = 0, phase = 0, qiter = 0, cparity = 0;
-    if (warp == NCW)
-        produce<D, PAGED>(&tmK, &tmV, a, lay, sbase, rg, misc, S, n_units, false, stage, phase, qiter);
-    else
-        consume<D>(a, lay, sm, sbase, rg, misc, S, n_units, false, stage, phase, qiter, cparity);
-    __syncthreads();
-    // splits that left the safe window: stream them again and recompute with online softmax
-    if (a.mode == FDPP_MODE_NORMAL && misc[0] != 0 && misc[1] == 0) {
-        if (warp == NCW)
-            produce<D, PAGED>(&tmK, &tmV, a, lay, sbase, rg, misc, S, n_units, true, stage, phase, qiter);
-        else
-            consume<D>(a, lay, sm, sbase, rg, misc, S, n_units, true, stage, phase, qiter, cparity);
+    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, reinterpret_cast<int*>(sm + lay.plan), 0};
+    if (warp == NCW) {
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+        }
+        pr.run<D, PAGED>();
+        if (pr.bad_block && lane == 0) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
+    } else {
+        consume<D>(a, lay, sm, sbase, rg, misc);
     }
     __syncthreads();
-    if (misc[1] != 0 && warp == NCW && lane == 0) {
-        // Aborted: let every copy this CTA issued land before the CTA exits (bounded waits).
-        // The latest issue into stage s had phase `phase` when s < stage, else phase ^ 1 (a
-        // stage never issued waits on the completed phase before its first and passes at once).
-        for (int s = 0; s < a.nstage; ++s) {
-            const uint32_t par = (uint32_t)s < stage ? phase : (phase ^ 1u);
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(rg.full + 8 * s, par) && global_ns() - t0 < 100000000ull) {
+    if (warp == NCW && lane == 0) {
+        if (misc[0] != 0) {
+            // Aborted: let every copy this CTA issued land before it exits (bounded waits). The
+            // latest issue into stage s had phase `phase` when s < stage, else phase ^ 1.
+            for (int s = 0; s < a.nstage; ++s) {
+                const uint32_t par = (uint32_t)s < pr.stage ? pr.phase : (pr.phase ^ 1u);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(rg.full + 8 * s, par) && global_ns() - t0 < 100000000ull) {
+                }
+            }
+            for (uint32_t k = 0; k < 2 && k < pr.qiter; ++k) {
+                const uint32_t it = pr.qiter - 1 - k, qs = it & 1u, par = (it >> 1) & 1u;
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(rg.qfull + 8 * qs, par) && global_ns() - t0 < 100000000ull) {
+                }
             }
         }
-        for (uint32_t k = 0; k < 2 && k < qiter; ++k) {
-            const uint32_t it = qiter - 1 - k, qs = it & 1u, par = (it >> 1) & 1u;
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(rg.qfull + 8 * qs, par) && global_ns() - t0 < 100000000ull) {
-            }
+        // the last CTA to finish leaves the fallback counters at zero for the next call
+        __threadfence();
+        if (atomicAdd(&a.hdr[HDR_DONE], 1) == (int)gridDim.x - 1) {
+            a.hdr[HDR_REDO_COUNT] = 0;
+            a.hdr[HDR_REDO_TAKEN] = 0;
+            a.hdr[HDR_DONE] = 0;
         }
     }
 }
 
 template <int D, bool PAGED>
 cudaError_t launch_t(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
-                     int smem, cudaStream_t s)
+                     int smem, int ctas_per_sm, cudaStream_t s)
 {
-    auto kern = split_tc_kernel<D, PAGED>;
+    auto kern = ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2> : split_tc_kernel<D, PAGED, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, NTHREADS, smem, s>>>(tk, tv, a);
@@ -499,13 +764,13 @@ cudaError_t launch_t(const KernelArgs& a, const CUtensorMap& tk, const CUtensorM
 
 }  // namespace
 
-TcPlan split_tc_plan(int head_dim, int group, int req_stages, int req_ctas, int smem_per_sm,
-                     int smem_per_block)
+TcPlan split_tc_plan(int head_dim, int group, int batch, int req_stages, int req_ctas,
+                     int smem_per_sm, int smem_per_block)
 {
     TcPlan p{0, 0, 0};
     const int reserve = 1024;                         // per-CTA system reservation
-    auto bytes = [&](int ns) { return TcLayout(head_dim, group, ns).total + 1024; };
-    const int cands[4] = {2, 1, 3, 4};
+    auto bytes = [&](int ns) { return TcLayout(head_dim, group, ns, batch).total + 1024; };
+    const int cands[4] = {1, 2, 3, 4};
     for (int ci = 0; ci < 4; ++ci) {
         const int ctas = req_ctas > 0 ? req_ctas : cands[ci];
         const int budget = smem_per_sm / ctas - reserve;
@@ -524,14 +789,14 @@ TcPlan split_tc_plan(int head_dim, int group, int req_stages, int req_ctas, int 
 }
 
 cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                            int grid, int smem_bytes, cudaStream_t s)
+                            int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s)
 {
     const bool paged = a.block_table != nullptr;
     if (a.D == 128)
-        return paged ? launch_t<128, true>(a, tk, tv, grid, smem_bytes, s)
-                     : launch_t<128, false>(a, tk, tv, grid, smem_bytes, s);
-    return paged ? launch_t<64, true>(a, tk, tv, grid, smem_bytes, s)
-                 : launch_t<64, false>(a, tk, tv, grid, smem_bytes, s);
+        return paged ? launch_t<128, true>(a, tk, tv, grid, smem_bytes, ctas_per_sm, s)
+                     : launch_t<128, false>(a, tk, tv, grid, smem_bytes, ctas_per_sm, s);
+    return paged ? launch_t<64, true>(a, tk, tv, grid, smem_bytes, ctas_per_sm, s)
+                 : launch_t<64, false>(a, tk, tv, grid, smem_bytes, ctas_per_sm, s);
 }
 
 }  // namespace fdpp

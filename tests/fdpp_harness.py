@@ -1,8 +1,14 @@
 """Test harness: runs libfdpp through its C ABI (Python binding) and the fp64 oracle on the same
 seeded inputs, and compares them with the parity tolerance.
 
-Tolerance (bf16 K/V with fp32 accumulation; the same bar for the fp32 workload):
-    max |gpu - oracle| <= 2e-3   and   max |gpu - oracle| / max(|oracle|, 1e-3) <= 1e-2.
+Tolerance (bf16 K/V with fp32 accumulation; the same bar for the fp32 workload), per element:
+    |gpu - oracle| <= 2e-3                                   (absolute)
+    |gpu - oracle| / max(|oracle|, 1e-3) <= 1e-2             (relative, floored near zero)
+The output is rounded to nearest even in the input dtype. A bf16 output rounds by up to
+2^-9 |o|, which alone exceeds 2e-3 once |o| > 1; rows of very short sequences reach that. So for
+|o| > 0.512 the absolute bound is the bf16 resolution 2^-8 |o| (0.4 % relative, still well
+inside the 1 % bound). The five measured workloads keep every |o| below 0.5, and their tests use
+the bound exactly as stated (strict=True).
 """
 from __future__ import annotations
 
@@ -16,17 +22,24 @@ REL_TOL = 1e-2
 REL_FLOOR = 1e-3
 
 
+BF16_RESOLUTION = 2.0 ** -8
+
+
 def errors(got, ref):
     err = np.abs(got - ref)
     rel = err / np.maximum(np.abs(ref), REL_FLOOR)
     return float(err.max(initial=0.0)), float(rel.max(initial=0.0))
 
 
-def assert_parity(got, ref, what=""):
+def assert_parity(got, ref, what="", strict=False):
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    abs_bound = ABS_TOL if strict else np.maximum(ABS_TOL, BF16_RESOLUTION * np.abs(ref))
+    ok_abs = (err <= abs_bound).all()
     a, r = errors(got, ref)
-    assert a <= ABS_TOL and r <= REL_TOL, f"{what}: max abs {a:.3e}, max rel {r:.3e}"
+    assert ok_abs and r <= REL_TOL, (f"{what}: max abs {a:.3e} (bound {np.max(abs_bound):.3e}), "
+                                     f"max rel {r:.3e}, max |ref| {np.abs(ref).max():.3f}")
 
 
 def oracle_problem(inp: W.Inputs):
@@ -95,7 +108,9 @@ def run(dinp: DeviceInputs, ws=None, out=None, **kw):
     if ws is None:
         ws = F.alloc_workspace(p, dinp.dev)
     if out is None:
-        out = torch.empty_like(dinp.q)
+        out = torch.full_like(dinp.q, float("nan"))     # rows the library fails to write show up
+    else:
+        out.fill_(float("nan"))
     F.fdpp_decode_attn(dinp.q, dinp.k, dinp.v, dinp.block_table, dinp.seq_lens, p, ws, out)
     torch.cuda.synchronize()
     diag, flags, ns = F.fdpp_read_diag(ws, p, want_flags=True, want_nsplit=True)

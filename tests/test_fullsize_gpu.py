@@ -43,7 +43,14 @@ def test_full_size(wl):
     rows = _sample_rows(inp, N_SAMPLE_ROWS, wl.seed)
     ref = H.oracle_out(inp, rows=rows)
     g = got.reshape(wl.batch, wl.num_q_heads, wl.head_dim)[rows[:, 0], rows[:, 1]]
-    H.assert_parity(g, ref, wl.name)
+    # the stated bound, verbatim, on every row whose output stays below 0.5 in magnitude (all
+    # rows of the N(0,1) workloads); rows dominated by an injected hot key carry a single V row
+    # (|o| up to ~4), where the bf16 output's own rounding can exceed 2e-3
+    small = np.abs(ref).max(axis=1) < 0.5
+    if wl.stress_frac == 0:
+        assert small.all()
+    H.assert_parity(g[small], ref[small], wl.name, strict=True)
+    H.assert_parity(g[~small], ref[~small], wl.name + " hot rows")
     if wl.stress_frac == 0:
         assert diag["n_flagged_row_splits"] == 0
     else:
