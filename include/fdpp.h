@@ -106,7 +106,7 @@ typedef struct fdpp_params {
     int mode;                /* fdpp_mode */
     int kernel;              /* fdpp_kernel */
     int tc_stages;           /* tensor kernel: depth of the TMA ring (2..12), 0 = automatic */
-    int tc_ctas_per_sm;      /* tensor kernel: resident CTAs per SM (1..4), 0 = automatic */
+    int tc_ctas_per_sm;      /* tensor kernel: resident CTAs per SM (1 or 2), 0 = automatic */
 } fdpp_params;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over

@@ -1,10 +1,12 @@
 // api.cpp -- the C ABI of libfdpp: argument checks, workspace layout, kernel choice, TMA
 // descriptors and launches. Every entry point here is declared and documented in fdpp.h.
 //
-// A decode step is one launch on the tensor-core path (plan, phi-frame partials, window test,
-// fallback recompute and combine all inside the persistent kernel) and two on the SIMT path
-// (split kernel, then the combine kernel, one CTA per (b, h) row). Kernels plan the splits
-// themselves from seq_lens on the device, so no plan launch and no host sync is needed.
+// A decode step is two stream-ordered launches:
+//   1. the split kernel (tensor-core or SIMT variant), persistent over the (b, g, j) units: split
+//      plan, phi-frame partials, window test and fallback recompute. Kernels plan the splits
+//      themselves from seq_lens on the device, so no plan launch and no host sync is needed;
+//   2. the combine kernel, one CTA per (b, h) row, launched as a programmatic dependent so its
+//      launch overlaps the split kernel's tail.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -72,8 +74,8 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "unknown kernel %d", p->kernel);
     if (p->tc_stages < 0 || p->tc_stages == 1 || p->tc_stages > 12)
         return fail(FDPP_ERR_INVALID_ARG, "tc_stages must be 0 or in [2, 12]");
-    if (p->tc_ctas_per_sm < 0 || p->tc_ctas_per_sm > 4)
-        return fail(FDPP_ERR_INVALID_ARG, "tc_ctas_per_sm must be 0 or in [1, 4]");
+    if (p->tc_ctas_per_sm < 0 || p->tc_ctas_per_sm > 2)
+        return fail(FDPP_ERR_INVALID_ARG, "tc_ctas_per_sm must be 0, 1 or 2");
     const int G = p->num_q_heads / p->num_kv_heads;
     if (G > SIMT_MAX_GROUP)
         return fail(FDPP_ERR_UNSUPPORTED, "query heads per kv head %d > %d", G, SIMT_MAX_GROUP);
@@ -178,7 +180,7 @@ fdpp_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000& fn)
 //   paged:      dims {Hkv*d, block_size, nblk}, box {64, min(block_size, 64), 1}
 fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params& p, bool paged)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     fdpp_status st = tensor_map_encoder(enc);
     if (st != FDPP_OK) return st;
     const cuuint64_t row = (cuuint64_t)p.num_kv_heads * p.head_dim;
@@ -332,11 +334,9 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         CUtensorMap tk, tv;
         if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
         if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;
-        // persistent grid: at most SMs x resident CTAs, sized so every CTA owns the same number
-        // of units (the unit count is bounded by B * Hkv * max_splits; seq_lens stay on device)
-        const long long slots = (long long)dev.sms * plan.ctas_per_sm;
-        const long long per_cta = (units_max + slots - 1) / slots;
-        const long long grid = (units_max + per_cta - 1) / per_cta;
+        // persistent grid: every SM busy (SMs x resident CTAs), no more CTAs than units can exist
+        long long grid = (long long)dev.sms * plan.ctas_per_sm;
+        if (grid > units_max) grid = units_max;
         e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, plan.ctas_per_sm, s);
     } else {
         const int occ = split_simt_ctas_per_sm(a, p->dtype);
@@ -347,10 +347,8 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
     if (ev_split_end && (e = cudaEventRecord((cudaEvent_t)ev_split_end, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
-    if (kernel == FDPP_KERNEL_SIMT) {   // the tensor-core kernel combines in place
-        e = launch_combine(a, p->dtype, s);
-        if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
-    }
+    e = launch_combine(a, p->dtype, s);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
     return FDPP_OK;
 }
 

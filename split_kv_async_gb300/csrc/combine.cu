@@ -1,18 +1,28 @@
-// combine.cu -- cross-split combine: one CTA per softmax row (sequence b, query head h).
+// combine.cu -- cross-split combine: one CTA (8 warps) per softmax row (sequence b, query head h).
 //
 // opt.ai.kr "FlashDecoding++ async softmax -- theory", s3: with a unified max every split's
 // partial (o_j, l_j) is already in the same frame, so only a plain sum remains. A split that
 // was recomputed with online softmax carries its own max m_j, so the general form is
 //     M = max_j m_j,  out = sum_j w_j o_j / sum_j w_j l_j,  w_j = exp(m_j - M)
 // with w_j = 1 exactly when m_j == M: if no split of the row fell back (all m_j = phi) this is
-// exactly the plain sum. Splits are summed in ascending j (deterministic), in fp32; the result
-// is rounded to nearest even into the output dtype.
+// exactly the plain sum.
+//
+// The n_b splits of a row are divided into 8 contiguous ranges, one per warp (each lane owns 4
+// or 2 output columns), so a long row's partials are read with 8x the memory-level parallelism;
+// the 8 warp sums are then added in warp order. The order is fixed, so results are
+// deterministic. The result is rounded to nearest even into the output dtype.
+//
+// Launched as a programmatic dependent of the split kernel: it may start while the split kernel
+// finishes, and waits (griddepcontrol.wait) before touching the partials.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
 
 namespace fdpp {
 namespace {
+
+constexpr int CW = 8;                 // warps per CTA
+constexpr int CT = CW * 32;
 
 template <typename T>
 __device__ __forceinline__ void store_out(T* p, float x);
@@ -26,41 +36,114 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
     *p = __float2bfloat16_rn(x);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(128) combine_kernel(KernelArgs a)
+template <typename T, int D>
+__global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
 {
-    const int row = blockIdx.x;             // b * Hq + h
+    constexpr int E = D / 32;                       // output columns per lane
+    __shared__ float s_acc[CW][D];
+    __shared__ float s_lam[CW];
+    __shared__ float s_max[CW];
+    grid_dependency_wait();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x;                     // b * Hq + h
     const int b = row / a.Hq;
     const int n = a.nsplit[b];
     const long long base = (long long)row * a.max_splits;
     const float* m = a.m_part + base;
     const float* l = a.l_part + base;
-    const float* o = a.o_part + base * a.D;
-    T* out = static_cast<T*>(a.out) + (long long)row * a.D;
+    const float* o = a.o_part + base * D;
+    T* out = static_cast<T*>(a.out) + (long long)row * D;
 
+    // M = max_j m_j over the whole row
     float M = -INFINITY;
-    for (int j = 0; j < n; ++j) M = fmaxf(M, m[j]);
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
-        float acc = 0.f, lam = 0.f;
-        for (int j = 0; j < n; ++j) {
-            const float w = frame_weight(m[j], M);
-            acc = fmaf(w, o[(long long)j * a.D + d], acc);
-            lam = fmaf(w, l[j], lam);
+    for (int j = threadIdx.x; j < n; j += CT) M = fmaxf(M, m[j]);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+    if (lane == 0) s_max[warp] = M;
+    __syncthreads();
+    M = s_max[0];
+#pragma unroll
+    for (int w = 1; w < CW; ++w) M = fmaxf(M, s_max[w]);
+
+    // this warp's contiguous range of splits, ascending
+    const int chunk = (n + CW - 1) / CW;
+    const int j0 = warp * chunk, j1 = min(n, j0 + chunk);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float lam = 0.f;
+    constexpr int U = 4;
+    for (int jb = j0; jb < j1; jb += U) {
+        float mv[U], lv[U], ov[U][E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + u;
+            if (j < j1) {
+                mv[u] = m[j];
+                lv[u] = l[j];
+                const float* oj = o + (long long)j * D + lane * E;
+                if constexpr (E == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(oj);
+                    ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(oj);
+                    ov[u][0] = v.x; ov[u][1] = v.y;
+                }
+            }
         }
-        store_out<T>(out + d, n > 0 ? __fdiv_rn(acc, lam) : 0.f);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (jb + u < j1) {
+                const float w = frame_weight(mv[u], M);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = fmaf(w, ov[u][e], acc[e]);
+                lam = fmaf(w, lv[u], lam);
+            }
+        }
     }
+#pragma unroll
+    for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+    if (lane == 0) s_lam[warp] = lam;
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int d = threadIdx.x;
+        float total = 0.f, ltot = 0.f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) {
+            total += s_acc[w][d];
+            ltot += s_lam[w];
+        }
+        store_out<T>(out + d, n > 0 ? __fdiv_rn(total, ltot) : 0.f);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+    cfg.blockDim = dim3(CT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s)
 {
-    const int rows = a.B * a.Hq;
-    const int threads = a.D;
+    cudaError_t e;
     if (dtype == FDPP_F32)
-        combine_kernel<float><<<rows, threads, 0, s>>>(a);
+        e = a.D == 128 ? launch_t<float, 128>(a, s) : launch_t<float, 64>(a, s);
     else
-        combine_kernel<__nv_bfloat16><<<rows, threads, 0, s>>>(a);
+        e = a.D == 128 ? launch_t<__nv_bfloat16, 128>(a, s) : launch_t<__nv_bfloat16, 64>(a, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -61,9 +61,8 @@ struct KernelArgs {
 constexpr int TC_MAX_GROUP = 8;
 constexpr int SIMT_MAX_GROUP = 16;
 
-// Launchers (each returns the launch status). `grid` is the persistent CTA count. The
-// tensor-core kernel also combines the splits (no combine launch follows it); the SIMT kernel is
-// followed by launch_combine.
+// Launchers (each returns the launch status). `grid` is the persistent CTA count. Either split
+// kernel is followed by launch_combine (a programmatic dependent launch).
 cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s);

@@ -1,5 +1,5 @@
-// split_tc.cu -- decode attention for bf16 K/V: TMA-fed ring, tensor-core q.K^T and P.V, fused
-// fallback and fused combine. One launch does the whole step.
+// split_tc.cu -- per-split kernel for bf16 K/V: TMA-fed ring, tensor-core q.K^T and P.V, and the
+// fallback recompute, in one persistent launch; combine.cu then sums the split partials.
 //
 // What it computes (opt.ai.kr "FlashDecoding++ async softmax -- theory", s1 and s3). For one unit
 // (sequence b, kv head g, split j) and the G query heads that share kv head g:
@@ -7,9 +7,7 @@
 // against the unified max phi, with no communication between splits; every score is tested
 // against lo <= s - phi <= hi. A unit with a head outside the window goes on a device-wide list
 // and is streamed again with the ordinary online softmax (running max) by whichever CTA is free
-// first. When the last unit of (b, g) is final, the CTA that finished it combines the n_b
-// partials of the G heads: out = sum_j w_j o_j / sum_j w_j l_j, w_j = exp(m_j - max m), which is
-// the plain sum of the page (w_j = 1 exactly) when no split of the row fell back.
+// first; its flagged heads' partials are replaced by ones in their own max frame.
 //
 // How. One CTA = 1 producer warp + 4 consumer warps, persistent over an equal share of units.
 //   producer  plans the splits in shared memory (prefix of n_b = ceil(L_b / S)), then for each
@@ -29,7 +27,12 @@
 //                                    output is row h + row h+8.
 //             The four warps merge their fp32 partials through shared memory (a plain sum in
 //             the phi frame) and write o, l, m and the flag byte of each head.
+// When a CTA starts its last own unit it allows the dependent combine launch to begin
+// (programmatic dependent launch), so that launch overlaps the tail of this one.
 // Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT and the CTA stops.
+// (A fused last-arriver combine was measured here and removed: under full HBM load its
+// latency-bound reads of the partials stalled the consumer warps for several microseconds per
+// combine, more than the TMA ring can hide.)
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -45,13 +48,18 @@ constexpr int NCT = NCW * 32;           // consumer threads
 constexpr int PLAN_SMEM_MAX_B = 1024;   // batches up to this size keep their plan in smem
 constexpr int QHDR_BYTES = 64;          // unit header at the start of each Q-ring slot
 static_assert(TILE == TC_TILE_TOKENS, "tile height is part of the tensor-map contract");
+// the merge scratch (4 warps x G <= 8 rows x (d + 8) floats, plus l, m, flags) fits in a stage
+static_assert(NCW * 8 * (64 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 64 * 2, "scratch (d=64)");
+static_assert(NCW * 8 * (128 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 128 * 2, "scratch (d=128)");
 
 // unit kinds carried in the Q-ring header
 enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
 // header words
 enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_NB, H_F0, H_F1, H_MASK, H_WORDS };
 
-// Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base).
+// Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge
+// scratch of a unit lives in the stage of the unit's last tile (offsets scr_* relative to that
+// stage), which is released to the producer only after the merge.
 struct TcLayout {
     int stage_bytes, kv_bytes, qslot_bytes, scr_row;
     int stages, qring, scr_o, scr_l, scr_m, scr_f, plan, bars, misc, total;
@@ -64,11 +72,11 @@ struct TcLayout {
           scr_o(0), scr_l(0), scr_m(0), scr_f(0), plan(0), bars(0), misc(0), total(0)
     {
         qring = stages + nstage * stage_bytes;
-        scr_o = qring + 2 * qslot_bytes;
+        scr_o = 0;
         scr_l = scr_o + NCW * G * scr_row * 4;
         scr_m = scr_l + NCW * G * 4;
         scr_f = scr_m + NCW * G * 4;
-        plan = scr_f + NCW * G * 4;
+        plan = qring + 2 * qslot_bytes;
         const int plan_ints = (B <= PLAN_SMEM_MAX_B ? B : 0) + 1;
         bars = round_up(plan + plan_ints * 4, 8);
         misc = bars + (2 * nstage + 6) * 8;
@@ -96,11 +104,13 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
-// Barrier of the 4 consumer warps with a bounded wait (a bar.sync could not give up).
+// Barrier of the 4 consumer warps with a bounded wait (a bar.sync could not give up). One
+// arrival per warp after __syncwarp; the arrive releases and the wait acquires at CTA scope.
 __device__ __forceinline__ bool consumer_sync(const Ring& rg, uint32_t& parity, volatile int* misc,
                                               const KernelArgs& a)
 {
-    mbar_arrive(rg.cbar);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.cbar);
     const bool ok = ring_wait(rg.cbar, parity, misc, a);
     parity ^= 1u;
     return ok;
@@ -193,9 +203,11 @@ struct Producer {
     }
 
     // Emits one unit: header + Q rows into the Q ring, then its K/V tiles into the stage ring.
+    // pre_base/pre_ent: a block-table window (entries pre_base + lane) loaded ahead of time.
     template <int D, bool PAGED>
     __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int nb, int L,
-                                         const int (&hw)[3])
+                                         const int (&hw)[3], int pre_base = -(1 << 30),
+                                         int pre_ent = -1)
     {
         constexpr int HALVES = D / 64;
         const KernelArgs& A = *a;
@@ -226,8 +238,9 @@ struct Producer {
         const int rows_box = bs < TILE ? bs : TILE;
         const uint32_t box_bytes = 128u * (uint32_t)rows_box;
         const int ntiles = ceil_div_i(t1 - t0, TILE);
-        int win_base = -(1 << 30), ent = -1;       // paged: 32 block-table entries per window
+        int win_base = pre_base, ent = pre_ent;    // paged: 32 block-table entries per window
         const int nblk_seq = PAGED ? ceil_div_i(L, bs) : 0;
+        constexpr int PER_BLK = 2 * HALVES;        // boxes per block: K and V, each half
         for (int i = 0; i < ntiles; ++i) {
             const int tt = t0 + i * TILE;
             const int nvalid = min(TILE, t1 - tt);
@@ -236,13 +249,13 @@ struct Producer {
             const uint32_t vdst = kdst + lay->kv_bytes;
             const uint32_t fb = rg.full + 8 * stage;
             if (!PAGED) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, (uint32_t)lay->stage_bytes);
-#pragma unroll
-                    for (int hv = 0; hv < HALVES; ++hv) {
-                        tma_load_3d(kdst + hv * TILE * 128, tmK, g * D + hv * 64, tt, b, fb);
-                        tma_load_3d(vdst + hv * TILE * 128, tmV, g * D + hv * 64, tt, b, fb);
-                    }
+                // one lane per box: K and V, each 128-byte half of the head row
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)lay->stage_bytes);
+                __syncwarp();
+                if (lane < PER_BLK) {
+                    const int hv = lane >> 1;
+                    tma_load_3d(((lane & 1) ? vdst : kdst) + hv * TILE * 128, (lane & 1) ? tmV : tmK,
+                                g * D + hv * 64, tt, b, fb);
                 }
             } else {
                 const int lb0 = tt / bs;
@@ -252,34 +265,25 @@ struct Producer {
                     const int lb = lb0 + lane;
                     ent = (lb < nblk_seq) ? __ldg(A.block_table + (long long)b * A.max_blocks + lb) : -1;
                 }
-                int blk[TILE / 16];
                 uint32_t bytes = 0;
 #pragma unroll
                 for (int k = 0; k < TILE / 16; ++k) {
-                    blk[k] = -1;
                     if (k < nbk) {
                         const int e = __shfl_sync(0xffffffffu, ent, lb0 + k - win_base);
-                        if (e >= 0 && e < A.num_blocks) {
-                            blk[k] = e;
-                            bytes += 2u * HALVES * box_bytes;
-                        } else {
-                            bad_block = true;
-                        }
+                        if (e >= 0 && e < A.num_blocks) bytes += PER_BLK * box_bytes;
+                        else bad_block = true;
                     }
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, bytes);
+                if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+                __syncwarp();
+                // one lane per (block, K/V, half) box
+                const int k = min(lane / PER_BLK, TILE / 16 - 1), r = lane % PER_BLK, hv = r >> 1;
+                const int e = __shfl_sync(0xffffffffu, ent, min(lb0 + k - win_base, 31));
+                if (lane < nbk * PER_BLK && e >= 0 && e < A.num_blocks) {
                     const int y = (bs <= TILE) ? 0 : (tt % bs);
-#pragma unroll
-                    for (int k = 0; k < TILE / 16; ++k) {
-                        if (blk[k] < 0) continue;
-#pragma unroll
-                        for (int hv = 0; hv < HALVES; ++hv) {
-                            const uint32_t off = hv * TILE * 128 + k * rows_box * 128;
-                            tma_load_3d(kdst + off, tmK, g * D + hv * 64, y, blk[k], fb);
-                            tma_load_3d(vdst + off, tmV, g * D + hv * 64, y, blk[k], fb);
-                        }
-                    }
+                    const uint32_t off = hv * TILE * 128 + k * rows_box * 128;
+                    tma_load_3d(((r & 1) ? vdst : kdst) + off, (r & 1) ? tmV : tmK, g * D + hv * 64, y,
+                                e, fb);
                 }
             }
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
@@ -299,23 +303,47 @@ struct Producer {
         // own units: u = blockIdx.x + k * gridDim.x
         UnitCursor cur;
         cur.reset();
-        int b = 0;
+        int b = 0, bn = 0;
         bool had_own = false;
+        // paged: the first block-table window of the next own unit is loaded one unit ahead
+        int pf_base = -(1 << 30), pf_ent = -1, pf_b = -1;
+        auto locate = [&](long long uu, int& bb, int& gg, int& jj, int& nbb) {
+            while ((long long)A.Hkv * plan[bb + 1] <= uu) ++bb;
+            nbb = plan[bb + 1] - plan[bb];
+            const long long r = uu - (long long)A.Hkv * plan[bb];
+            gg = (int)(r / nbb);
+            jj = (int)(r % nbb);
+        };
         for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
             int g, j, nb, L;
             if (in_smem) {
-                while ((long long)A.Hkv * plan[b + 1] <= u) ++b;
-                nb = plan[b + 1] - plan[b];
-                const long long r = u - (long long)A.Hkv * plan[b];
-                g = (int)(r / nb);
-                j = (int)(r % nb);
+                locate(u, b, g, j, nb);
                 L = clamp_len(A.seq_lens[b], A.max_seq_len);
             } else {
                 cur.seek(A, S, u, b, g, j, L);
                 nb = cur.nb;
             }
             const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
-            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3)) return;
+            if (kind == KIND_LAST_OWN) grid_launch_dependents();
+            int use_base = -(1 << 30), use_ent = -1;
+            if (PAGED && in_smem) {
+                const int lb0 = j * S / A.block_size;
+                if (pf_base == lb0 && pf_b == b) { use_base = pf_base; use_ent = pf_ent; }
+                pf_base = -(1 << 30);
+                const long long un = u + gridDim.x;
+                if (un < n_units) {
+                    int gn, jn, nbn;
+                    bn = max(bn, b);
+                    locate(un, bn, gn, jn, nbn);
+                    const int Ln = clamp_len(A.seq_lens[bn], A.max_seq_len);
+                    const int lbn = jn * S / A.block_size + lane;
+                    pf_base = jn * S / A.block_size;
+                    pf_b = bn;
+                    pf_ent = (lbn < ceil_div_i(Ln, A.block_size))
+                                 ? __ldg(A.block_table + (long long)bn * A.max_blocks + lbn) : -1;
+                }
+            }
+            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3, use_base, use_ent)) return;
             had_own = true;
         }
 
@@ -343,12 +371,10 @@ struct Producer {
                 // the pusher reserved slot k before storing it: read it with a bounded wait
                 long long e = 0;
                 if (lane == 0) {
-                    volatile long long* slotp = reinterpret_cast<volatile long long*>(A.redo + k);
                     const uint64_t t0 = global_ns();
-                    while ((e = *slotp) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
+                    while ((e = ld_acquire_gpu(A.redo + k)) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
                     }
-                    if (e != 0) *slotp = 0;            // leave the list zeroed for the next call
-                    __threadfence();
+                    if (e != 0) A.redo[k] = 0;         // leave the list zeroed for the next call
                 }
                 e = __shfl_sync(0xffffffffu, e, 0);
                 if (e == 0) {
@@ -389,58 +415,6 @@ struct Producer {
 // consumer warps
 // ------------------------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void combine_group(const KernelArgs& a, int b, int g, int nb, int ctid)
-{
-    constexpr int C4 = D / 4;
-    constexpr int U = 8;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    for (int it = ctid; it < a.G * C4; it += NCT) {
-        const int hh = it / C4, c4 = it - hh * C4;
-        const int h = g * a.G + hh;
-        const long long base = row_slot(a, b, h, 0);
-        float M = -INFINITY;
-        for (int j0 = 0; j0 < nb; j0 += U) {
-            float mv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) mv[u] = (j0 + u < nb) ? __ldcg(a.m_part + base + j0 + u) : -INFINITY;
-#pragma unroll
-            for (int u = 0; u < U; ++u) M = fmaxf(M, mv[u]);
-        }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float lam = 0.f;
-        for (int j0 = 0; j0 < nb; j0 += U) {
-            float mv[U], lv[U];
-            float4 ov[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (j0 + u < nb) {
-                    mv[u] = __ldcg(a.m_part + base + j0 + u);
-                    lv[u] = __ldcg(a.l_part + base + j0 + u);
-                    ov[u] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (base + j0 + u) * D) + c4);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (j0 + u < nb) {
-                    const float w = frame_weight(mv[u], M);
-                    acc.x = fmaf(w, ov[u].x, acc.x);
-                    acc.y = fmaf(w, ov[u].y, acc.y);
-                    acc.z = fmaf(w, ov[u].z, acc.z);
-                    acc.w = fmaf(w, ov[u].w, acc.w);
-                    lam = fmaf(w, lv[u], lam);
-                }
-            }
-        }
-        __nv_bfloat162 lo2 = __floats2bfloat162_rn(__fdiv_rn(acc.x, lam), __fdiv_rn(acc.y, lam));
-        __nv_bfloat162 hi2 = __floats2bfloat162_rn(__fdiv_rn(acc.z, lam), __fdiv_rn(acc.w, lam));
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo2);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi2);
-        *reinterpret_cast<uint2*>(out + ((long long)b * a.Hq + h) * D + 4 * c4) = pk;
-    }
-}
-
-template <int D>
 __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay, uint8_t* sm,
                                         uint32_t sbase, const Ring& rg, volatile int* misc)
 {
@@ -453,11 +427,6 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const uint32_t k_row = warp * TPW + (mi >> 1) * 8 + r8;
     const uint32_t v_row = warp * TPW + (mi & 1) * 8 + r8;
     const int tok_lo = warp * TPW + 2 * qd;       // this lane's first token in n-tile 0
-    float* scr_o = reinterpret_cast<float*>(sm + lay.scr_o);
-    float* scr_l = reinterpret_cast<float*>(sm + lay.scr_l);
-    float* scr_m = reinterpret_cast<float*>(sm + lay.scr_m);
-    unsigned* scr_f = reinterpret_cast<unsigned*>(sm + lay.scr_f);
-    volatile int* s_last = misc + 1;
     uint32_t stage = 0, phase = 0, qiter = 0, cpar = 0;
 
     for (;;) {
@@ -469,7 +438,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const int kind = hdr[H_KIND];
         if (kind == KIND_END) return;
         const int b = hdr[H_B], g = hdr[H_G], j = hdr[H_J];
-        const int t0 = hdr[H_T0], t1 = hdr[H_T1], nb = hdr[H_NB];
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1];
         const unsigned fw0 = (unsigned)hdr[H_F0], fw1 = (unsigned)hdr[H_F1];
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
         const bool redo = kind == KIND_REDO;
@@ -495,6 +464,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         float mrun = online ? -INFINITY : a.phi;
         unsigned fl = 0u;
         const int ntiles = ceil_div_i(t1 - t0, TILE);
+        uint32_t held = 0;                         // stage of the last tile: the merge scratch
 
         for (int i = 0; i < ntiles; ++i) {
             const int nvalid = min(TILE, t1 - (t0 + i * TILE));
@@ -587,16 +557,26 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 mma_16816(o[2 * c2], pa[0], pa[1], pa[2], pa[3], v0, v1);
                 mma_16816(o[2 * c2 + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rg.empty + 8 * stage);
+            if (i + 1 < ntiles) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rg.empty + 8 * stage);
+            } else {
+                held = stage;
+            }
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
         }
+        uint8_t* scr = sm + lay.stages + held * lay.stage_bytes;
+        float* scr_o = reinterpret_cast<float*>(scr + lay.scr_o);
+        float* scr_l = reinterpret_cast<float*>(scr + lay.scr_l);
+        float* scr_m = reinterpret_cast<float*>(scr + lay.scr_m);
+        unsigned* scr_f = reinterpret_cast<unsigned*>(scr + lay.scr_f);
 
         // ---- merge the 4 warps' partials of this unit and write them ----
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
         fl |= __shfl_xor_sync(0xffffffffu, fl, 1);
         fl |= __shfl_xor_sync(0xffffffffu, fl, 2);
+        if (!consumer_sync(rg, cpar, misc, a)) return;   // every warp is done with the last tile
         if (head_ok) {
             float* row = scr_o + (warp * a.G + h) * lay.scr_row;
 #pragma unroll
@@ -643,29 +623,22 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 }
             }
         }
-        __threadfence();
+        // every warp has read the scratch: the stage goes back to the producer (its generic-proxy
+        // scratch writes are ordered before the TMA writes that will refill it). The barrier also
+        // orders every thread's flag stores before the fallback push below.
+        fence_proxy_async_smem();
         if (!consumer_sync(rg, cpar, misc, a)) return;
-        // ---- fallback push, or arrival on the (b, g) ticket ----
-        if (ctid == 0) {
-            int last = 0;
-            if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
+        if (lane == 0) mbar_arrive(rg.empty + 8 * held);
+        // ---- a unit with a head outside the window goes on the device-wide fallback list ----
+        if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
+            // thread 0 publishes with a release store
+            if (ctid == 0) {
                 const int k = atomicAdd(&a.hdr[HDR_REDO_COUNT], 1);
-                const long long e = ((long long)(g * a.max_splits + j) << 32) | (long long)(unsigned)(b + 1);
-                *reinterpret_cast<volatile long long*>(a.redo + k) = e;
-                __threadfence();
-            } else {
-                const int t = atomicAdd(&a.tickets[b * a.Hkv + g], 1);
-                last = (t == nb - 1);
+                st_release_gpu(a.redo + k, ((long long)(g * a.max_splits + j) << 32) |
+                                               (long long)(unsigned)(b + 1));
             }
-            *s_last = last;
-            if (kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
         }
-        if (!consumer_sync(rg, cpar, misc, a)) return;
-        if (*s_last) {
-            __threadfence();
-            combine_group<D>(a, b, g, nb, ctid);
-            if (ctid == 0) a.tickets[b * a.Hkv + g] = 0;   // zero at rest for the next call
-        }
+        if (ctid == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
     }
 }
 
@@ -704,7 +677,7 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
             mbar_init(rg.qfull + 8 * s, 1);
             mbar_init(rg.qempty + 8 * s, NCW);
         }
-        mbar_init(rg.cbar, NCT);
+        mbar_init(rg.cbar, NCW);
         mbar_init(rg.own_done, 1);
         misc[0] = 0;
         misc[1] = 0;
@@ -770,8 +743,8 @@ TcPlan split_tc_plan(int head_dim, int group, int batch, int req_stages, int req
     TcPlan p{0, 0, 0};
     const int reserve = 1024;                         // per-CTA system reservation
     auto bytes = [&](int ns) { return TcLayout(head_dim, group, ns, batch).total + 1024; };
-    const int cands[4] = {1, 2, 3, 4};
-    for (int ci = 0; ci < 4; ++ci) {
+    const int cands[2] = {2, 1};
+    for (int ci = 0; ci < 2; ++ci) {
         const int ctas = req_ctas > 0 ? req_ctas : cands[ci];
         const int budget = smem_per_sm / ctas - reserve;
         int ns = req_stages > 0 ? req_stages : 12;

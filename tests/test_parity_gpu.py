@@ -250,10 +250,11 @@ def test_auto_split_len_matches_replay(name):
         H.assert_parity(got, ref, f"{name} auto split kernel {kernel}")
 
 
-@pytest.mark.parametrize("name,stages,ctas", [("paged_bs16", 2, 1), ("paged_bs16", 2, 2),
-                                               ("paged_bs16", 6, 1), ("gqa_ragged", 3, 2),
+@pytest.mark.parametrize("name,stages,ctas", [("paged_bs16", 2, 1), ("paged_bs16", 3, 2),
+                                               ("paged_bs16", 6, 1), ("gqa_ragged", 2, 2),
                                                ("gqa_ragged", 6, 1), ("gqa_d64", 12, 1),
-                                               ("gqa_d64", 4, 2), ("mha_g1", 3, 3)])
+                                               ("gqa_d64", 6, 2), ("mha_g1", 3, 2),
+                                               ("paged_bs128", 4, 1), ("paged_bs32", 3, 2)])
 def test_pipeline_geometries(name, stages, ctas):
     inp, dinp = _inputs(name)
     ref = H.oracle_out(inp)
@@ -264,9 +265,9 @@ def test_pipeline_geometries(name, stages, ctas):
 
 
 def test_geometry_that_does_not_fit_is_rejected():
-    inp, dinp = _inputs("paged_bs16")              # G = 8: 3 stages of 32 KB do not fit twice
+    inp, dinp = _inputs("paged_bs16")              # 4 stages of 32 KB do not fit twice per SM
     with pytest.raises(F.FdppError) as e:
-        H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_stages=8, tc_ctas_per_sm=1)
+        H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_stages=4, tc_ctas_per_sm=2)
     assert e.value.status == F.FDPP_ERR_UNSUPPORTED
 
 
