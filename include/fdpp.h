@@ -168,6 +168,28 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
                                    void* out, fdpp_stream stream, void* ev_split_begin,
                                    void* ev_split_end);
 
+/* Size in bytes of the device array behind fdpp_decode_attn_noalloc (16 MiB per GPU). */
+#define FDPP_NOALLOC_WORKSPACE_BYTES (16u << 20)
+
+/* fdpp_decode_attn for callers that cannot allocate device memory: a plugin inside a runtime
+ * that owns every device allocation and offers no allocator, or a serving loop whose memory is
+ * fixed at start-up and may not call cudaMalloc (or any allocating library) afterwards. The
+ * pages have no counterpart to this entry point; it is a deployment convenience.
+ * It needs no workspace: its scratch is one library-owned device array of
+ * FDPP_NOALLOC_WORKSPACE_BYTES that every GPU loading the library keeps until the process
+ * exits. It allocates nothing and frees nothing. Arguments are those of fdpp_decode_attn.
+ *   - Problems whose fdpp_workspace_size exceeds FDPP_NOALLOC_WORKSPACE_BYTES are rejected
+ *     with FDPP_ERR_WORKSPACE before anything is enqueued (fdpp_last_error() says by how much).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     on the host; make that first call before any stream capture on that device.
+ *   - Each call clears, on `stream`, the part of the array that must start at zero, then runs
+ *     the same kernels as fdpp_decode_attn. All calls share the array and it keeps the last
+ *     call's contents: calls that overlap on the GPU (unordered streams or threads) race on it
+ *     and produce wrong results. Calls ordered on one stream are safe. */
+fdpp_status fdpp_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     const fdpp_params* p, void* out, fdpp_stream stream);
+
 /* Reads what the last call left in `workspace` (synchronous device-to-host copies; call after
  * that call's stream has been synchronised). diag: HOST, required. flags_host: HOST uint8
  * [B][Hq][max_splits] or NULL. nsplit_host: HOST int32 [B] (splits per sequence) or NULL.

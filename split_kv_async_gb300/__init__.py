@@ -30,7 +30,9 @@ FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 
 # Names every build of the library exports (the C ABI of include/fdpp.h).
 EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fdpp_decode_attn",
-            "fdpp_decode_attn_timed", "fdpp_read_diag", "fdpp_status_str", "fdpp_last_error")
+            "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_read_diag",
+            "fdpp_status_str", "fdpp_last_error")
+FDPP_NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 
 class FdppError(RuntimeError):
@@ -86,6 +88,8 @@ def _load() -> ctypes.CDLL:
     lib.fdpp_decode_attn_timed.argtypes = [vp, vp, vp, vp, vp, P, vp, ctypes.c_size_t, vp, vp, vp,
                                            vp]
     lib.fdpp_decode_attn_timed.restype = ctypes.c_int
+    lib.fdpp_decode_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp, vp]
+    lib.fdpp_decode_attn_noalloc.restype = ctypes.c_int
     lib.fdpp_read_diag.argtypes = [vp, ctypes.c_size_t, P, ctypes.POINTER(fdpp_diag), vp, vp]
     lib.fdpp_read_diag.restype = ctypes.c_int
     lib.fdpp_status_str.argtypes = [ctypes.c_int]
@@ -166,6 +170,15 @@ def fdpp_decode_attn_timed(q, k_cache, v_cache, block_table, seq_lens, p: fdpp_p
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _stream_handle(stream), None if ev_split_begin is None else ev_split_begin.cuda_event,
         None if ev_split_end is None else ev_split_end.cuda_event), "fdpp_decode_attn_timed")
+
+
+def fdpp_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, p: fdpp_params, out,
+                             stream=None) -> None:
+    """The decode step for callers that cannot allocate: no workspace argument, the library's
+    own static device array is the scratch (see include/fdpp.h for its size and sharing rules)."""
+    _check(lib.fdpp_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                        _ptr(seq_lens), ctypes.byref(p), _ptr(out),
+                                        _stream_handle(stream)), "fdpp_decode_attn_noalloc")
 
 
 def fdpp_read_diag(workspace, p: fdpp_params, want_flags=False, want_nsplit=False):

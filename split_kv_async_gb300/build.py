@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfdpp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cpp", "split_tc.cu", "split_simt.cu", "combine.cu"]
+SOURCES = ["api.cpp", "split_tc.cu", "split_simt.cu", "combine.cu", "no_alloc.cu"]
 HEADERS = ["fdpp_internal.h", "device_common.cuh"]
 
 

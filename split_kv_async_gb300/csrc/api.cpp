@@ -202,6 +202,14 @@ fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params&
 
 }  // namespace
 
+namespace fdpp {
+// Bytes at the start of a workspace for `p` that hold the state which must be zero before a call:
+// header, plan, tickets and the fallback list (everything before the flag bytes).
+size_t workspace_zero_prefix(const fdpp_params& p) { return layout_of(p).flags; }
+// Sets the reason fdpp_last_error() reports on this thread.
+void set_last_error(const char* what) { g_last_error = what; }
+}  // namespace fdpp
+
 extern "C" {
 
 const char* fdpp_status_str(fdpp_status s)

@@ -68,6 +68,11 @@ cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CU
                             int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s);
 cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
 
+// Bytes at the front of a workspace for `p` that must be zero when a call starts.
+size_t workspace_zero_prefix(const fdpp_params& p);
+// Sets the reason fdpp_last_error() reports on this thread.
+void set_last_error(const char* what);
+
 // Resident CTAs per SM of the SIMT split kernel for this shape (0 if it cannot launch).
 int split_simt_ctas_per_sm(const KernelArgs& a, int dtype);
 
