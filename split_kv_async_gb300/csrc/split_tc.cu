@@ -418,15 +418,25 @@ template <int D>
 __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay, uint8_t* sm,
                                         uint32_t sbase, const Ring& rg, volatile int* misc)
 {
-    constexpr int KS = D / 16;           // k-steps of q.K^T, and column pairs of P.V
-    constexpr int NT = D / 8;            // n-tiles of the output
+    // The tile is computed transposed, tokens on the MMA's M dimension and heads on N:
+    //   S^T[16 tok x 8 heads] = K[16 x d] Q^T[d x 8]      (d/16 MMAs)
+    //   O^T[d x 8 heads]     += V^T[d x 16 tok] P^T[16 x 8] (d/16 MMAs, d on M)
+    // Fragment roles for lane = 4 r + qd: S^T and O^T rows r and r+8 (a token, resp. a d),
+    // columns 2qd and 2qd+1 (two heads). P^T is turned into the B operand of the second MMA
+    // with movmatrix.trans. P is carried as bf16 hi + lo: for G <= 4 the lo part rides in head
+    // columns 4..7 (unused otherwise), so P.V costs d/16 MMAs; for G > 4 hi and lo go through
+    // two MMAs into the same accumulator.
+    constexpr int KS = D / 16;           // k-steps of S^T, and m-tiles of O^T
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ctid = threadIdx.x;
-    const int h = lane >> 2, qd = lane & 3;       // head row and column pair of this lane
+    const int r = lane >> 2, qd = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;      // ldmatrix: matrix and row of this lane
-    const bool head_ok = h < a.G;
-    const uint32_t k_row = warp * TPW + (mi >> 1) * 8 + r8;
-    const uint32_t v_row = warp * TPW + (mi & 1) * 8 + r8;
-    const int tok_lo = warp * TPW + 2 * qd;       // this lane's first token in n-tile 0
+    const bool pack_lo = a.G <= 4;
+    const bool q_ok = r < a.G;                    // this lane supplies Q row (head) r
+    const uint32_t k_row = warp * TPW + (mi & 1) * 8 + r8;
+    const uint32_t v_row = warp * TPW + (mi >> 1) * 8 + r8;
+    const int tok_r = warp * TPW + r;             // this lane's tokens: tok_r and tok_r + 8
+    const int tok_q = warp * TPW + 2 * qd;        // tokens of this lane's V^T fragment columns
+    const int head0 = 2 * qd;                     // this lane's heads: head0, head0 + 1
     uint32_t stage = 0, phase = 0, qiter = 0, cpar = 0;
 
     for (;;) {
@@ -444,25 +454,26 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const bool redo = kind == KIND_REDO;
         const bool online = redo || (a.mode == FDPP_MODE_FORCE_ONLINE);
 
-        uint32_t qa[KS][2];
+        uint32_t qb[KS][2];                        // B operand of S^T: Q^T, column r = head r
         {
-            const uint8_t* qb = slot + QHDR_BYTES;
+            const uint8_t* qp = slot + QHDR_BYTES;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                qa[ks][0] = head_ok ? *reinterpret_cast<const uint32_t*>(qb + (h * D + ks * 16 + 2 * qd) * 2) : 0u;
-                qa[ks][1] = head_ok ? *reinterpret_cast<const uint32_t*>(qb + (h * D + ks * 16 + 8 + 2 * qd) * 2) : 0u;
+                qb[ks][0] = q_ok ? *reinterpret_cast<const uint32_t*>(qp + (r * D + ks * 16 + 2 * qd) * 2) : 0u;
+                qb[ks][1] = q_ok ? *reinterpret_cast<const uint32_t*>(qp + (r * D + ks * 16 + 8 + 2 * qd) * 2) : 0u;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(rg.qempty + 8 * qs);
             ++qiter;
         }
 
-        float o[NT][4];
+        float o[KS][4];                            // O^T rows 16mt + r (+8), heads head0, head0+1
 #pragma unroll
-        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float lsum = 0.f;
-        float mrun = online ? -INFINITY : a.phi;
-        unsigned fl = 0u;
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float lsum[2] = {0.f, 0.f};
+        float mrun[2] = {online ? -INFINITY : a.phi, online ? -INFINITY : a.phi};
+        unsigned fl[2] = {0u, 0u};
+        const bool hv[2] = {head0 < a.G, head0 + 1 < a.G};
         const int ntiles = ceil_div_i(t1 - t0, TILE);
         uint32_t held = 0;                         // stage of the last tile: the merge scratch
 
@@ -472,90 +483,102 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
             const uint32_t vb = kb + lay.kv_bytes;
 
-            // S = Q K^T for this warp's 16 tokens (two n-tiles of 8 tokens), two chains each
-            float sa[2][2][4];
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) sa[c][nt][0] = sa[c][nt][1] = sa[c][nt][2] = sa[c][nt][3] = 0.f;
+            // S^T = K Q^T for this warp's 16 tokens, two accumulation chains
+            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int chunk = 2 * ks + (mi & 1);
+                const int chunk = 2 * ks + (mi >> 1);
                 const uint32_t addr = kb + (chunk >> 3) * (TILE * 128) + k_row * 128 + (((chunk & 7) ^ r8) << 4);
                 uint32_t k0, k1, k2, k3;
                 ldsm_x4(addr, k0, k1, k2, k3);
-                mma_16816(sa[ks & 1][0], qa[ks][0], 0u, qa[ks][1], 0u, k0, k1);
-                mma_16816(sa[ks & 1][1], qa[ks][0], 0u, qa[ks][1], 0u, k2, k3);
+                mma_16816(sa[ks & 1], k0, k1, k2, k3, qb[ks][0], qb[ks][1]);
+            }
+            // element e of sa: token tok_r + 8 (e >> 1), head head0 + (e & 1)
+            float sv[4];
+            bool valid[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
+                valid[e] = hv[e & 1] && (tok_r + 8 * (e >> 1) < nvalid);
+                if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], a.phi), a.lo, a.hi);
             }
 
-            float s[2][2];
-            bool valid[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    s[nt][e] = __fmul_rn(sa[0][nt][e] + sa[1][nt][e], a.scale);
-                    valid[nt][e] = head_ok && (tok_lo + 8 * nt + e < nvalid);
-                    if (valid[nt][e]) fl |= classify(__fsub_rn(s[nt][e], a.phi), a.lo, a.hi);
-                }
-
-            float p[2][2];
+            float p[4];
             if (!online) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        p[nt][e] = valid[nt][e] ? __expf(__fsub_rn(s[nt][e], a.phi)) : 0.f;
+                for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], a.phi)) : 0.f;
             } else {
-                float tmax = -INFINITY;
+                float corr[2];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        if (valid[nt][e]) tmax = fmaxf(tmax, s[nt][e]);
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-                const float mnew = fmaxf(mrun, tmax);
-                const float corr = (mrun == mnew) ? 1.f : (mrun == -INFINITY ? 0.f : __expf(mrun - mnew));
-                if (corr != 1.f) {
-                    lsum *= corr;
-#pragma unroll
-                    for (int n = 0; n < NT; ++n) { o[n][0] *= corr; o[n][1] *= corr; o[n][2] *= corr; o[n][3] *= corr; }
+                for (int c = 0; c < 2; ++c) {
+                    float tmax = -INFINITY;
+                    if (valid[c]) tmax = sv[c];
+                    if (valid[c + 2]) tmax = fmaxf(tmax, sv[c + 2]);
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                    const float mnew = fmaxf(mrun[c], tmax);
+                    corr[c] = (mrun[c] == mnew) ? 1.f : (mrun[c] == -INFINITY ? 0.f : __expf(mrun[c] - mnew));
+                    mrun[c] = mnew;
+                    lsum[c] *= corr[c];
+                    p[c] = valid[c] ? __expf(sv[c] - mnew) : 0.f;
+                    p[c + 2] = valid[c + 2] ? __expf(sv[c + 2] - mnew) : 0.f;
                 }
-                mrun = mnew;
+                // columns 4..7 of lanes qd >= 2 hold the lo part of heads 0..3 (G <= 4)
+                float oc[2] = {corr[0], corr[1]};
+                if (pack_lo) {
+                    const float x0 = __shfl_xor_sync(0xffffffffu, corr[0], 2);
+                    const float x1 = __shfl_xor_sync(0xffffffffu, corr[1], 2);
+                    if (qd >= 2) { oc[0] = x0; oc[1] = x1; }
+                }
+                if (oc[0] != 1.f || oc[1] != 1.f) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        p[nt][e] = valid[nt][e] ? __expf(s[nt][e] - mnew) : 0.f;
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[mt][0] *= oc[0]; o[mt][2] *= oc[0];
+                        o[mt][1] *= oc[1]; o[mt][3] *= oc[1];
+                    }
+                }
             }
-            lsum += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+            lsum[0] += p[0] + p[2];
+            lsum[1] += p[1] + p[3];
 
-            // A operand of P.V: rows 0..7 = bf16(p), rows 8..15 = bf16(p - bf16(p))
-            uint32_t pa[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(p[nt][0], p[nt][1]);
-                const float2 hf = __bfloat1622float2(hi);
-                pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&hi);
-                pa[2 * nt + 1] = pack_bf16x2(p[nt][0] - hf.x, p[nt][1] - hf.y);
+            // P^T as the B operand of O^T += V^T P^T (tokens x heads), hi and lo bf16 parts
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
+            const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            uint32_t x_hi0 = *reinterpret_cast<const uint32_t*>(&h01);
+            uint32_t x_hi1 = *reinterpret_cast<const uint32_t*>(&h23);
+            const uint32_t x_lo0 = pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
+            const uint32_t x_lo1 = pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
+            uint32_t b_hi0, b_hi1, b_lo0 = 0u, b_lo1 = 0u;
+            if (pack_lo) {
+                const uint32_t y0 = __shfl_xor_sync(0xffffffffu, x_lo0, 2);
+                const uint32_t y1 = __shfl_xor_sync(0xffffffffu, x_lo1, 2);
+                if (qd >= 2) { x_hi0 = y0; x_hi1 = y1; }
+                b_hi0 = movmatrix_trans(x_hi0);
+                b_hi1 = movmatrix_trans(x_hi1);
+            } else {
+                b_hi0 = movmatrix_trans(x_hi0);
+                b_hi1 = movmatrix_trans(x_hi1);
+                b_lo0 = movmatrix_trans(x_lo0);
+                b_lo1 = movmatrix_trans(x_lo1);
             }
 
             // V rows past the valid tokens may hold anything (NaN included): mask them to zero
             uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
             if (nvalid < TILE) {
-                vm_lo = (tok_lo < nvalid ? 0x0000ffffu : 0u) | (tok_lo + 1 < nvalid ? 0xffff0000u : 0u);
-                vm_hi = (tok_lo + 8 < nvalid ? 0x0000ffffu : 0u) | (tok_lo + 9 < nvalid ? 0xffff0000u : 0u);
+                vm_lo = (tok_q < nvalid ? 0x0000ffffu : 0u) | (tok_q + 1 < nvalid ? 0xffff0000u : 0u);
+                vm_hi = (tok_q + 8 < nvalid ? 0x0000ffffu : 0u) | (tok_q + 9 < nvalid ? 0xffff0000u : 0u);
             }
 #pragma unroll
-            for (int c2 = 0; c2 < KS; ++c2) {
-                const int chunk = 2 * c2 + (mi >> 1);
+            for (int mt = 0; mt < KS; ++mt) {
+                const int chunk = 2 * mt + (mi & 1);
                 const uint32_t addr = vb + (chunk >> 3) * (TILE * 128) + v_row * 128 + (((chunk & 7) ^ r8) << 4);
                 uint32_t v0, v1, v2, v3;
                 ldsm_x4_t(addr, v0, v1, v2, v3);
-                v0 &= vm_lo; v2 &= vm_lo; v1 &= vm_hi; v3 &= vm_hi;
-                mma_16816(o[2 * c2], pa[0], pa[1], pa[2], pa[3], v0, v1);
-                mma_16816(o[2 * c2 + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
+                v0 &= vm_lo; v1 &= vm_lo; v2 &= vm_hi; v3 &= vm_hi;
+                mma_16816(o[mt], v0, v1, v2, v3, b_hi0, b_hi1);
+                if (!pack_lo) mma_16816(o[mt], v0, v1, v2, v3, b_lo0, b_lo1);
             }
             if (i + 1 < ntiles) {
                 __syncwarp();
@@ -571,21 +594,35 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         float* scr_m = reinterpret_cast<float*>(scr + lay.scr_m);
         unsigned* scr_f = reinterpret_cast<unsigned*>(scr + lay.scr_f);
 
-        // ---- merge the 4 warps' partials of this unit and write them ----
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-        fl |= __shfl_xor_sync(0xffffffffu, fl, 1);
-        fl |= __shfl_xor_sync(0xffffffffu, fl, 2);
-        if (!consumer_sync(rg, cpar, misc, a)) return;   // every warp is done with the last tile
-        if (head_ok) {
-            float* row = scr_o + (warp * a.G + h) * lay.scr_row;
+        // ---- this warp's partial: reduce over its 16 tokens (lanes r), fold in the lo part ----
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-                *reinterpret_cast<float2*>(row + 8 * n + 2 * qd) = make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
-            if (qd == 0) {
-                scr_l[warp * a.G + h] = lsum;
-                scr_m[warp * a.G + h] = mrun;
-                scr_f[warp * a.G + h] = fl;
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], sh);
+                fl[c] |= __shfl_xor_sync(0xffffffffu, fl[c], sh);
+            }
+        }
+        if (pack_lo) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
+        }
+        if (!consumer_sync(rg, cpar, misc, a)) return;   // every warp is done with the last tile
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            if (!hv[c] || (pack_lo && qd >= 2)) continue;
+            float* row = scr_o + (warp * a.G + head0 + c) * lay.scr_row;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                row[16 * mt + r] = o[mt][c];
+                row[16 * mt + r + 8] = o[mt][c + 2];
+            }
+            if (r == 0) {
+                scr_l[warp * a.G + head0 + c] = lsum[c];
+                scr_m[warp * a.G + head0 + c] = mrun[c];
+                scr_f[warp * a.G + head0 + c] = fl[c];
             }
         }
         if (!consumer_sync(rg, cpar, misc, a)) return;
