@@ -58,6 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--mode", type=int, default=0, help="fdpp_mode (0 normal, 1 fast, 2 online)")
     ap.add_argument("--tc-stages", type=int, default=0)
     ap.add_argument("--tc-ctas", type=int, default=0)
+    ap.add_argument("--tc-prefetch", type=int, default=0)
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -343,7 +344,7 @@ def run_fdpp(args, dist: Dist):
               head_dim=wl.head_dim, dtype=F.FDPP_F32 if wl.dtype == "f32" else F.FDPP_BF16,
               max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
               split_len=split_len, mode=args.mode, kernel=args.kernel, tc_stages=args.tc_stages,
-              tc_ctas_per_sm=args.tc_ctas)
+              tc_ctas_per_sm=args.tc_ctas, tc_prefetch=args.tc_prefetch)
     if wl.paged:
         kw.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
                   num_kv_blocks=inp.num_kv_blocks,

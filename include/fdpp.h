@@ -107,6 +107,8 @@ typedef struct fdpp_params {
     int kernel;              /* fdpp_kernel */
     int tc_stages;           /* tensor kernel: depth of the TMA ring (2..12), 0 = automatic */
     int tc_ctas_per_sm;      /* tensor kernel: resident CTAs per SM (1 or 2), 0 = automatic */
+    int tc_prefetch;         /* tensor kernel: L2 prefetch distance in 64-token tiles ahead of the
+                                TMA ring (1..32); 0 = automatic (off), -1 = off */
 } fdpp_params;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over

@@ -55,6 +55,7 @@ class fdpp_params(ctypes.Structure):
         ("hi", ctypes.c_float),
         ("split_len", ctypes.c_int), ("mode", ctypes.c_int), ("kernel", ctypes.c_int),
         ("tc_stages", ctypes.c_int), ("tc_ctas_per_sm", ctypes.c_int),
+        ("tc_prefetch", ctypes.c_int),
     ]
 
 
@@ -110,10 +111,10 @@ def _check(status: int, where: str) -> None:
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, scale,
                 phi=0.0, lo=-30.0, hi=10.0, split_len=0, block_size=0, max_blocks_per_seq=0,
                 num_kv_blocks=0, mode=FDPP_MODE_NORMAL, kernel=FDPP_KERNEL_AUTO, tc_stages=0,
-                tc_ctas_per_sm=0) -> fdpp_params:
+                tc_ctas_per_sm=0, tc_prefetch=0) -> fdpp_params:
     return fdpp_params(batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, block_size,
                        max_blocks_per_seq, num_kv_blocks, scale, phi, lo, hi, split_len, mode,
-                       kernel, tc_stages, tc_ctas_per_sm)
+                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch)
 
 
 def fdpp_max_splits(p: fdpp_params) -> int:

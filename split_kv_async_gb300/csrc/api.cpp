@@ -76,6 +76,8 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "tc_stages must be 0 or in [2, 12]");
     if (p->tc_ctas_per_sm < 0 || p->tc_ctas_per_sm > 2)
         return fail(FDPP_ERR_INVALID_ARG, "tc_ctas_per_sm must be 0, 1 or 2");
+    if (p->tc_prefetch < -1 || p->tc_prefetch > 32)
+        return fail(FDPP_ERR_INVALID_ARG, "tc_prefetch must be -1, 0 or in [1, 32]");
     const int G = p->num_q_heads / p->num_kv_heads;
     if (G > SIMT_MAX_GROUP)
         return fail(FDPP_ERR_UNSUPPORTED, "query heads per kv head %d > %d", G, SIMT_MAX_GROUP);
@@ -339,6 +341,8 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
             return fail(FDPP_ERR_UNSUPPORTED, "no tensor-kernel geometry fits (stages %d, CTAs/SM %d)",
                         p->tc_stages, p->tc_ctas_per_sm);
         a.nstage = plan.nstage;
+        // L2 prefetch ahead of the ring measured slower on every workload here: off unless asked
+        a.pf_tiles = p->tc_prefetch > 0 ? p->tc_prefetch : 0;
         CUtensorMap tk, tv;
         if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
         if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;

@@ -54,6 +54,7 @@ struct KernelArgs {
     int mode;
     int kernel_id;
     int nstage;                   // tensor kernel: TMA ring depth
+    int pf_tiles;                 // tensor kernel: L2 prefetch distance in tiles (0 = off)
 };
 
 // Tensor-core kernel shape limits (bf16, G <= 8 so that the hi and lo halves of P fit the

@@ -124,6 +124,11 @@ __device__ __forceinline__ long long row_slot(const KernelArgs& a, int b, int h,
 // ------------------------------------------------------------------------------------------
 // producer warp
 // ------------------------------------------------------------------------------------------
+// The unit the producer streams after the current one (for L2 prefetch across units).
+struct NextUnit {
+    int valid, b, g, t0, t1, win_base, ent;
+};
+
 struct Producer {
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
@@ -202,12 +207,43 @@ struct Producer {
         return n_units;
     }
 
-    // Emits one unit: header + Q rows into the Q ring, then its K/V tiles into the stage ring.
+    // L2 prefetch of one 64-token tile of kv head g (no shared memory, no barrier): the tile's
+    // DRAM reads start before a ring stage is free for it, so the ring's own TMA load hits L2.
+    // Paged: only blocks inside the given block-table window are prefetched.
+    template <int D, bool PAGED>
+    __device__ __forceinline__ void prefetch_tile(int b, int g, int tt, int t1, int win_base, int ent)
+    {
+        constexpr int HALVES = D / 64;
+        constexpr int PER_BLK = 2 * HALVES;
+        const KernelArgs& A = *a;
+        const int lane = threadIdx.x & 31;
+        const int nvalid = min(TILE, t1 - tt);
+        if (nvalid <= 0) return;
+        if (!PAGED) {
+            if (lane < PER_BLK) {
+                const int hv = lane >> 1;
+                tma_prefetch_3d((lane & 1) ? tmV : tmK, g * D + hv * 64, tt, b);
+            }
+        } else {
+            const int bs = A.block_size;
+            const int lb0 = tt / bs;
+            const int nbk = (bs <= TILE) ? ceil_div_i(nvalid, bs) : 1;
+            if (lb0 < win_base || lb0 + nbk > win_base + 32) return;
+            const int k = min(lane / PER_BLK, TILE / 16 - 1), r = lane % PER_BLK, hv = r >> 1;
+            const int e = __shfl_sync(0xffffffffu, ent, min(lb0 + k - win_base, 31));
+            if (lane < nbk * PER_BLK && e >= 0 && e < A.num_blocks)
+                tma_prefetch_3d((r & 1) ? tmV : tmK, g * D + hv * 64, (bs <= TILE) ? 0 : (tt % bs), e);
+        }
+    }
+
+    // Emits one unit: header + Q rows into the Q ring, then its K/V tiles into the stage ring,
+    // prefetching into L2 the tile `pf` places ahead (in this unit, or in `nx`, the next one).
     // pre_base/pre_ent: a block-table window (entries pre_base + lane) loaded ahead of time.
     template <int D, bool PAGED>
     __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int nb, int L,
                                          const int (&hw)[3], int pre_base = -(1 << 30),
-                                         int pre_ent = -1)
+                                         int pre_ent = -1, const NextUnit* nx = nullptr,
+                                         bool first = false)
     {
         constexpr int HALVES = D / 64;
         const KernelArgs& A = *a;
@@ -241,6 +277,15 @@ struct Producer {
         int win_base = pre_base, ent = pre_ent;    // paged: 32 block-table entries per window
         const int nblk_seq = PAGED ? ceil_div_i(L, bs) : 0;
         constexpr int PER_BLK = 2 * HALVES;        // boxes per block: K and V, each half
+        const int pf = A.pf_tiles;
+        if (PAGED && pf > 0 && win_base == -(1 << 30)) {   // the unit's first window, now
+            win_base = t0 / bs;
+            const int lb = win_base + lane;
+            ent = (lb < nblk_seq) ? __ldg(A.block_table + (long long)b * A.max_blocks + lb) : -1;
+        }
+        if (first && pf > 0)                       // the CTA's first unit: nothing was prefetched
+            for (int ti = 1; ti <= pf && ti < ntiles; ++ti)
+                prefetch_tile<D, PAGED>(b, g, t0 + ti * TILE, t1, win_base, ent);
         for (int i = 0; i < ntiles; ++i) {
             const int tt = t0 + i * TILE;
             const int nvalid = min(TILE, t1 - tt);
@@ -286,6 +331,15 @@ struct Producer {
                                 e, fb);
                 }
             }
+            if (pf > 0) {
+                const int ti = i + pf;
+                if (ti < ntiles) {
+                    prefetch_tile<D, PAGED>(b, g, t0 + ti * TILE, t1, win_base, ent);
+                } else if (nx && nx->valid) {
+                    const int tn = nx->t0 + (ti - ntiles) * TILE;
+                    if (tn < nx->t1) prefetch_tile<D, PAGED>(nx->b, nx->g, tn, nx->t1, nx->win_base, nx->ent);
+                }
+            }
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
         }
         return true;
@@ -326,24 +380,36 @@ struct Producer {
             const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
             if (kind == KIND_LAST_OWN) grid_launch_dependents();
             int use_base = -(1 << 30), use_ent = -1;
-            if (PAGED && in_smem) {
+            NextUnit nx{0, 0, 0, 0, 0, -(1 << 30), -1};
+            if (PAGED) {
                 const int lb0 = j * S / A.block_size;
                 if (pf_base == lb0 && pf_b == b) { use_base = pf_base; use_ent = pf_ent; }
                 pf_base = -(1 << 30);
-                const long long un = u + gridDim.x;
-                if (un < n_units) {
-                    int gn, jn, nbn;
-                    bn = max(bn, b);
-                    locate(un, bn, gn, jn, nbn);
-                    const int Ln = clamp_len(A.seq_lens[bn], A.max_seq_len);
+            }
+            const long long un = u + gridDim.x;
+            if (un < n_units && in_smem) {
+                // the next own unit: located now, and (paged) its first block-table window
+                // loaded one unit ahead
+                int gn, jn, nbn;
+                bn = max(bn, b);
+                locate(un, bn, gn, jn, nbn);
+                const int Ln = clamp_len(A.seq_lens[bn], A.max_seq_len);
+                nx.valid = 1;
+                nx.b = bn;
+                nx.g = gn;
+                nx.t0 = jn * S;
+                nx.t1 = min(nx.t0 + S, Ln);
+                if (PAGED) {
                     const int lbn = jn * S / A.block_size + lane;
                     pf_base = jn * S / A.block_size;
                     pf_b = bn;
                     pf_ent = (lbn < ceil_div_i(Ln, A.block_size))
                                  ? __ldg(A.block_table + (long long)bn * A.max_blocks + lbn) : -1;
+                    nx.win_base = pf_base;
+                    nx.ent = pf_ent;
                 }
             }
-            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3, use_base, use_ent)) return;
+            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3, use_base, use_ent, &nx, !had_own)) return;
             had_own = true;
         }
 

@@ -78,6 +78,8 @@ def test_max_splits_and_workspace_size():
     ("kernel", 9, F.FDPP_ERR_INVALID_ARG),
     ("tc_stages", 1, F.FDPP_ERR_INVALID_ARG),
     ("tc_ctas_per_sm", 3, F.FDPP_ERR_INVALID_ARG),
+    ("tc_prefetch", 33, F.FDPP_ERR_INVALID_ARG),
+    ("tc_prefetch", -2, F.FDPP_ERR_INVALID_ARG),
 ])
 def test_bad_params_are_rejected_on_the_host(field, value, status):
     p = _gqa_params()

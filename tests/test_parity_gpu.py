@@ -264,6 +264,18 @@ def test_pipeline_geometries(name, stages, ctas):
     assert diag["error_bits"] == 0
 
 
+@pytest.mark.parametrize("name", ["paged_bs16", "gqa_ragged", "paged_bs128"])
+@pytest.mark.parametrize("prefetch", [-1, 1, 12])
+def test_l2_prefetch_distances(name, prefetch):
+    """The L2 prefetch ahead of the TMA ring moves no data the kernel reads: any distance (or
+    none) gives bit-identical results."""
+    inp, dinp = _inputs(name)
+    base, _, _, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    got, diag, _, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_prefetch=prefetch)
+    np.testing.assert_array_equal(got, base)
+    assert diag["error_bits"] == 0
+
+
 def test_geometry_that_does_not_fit_is_rejected():
     inp, dinp = _inputs("paged_bs16")              # 4 stages of 32 KB do not fit twice per SM
     with pytest.raises(F.FdppError) as e:
