@@ -198,7 +198,8 @@ def measured_peaks():
 
 def split_kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("split_tc.cu", "split_simt.cu", "device_common.cuh"):
+    for name in ("split_tc.cu", "split_simt.cu", "combine.cu", "device_common.cuh",
+                 "fdpp_internal.h"):
         with open(os.path.join(ROOT, "split_kv_async_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -114,7 +114,6 @@ WsLayout layout_of(const fdpp_params& p)
     size_t off = 0;
     w.header = off;  off = align256(off + HDR_WORDS * 4);
     w.nsplit = off;  off = align256(off + (size_t)p.batch * 4);
-    w.tickets = off; off = align256(off + (size_t)p.batch * p.num_kv_heads * 4);
     w.redo = off;    off = align256(off + (size_t)p.batch * p.num_kv_heads * w.max_splits * 8);
     w.flags = off;   off = align256(off + slots);
     w.m_part = off;  off = align256(off + slots * 4);
@@ -206,7 +205,7 @@ fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params&
 
 namespace fdpp {
 // Bytes at the start of a workspace for `p` that hold the state which must be zero before a call:
-// header, plan, tickets and the fallback list (everything before the flag bytes).
+// header, plan and the fallback list (everything before the flag bytes).
 size_t workspace_zero_prefix(const fdpp_params& p) { return layout_of(p).flags; }
 // Sets the reason fdpp_last_error() reports on this thread.
 void set_last_error(const char* what) { g_last_error = what; }
@@ -304,7 +303,6 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     a.out = out;
     a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
     a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
-    a.tickets = reinterpret_cast<int32_t*>(ws + w.tickets);
     a.redo = reinterpret_cast<long long*>(ws + w.redo);
     a.flags = ws + w.flags;
     a.m_part = reinterpret_cast<float*>(ws + w.m_part);

@@ -27,7 +27,7 @@ enum {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-    size_t header, nsplit, tickets, redo, flags, m_part, l_part, o_part, total;
+    size_t header, nsplit, redo, flags, m_part, l_part, o_part, total;
     int max_splits;
 };
 
@@ -41,7 +41,6 @@ struct KernelArgs {
     void* out;
     int32_t* hdr;
     int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
-    int32_t* tickets;             // [B][Hkv], zero at rest
     long long* redo;              // fallback list [B*Hkv*max_splits] of (b+1, g*max_splits+j)
     uint8_t* flags;               // [B][Hq][max_splits]
     float* m_part;                // [B][Hq][max_splits]

@@ -54,7 +54,7 @@ def test_max_splits_and_workspace_size():
     assert F.fdpp_max_splits(p) == 8
     ws = F.fdpp_workspace_size(p)
     slots = 8 * 32 * 8
-    # partials o (d floats), l, m and a flag byte per slot, plus header/plan/tickets
+    # partials o (d floats), l, m and a flag byte per slot, plus header, plan and fallback list
     assert slots * (128 * 4 + 4 + 4 + 1) <= ws <= slots * (128 * 4 + 4 + 4 + 1) + 64 * 1024
     assert ws % 256 == 0
     p0 = _gqa_params(split_len=0)
