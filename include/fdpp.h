@@ -133,9 +133,16 @@ typedef struct fdpp_diag {
  * S, ceil(max_seq_len / FDPP_AUTO_MIN_SPLIT) for S == 0. Returns -1 on invalid params. */
 int fdpp_max_splits(const fdpp_params* p);
 
+/* The tensor kernel cuts the 64-token tiles of all (b, g, j) units into at most this many
+ * equal parts, one per CTA, so that every CTA streams the same number of bytes. A part that
+ * begins inside a split leaves its share of that split in one extra slot of the workspace. */
+#define FDPP_TC_MAX_PARTS 512
+
 /* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
  * holds the split plan, the per-split partials (o: fp32 [B][Hq][max_splits][d]; l, m: fp32
- * [B][Hq][max_splits]), the flag bytes [B][Hq][max_splits] and a small header. */
+ * [B][Hq][max_splits]), the flag bytes [B][Hq][max_splits], FDPP_TC_MAX_PARTS extra slots of
+ * G = Hq / Hkv rows each (o, l, m and flags, like a split's), the fallback list and a small
+ * header. */
 fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
 
 /* Zeroes a workspace (stream-ordered). Call once after allocating it; it also clears the

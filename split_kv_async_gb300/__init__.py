@@ -33,6 +33,7 @@ EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fd
             "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_read_diag",
             "fdpp_status_str", "fdpp_last_error")
 FDPP_NOALLOC_WORKSPACE_BYTES = 16 << 20
+FDPP_TC_MAX_PARTS = 512
 
 
 class FdppError(RuntimeError):

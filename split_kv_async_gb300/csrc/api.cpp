@@ -114,11 +114,21 @@ WsLayout layout_of(const fdpp_params& p)
     size_t off = 0;
     w.header = off;  off = align256(off + HDR_WORDS * 4);
     w.nsplit = off;  off = align256(off + (size_t)p.batch * 4);
-    w.redo = off;    off = align256(off + (size_t)p.batch * p.num_kv_heads * w.max_splits * 8);
+    w.tstart = off;  off = align256(off + ((size_t)p.batch + 1) * 4);
+    // a fallback entry per unit, plus one per part for units cut in two
+    const size_t entries = (size_t)p.batch * p.num_kv_heads * w.max_splits + TC_MAX_PARTS;
+    w.redo = off;    off = align256(off + entries * REDO_WORDS * 8);
     w.flags = off;   off = align256(off + slots);
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
     w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
+    // extra slots of the tensor kernel's parts (G rows each)
+    const size_t G = (size_t)(p.num_q_heads / p.num_kv_heads);
+    const size_t xrows = (size_t)TC_MAX_PARTS * G;
+    w.xf = off;      off = align256(off + xrows);
+    w.xm = off;      off = align256(off + xrows * 4);
+    w.xl = off;      off = align256(off + xrows * 4);
+    w.xo = off;      off = align256(off + xrows * (size_t)p.head_dim * 4);
     w.total = off;
     return w;
 }
@@ -303,11 +313,16 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     a.out = out;
     a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
     a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
+    a.tstart = reinterpret_cast<int32_t*>(ws + w.tstart);
     a.redo = reinterpret_cast<long long*>(ws + w.redo);
     a.flags = ws + w.flags;
     a.m_part = reinterpret_cast<float*>(ws + w.m_part);
     a.l_part = reinterpret_cast<float*>(ws + w.l_part);
     a.o_part = reinterpret_cast<float*>(ws + w.o_part);
+    a.xf = ws + w.xf;
+    a.xm = reinterpret_cast<float*>(ws + w.xm);
+    a.xl = reinterpret_cast<float*>(ws + w.xl);
+    a.xo = reinterpret_cast<float*>(ws + w.xo);
     a.B = p->batch;
     a.Hq = p->num_q_heads;
     a.Hkv = p->num_kv_heads;
@@ -344,9 +359,12 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         CUtensorMap tk, tv;
         if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
         if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;
-        // persistent grid: every SM busy (SMs x resident CTAs), no more CTAs than units can exist
+        // persistent grid: every SM busy (SMs x resident CTAs). Batches whose plan fits in shared
+        // memory are cut into equal parts of tiles, one per CTA (the kernel uses at most
+        // TC_MAX_PARTS); larger ones are dealt out as whole units, no more CTAs than units.
         long long grid = (long long)dev.sms * plan.ctas_per_sm;
-        if (grid > units_max) grid = units_max;
+        if (grid > TC_MAX_PARTS) grid = TC_MAX_PARTS;
+        if (p->batch > TC_PLAN_SMEM_MAX_B && grid > units_max) grid = units_max;
         e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, plan.ctas_per_sm, s);
     } else {
         const int occ = split_simt_ctas_per_sm(a, p->dtype);

@@ -12,8 +12,16 @@
 // the 8 warp sums are then added in warp order. The order is fixed, so results are
 // deterministic. The result is rounded to nearest even into the output dtype.
 //
+// Extra slots. The tensor kernel cuts the 64-token tiles of all units (order b, g, j) into P
+// equal parts, part c = tiles [floor(c T / P), floor((c + 1) T / P)). A part that starts inside
+// a split (not on its first tile) computed that split's partial over its own tiles only and left
+// it in extra slot c, in the phi frame or, if recomputed, in its own max frame. Partials of
+// disjoint token sets of one split add up like those of different splits, so the combine adds
+// each extra slot in with the same weights, and ORs its flag byte into the split's flag byte.
+//
 // Launched as a programmatic dependent of the split kernel: it may start while the split kernel
-// finishes, and waits (griddepcontrol.wait) before touching the partials.
+// finishes, and waits (griddepcontrol.wait) before touching the partials. It lets the kernel
+// after it launch early in turn (the next call's split kernel is a programmatic dependent too).
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -43,12 +51,43 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
     __shared__ float s_acc[CW][D];
     __shared__ float s_lam[CW];
     __shared__ float s_max[CW];
+    // the next call's split kernel may launch now; it waits for this grid to complete before
+    // it touches global memory
+    grid_launch_dependents();
     grid_dependency_wait();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x;                     // b * Hq + h
+    // the split kernel has finished: its fallback-list counters go back to zero for the next call
+    if (row == 0 && threadIdx.x == 0) {
+        a.hdr[HDR_REDO_COUNT] = 0;
+        a.hdr[HDR_REDO_TAKEN] = 0;
+    }
     const int b = row / a.Hq;
+    const int hh = row - b * a.Hq - (row - b * a.Hq) / a.G * a.G;   // head within its group
     const int n = a.nsplit[b];
+
+    // Parts that may start inside this row's units: the row's kv head owns tiles [W, W + nt).
+    const int P = a.hdr[HDR_PARTS];
+    long long W = 0, tiles = 1;
+    int nt = 0, TS = 1, c_lo = 0, c_hi = -1;
+    if (P > 0 && n > 0) {
+        tiles = a.hdr[HDR_TILES];
+        TS = (a.hdr[HDR_SPLIT] + 63) / 64;
+        nt = a.tstart[b + 1] - a.tstart[b];
+        W = (long long)a.Hkv * a.tstart[b] + (long long)((row - b * a.Hq) / a.G) * nt;
+        c_lo = (int)(((W + 1) * P + tiles - 1) / tiles);   // first part starting after tile W
+        c_hi = (int)(((W + nt) * P - 1) / tiles);           // last part starting before W + nt
+    }
+    // extra slot of part c belongs to split jx of this row, or c left none here
+    auto extra_split = [&](int c) -> int {
+        const long long k = (long long)c * tiles / P - W;
+        if (k <= 0 || k >= nt || k % TS == 0) return -1;
+        return (int)(k / TS);
+    };
+    const float* xm = a.xm + hh;
+    const float* xl = a.xl + hh;
+    const float* xo = a.xo + (long long)hh * D;
     const long long base = (long long)row * a.max_splits;
     const float* m = a.m_part + base;
     const float* l = a.l_part + base;
@@ -58,6 +97,18 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
     // M = max_j m_j over the whole row
     float M = -INFINITY;
     for (int j = threadIdx.x; j < n; j += CT) M = fmaxf(M, m[j]);
+    for (int c = c_lo + threadIdx.x; c <= c_hi; c += CT) {
+        const int jx = extra_split(c);
+        if (jx >= 0) {
+            M = fmaxf(M, xm[(long long)c * a.G]);
+            // the split's flag byte also covers the extra slot's tokens
+            uint8_t* fb = a.flags + (long long)row * a.max_splits + jx;
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(fb);
+            const unsigned sh = (unsigned)(addr & 3u) * 8u;
+            atomicOr(reinterpret_cast<unsigned*>(addr & ~uintptr_t(3)),
+                     (unsigned)a.xf[(long long)c * a.G + hh] << sh);
+        }
+    }
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
     if (lane == 0) s_max[warp] = M;
@@ -101,6 +152,15 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
                 lam = fmaf(w, lv[u], lam);
             }
         }
+    }
+    // extra slots, one part per warp in turn
+    for (int c = c_lo + warp; c <= c_hi; c += CW) {
+        if (extra_split(c) < 0) continue;
+        const float w = frame_weight(xm[(long long)c * a.G], M);
+        const float* oc = xo + (long long)c * a.G * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, oc[e], acc[e]);
+        lam = fmaf(w, xl[(long long)c * a.G], lam);
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];

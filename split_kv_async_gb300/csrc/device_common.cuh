@@ -98,6 +98,7 @@ __device__ __forceinline__ void block_plan(const KernelArgs& a, long long* red, 
         a.hdr[HDR_KERNEL] = a.kernel_id;
         a.hdr[HDR_BATCH] = a.B;
         a.hdr[HDR_MAXSPLITS] = a.max_splits;
+        a.hdr[HDR_PARTS] = 0;                           // whole units only: no extra slots
         if (bad) atomicOr((unsigned*)&a.hdr[HDR_ERR], (unsigned)FDPP_ERRBIT_SEQ_LEN);
     }
     S_out = S;
@@ -291,6 +292,13 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v)
 __device__ __forceinline__ void st_release_gpu(long long* p, long long v)
 {
     asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ long long ld_acquire_gpu(const long long* p)

@@ -19,17 +19,30 @@ enum {
     HDR_ERR = 3,        // sticky FDPP_ERRBIT_* (atomicOr)
     HDR_BATCH = 4,      // B of the last call
     HDR_MAXSPLITS = 5,  // partial slots per row
-    HDR_REDO_COUNT = 8, // fallback list: units pushed (zero at rest)
-    HDR_REDO_TAKEN = 9, // fallback list: units claimed (zero at rest)
-    HDR_DONE = 10,      // CTAs finished (zero at rest)
+    HDR_REDO_COUNT = 8, // fallback list: entries pushed (zeroed by the combine kernel)
+    HDR_REDO_TAKEN = 9, // fallback list: entries claimed (zeroed by the combine kernel);
+                        //   words 8 and 9 are read together as one 8-byte word
+    HDR_PARTS = 11,     // tensor kernel: parts P of the tile-balanced partition (0: none)
+    HDR_TILES = 12,     // tensor kernel: 64-token tiles T of all units together
     HDR_WORDS = 64
 };
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-    size_t header, nsplit, redo, flags, m_part, l_part, o_part, total;
+    size_t header, nsplit, tstart, redo, flags, m_part, l_part, o_part, xf, xm, xl, xo, total;
     int max_splits;
 };
+
+// The tensor kernel cuts the tiles of all units into at most this many equal parts, one per
+// CTA. A part that starts inside a unit leaves that unit's partial of its own tiles in an
+// extra slot (one per part), which the combine adds in.
+constexpr int TC_MAX_PARTS = FDPP_TC_MAX_PARTS;
+// Batches up to this size keep their split plan in the tensor kernel's shared memory (and are
+// cut into parts); larger batches are dealt out to the CTAs as whole units.
+constexpr int TC_PLAN_SMEM_MAX_B = 1024;
+// Fallback list entry: 4 x int64 = {(b + 1) | (g * max_splits + j) << 32,
+// t0 | t1 << 32 (token range of the segment), dest (-1: split slot j, else extra slot), 0}.
+constexpr int REDO_WORDS = 4;
 
 // Everything a kernel of this library needs about one call. Plain pointers and sizes.
 struct KernelArgs {
@@ -41,11 +54,16 @@ struct KernelArgs {
     void* out;
     int32_t* hdr;
     int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
-    long long* redo;              // fallback list [B*Hkv*max_splits] of (b+1, g*max_splits+j)
+    int32_t* tstart;              // [B + 1] tile prefix of the sequences (tensor kernel, CTA 0)
+    long long* redo;              // fallback list, REDO_WORDS per entry (tensor kernel)
     uint8_t* flags;               // [B][Hq][max_splits]
     float* m_part;                // [B][Hq][max_splits]
     float* l_part;                // [B][Hq][max_splits]
     float* o_part;                // [B][Hq][max_splits][D]
+    uint8_t* xf;                  // extra slots [TC_MAX_PARTS][G]: flags,
+    float* xm;                    //   m,
+    float* xl;                    //   l,
+    float* xo;                    //   o [TC_MAX_PARTS][G][D]
     int B, Hq, Hkv, G, D;
     int max_seq_len, block_size, max_blocks, num_blocks;
     int split_req, max_splits, num_sms;

@@ -5,29 +5,34 @@
 // (sequence b, kv head g, split j) and the G query heads that share kv head g:
 //     s_t = scale <q_h, k_t>, p_t = exp(s_t - phi), l = sum p_t, o = sum p_t v_t    (fast pass)
 // against the unified max phi, with no communication between splits; every score is tested
-// against lo <= s - phi <= hi. A unit with a head outside the window goes on a device-wide list
-// and is streamed again with the ordinary online softmax (running max) by whichever CTA is free
-// first; its flagged heads' partials are replaced by ones in their own max frame.
+// against lo <= s - phi <= hi. A segment (see below) with a head outside the window goes on a
+// device-wide list and is streamed again with the ordinary online softmax (running max) by
+// whichever CTA is free first; its flagged heads' partials are replaced by ones in their own
+// max frame.
 //
-// How. One CTA = 1 producer warp + 4 consumer warps, persistent over an equal share of units.
-//   producer  plans the splits in shared memory (prefix of n_b = ceil(L_b / S)), then for each
-//             unit writes a small header into a Q-ring slot and bulk-copies the unit's G query
-//             rows there (this slot is also how consumers learn which unit comes next), and
+// How. One CTA = 1 producer warp + 4 consumer warps, persistent over an equal share of tiles.
+//   work      the 64-token tiles of all units, in unit order (b, g, j), are cut into P equal
+//             parts, one per CTA, so every CTA streams the same bytes whatever the unit count
+//             (whole units dealt round-robin would leave a last wave of few CTAs). A part is a
+//             run of segments, each the part's tiles of one unit. A segment that is not the
+//             unit's first writes its partial to the part's extra slot; combine.cu adds it in.
+//   producer  plans the splits in shared memory (prefixes of n_b = ceil(L_b / S) and of the
+//             tiles per sequence), then for each segment writes a small header into a Q-ring
+//             slot and bulk-copies the unit's G query rows there (this slot is also how
+//             consumers learn which segment comes next), and
 //             streams 64-token K and V tiles of head g with 3-D TMA loads (128-byte swizzle)
 //             into a ring of `nstage` stages (mbarriers: full = bytes landed, empty = the four
 //             consumer warps released the stage). A paged cache is read one block per box,
-//             block-table entries fetched 32 at a time by the warp. After its own units it
-//             claims fallback units from the list until it is empty, then sends a sentinel.
-//   consumers each own 16 tokens of a tile:
-//             S[16 x 16] = Q K^T     mma.m16n8k16 bf16 -> fp32; rows 0..G-1 = the G heads, so
-//                                    each K byte read from HBM feeds all G heads once;
+//             block-table entries fetched 32 at a time by the warp. After its own part it
+//             claims fallback segments from the list until it is empty, then sends a sentinel.
+//   consumers each own 16 tokens of a tile and compute it transposed (tokens on M, heads on N):
+//             S^T = K Q^T            mma.m16n8k16 bf16 -> fp32, columns = the G heads, so each
+//                                    K byte read from HBM feeds all G heads once;
 //             P = exp(S - phi), window test;
-//             O += [P_hi ; P_lo] V   P split into bf16 hi + lo parts stacked in the 16 rows of
-//                                    the A tile (G <= 8): P.V keeps ~16 mantissa bits; head h's
-//                                    output is row h + row h+8.
+//             O^T += V^T P^T         P carried as bf16 hi + lo parts (~16 mantissa bits).
 //             The four warps merge their fp32 partials through shared memory (a plain sum in
 //             the phi frame) and write o, l, m and the flag byte of each head.
-// When a CTA starts its last own unit it allows the dependent combine launch to begin
+// When a CTA starts its last own segment it allows the dependent combine launch to begin
 // (programmatic dependent launch), so that launch overlaps the tail of this one.
 // Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT and the CTA stops.
 // (A fused last-arriver combine was measured here and removed: under full HBM load its
@@ -45,7 +50,7 @@ constexpr int TPW = 16;                 // tokens per consumer warp and tile
 constexpr int TILE = NCW * TPW;         // tokens per tile
 constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr int NCT = NCW * 32;           // consumer threads
-constexpr int PLAN_SMEM_MAX_B = 1024;   // batches up to this size keep their plan in smem
+constexpr int PLAN_SMEM_MAX_B = TC_PLAN_SMEM_MAX_B;
 constexpr int QHDR_BYTES = 64;          // unit header at the start of each Q-ring slot
 static_assert(TILE == TC_TILE_TOKENS, "tile height is part of the tensor-map contract");
 // the merge scratch (4 warps x G <= 8 rows x (d + 8) floats, plus l, m, flags) fits in a stage
@@ -55,7 +60,7 @@ static_assert(NCW * 8 * (128 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 128 * 2, "
 // unit kinds carried in the Q-ring header
 enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
 // header words
-enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_NB, H_F0, H_F1, H_MASK, H_WORDS };
+enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_WORDS };
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge
 // scratch of a unit lives in the stage of the unit's last tile (offsets scr_* relative to that
@@ -77,7 +82,7 @@ struct TcLayout {
         scr_m = scr_l + NCW * G * 4;
         scr_f = scr_m + NCW * G * 4;
         plan = qring + 2 * qslot_bytes;
-        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? B : 0) + 1;
+        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 3 * B + 2 : 0) + 1;
         bars = round_up(plan + plan_ints * 4, 8);
         misc = bars + (2 * nstage + 6) * 8;
         total = misc + 16;
@@ -138,13 +143,16 @@ struct Producer {
     uint32_t sbase;
     uint8_t* smp;              // generic pointer to the same shared-memory base
     volatile int* misc;
-    int* plan;                 // smem prefix of n_b (B <= PLAN_SMEM_MAX_B), else unused
-    int S;
+    int* plan;                 // smem (B <= PLAN_SMEM_MAX_B): prefix of n_b [B + 1],
+    int* tplan;                //   prefix of the tiles of each sequence [B + 1],
+    int* lplan;                //   clamped L_b [B]
+    int S = 0, TS = 0;         // split length, tiles of a full split
     uint32_t stage = 0, phase = 0, qiter = 0;
     bool bad_block = false;
 
-    // Split plan: S, n_b prefix in smem (or a global walk for large batches), unit count.
-    __device__ __forceinline__ int make_plan()
+    // Split plan: S, the n_b and tile prefixes in smem (or a global walk for large batches),
+    // the unit count; T = 64-token tiles of all units.
+    __device__ __forceinline__ int make_plan(long long& T)
     {
         const KernelArgs& A = *a;
         const int lane = threadIdx.x & 31;
@@ -156,34 +164,48 @@ struct Producer {
             bad |= (L < 0 || L > A.max_seq_len);
             const int Lc = clamp_len(L, A.max_seq_len);
             sum += Lc;
-            if (in_smem) plan[b] = Lc;
+            if (in_smem) lplan[b] = Lc;
         }
         sum = warp_sum(sum);
         bad = __any_sync(0xffffffffu, bad);
         S = auto_split_len(sum, A);
+        TS = ceil_div_i(S, TILE);
         int run = 0;
+        long long trun = 0;
+        __syncwarp();
         for (int base = 0; base < A.B; base += 32) {
             const int b = base + lane;
             int nb = 0;
+            long long nt = 0;
             if (b < A.B) {
-                const int Lc = in_smem ? plan[b] : clamp_len(A.seq_lens[b], A.max_seq_len);
+                const int Lc = in_smem ? lplan[b] : clamp_len(A.seq_lens[b], A.max_seq_len);
                 nb = min(ceil_div_i(Lc, S), A.max_splits);
+                if (nb > 0)
+                    nt = (long long)(nb - 1) * TS + ceil_div_i(min(Lc - (nb - 1) * S, S), TILE);
             }
             int incl = nb;
+            long long tincl = nt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+                const long long ty = __shfl_up_sync(0xffffffffu, tincl, o);
+                if (lane >= o) { incl += y; tincl += ty; }
             }
             __syncwarp();
             if (b < A.B) {
-                if (in_smem) plan[b] = run + incl - nb;
-                if (blockIdx.x == 0) A.nsplit[b] = nb;
+                const int tfirst = (int)(trun + tincl - nt);
+                if (in_smem) { plan[b] = run + incl - nb; tplan[b] = tfirst; }
+                if (blockIdx.x == 0) { A.nsplit[b] = nb; A.tstart[b] = tfirst; }
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
+            trun += __shfl_sync(0xffffffffu, tincl, 31);
         }
-        if (in_smem && lane == 0) plan[A.B] = run;
+        if (lane == 0) {
+            if (in_smem) { plan[A.B] = run; tplan[A.B] = (int)trun; }
+            if (blockIdx.x == 0) A.tstart[A.B] = (int)trun;
+        }
         __syncwarp();
+        T = trun * A.Hkv;
         const int n_units = run * A.Hkv;
         if (blockIdx.x == 0) {
             if (lane == 0) {
@@ -236,26 +258,27 @@ struct Producer {
         }
     }
 
-    // Emits one unit: header + Q rows into the Q ring, then its K/V tiles into the stage ring,
-    // prefetching into L2 the tile `pf` places ahead (in this unit, or in `nx`, the next one).
+    // Emits one segment: tokens [t0, t1) of unit (b, g, j), whose partial goes to `dest` (-1:
+    // the split's own slot, else extra slot `dest`). Header + Q rows go into the Q ring, then
+    // the K/V tiles into the stage ring, prefetching into L2 the tile `pf` places ahead (in this
+    // segment, or in `nx`, the next one).
     // pre_base/pre_ent: a block-table window (entries pre_base + lane) loaded ahead of time.
     template <int D, bool PAGED>
-    __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int nb, int L,
-                                         const int (&hw)[3], int pre_base = -(1 << 30),
+    __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int t0, int t1, int L,
+                                         int dest, const int (&hw)[3], int pre_base = -(1 << 30),
                                          int pre_ent = -1, const NextUnit* nx = nullptr,
                                          bool first = false)
     {
         constexpr int HALVES = D / 64;
         const KernelArgs& A = *a;
         const int lane = threadIdx.x & 31;
-        const int t0 = j * S, t1 = min(t0 + S, L);
         const uint32_t qs = qiter & 1u;
         if (!ring_wait(rg.qempty + 8 * qs, ((qiter >> 1) & 1u) ^ 1u, misc, A)) return false;
         const uint32_t slot = sbase + lay->qring + qs * lay->qslot_bytes;
         if (lane == 0) {
             int* hdr = reinterpret_cast<int*>(smp + lay->qring + qs * lay->qslot_bytes);
             hdr[H_KIND] = kind; hdr[H_B] = b; hdr[H_G] = g; hdr[H_J] = j;
-            hdr[H_T0] = t0; hdr[H_T1] = t1; hdr[H_NB] = nb;
+            hdr[H_T0] = t0; hdr[H_T1] = t1; hdr[H_DEST] = dest;
             hdr[H_F0] = hw[0]; hdr[H_F1] = hw[1]; hdr[H_MASK] = hw[2];
             if (kind == KIND_END) {
                 mbar_arrive(rg.qfull + 8 * qs);
@@ -278,12 +301,12 @@ struct Producer {
         const int nblk_seq = PAGED ? ceil_div_i(L, bs) : 0;
         constexpr int PER_BLK = 2 * HALVES;        // boxes per block: K and V, each half
         const int pf = A.pf_tiles;
-        if (PAGED && pf > 0 && win_base == -(1 << 30)) {   // the unit's first window, now
+        if (PAGED && pf > 0 && win_base == -(1 << 30)) {   // the segment's first window, now
             win_base = t0 / bs;
             const int lb = win_base + lane;
             ent = (lb < nblk_seq) ? __ldg(A.block_table + (long long)b * A.max_blocks + lb) : -1;
         }
-        if (first && pf > 0)                       // the CTA's first unit: nothing was prefetched
+        if (first && pf > 0)                       // the CTA's first segment: nothing prefetched
             for (int ti = 1; ti <= pf && ti < ntiles; ++ti)
                 prefetch_tile<D, PAGED>(b, g, t0 + ti * TILE, t1, win_base, ent);
         for (int i = 0; i < ntiles; ++i) {
@@ -345,76 +368,119 @@ struct Producer {
         return true;
     }
 
+    // The first block-table window (32 entries from the block holding token t0) of a segment
+    // that will be emitted next, loaded one segment ahead.
+    __device__ __forceinline__ int window_entry(int b, int t0, int L) const
+    {
+        const KernelArgs& A = *a;
+        const int lb = t0 / A.block_size + (int)(threadIdx.x & 31);
+        return lb < ceil_div_i(L, A.block_size) ? __ldg(A.block_table + (long long)b * A.max_blocks + lb)
+                                                : -1;
+    }
+
+    // Own work, tile-balanced: the T tiles of all units (in unit order b, g, j) are cut into P
+    // equal parts and CTA c streams part c, [c T / P, (c + 1) T / P). A part that starts inside
+    // a unit writes that unit's partial of its tiles to extra slot c; every other segment
+    // writes the split's own slot.
+    template <int D, bool PAGED>
+    __device__ __forceinline__ bool run_parts(long long T, int P, bool& had_own)
+    {
+        const KernelArgs& A = *a;
+        const int c = blockIdx.x;
+        if (c >= P) return true;
+        const long long tb = (long long)c * T / P, te = (long long)(c + 1) * T / P;
+        const int zero3[3] = {0, 0, 0};
+        struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
+        int cb = 0;
+        auto seg_at = [&](long long t, Seg& s) {
+            while ((long long)A.Hkv * tplan[cb + 1] <= t) ++cb;
+            const int ntb = tplan[cb + 1] - tplan[cb];
+            const int r = (int)(t - (long long)A.Hkv * tplan[cb]);
+            s.b = cb;
+            s.g = r / ntb;
+            const int k = r - s.g * ntb;             // tile of sequence cb, head s.g
+            s.j = k / TS;
+            const int ilo = k - s.j * TS;
+            const int nb = plan[cb + 1] - plan[cb];
+            s.L = lplan[cb];
+            const int nu = (s.j < nb - 1) ? TS : ntb - (nb - 1) * TS;
+            const int ihi = (int)min((long long)nu, ilo + (te - t));
+            s.t0 = s.j * S + ilo * TILE;
+            s.t1 = min(s.j * S + ihi * TILE, min((s.j + 1) * S, s.L));
+            s.ntile = ihi - ilo;
+            s.dest = ilo == 0 ? -1 : c;
+        };
+        Seg cur, nxt;
+        long long t = tb;
+        seg_at(t, cur);
+        int cur_ent = PAGED ? window_entry(cur.b, cur.t0, cur.L) : -1;
+        for (;;) {
+            const long long tn = t + cur.ntile;
+            const bool last = tn >= te;
+            NextUnit nx{0, 0, 0, 0, 0, -(1 << 30), -1};
+            int nxt_ent = -1;
+            if (!last) {
+                seg_at(tn, nxt);
+                if (PAGED) nxt_ent = window_entry(nxt.b, nxt.t0, nxt.L);
+                nx = NextUnit{1, nxt.b, nxt.g, nxt.t0, nxt.t1,
+                              PAGED ? nxt.t0 / A.block_size : -(1 << 30), nxt_ent};
+            }
+            if (last) grid_launch_dependents();
+            if (!emit<D, PAGED>(last ? KIND_LAST_OWN : KIND_OWN, cur.b, cur.g, cur.j, cur.t0, cur.t1,
+                                cur.L, cur.dest, zero3,
+                                PAGED ? cur.t0 / A.block_size : -(1 << 30), cur_ent, &nx, !had_own))
+                return false;
+            had_own = true;
+            if (last) break;
+            t = tn;
+            cur = nxt;
+            cur_ent = nxt_ent;
+        }
+        return true;
+    }
+
+    // Own work for batches whose plan is not kept in shared memory: whole units
+    // u = blockIdx.x + k * gridDim.x, found by a walk over seq_lens.
+    template <int D, bool PAGED>
+    __device__ __forceinline__ bool run_units(int n_units, bool& had_own)
+    {
+        const KernelArgs& A = *a;
+        const int zero3[3] = {0, 0, 0};
+        UnitCursor cur;
+        cur.reset();
+        for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+            int b, g, j, L;
+            cur.seek(A, S, u, b, g, j, L);
+            const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
+            if (kind == KIND_LAST_OWN) grid_launch_dependents();
+            const int t0 = j * S, t1 = min(t0 + S, L);
+            if (!emit<D, PAGED>(kind, b, g, j, t0, t1, L, -1, zero3, -(1 << 30), -1, nullptr, !had_own))
+                return false;
+            had_own = true;
+        }
+        return true;
+    }
+
     template <int D, bool PAGED>
     __device__ __forceinline__ void run()
     {
         const KernelArgs& A = *a;
         const int lane = threadIdx.x & 31;
-        const int n_units = make_plan();
+        long long T = 0;
+        const int n_units = make_plan(T);
         const bool in_smem = A.B <= PLAN_SMEM_MAX_B;
-        const int zero3[3] = {0, 0, 0};
-
-        // own units: u = blockIdx.x + k * gridDim.x
-        UnitCursor cur;
-        cur.reset();
-        int b = 0, bn = 0;
-        bool had_own = false;
-        // paged: the first block-table window of the next own unit is loaded one unit ahead
-        int pf_base = -(1 << 30), pf_ent = -1, pf_b = -1;
-        auto locate = [&](long long uu, int& bb, int& gg, int& jj, int& nbb) {
-            while ((long long)A.Hkv * plan[bb + 1] <= uu) ++bb;
-            nbb = plan[bb + 1] - plan[bb];
-            const long long r = uu - (long long)A.Hkv * plan[bb];
-            gg = (int)(r / nbb);
-            jj = (int)(r % nbb);
-        };
-        for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-            int g, j, nb, L;
-            if (in_smem) {
-                locate(u, b, g, j, nb);
-                L = clamp_len(A.seq_lens[b], A.max_seq_len);
-            } else {
-                cur.seek(A, S, u, b, g, j, L);
-                nb = cur.nb;
-            }
-            const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
-            if (kind == KIND_LAST_OWN) grid_launch_dependents();
-            int use_base = -(1 << 30), use_ent = -1;
-            NextUnit nx{0, 0, 0, 0, 0, -(1 << 30), -1};
-            if (PAGED) {
-                const int lb0 = j * S / A.block_size;
-                if (pf_base == lb0 && pf_b == b) { use_base = pf_base; use_ent = pf_ent; }
-                pf_base = -(1 << 30);
-            }
-            const long long un = u + gridDim.x;
-            if (un < n_units && in_smem) {
-                // the next own unit: located now, and (paged) its first block-table window
-                // loaded one unit ahead
-                int gn, jn, nbn;
-                bn = max(bn, b);
-                locate(un, bn, gn, jn, nbn);
-                const int Ln = clamp_len(A.seq_lens[bn], A.max_seq_len);
-                nx.valid = 1;
-                nx.b = bn;
-                nx.g = gn;
-                nx.t0 = jn * S;
-                nx.t1 = min(nx.t0 + S, Ln);
-                if (PAGED) {
-                    const int lbn = jn * S / A.block_size + lane;
-                    pf_base = jn * S / A.block_size;
-                    pf_b = bn;
-                    pf_ent = (lbn < ceil_div_i(Ln, A.block_size))
-                                 ? __ldg(A.block_table + (long long)bn * A.max_blocks + lbn) : -1;
-                    nx.win_base = pf_base;
-                    nx.ent = pf_ent;
-                }
-            }
-            if (!emit<D, PAGED>(kind, b, g, j, nb, L, zero3, use_base, use_ent, &nx, !had_own)) return;
-            had_own = true;
+        const int P = (in_smem && T > 0 && T < (1ll << 31))
+                          ? (int)min(min((long long)gridDim.x, T), (long long)TC_MAX_PARTS) : 0;
+        if (blockIdx.x == 0 && lane == 0) {
+            A.hdr[HDR_PARTS] = P;
+            A.hdr[HDR_TILES] = P > 0 ? (int)T : 0;
         }
+        bool had_own = false;
+        const bool ok = P > 0 ? run_parts<D, PAGED>(T, P, had_own) : run_units<D, PAGED>(n_units, had_own);
+        if (!ok) return;
 
         if (A.mode == FDPP_MODE_NORMAL) {
-            // the consumers push this CTA's flagged units before they report the own units done
+            // the consumers push this CTA's flagged segments before they report the own work done
             if (had_own && !ring_wait(rg.own_done, 0u, misc, A)) return;
             int* cnt = &A.hdr[HDR_REDO_COUNT];
             int* taken = &A.hdr[HDR_REDO_TAKEN];
@@ -423,8 +489,11 @@ struct Producer {
                 bool got = false, stop = false;
                 if (lane == 0) {
                     for (;;) {
-                        const int t = atomicAdd(taken, 0);
-                        const int c = atomicAdd(cnt, 0);
+                        // count (word HDR_REDO_COUNT) and taken (the next word) in one read
+                        const unsigned long long both = ld_relaxed_gpu_u64(
+                            reinterpret_cast<const unsigned long long*>(cnt));
+                        const int c = (int)(unsigned)(both & 0xffffffffull);
+                        const int t = (int)(unsigned)(both >> 32);
                         if (t >= c) { stop = true; break; }
                         if (atomicCAS(taken, t, t + 1) == t) { k = t; got = true; break; }
                     }
@@ -434,15 +503,22 @@ struct Producer {
                 got = __shfl_sync(0xffffffffu, got, 0);
                 k = __shfl_sync(0xffffffffu, k, 0);
                 if (!got) continue;
-                // the pusher reserved slot k before storing it: read it with a bounded wait
-                long long e = 0;
+                // the pusher reserved entry k before storing it: read it with a bounded wait
+                long long e = 0, rng = 0, dst = 0;
                 if (lane == 0) {
+                    long long* ent = A.redo + (long long)k * REDO_WORDS;
                     const uint64_t t0 = global_ns();
-                    while ((e = ld_acquire_gpu(A.redo + k)) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
+                    while ((e = ld_acquire_gpu(ent)) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
                     }
-                    if (e != 0) A.redo[k] = 0;         // leave the list zeroed for the next call
+                    if (e != 0) {
+                        rng = __ldcg(ent + 1);
+                        dst = __ldcg(ent + 2);
+                        ent[0] = 0;                    // leave the list zeroed for the next call
+                    }
                 }
                 e = __shfl_sync(0xffffffffu, e, 0);
+                rng = __shfl_sync(0xffffffffu, rng, 0);
+                dst = __shfl_sync(0xffffffffu, dst, 0);
                 if (e == 0) {
                     if (lane == 0) { misc[0] = 1; set_error(A, FDPP_ERRBIT_TIMEOUT); }
                     return;
@@ -450,13 +526,14 @@ struct Producer {
                 const int rb = (int)(e & 0xffffffffll) - 1;
                 const int gj = (int)(e >> 32);
                 const int rg_ = gj / A.max_splits, rj = gj % A.max_splits;
+                const int st0 = (int)(rng & 0xffffffffll), st1 = (int)(rng >> 32);
+                const int dest = (int)dst;
                 const int L = clamp_len(A.seq_lens[rb], A.max_seq_len);
-                const int nb = min(ceil_div_i(L, S), A.max_splits);
-                // flag bytes of the G heads (written by the pushing CTA before its push)
+                // flag bytes of the segment's G heads (written by the pushing CTA before its push)
                 int hw[3] = {0, 0, 0};
                 if (lane < A.G) {
-                    const unsigned f = __ldcg(A.flags + row_slot(A, rb, rg_ * A.G + lane, rj));
-                    hw[0] = 0; hw[1] = 0;
+                    const unsigned f = dest < 0 ? __ldcg(A.flags + row_slot(A, rb, rg_ * A.G + lane, rj))
+                                                : __ldcg(A.xf + (long long)dest * A.G + lane);
                     const unsigned sh = (unsigned)(lane & 3) * 8u;
                     const unsigned w0 = lane < 4 ? (f << sh) : 0u;
                     const unsigned w1 = lane >= 4 ? (f << sh) : 0u;
@@ -469,11 +546,11 @@ struct Producer {
                     hw[1] |= __shfl_xor_sync(0xffffffffu, hw[1], o);
                     hw[2] |= __shfl_xor_sync(0xffffffffu, hw[2], o);
                 }
-                if (!emit<D, PAGED>(KIND_REDO, rb, rg_, rj, nb, L, hw)) return;
+                if (!emit<D, PAGED>(KIND_REDO, rb, rg_, rj, st0, st1, L, dest, hw)) return;
             }
         }
         const int zeros[3] = {0, 0, 0};
-        emit<D, PAGED>(KIND_END, 0, 0, 0, 0, 0, zeros);
+        emit<D, PAGED>(KIND_END, 0, 0, 0, 0, 0, 0, -1, zeros);
     }
 };
 
@@ -514,7 +591,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const int kind = hdr[H_KIND];
         if (kind == KIND_END) return;
         const int b = hdr[H_B], g = hdr[H_G], j = hdr[H_J];
-        const int t0 = hdr[H_T0], t1 = hdr[H_T1];
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], dest = hdr[H_DEST];
         const unsigned fw0 = (unsigned)hdr[H_F0], fw1 = (unsigned)hdr[H_F1];
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
         const bool redo = kind == KIND_REDO;
@@ -693,36 +770,67 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         }
         if (!consumer_sync(rg, cpar, misc, a)) return;
         const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
-        for (int idx = ctid; idx < a.G * D; idx += NCT) {
-            const int hh = idx / D, d = idx - hh * D;
-            if (!((write_mask >> hh) & 1u)) continue;
-            float M = scr_m[hh];
+        // The four warp partials of each head, summed in warp order. In the phi frame every
+        // warp's m is phi and each weight is exactly 1, so the sum needs no exponentials.
+        // Destination: the split's own slot (heads max_splits slots apart) or the extra slot of
+        // a part that began inside the unit (heads adjacent).
+        float* o_dst = dest < 0 ? a.o_part + row_slot(a, b, g * a.G, j) * D
+                                : a.xo + (long long)dest * a.G * D;
+        const long long o_hstride = dest < 0 ? (long long)a.max_splits * D : (long long)D;
+        {
+            constexpr int HPP = NCT / D;           // heads per pass of the 128 threads
+            const int d = ctid % D, hsub = ctid / D;
 #pragma unroll
-            for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
-            float acc = 0.f;
+            for (int k = 0; k < TC_MAX_GROUP / HPP; ++k) {
+                const int hh = k * HPP + hsub;
+                if (hh < a.G && ((write_mask >> hh) & 1u)) {
+                    float acc = 0.f;
+                    if (!online) {
 #pragma unroll
-            for (int w = 0; w < NCW; ++w)
-                acc = fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_o[(w * a.G + hh) * lay.scr_row + d], acc);
-            a.o_part[row_slot(a, b, g * a.G + hh, j) * D + d] = acc;
+                        for (int w = 0; w < NCW; ++w) acc += scr_o[(w * a.G + hh) * lay.scr_row + d];
+                    } else {
+                        float M = scr_m[hh];
+#pragma unroll
+                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
+#pragma unroll
+                        for (int w = 0; w < NCW; ++w)
+                            acc = fmaf(frame_weight(scr_m[w * a.G + hh], M),
+                                       scr_o[(w * a.G + hh) * lay.scr_row + d], acc);
+                    }
+                    o_dst[hh * o_hstride + d] = acc;
+                }
+            }
         }
-        unsigned unit_out = 0u;                   // heads of this unit outside the window
-        for (int hh = 0; hh < a.G; ++hh) {
-            unsigned f = scr_f[hh];
-            for (int w = 1; w < NCW; ++w) f |= scr_f[w * a.G + hh];
-            if (f & FDPP_FLAG_OUT) unit_out |= 1u << hh;
-            if (ctid == hh && ((write_mask >> hh) & 1u)) {
-                float M = scr_m[hh];
+        // l, m and the flag byte: lane hh of warp 0 for head hh
+        unsigned unit_out = 0u;                   // heads of this segment outside the window
+        if (warp == 0) {
+            const int hh = lane;
+            unsigned f = 0u;
+            float M = 0.f, lam = 0.f;
+            if (hh < a.G) {
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) f |= scr_f[w * a.G + hh];
+                M = scr_m[hh];
+#pragma unroll
                 for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
-                float lam = 0.f;
-                for (int w = 0; w < NCW; ++w) lam = fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_l[w * a.G + hh], lam);
-                const long long r = row_slot(a, b, g * a.G + hh, j);
-                a.l_part[r] = lam;
-                a.m_part[r] = M;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w)
+                    lam = online ? fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_l[w * a.G + hh], lam)
+                                 : lam + scr_l[w * a.G + hh];
+            }
+            unit_out = __ballot_sync(0xffffffffu, hh < a.G && (f & FDPP_FLAG_OUT));
+            if (hh < a.G && ((write_mask >> hh) & 1u)) {
+                const long long r = dest < 0 ? row_slot(a, b, g * a.G + hh, j) : (long long)dest * a.G + hh;
+                float* lp = dest < 0 ? a.l_part : a.xl;
+                float* mp = dest < 0 ? a.m_part : a.xm;
+                uint8_t* fp = dest < 0 ? a.flags : a.xf;
+                lp[r] = lam;
+                mp[r] = M;
                 if (redo) {
                     const unsigned f0 = ((hh < 4 ? fw0 : fw1) >> ((hh & 3) * 8)) & 0xffu;
-                    a.flags[r] = (uint8_t)(f0 | FDPP_FLAG_RECOMPUTED);
+                    fp[r] = (uint8_t)(f0 | FDPP_FLAG_RECOMPUTED);
                 } else {
-                    a.flags[r] = (uint8_t)(f | (online ? FDPP_FLAG_RECOMPUTED : 0u));
+                    fp[r] = (uint8_t)(f | (online ? FDPP_FLAG_RECOMPUTED : 0u));
                 }
             }
         }
@@ -732,13 +840,16 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         fence_proxy_async_smem();
         if (!consumer_sync(rg, cpar, misc, a)) return;
         if (lane == 0) mbar_arrive(rg.empty + 8 * held);
-        // ---- a unit with a head outside the window goes on the device-wide fallback list ----
+        // ---- a segment with a head outside the window goes on the device-wide fallback list ----
         if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
-            // thread 0 publishes with a release store
+            // thread 0 fills the entry, then publishes its first word with a release store
             if (ctid == 0) {
                 const int k = atomicAdd(&a.hdr[HDR_REDO_COUNT], 1);
-                st_release_gpu(a.redo + k, ((long long)(g * a.max_splits + j) << 32) |
-                                               (long long)(unsigned)(b + 1));
+                long long* ent = a.redo + (long long)k * REDO_WORDS;
+                ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
+                ent[2] = dest;
+                st_release_gpu(ent, ((long long)(g * a.max_splits + j) << 32) |
+                                        (long long)(unsigned)(b + 1));
             }
         }
         if (ctid == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
@@ -787,8 +898,12 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent: no global memory is read or written before the
+    // previous kernel on the stream has completed
+    grid_dependency_wait();
 
-    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, reinterpret_cast<int*>(sm + lay.plan), 0};
+    int* plan = reinterpret_cast<int*>(sm + lay.plan);
+    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1), plan + 2 * (a.B + 1)};
     if (warp == NCW) {
         if (lane == 0) {
             prefetch_tensormap(&tmK);
@@ -817,13 +932,6 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
                 }
             }
         }
-        // the last CTA to finish leaves the fallback counters at zero for the next call
-        __threadfence();
-        if (atomicAdd(&a.hdr[HDR_DONE], 1) == (int)gridDim.x - 1) {
-            a.hdr[HDR_REDO_COUNT] = 0;
-            a.hdr[HDR_REDO_TAKEN] = 0;
-            a.hdr[HDR_DONE] = 0;
-        }
     }
 }
 
@@ -834,7 +942,21 @@ cudaError_t launch_t(const KernelArgs& a, const CUtensorMap& tk, const CUtensorM
     auto kern = ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2> : split_tc_kernel<D, PAGED, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NTHREADS, smem, s>>>(tk, tv, a);
+    // a programmatic dependent of the previous kernel on the stream (the previous call's combine
+    // lets it launch early): its CTAs start while that kernel finishes and wait for it to
+    // complete before touching global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -42,6 +42,15 @@ def test_params_struct_matches_header_field_order():
     assert names == [n for n, _ in F.fdpp_diag._fields_]
 
 
+def test_binding_constants_match_header_defines():
+    text = open(HEADER).read()
+    found = re.findall(r"#define (FDPP_\w+) \(?(\d+)u?(?: << (\d+))?", text)
+    defines = {name: int(v) << int(sh or 0) for name, v, sh in found}
+    for name in ("FDPP_AUTO_UNITS_PER_SM", "FDPP_AUTO_GRANULE", "FDPP_AUTO_MIN_SPLIT",
+                 "FDPP_TC_MAX_PARTS", "FDPP_NOALLOC_WORKSPACE_BYTES"):
+        assert getattr(F, name) == defines[name], name
+
+
 def _gqa_params(**kw):
     base = dict(batch=8, num_q_heads=32, num_kv_heads=8, head_dim=128, dtype=F.FDPP_BF16,
                 max_seq_len=4096, scale=float(np.float32(128 ** -0.5)), split_len=512)
@@ -53,8 +62,9 @@ def test_max_splits_and_workspace_size():
     p = _gqa_params()
     assert F.fdpp_max_splits(p) == 8
     ws = F.fdpp_workspace_size(p)
-    slots = 8 * 32 * 8
-    # partials o (d floats), l, m and a flag byte per slot, plus header, plan and fallback list
+    # partials o (d floats), l, m and a flag byte per split slot and per extra slot (G = 4 rows
+    # for each of FDPP_TC_MAX_PARTS parts), plus header, plan and fallback list
+    slots = 8 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 4
     assert slots * (128 * 4 + 4 + 4 + 1) <= ws <= slots * (128 * 4 + 4 + 4 + 1) + 64 * 1024
     assert ws % 256 == 0
     p0 = _gqa_params(split_len=0)

@@ -151,13 +151,13 @@ def test_runs_are_bit_identical():
         np.testing.assert_array_equal(a, b)
 
 
-def _stress_inputs(batch=8, seq_len=1024, split_len=256, frac=0.05, seed_offset=0):
+def _stress_inputs(batch=8, seq_len=1024, split_len=256, frac=0.05, seed_offset=0, **kw):
     """Hot-key workload whose scores all sit at least 1e-3 from a window edge (the decision
     replay compares booleans; a score closer than that could round either way in fp32).
     Seeds advance deterministically until the margin holds."""
     for k in range(16):
         wl = W.STRESS.replace(batch=batch, seq_len=seq_len, split_len=split_len,
-                              stress_frac=frac, seed=W.STRESS.seed + 101 * (seed_offset + k))
+                              stress_frac=frac, seed=W.STRESS.seed + 101 * (seed_offset + k), **kw)
         inp = W.generate(wl)
         ms = -(-seq_len // split_len)
         flags, margin = H.oracle_flags(inp, split_len, ms)
@@ -183,10 +183,43 @@ def test_fallback_decisions_and_results(kernel):
     H.assert_parity(got, ref, f"stress {kernel}")
 
 
+def _check_fallback(inp, oflags, what):
+    dinp = H.DeviceInputs(inp)
+    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    np.testing.assert_array_equal(flags & 0x0F, oflags)
+    hot_rows = (oflags & oracle.FLAG_OUT) != 0
+    assert hot_rows.sum() >= len(inp.hot)
+    np.testing.assert_array_equal((flags & F.FDPP_FLAG_RECOMPUTED) != 0, hot_rows)
+    assert diag["error_bits"] == 0
+    H.assert_parity(got, H.oracle_out(inp), what)
+    return diag
+
+
+def test_one_split_spread_over_many_parts():
+    """The tensor kernel cuts the tiles of all units into equal parts, one per CTA. One split of
+    64 tiles becomes 64 one-tile parts: 63 of them leave their share in an extra slot that the
+    combine adds in, and the hot key's share is recomputed from its own extra slot. The flag
+    byte of the split is the OR over all its parts."""
+    inp, oflags = _stress_inputs(batch=1, seq_len=4096, split_len=4096, frac=1.0,
+                                 num_q_heads=4, num_kv_heads=1)
+    assert inp.hot and inp.hot[0][3] >= 64           # the hot key is not in the first part
+    diag = _check_fallback(inp, oflags, "one split over 64 parts")
+    assert diag["n_units"] == 1
+
+
+def test_batch_beyond_the_shared_memory_plan():
+    """Batches above 1024 sequences are dealt out to the CTAs as whole units (no extra slots);
+    results, decisions and the fallback must be the same as for the part-balanced path."""
+    inp, oflags = _stress_inputs(batch=1100, seq_len=256, split_len=128, frac=0.01,
+                                 num_q_heads=8, num_kv_heads=2, head_dim=64)
+    diag = _check_fallback(inp, oflags, "batch 1100")
+    assert diag["n_units"] == 1100 * 2 * 2
+
+
 @pytest.mark.parametrize("kernel", ["tensor", "simt"])
 def test_fallback_state_resets_between_calls(kernel):
-    """The fused path keeps per-(b, g) tickets and a device-wide fallback list in the workspace;
-    both must be back at zero after every call, so repeated calls on one workspace agree."""
+    """The device-wide fallback list and its counters live in the workspace and must be back at
+    zero after every call, so repeated calls on one workspace agree."""
     inp, oflags = _stress_inputs(seed_offset=3)
     dinp = H.DeviceInputs(inp)
     kid = F.FDPP_KERNEL_TENSOR if kernel == "tensor" else F.FDPP_KERNEL_SIMT
