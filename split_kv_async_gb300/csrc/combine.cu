@@ -7,10 +7,12 @@
 // with w_j = 1 exactly when m_j == M: if no split of the row fell back (all m_j = phi) this is
 // exactly the plain sum.
 //
-// The n_b splits of a row are divided into 8 contiguous ranges, one per warp (each lane owns 4
-// or 2 output columns), so a long row's partials are read with 8x the memory-level parallelism;
-// the 8 warp sums are then added in warp order. The order is fixed, so results are
-// deterministic. The result is rounded to nearest even into the output dtype.
+// The row's partials (its n_b splits, then its extra slots) are divided into contiguous ranges,
+// one per warp of the row (each lane owns 4 or 2 output columns), read 4 at a time per lane; the
+// warp sums are then added in warp order. A row gets 8 warps while the rows fit on the GPU at
+// that width, and fewer when there are many rows, so that all rows are in flight at once. The
+// order is fixed, so results are deterministic. The result is rounded to nearest even into the
+// output dtype.
 //
 // Extra slots. The tensor kernel cuts the 64-token tiles of all units (order b, g, j) into P
 // equal parts, part c = tiles [floor(c T / P), floor((c + 1) T / P)). A part that starts inside
@@ -45,7 +47,7 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
+__global__ void __launch_bounds__(CT, 3) combine_kernel(KernelArgs a, int wpr)
 {
     constexpr int E = D / 32;                       // output columns per lane
     __shared__ float s_acc[CW][D];
@@ -57,15 +59,19 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
     grid_dependency_wait();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x;                     // b * Hq + h
+    const int rpc = CW / wpr;                       // rows of this CTA, wpr warps each
+    const int rl = warp / wpr, wr = warp - rl * wpr;
+    const int row = blockIdx.x * rpc + rl;          // b * Hq + h
+    const bool live = row < a.B * a.Hq;
     // the split kernel has finished: its fallback-list counters go back to zero for the next call
-    if (row == 0 && threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         a.hdr[HDR_REDO_COUNT] = 0;
         a.hdr[HDR_REDO_TAKEN] = 0;
     }
-    const int b = row / a.Hq;
-    const int hh = row - b * a.Hq - (row - b * a.Hq) / a.G * a.G;   // head within its group
-    const int n = a.nsplit[b];
+    const int b = live ? row / a.Hq : 0;
+    const int h = live ? row - b * a.Hq : 0;
+    const int hh = h - h / a.G * a.G;               // head within its group
+    const int n = live ? a.nsplit[b] : 0;
 
     // Parts that may start inside this row's units: the row's kv head owns tiles [W, W + nt).
     const int P = a.hdr[HDR_PARTS];
@@ -75,15 +81,20 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
         tiles = a.hdr[HDR_TILES];
         TS = (a.hdr[HDR_SPLIT] + 63) / 64;
         nt = a.tstart[b + 1] - a.tstart[b];
-        W = (long long)a.Hkv * a.tstart[b] + (long long)((row - b * a.Hq) / a.G) * nt;
+        W = (long long)a.Hkv * a.tstart[b] + (long long)(h / a.G) * nt;
         c_lo = (int)(((W + 1) * P + tiles - 1) / tiles);   // first part starting after tile W
         c_hi = (int)(((W + nt) * P - 1) / tiles);           // last part starting before W + nt
     }
-    // extra slot of part c belongs to split jx of this row, or c left none here
+    // extra slot of part c belongs to split jx of this row, or c left none here. Part c starts at
+    // floor(c tiles / P) = c q + floor(c r / P) with tiles = q P + r (32-bit arithmetic per part).
+    const long long q_p = P > 0 ? tiles / P : 0;
+    const int r_p = P > 0 ? (int)(tiles - q_p * P) : 0;
     auto extra_split = [&](int c) -> int {
-        const long long k = (long long)c * tiles / P - W;
-        if (k <= 0 || k >= nt || k % TS == 0) return -1;
-        return (int)(k / TS);
+        const long long k = (long long)c * q_p + (c * r_p) / P - W;
+        if (k <= 0 || k >= nt) return -1;
+        const int ki = (int)k;
+        const int jx = ki / TS;
+        return ki == jx * TS ? -1 : jx;
     };
     const float* xm = a.xm + hh;
     const float* xl = a.xl + hh;
@@ -92,12 +103,20 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
     const float* m = a.m_part + base;
     const float* l = a.l_part + base;
     const float* o = a.o_part + base * D;
-    T* out = static_cast<T*>(a.out) + (long long)row * D;
 
-    // M = max_j m_j over the whole row
+    // The row's entries: its n splits, then the candidate extra slots c_lo .. c_hi (those that
+    // are not extra slots of this row are skipped). Entry e < n is split e.
+    const int n_c = c_hi >= c_lo ? c_hi - c_lo + 1 : 0;
+    const int n_e = n + n_c;
+
+    // M = max over the row's partials; the extra slots' flag bytes are ORed into their splits'
     float M = -INFINITY;
-    for (int j = threadIdx.x; j < n; j += CT) M = fmaxf(M, m[j]);
-    for (int c = c_lo + threadIdx.x; c <= c_hi; c += CT) {
+    for (int e = wr * 32 + lane; e < n_e; e += wpr * 32) {
+        if (e < n) {
+            M = fmaxf(M, m[e]);
+            continue;
+        }
+        const int c = c_lo + (e - n);
         const int jx = extra_split(c);
         if (jx >= 0) {
             M = fmaxf(M, xm[(long long)c * a.G]);
@@ -113,27 +132,42 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
     for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
     if (lane == 0) s_max[warp] = M;
     __syncthreads();
-    M = s_max[0];
-#pragma unroll
-    for (int w = 1; w < CW; ++w) M = fmaxf(M, s_max[w]);
+    M = s_max[rl * wpr];
+    for (int w = 1; w < wpr; ++w) M = fmaxf(M, s_max[rl * wpr + w]);
 
-    // this warp's contiguous range of splits, ascending
-    const int chunk = (n + CW - 1) / CW;
-    const int j0 = warp * chunk, j1 = min(n, j0 + chunk);
+    // this warp's contiguous range of the row's entries, ascending, U loads in flight per lane
+    const int per = (n_e + wpr - 1) / wpr;
+    const int e0 = wr * per, e1 = min(n_e, e0 + per);
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float lam = 0.f;
     constexpr int U = 4;
-    for (int jb = j0; jb < j1; jb += U) {
+    for (int eb = e0; eb < e1; eb += U) {
         float mv[U], lv[U], ov[U][E];
+        bool ok[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int j = jb + u;
-            if (j < j1) {
-                mv[u] = m[j];
-                lv[u] = l[j];
-                const float* oj = o + (long long)j * D + lane * E;
+            const int e = eb + u;
+            ok[u] = false;
+            const float *pm = m, *pl = l, *po = o;
+            if (e < e1) {
+                if (e < n) {
+                    pm = m + e; pl = l + e; po = o + (long long)e * D;
+                    ok[u] = true;
+                } else {
+                    const int c = c_lo + (e - n);
+                    if (extra_split(c) >= 0) {
+                        pm = xm + (long long)c * a.G; pl = xl + (long long)c * a.G;
+                        po = xo + (long long)c * a.G * D;
+                        ok[u] = true;
+                    }
+                }
+            }
+            if (ok[u]) {
+                mv[u] = *pm;
+                lv[u] = *pl;
+                const float* oj = po + lane * E;
                 if constexpr (E == 4) {
                     const float4 v = *reinterpret_cast<const float4*>(oj);
                     ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
@@ -145,7 +179,7 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (jb + u < j1) {
+            if (ok[u]) {
                 const float w = frame_weight(mv[u], M);
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[e] = fmaf(w, ov[u][e], acc[e]);
@@ -153,36 +187,43 @@ __global__ void __launch_bounds__(CT) combine_kernel(KernelArgs a)
             }
         }
     }
-    // extra slots, one part per warp in turn
-    for (int c = c_lo + warp; c <= c_hi; c += CW) {
-        if (extra_split(c) < 0) continue;
-        const float w = frame_weight(xm[(long long)c * a.G], M);
-        const float* oc = xo + (long long)c * a.G * D + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, oc[e], acc[e]);
-        lam = fmaf(w, xl[(long long)c * a.G], lam);
-    }
 #pragma unroll
     for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
     if (lane == 0) s_lam[warp] = lam;
     __syncthreads();
-    if (threadIdx.x < D) {
-        const int d = threadIdx.x;
-        float total = 0.f, ltot = 0.f;
+    // the row's warp sums in warp order; the first warp of the row writes the output
+    if (live && wr == 0) {
+        T* out = static_cast<T*>(a.out) + (long long)row * D;
+        float ltot = 0.f;
+        for (int w = 0; w < wpr; ++w) ltot += s_lam[rl * wpr + w];
 #pragma unroll
-        for (int w = 0; w < CW; ++w) {
-            total += s_acc[w][d];
-            ltot += s_lam[w];
+        for (int e = 0; e < E; ++e) {
+            const int d = lane + 32 * e;
+            float total = 0.f;
+            for (int w = 0; w < wpr; ++w) total += s_acc[rl * wpr + w][d];
+            store_out<T>(out + d, n > 0 ? __fdiv_rn(total, ltot) : 0.f);
         }
-        store_out<T>(out + d, n > 0 ? __fdiv_rn(total, ltot) : 0.f);
     }
+}
+
+// Warps per row: 8 while the rows fit the GPU about once at that width, fewer for many rows
+// (a row's partials are then read by fewer warps, but all rows are in flight together).
+int warps_per_row(long long rows, int num_sms)
+{
+    const long long resident = (long long)num_sms * 3 * CW;     // 3 CTAs of CW warps per SM
+    int w = CW;
+    while (w > 1 && rows * w > resident) w >>= 1;
+    return w;
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
 {
+    const long long rows = (long long)a.B * a.Hq;
+    const int wpr = warps_per_row(rows, a.num_sms);
+    const int rpc = CW / wpr;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+    cfg.gridDim = dim3((unsigned)((rows + rpc - 1) / rpc));
     cfg.blockDim = dim3(CT);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -191,7 +232,7 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D>, a);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D>, a, wpr);
 }
 
 }  // namespace

@@ -216,6 +216,22 @@ def test_batch_beyond_the_shared_memory_plan():
     assert diag["n_units"] == 1100 * 2 * 2
 
 
+def test_many_rows_share_combine_blocks():
+    """735 softmax rows: the combine gives a row fewer than 8 warps when the rows would not fit
+    on the GPU at once, and packs several rows into one block (the last block has a row to
+    spare). Every row must still be right."""
+    wl = _wl(W.GQA, name="many_rows", batch=245, num_q_heads=3, num_kv_heads=3, head_dim=64,
+             seq_len=300, split_len=64)
+    rng = np.random.default_rng(7)
+    inp = W.generate(wl, seq_lens=rng.integers(1, 301, size=245).astype(np.int32))
+    dinp = H.DeviceInputs(inp)
+    ref = H.oracle_out(inp)
+    for kernel in _kernels(inp):
+        got, diag, _, _, _ = H.run(dinp, kernel=kernel)
+        assert diag["error_bits"] == 0
+        H.assert_parity(got, ref, f"many rows kernel {kernel}")
+
+
 @pytest.mark.parametrize("kernel", ["tensor", "simt"])
 def test_fallback_state_resets_between_calls(kernel):
     """The device-wide fallback list and its counters live in the workspace and must be back at
