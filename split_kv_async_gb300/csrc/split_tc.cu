@@ -388,7 +388,11 @@ struct Producer {
         const KernelArgs& A = *a;
         const int c = blockIdx.x;
         if (c >= P) return true;
-        const long long tb = (long long)c * T / P, te = (long long)(c + 1) * T / P;
+        // floor(c T / P) = c q + floor(c r / P) with T = q P + r: no 64-bit division
+        const long long q = T / P;
+        const int r = (int)(T - q * P);
+        const long long tb = (long long)c * q + (c * r) / P;
+        const long long te = (long long)(c + 1) * q + ((c + 1) * r) / P;
         const int zero3[3] = {0, 0, 0};
         struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
         int cb = 0;
@@ -417,9 +421,13 @@ struct Producer {
         for (;;) {
             const long long tn = t + cur.ntile;
             const bool last = tn >= te;
+            // The next segment is located after this one is issued (its block-table window is
+            // loaded while the ring holds this segment's tiles), unless the L2 prefetch wants
+            // its first tiles now.
             NextUnit nx{0, 0, 0, 0, 0, -(1 << 30), -1};
             int nxt_ent = -1;
-            if (!last) {
+            const bool ahead = !last && A.pf_tiles > 0;
+            if (ahead) {
                 seg_at(tn, nxt);
                 if (PAGED) nxt_ent = window_entry(nxt.b, nxt.t0, nxt.L);
                 nx = NextUnit{1, nxt.b, nxt.g, nxt.t0, nxt.t1,
@@ -432,6 +440,10 @@ struct Producer {
                 return false;
             had_own = true;
             if (last) break;
+            if (!ahead) {
+                seg_at(tn, nxt);
+                if (PAGED) nxt_ent = window_entry(nxt.b, nxt.t0, nxt.L);
+            }
             t = tn;
             cur = nxt;
             cur_ent = nxt_ent;
