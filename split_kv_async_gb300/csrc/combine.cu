@@ -9,8 +9,8 @@
 //
 // The row's partials (its n_b splits, then its extra slots) are divided into contiguous ranges,
 // one per warp of the row (each lane owns 4 or 2 output columns), read 4 at a time per lane; the
-// warp sums are then added in warp order. A row gets 8 warps while the rows fit on the GPU at
-// that width, and fewer when there are many rows, so that all rows are in flight at once. The
+// warp sums are then added in warp order. A row gets up to 32 warps while the rows fit on the
+// GPU at that width, and fewer when there are many rows, so that all rows are in flight. The
 // order is fixed, so results are deterministic. The result is rounded to nearest even into the
 // output dtype.
 //
@@ -31,8 +31,8 @@
 namespace fdpp {
 namespace {
 
-constexpr int CW = 8;                 // warps per CTA
-constexpr int CT = CW * 32;
+constexpr int CW = 8;                 // warps per CTA of the many-rows build
+constexpr int CW_WIDE = 32;           // warps per CTA when a few long rows take 16 or 32 warps each
 
 template <typename T>
 __device__ __forceinline__ void store_out(T* p, float x);
@@ -46,20 +46,20 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
     *p = __float2bfloat16_rn(x);
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(CT, 3) combine_kernel(KernelArgs a, int wpr)
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(KernelArgs a, int wpr)
 {
     constexpr int E = D / 32;                       // output columns per lane
-    __shared__ float s_acc[CW][D];
-    __shared__ float s_lam[CW];
-    __shared__ float s_max[CW];
+    __shared__ float s_acc[NW][D];
+    __shared__ float s_lam[NW];
+    __shared__ float s_max[NW];
     // the next call's split kernel may launch now; it waits for this grid to complete before
     // it touches global memory
     grid_launch_dependents();
     grid_dependency_wait();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rpc = CW / wpr;                       // rows of this CTA, wpr warps each
+    const int rpc = NW / wpr;                       // rows of this CTA, wpr warps each
     const int rl = warp / wpr, wr = warp - rl * wpr;
     const int row = blockIdx.x * rpc + rl;          // b * Hq + h
     const bool live = row < a.B * a.Hq;
@@ -206,12 +206,13 @@ __global__ void __launch_bounds__(CT, 3) combine_kernel(KernelArgs a, int wpr)
     }
 }
 
-// Warps per row: 8 while the rows fit the GPU about once at that width, fewer for many rows
-// (a row's partials are then read by fewer warps, but all rows are in flight together).
+// Warps per row: up to 32 while the rows fit on the GPU at that width (a long row's partials
+// are then read by many warps at once), fewer for many rows, so that all rows are in flight
+// together.
 int warps_per_row(long long rows, int num_sms)
 {
-    const long long resident = (long long)num_sms * 3 * CW;     // 3 CTAs of CW warps per SM
-    int w = CW;
+    const long long resident = (long long)num_sms * 3 * CW;     // 3 CTAs of 8 warps per SM
+    int w = CW_WIDE;
     while (w > 1 && rows * w > resident) w >>= 1;
     return w;
 }
@@ -221,10 +222,11 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
 {
     const long long rows = (long long)a.B * a.Hq;
     const int wpr = warps_per_row(rows, a.num_sms);
-    const int rpc = CW / wpr;
+    const int nw = wpr > CW ? CW_WIDE : CW;
+    const int rpc = nw / wpr;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((rows + rpc - 1) / rpc));
-    cfg.blockDim = dim3(CT);
+    cfg.blockDim = dim3((unsigned)(nw * 32));
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -232,7 +234,8 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D>, a, wpr);
+    if (nw == CW_WIDE) return cudaLaunchKernelEx(&cfg, combine_kernel<T, D, CW_WIDE>, a, wpr);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D, CW>, a, wpr);
 }
 
 }  // namespace
