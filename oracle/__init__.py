@@ -17,9 +17,13 @@ the passage of the pages it follows:
 * ``split_method``     -- the method's steps in fp64: phi-frame partials per split, detect,
   online recompute, max-rescaled (plain when nothing fell back) sum.
 * ``split_len`` / ``plan`` -- the split scheduler restated: n_b = ceil(L_b / S).
+* ``score_ranges`` / ``pick_phi`` -- phi observed in advance (same page, section 3): the score
+  range of every row-split on sample inputs, and per head the phi that keeps the most row-splits
+  inside the window (the reading is stated in oracle.c, R8).
 
-Parity status: every function above is pinned by ``tests/test_oracle_pins.py``; phi calibration is
-not part of the oracle (parity unpinned: the pages give no calibration procedure).
+``window_flags`` and ``split_method`` take an optional per-head phi (oracle.c, R7).
+
+Parity status: every function above is pinned by ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
 
@@ -81,12 +85,18 @@ def _load():
                                                  ctypes.c_int, ctypes.c_double, vp, ctypes.c_int]
             lib.or_attention_shifted.restype = ctypes.c_int
             lib.or_window_flags.argtypes = [P, vp, vp, ip, ip, ctypes.c_int, ctypes.c_int, vp, vp,
-                                            ctypes.c_int]
+                                            vp, ctypes.c_int]
             lib.or_window_flags.restype = ctypes.c_int
             lib.or_split_method.argtypes = [P, vp, vp, vp, ip, ip, ip, ctypes.c_int, ctypes.c_int,
-                                            ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp,
+                                            ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                             ctypes.c_int]
             lib.or_split_method.restype = ctypes.c_int
+            lib.or_score_ranges.argtypes = [P, vp, vp, ip, ip, ctypes.c_int, ctypes.c_int, vp, vp,
+                                            ctypes.c_int]
+            lib.or_score_ranges.restype = ctypes.c_int
+            lib.or_pick_phi.argtypes = [vp, vp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_double, ctypes.c_double, ctypes.c_double, vp, vp]
+            lib.or_pick_phi.restype = ctypes.c_int
             lib.or_split_len.argtypes = [ip] + [ctypes.c_int] * 8
             lib.or_split_len.restype = ctypes.c_int
             lib.or_plan.argtypes = [ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -159,21 +169,61 @@ def attention_shifted(prob, q, k, v, seq_lens, shift=None, block_table=None, row
     return out
 
 
-def window_flags(prob, q, k, seq_lens, split_len, max_splits, block_table=None, n_threads=0):
+def _phi_arg(prob, phi_heads):
+    if phi_heads is None:
+        return None
+    a = np.ascontiguousarray(phi_heads, dtype=np.float32).reshape(-1)
+    if a.size != prob.num_q_heads:
+        raise ValueError("phi_heads needs one value per query head")
+    return a
+
+
+def window_flags(prob, q, k, seq_lens, split_len, max_splits, block_table=None, phi_heads=None,
+                 n_threads=0):
     """Returns (flags uint8 [B][Hq][max_splits], row_margin float64 [B][Hq])."""
     lib = _load()
     q, k = (_kv_array(x, prob.dtype) for x in (q, k))
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    ph = _phi_arg(prob, phi_heads)
     flags = np.zeros((prob.batch, prob.num_q_heads, max_splits), dtype=np.uint8)
     margin = np.zeros((prob.batch, prob.num_q_heads), dtype=np.float64)
     lib.or_window_flags(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), split_len,
-                        max_splits, _ptr(flags), _ptr(margin), n_threads)
+                        max_splits, _ptr(flags), _ptr(margin), _ptr(ph), n_threads)
     return flags, margin
 
 
+def score_ranges(prob, q, k, seq_lens, split_len, max_splits, block_table=None, n_threads=0):
+    """Least and greatest score of every row-split: (smin, smax) float64 [B][Hq][max_splits],
+    NaN past a sequence's splits."""
+    lib = _load()
+    q, k = (_kv_array(x, prob.dtype) for x in (q, k))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
+    smin = np.zeros((prob.batch, prob.num_q_heads, max_splits), dtype=np.float64)
+    smax = np.zeros_like(smin)
+    lib.or_score_ranges(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), split_len,
+                        max_splits, _ptr(smin), _ptr(smax), n_threads)
+    return smin, smax
+
+
+def pick_phi(smin, smax, nsplit, lo, hi, fallback):
+    """Per-head phi from score ranges [B][Hq][max_splits] (oracle.c, R8). Returns (phi float64
+    [Hq], kept int32 [Hq]: the row-splits each head's phi keeps inside the window)."""
+    lib = _load()
+    smin = np.ascontiguousarray(smin, dtype=np.float64)
+    smax = np.ascontiguousarray(smax, dtype=np.float64)
+    B, Hq, ms = smin.shape
+    ns = np.ascontiguousarray(nsplit, dtype=np.int32)
+    phi = np.zeros(Hq, dtype=np.float64)
+    kept = np.zeros(Hq, dtype=np.int32)
+    lib.or_pick_phi(_ptr(smin), _ptr(smax), _ptr(ns), B, Hq, ms, float(lo), float(hi),
+                    float(fallback), _ptr(phi), _ptr(kept))
+    return phi, kept
+
+
 def split_method(prob, q, k, v, seq_lens, split_len, max_splits, mode=MODE_NORMAL,
-                 block_table=None, rows=None, want_partials=False, n_threads=0):
+                 block_table=None, rows=None, want_partials=False, phi_heads=None, n_threads=0):
     """The method's steps in fp64. Returns dict(out, flags[, part_o, part_l, part_m])."""
     lib = _load()
     q, k, v = (_kv_array(x, prob.dtype) for x in (q, k, v))
@@ -187,10 +237,11 @@ def split_method(prob, q, k, v, seq_lens, split_len, max_splits, mode=MODE_NORMA
         res["part_o"] = np.zeros((n, max_splits, d), dtype=np.float64)
         res["part_l"] = np.zeros((n, max_splits), dtype=np.float64)
         res["part_m"] = np.zeros((n, max_splits), dtype=np.float64)
+    ph = _phi_arg(prob, phi_heads)
     lib.or_split_method(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
                         _ptr(r), n, split_len, max_splits, mode, _ptr(res["out"]),
                         _ptr(res.get("part_o")), _ptr(res.get("part_l")),
-                        _ptr(res.get("part_m")), _ptr(res["flags"]), n_threads)
+                        _ptr(res.get("part_m")), _ptr(res["flags"]), _ptr(ph), n_threads)
     return res
 
 

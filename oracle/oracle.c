@@ -33,6 +33,11 @@
  *       m_j = phi and this is exactly the plain sum of [theory] s3.
  *   R5  Only tokens t < L_b take part. L_b == 0 gives an all-zero output row.
  *   R6  scale, phi, lo and hi are the float32 values the caller passes, widened to double.
+ *   R7  phi may be given per query head (a float32 per head); the same steps then use each
+ *       head's own value. A single phi is the case where every head has the same value.
+ *   R8  "phi is set by observing the distribution in advance" ([theory] s3) is read as: on
+ *       sample inputs, phi_h is a value that keeps the most row-splits of head h inside the
+ *       window; among all values that do, the middle of the widest closed run of them.
  *
  * Precision: every value is widened exactly to double (bf16 and fp32 both widen exactly);
  * all arithmetic is double. Threads: rows are independent, and are spread over pthreads.
@@ -309,7 +314,14 @@ typedef struct {
     int S, max_splits;
     uint8_t* flags;         /* [B][Hq][max_splits] */
     double* row_margin;     /* [B*Hq]: min over valid t of min(|x - lo|, |x - hi|), x = s - phi */
+    const float* phi_heads; /* [Hq] or NULL (p->phi for every head) */
 } or_flag_ctx;
+
+/* The unified max of head h: the head's own value when per-head values are given (R7). */
+static double or_phi(const or_problem* p, const float* phi_heads, int h)
+{
+    return phi_heads ? (double)phi_heads[h] : (double)p->phi;
+}
 
 static uint8_t or_classify(double x, double lo, double hi)
 {
@@ -331,7 +343,7 @@ static void or_flag_row(void* vctx, int r)
     if (L > 0) {
         double* s = (double*)malloc(sizeof(double) * (size_t)L);
         or_scores(p, c->q, c->k, c->table, b, h, L, s);
-        double phi = (double)p->phi, lo = (double)p->lo, hi = (double)p->hi;
+        double phi = or_phi(p, c->phi_heads, h), lo = (double)p->lo, hi = (double)p->hi;
         for (int t = 0; t < L; ++t) {
             double x = s[t] - phi;
             int j = t / c->S;
@@ -345,12 +357,13 @@ static void or_flag_row(void* vctx, int r)
     if (c->row_margin) c->row_margin[r] = margin;
 }
 
-/* flags[b][h][j] for every row; entries with j >= n_b stay 0. row_margin may be NULL. */
+/* flags[b][h][j] for every row; entries with j >= n_b stay 0. row_margin and phi_heads may be
+ * NULL. */
 int or_window_flags(const or_problem* p, const void* q, const void* k,
                     const int32_t* block_table, const int32_t* seq_lens, int S, int max_splits,
-                    uint8_t* flags, double* row_margin, int n_threads)
+                    uint8_t* flags, double* row_margin, const float* phi_heads, int n_threads)
 {
-    or_flag_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, flags, row_margin };
+    or_flag_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, flags, row_margin, phi_heads };
     return or_parallel_rows(or_flag_row, &c, p->batch * p->num_q_heads, n_threads);
 }
 
@@ -383,6 +396,7 @@ typedef struct {
     double* part_l;    /* [n_rows][max_splits] or NULL */
     double* part_m;    /* [n_rows][max_splits] or NULL */
     uint8_t* flags;    /* [n_rows][max_splits] or NULL */
+    const float* phi_heads;   /* [Hq] or NULL */
 } or_split_ctx;
 
 static void or_split_row(void* vctx, int r)
@@ -405,7 +419,7 @@ static void or_split_row(void* vctx, int r)
     double* m = (double*)calloc((size_t)n, sizeof(double));
     uint8_t* f = (uint8_t*)calloc((size_t)n, 1);
     or_scores(p, c->q, c->k, c->table, b, h, L, s);
-    double phi = (double)p->phi, lo = (double)p->lo, hi = (double)p->hi;
+    double phi = or_phi(p, c->phi_heads, h), lo = (double)p->lo, hi = (double)p->hi;
 
     for (int j = 0; j < n; ++j) {
         int t0 = j * c->S, t1 = t0 + c->S < L ? t0 + c->S : L;
@@ -466,11 +480,138 @@ int or_split_method(const or_problem* p, const void* q, const void* k, const voi
                     const int32_t* block_table, const int32_t* seq_lens,
                     const int32_t* rows, int n_rows, int S, int max_splits, int mode,
                     double* out, double* part_o, double* part_l, double* part_m, uint8_t* flags,
-                    int n_threads)
+                    const float* phi_heads, int n_threads)
 {
     or_split_ctx c = { p, q, k, v, block_table, seq_lens, rows, S, max_splits, mode,
-                       out, part_o, part_l, part_m, flags };
+                       out, part_o, part_l, part_m, flags, phi_heads };
     return or_parallel_rows(or_split_row, &c, n_rows, n_threads);
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 5. calibration of phi from observed scores                                                 */
+/* ----------------------------------------------------------------------------------------- */
+/*
+ * [theory] s3: phi is set in advance by observing the score distribution; a block whose scores
+ * leave the window falls back. Read plainly (R8): record, on sample inputs, the range
+ * [min s, max s] of every row-split (b, h, j). The split keeps the fast path iff every score
+ * satisfies lo <= s - phi <= hi, i.e. iff phi lies in [max s - hi, min s - lo]. For head h, phi_h
+ * is a value inside the most such intervals; of all values that reach that count, the middle of
+ * the widest closed run. A head none of whose splits can be kept gets the fallback value.
+ */
+
+typedef struct {
+    const or_problem* p;
+    const void *q, *k;
+    const int32_t* table;
+    const int32_t* seq_lens;
+    int S, max_splits;
+    double *smin, *smax;    /* [B][Hq][max_splits] */
+} or_range_ctx;
+
+static void or_range_row(void* vctx, int r)
+{
+    or_range_ctx* c = (or_range_ctx*)vctx;
+    const or_problem* p = c->p;
+    int b = r / p->num_q_heads, h = r % p->num_q_heads;
+    int L = c->seq_lens[b];
+    double* lo = c->smin + (size_t)r * (size_t)c->max_splits;
+    double* hi = c->smax + (size_t)r * (size_t)c->max_splits;
+    for (int j = 0; j < c->max_splits; ++j) { lo[j] = NAN; hi[j] = NAN; }
+    if (L <= 0) return;
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+    for (int t = 0; t < L; ++t) {
+        int j = t / c->S;
+        if (j >= c->max_splits) break;
+        if (t % c->S == 0 || s[t] < lo[j]) lo[j] = s[t];
+        if (t % c->S == 0 || s[t] > hi[j]) hi[j] = s[t];
+    }
+    free(s);
+}
+
+/* smin / smax [B][Hq][max_splits]: the least and greatest score of each row-split over its valid
+ * tokens; NaN for j >= n_b. */
+int or_score_ranges(const or_problem* p, const void* q, const void* k, const int32_t* block_table,
+                    const int32_t* seq_lens, int S, int max_splits, double* smin, double* smax,
+                    int n_threads)
+{
+    or_range_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, smin, smax };
+    return or_parallel_rows(or_range_row, &c, p->batch * p->num_q_heads, n_threads);
+}
+
+static int or_cmp_double(const void* a, const void* b)
+{
+    double x = *(const double*)a, y = *(const double*)b;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/* Number of intervals [a_i, b_i] that contain x. */
+static int or_stab(const double* a, const double* bb, int n, double x)
+{
+    int c = 0;
+    for (int i = 0; i < n; ++i) c += (a[i] <= x && x <= bb[i]);
+    return c;
+}
+
+/* phi_out[h] (and count_out[h], the splits it keeps; may be NULL) from the score ranges of the
+ * row-splits j < nsplit[b], over all sequences b. Plain method: the kept count is constant on
+ * each endpoint and on each open gap between consecutive endpoints, so those are evaluated one by
+ * one, and the widest run of consecutive ones at the best count gives phi_h. */
+int or_pick_phi(const double* smin, const double* smax, const int32_t* nsplit, int batch,
+                int num_q_heads, int max_splits, double lo, double hi, double fallback,
+                double* phi_out, int32_t* count_out)
+{
+    size_t cap = (size_t)batch * (size_t)max_splits;
+    double* a = (double*)malloc(sizeof(double) * (cap + 1));
+    double* bb = (double*)malloc(sizeof(double) * (cap + 1));
+    double* x = (double*)malloc(sizeof(double) * (2 * cap + 1));
+    int* cnt = (int*)malloc(sizeof(int) * (4 * cap + 2));
+    for (int h = 0; h < num_q_heads; ++h) {
+        int n = 0;
+        for (int b = 0; b < batch; ++b) {
+            int nb = nsplit[b] < max_splits ? nsplit[b] : max_splits;
+            for (int j = 0; j < nb; ++j) {
+                size_t r = ((size_t)b * (size_t)num_q_heads + (size_t)h) * (size_t)max_splits + (size_t)j;
+                double lo_phi = smax[r] - hi, hi_phi = smin[r] - lo;
+                if (lo_phi == lo_phi && hi_phi == hi_phi && lo_phi <= hi_phi) {
+                    a[n] = lo_phi;
+                    bb[n] = hi_phi;
+                    ++n;
+                }
+            }
+        }
+        if (n == 0) {
+            phi_out[h] = fallback;
+            if (count_out) count_out[h] = 0;
+            continue;
+        }
+        int m = 0;
+        for (int i = 0; i < n; ++i) { x[m++] = a[i]; x[m++] = bb[i]; }
+        qsort(x, (size_t)m, sizeof(double), or_cmp_double);
+        int u = 0;
+        for (int i = 0; i < m; ++i) if (u == 0 || x[i] != x[u - 1]) x[u++] = x[i];
+        /* elements in order: point x0, gap (x0, x1), point x1, ..., point x_{u-1} */
+        int ne = 2 * u - 1, best = 0;
+        for (int e = 0; e < ne; ++e) {
+            double at = (e % 2 == 0) ? x[e / 2] : 0.5 * (x[e / 2] + x[e / 2 + 1]);
+            cnt[e] = or_stab(a, bb, n, at);
+            if (cnt[e] > best) best = cnt[e];
+        }
+        double best_w = -1.0, best_mid = 0.0;
+        for (int e = 0; e < ne;) {
+            if (cnt[e] != best) { ++e; continue; }
+            int f = e;
+            while (f + 1 < ne && cnt[f + 1] == best) ++f;
+            /* a run starts and ends on points (a gap at best count implies both its points) */
+            double left = x[e / 2], right = x[(f + 1) / 2];
+            if (right - left > best_w) { best_w = right - left; best_mid = 0.5 * (left + right); }
+            e = f + 1;
+        }
+        phi_out[h] = best_mid;
+        if (count_out) count_out[h] = best;
+    }
+    free(a); free(bb); free(x); free(cnt);
+    return 0;
 }
 
 /* Number of threads or_* calls use for n_threads == 0 (the host's online CPUs). */

@@ -368,3 +368,127 @@ def test_stress_injection_is_flagged_and_normal_inputs_are_not():
             for j in range(4):
                 if (b, h // wl.group, j) not in hot_units:
                     assert flags[b, h, j] == 0
+
+
+# ------------------------------------------------------------------------------------------
+# per-head phi and phi observed in advance (oracle.c, R7 and R8)
+# ------------------------------------------------------------------------------------------
+
+def test_per_head_phi_is_each_heads_own_scalar_phi():
+    """Per-head phi: head h decides exactly as the scalar-phi replay with phi = phi_h, and the
+    method's output is still the exact softmax (phi only moves where splits fall back)."""
+    q, k, v, sl = _rand_problem(11, B=2, Hq=4, Hkv=2, d=8, L=40)
+    q *= 3.0                                      # scores of a few units: some cross the window
+    S, ms = 8, 5
+    phis = np.array([-2.0, 0.0, 1.5, 4.0], np.float32)
+    prob = _prob(2, 4, 2, 8, 1.0, 40, lo=-6.0, hi=3.0)
+    f_heads, _ = oracle.window_flags(prob, q, k, sl, S, ms, phi_heads=phis)
+    assert f_heads.any() and not f_heads.all()
+    for h, ph in enumerate(phis):
+        prob_h = _prob(2, 4, 2, 8, 1.0, 40, phi=float(ph), lo=-6.0, hi=3.0)
+        f_h, _ = oracle.window_flags(prob_h, q, k, sl, S, ms)
+        np.testing.assert_array_equal(f_heads[:, h], f_h[:, h])
+    exact, _ = oracle.attention(prob, q, k, v, sl)
+    res = oracle.split_method(prob, q, k, v, sl, S, ms, phi_heads=phis)
+    np.testing.assert_allclose(res["out"], exact, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(res["flags"].reshape(f_heads.shape), f_heads)
+
+
+def test_score_ranges_closed_form():
+    """Keys along q give known scores: q = 8 e_0, k_t = c_t e_0, scale 1/8, so s_t = c_t
+    exactly (fp32). Each split's range is the min and max of its c_t."""
+    L, d, S = 11, 64, 4
+    c = np.array([3.0, -1.0, 2.5, 0.0, 7.0, 7.0, -4.0, 1.0, 0.5, -0.5, 9.0], np.float32)
+    q = np.zeros((1, 1, d), np.float32)
+    q[0, 0, 0] = 8.0
+    k = np.zeros((1, L, 1, d), np.float32)
+    k[0, :, 0, 0] = c
+    prob = _prob(1, 1, 1, d, 0.125, L)
+    smin, smax = oracle.score_ranges(prob, q, k, np.array([L], np.int32), S, 4)
+    np.testing.assert_array_equal(smin[0, 0, :3], [-1.0, -4.0, -0.5])
+    np.testing.assert_array_equal(smax[0, 0, :3], [3.0, 7.0, 9.0])
+    assert np.isnan(smin[0, 0, 3]) and np.isnan(smax[0, 0, 3])
+
+
+def test_score_ranges_agree_with_window_decisions():
+    """A row-split is inside the window for phi exactly when phi lies in
+    [max s - hi, min s - lo]: the ranges and the token-by-token decisions must agree for any
+    phi."""
+    q, k, v, sl = _rand_problem(12, B=3, Hq=4, Hkv=2, d=16, L=50)
+    q *= 2.0
+    S, ms, lo, hi = 8, 7, -3.0, 2.0
+    prob = _prob(3, 4, 2, 16, 0.25, 50, lo=lo, hi=hi)
+    smin, smax = oracle.score_ranges(prob, q, k, sl, S, ms)
+    nb = -(-sl // S)
+    for phi in (-1.0, 0.0, 0.7, 2.0):
+        f, _ = oracle.window_flags(_prob(3, 4, 2, 16, 0.25, 50, phi=phi, lo=lo, hi=hi), q, k, sl,
+                                   S, ms)
+        for b in range(3):
+            for j in range(nb[b]):
+                keep = (np.float64(smax[b, :, j]) - hi <= np.float32(phi)) & \
+                       (np.float32(phi) <= np.float64(smin[b, :, j]) - lo)
+                np.testing.assert_array_equal((f[b, :, j] & oracle.FLAG_OUT) == 0, keep)
+
+
+def _ranges_from_intervals(intervals, lo, hi):
+    """One head, one sequence: row-split ranges whose keep-interval [max - hi, min - lo] is the
+    given [a, b] (a > b gives a split that no phi can keep)."""
+    smin = np.array([[[b_ + lo for _, b_ in intervals]]], np.float64)
+    smax = np.array([[[a_ + hi for a_, _ in intervals]]], np.float64)
+    return smin, smax, np.array([len(intervals)], np.int32)
+
+
+@pytest.mark.parametrize("intervals,phi,kept", [
+    ([(0.0, 2.0), (1.0, 3.0), (5.0, 6.0)], 1.5, 2),        # best count 2 on [1, 2]
+    ([(0.0, 1.0), (2.0, 4.0)], 3.0, 1),                   # count 1 twice: the wider run wins
+    ([(0.0, 1.0), (1.0, 2.0)], 1.0, 2),                   # best count only at the shared point
+    ([(0.0, 1.0), (3.0, 4.0)], 0.5, 1),                   # equal widths: the first run
+    ([(2.0, 1.0), (4.0, 3.0)], -7.0, 0),                  # no split can be kept: fallback
+    ([(0.0, 10.0), (2.0, 3.0), (2.5, 8.0)], 2.75, 3),     # nested intervals
+])
+def test_pick_phi_examples(intervals, phi, kept):
+    lo, hi = -30.0, 10.0
+    smin, smax, ns = _ranges_from_intervals(intervals, lo, hi)
+    got, k = oracle.pick_phi(smin, smax, ns, lo, hi, fallback=-7.0)
+    assert got[0] == pytest.approx(phi, abs=1e-12)
+    assert k[0] == kept
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_pick_phi_is_the_best_count_by_brute_force(seed):
+    """Against a dense scan of candidate phi values: no phi keeps more splits than the pick, and
+    the picked phi keeps that many."""
+    rng = np.random.default_rng(seed)
+    lo, hi = -5.0, 2.0
+    n = 12
+    mid = rng.uniform(-10, 10, n)
+    width = rng.uniform(-1, 8, n)
+    intervals = [(m - w / 2, m + w / 2) for m, w in zip(mid, width)]
+    smin, smax, ns = _ranges_from_intervals(intervals, lo, hi)
+    phi, kept = oracle.pick_phi(smin, smax, ns, lo, hi, fallback=0.0)
+    a = np.array([i[0] for i in intervals])
+    b = np.array([i[1] for i in intervals])
+    grid = np.concatenate([np.linspace(-20, 20, 40001), a, b])
+    counts = ((a[None, :] <= grid[:, None]) & (grid[:, None] <= b[None, :])).sum(axis=1)
+    assert kept[0] == counts.max()
+    assert ((a <= phi[0]) & (phi[0] <= b)).sum() == counts.max()
+
+
+def test_picked_phi_keeps_exactly_the_counted_splits():
+    """Calibrating on sample inputs and replaying the decisions with the picked per-head phi
+    leaves exactly `kept` row-splits of each head inside the window."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, d, L, S = 4, 4, 2, 16, 96, 16
+    q = (rng.standard_normal((B, Hq, d)) * np.array([1, 3, 5, 8])[None, :, None]).astype(np.float32)
+    k = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    sl = rng.integers(20, L + 1, size=B).astype(np.int32)
+    lo, hi = -4.0, 3.0
+    prob = _prob(B, Hq, Hkv, d, 0.25, L, lo=lo, hi=hi)
+    ms = -(-L // S)
+    smin, smax = oracle.score_ranges(prob, q, k, sl, S, ms)
+    nb = (-(-sl // S)).astype(np.int32)
+    phi, kept = oracle.pick_phi(smin, smax, nb, lo, hi, fallback=0.0)
+    f, _ = oracle.window_flags(prob, q, k, sl, S, ms, phi_heads=phi.astype(np.float32))
+    for h in range(Hq):
+        inside = sum(int((f[b, h, j] & oracle.FLAG_OUT) == 0) for b in range(B) for j in range(nb[b]))
+        assert inside == kept[h]
