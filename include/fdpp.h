@@ -109,6 +109,9 @@ typedef struct fdpp_params {
     int tc_ctas_per_sm;      /* tensor kernel: resident CTAs per SM (1 or 2), 0 = automatic */
     int tc_prefetch;         /* tensor kernel: L2 prefetch distance in 64-token tiles ahead of the
                                 TMA ring (1..32); 0 = automatic (off), -1 = off */
+    const float* phi_heads;  /* DEVICE float32 [Hq], 4-byte aligned: the unified max of each query
+                                head (e.g. from fdpp_pick_phi), used in place of `phi`; NULL = the
+                                scalar `phi` for every head */
 } fdpp_params;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over
@@ -198,6 +201,32 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
 fdpp_status fdpp_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_table, const int32_t* seq_lens,
                                      const fdpp_params* p, void* out, fdpp_stream stream);
+
+/* Score range of every row-split, for choosing phi in advance (opt.ai.kr "FlashDecoding++ async
+ * softmax -- theory", section 3: phi is set by observing the score distribution beforehand).
+ * On sample inputs laid out as for fdpp_decode_attn (q, k_cache, block_table, seq_lens, p,
+ * workspace), writes for each (b, h, j) with j < nsplit[b] the least and greatest scaled score
+ * s = scale <q, k_t> over the split's tokens:
+ *   smin_host, smax_host  HOST float [B][Hq][max_splits] (NaN past a sequence's splits);
+ *   nsplit_host           HOST int32 [B] or NULL.
+ * V is not read. Enqueues one kernel on `stream` and waits for it (synchronous). Uses the
+ * workspace's partial arrays; phi, lo, hi, mode and kernel in p are ignored. */
+fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, const fdpp_params* p, void* workspace,
+                              size_t workspace_bytes, float* smin_host, float* smax_host,
+                              int32_t* nsplit_host, fdpp_stream stream);
+
+/* Per-head unified max from score ranges (host only, no CUDA call). A row-split stays on the
+ * fast path for phi iff lo <= s - phi <= hi for all its scores, i.e. iff phi lies in
+ * [smax - hi, smin - lo]. For each head h, phi_out[h] is a value inside the most such intervals
+ * of the row-splits j < nsplit[b] over all sequences b; of all values that reach that count, the
+ * middle of the widest closed run of them. A head with no split that any phi keeps gets
+ * `fallback`. smin, smax: HOST float [B][Hq][max_splits] as written by fdpp_score_ranges;
+ * nsplit: HOST int32 [B]; phi_out: HOST float [Hq]; kept_out: HOST int32 [Hq] (the row-splits
+ * each phi_out keeps) or NULL. */
+fdpp_status fdpp_pick_phi(const float* smin, const float* smax, const int32_t* nsplit, int batch,
+                          int num_q_heads, int max_splits, float lo, float hi, float fallback,
+                          float* phi_out, int32_t* kept_out);
 
 /* Reads what the last call left in `workspace` (synchronous device-to-host copies; call after
  * that call's stream has been synchronised). diag: HOST, required. flags_host: HOST uint8

@@ -30,8 +30,8 @@ FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 
 # Names every build of the library exports (the C ABI of include/fdpp.h).
 EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fdpp_decode_attn",
-            "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_read_diag",
-            "fdpp_status_str", "fdpp_last_error")
+            "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_score_ranges",
+            "fdpp_pick_phi", "fdpp_read_diag", "fdpp_status_str", "fdpp_last_error")
 FDPP_NOALLOC_WORKSPACE_BYTES = 16 << 20
 FDPP_TC_MAX_PARTS = 512
 
@@ -56,7 +56,7 @@ class fdpp_params(ctypes.Structure):
         ("hi", ctypes.c_float),
         ("split_len", ctypes.c_int), ("mode", ctypes.c_int), ("kernel", ctypes.c_int),
         ("tc_stages", ctypes.c_int), ("tc_ctas_per_sm", ctypes.c_int),
-        ("tc_prefetch", ctypes.c_int),
+        ("tc_prefetch", ctypes.c_int), ("phi_heads", ctypes.c_void_p),
     ]
 
 
@@ -92,6 +92,11 @@ def _load() -> ctypes.CDLL:
     lib.fdpp_decode_attn_timed.restype = ctypes.c_int
     lib.fdpp_decode_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp, vp]
     lib.fdpp_decode_attn_noalloc.restype = ctypes.c_int
+    lib.fdpp_score_ranges.argtypes = [vp, vp, vp, vp, P, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    lib.fdpp_score_ranges.restype = ctypes.c_int
+    lib.fdpp_pick_phi.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_float, ctypes.c_float, vp, vp]
+    lib.fdpp_pick_phi.restype = ctypes.c_int
     lib.fdpp_read_diag.argtypes = [vp, ctypes.c_size_t, P, ctypes.POINTER(fdpp_diag), vp, vp]
     lib.fdpp_read_diag.restype = ctypes.c_int
     lib.fdpp_status_str.argtypes = [ctypes.c_int]
@@ -112,10 +117,12 @@ def _check(status: int, where: str) -> None:
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, scale,
                 phi=0.0, lo=-30.0, hi=10.0, split_len=0, block_size=0, max_blocks_per_seq=0,
                 num_kv_blocks=0, mode=FDPP_MODE_NORMAL, kernel=FDPP_KERNEL_AUTO, tc_stages=0,
-                tc_ctas_per_sm=0, tc_prefetch=0) -> fdpp_params:
+                tc_ctas_per_sm=0, tc_prefetch=0, phi_heads=None) -> fdpp_params:
+    """phi_heads: a float32 device tensor [num_q_heads] (or its address), or None."""
+    ph = phi_heads if phi_heads is None or isinstance(phi_heads, int) else phi_heads.data_ptr()
     return fdpp_params(batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, block_size,
                        max_blocks_per_seq, num_kv_blocks, scale, phi, lo, hi, split_len, mode,
-                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch)
+                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch, ph)
 
 
 def fdpp_max_splits(p: fdpp_params) -> int:
@@ -181,6 +188,36 @@ def fdpp_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, p: fdpp
     _check(lib.fdpp_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                         _ptr(seq_lens), ctypes.byref(p), _ptr(out),
                                         _stream_handle(stream)), "fdpp_decode_attn_noalloc")
+
+
+def fdpp_score_ranges(q, k_cache, block_table, seq_lens, p: fdpp_params, workspace, stream=None):
+    """Least and greatest score of every row-split on sample inputs (synchronous). Returns
+    (smin, smax float32 numpy [B][Hq][max_splits], NaN past a sequence's splits; nsplit int32)."""
+    import numpy as np
+    ms = fdpp_max_splits(p)
+    smin = np.empty((p.batch, p.num_q_heads, ms), np.float32)
+    smax = np.empty_like(smin)
+    ns = np.empty(p.batch, np.int32)
+    _check(lib.fdpp_score_ranges(_ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(seq_lens),
+                                 ctypes.byref(p), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), smin.ctypes.data,
+                                 smax.ctypes.data, ns.ctypes.data, _stream_handle(stream)),
+           "fdpp_score_ranges")
+    return smin, smax, ns
+
+
+def fdpp_pick_phi(smin, smax, nsplit, lo, hi, fallback=0.0):
+    """Per-head phi from score ranges (host only). Returns (phi float32 [Hq], kept int32 [Hq])."""
+    import numpy as np
+    smin = np.ascontiguousarray(smin, dtype=np.float32)
+    smax = np.ascontiguousarray(smax, dtype=np.float32)
+    ns = np.ascontiguousarray(nsplit, dtype=np.int32)
+    B, Hq, ms = smin.shape
+    phi = np.empty(Hq, np.float32)
+    kept = np.empty(Hq, np.int32)
+    _check(lib.fdpp_pick_phi(smin.ctypes.data, smax.ctypes.data, ns.ctypes.data, B, Hq, ms,
+                             lo, hi, fallback, phi.ctypes.data, kept.ctypes.data), "fdpp_pick_phi")
+    return phi, kept
 
 
 def fdpp_read_diag(workspace, p: fdpp_params, want_flags=False, want_nsplit=False):

@@ -11,8 +11,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -78,6 +80,8 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "tc_ctas_per_sm must be 0, 1 or 2");
     if (p->tc_prefetch < -1 || p->tc_prefetch > 32)
         return fail(FDPP_ERR_INVALID_ARG, "tc_prefetch must be -1, 0 or in [1, 32]");
+    if (p->phi_heads && ((uintptr_t)p->phi_heads % 4) != 0)
+        return fail(FDPP_ERR_INVALID_ARG, "phi_heads must be 4-byte aligned");
     const int G = p->num_q_heads / p->num_kv_heads;
     if (G > SIMT_MAX_GROUP)
         return fail(FDPP_ERR_UNSUPPORTED, "query heads per kv head %d > %d", G, SIMT_MAX_GROUP);
@@ -211,6 +215,57 @@ fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params&
     return FDPP_OK;
 }
 
+// Everything the kernels of one call need: pointers into the caller's buffers and workspace,
+// and the shape.
+KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace, const void* q,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, void* out, int num_sms, int kernel)
+{
+    const fdpp_params* p = &P;
+    const bool paged = block_table != nullptr;
+    const int G = p->num_q_heads / p->num_kv_heads;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    KernelArgs a{};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
+    a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
+    a.tstart = reinterpret_cast<int32_t*>(ws + w.tstart);
+    a.redo = reinterpret_cast<long long*>(ws + w.redo);
+    a.flags = ws + w.flags;
+    a.m_part = reinterpret_cast<float*>(ws + w.m_part);
+    a.l_part = reinterpret_cast<float*>(ws + w.l_part);
+    a.o_part = reinterpret_cast<float*>(ws + w.o_part);
+    a.xf = ws + w.xf;
+    a.xm = reinterpret_cast<float*>(ws + w.xm);
+    a.xl = reinterpret_cast<float*>(ws + w.xl);
+    a.xo = reinterpret_cast<float*>(ws + w.xo);
+    a.B = p->batch;
+    a.Hq = p->num_q_heads;
+    a.Hkv = p->num_kv_heads;
+    a.G = G;
+    a.D = p->head_dim;
+    a.max_seq_len = p->max_seq_len;
+    a.block_size = paged ? p->block_size : 0;
+    a.max_blocks = paged ? p->max_blocks_per_seq : 0;
+    a.num_blocks = paged ? p->num_kv_blocks : 0;
+    a.split_req = p->split_len;
+    a.max_splits = w.max_splits;
+    a.num_sms = num_sms;
+    a.scale = p->scale;
+    a.phi = p->phi;
+    a.phi_heads = p->phi_heads;
+    a.lo = p->lo;
+    a.hi = p->hi;
+    a.mode = p->mode;
+    a.kernel_id = kernel;
+    return a;
+}
+
 }  // namespace
 
 namespace fdpp {
@@ -303,44 +358,8 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     DeviceInfo dev;
     if ((st = device_info(dev)) != FDPP_OK) return st;
 
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    KernelArgs a{};
-    a.q = q;
-    a.k = k_cache;
-    a.v = v_cache;
-    a.block_table = block_table;
-    a.seq_lens = seq_lens;
-    a.out = out;
-    a.hdr = reinterpret_cast<int32_t*>(ws + w.header);
-    a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
-    a.tstart = reinterpret_cast<int32_t*>(ws + w.tstart);
-    a.redo = reinterpret_cast<long long*>(ws + w.redo);
-    a.flags = ws + w.flags;
-    a.m_part = reinterpret_cast<float*>(ws + w.m_part);
-    a.l_part = reinterpret_cast<float*>(ws + w.l_part);
-    a.o_part = reinterpret_cast<float*>(ws + w.o_part);
-    a.xf = ws + w.xf;
-    a.xm = reinterpret_cast<float*>(ws + w.xm);
-    a.xl = reinterpret_cast<float*>(ws + w.xl);
-    a.xo = reinterpret_cast<float*>(ws + w.xo);
-    a.B = p->batch;
-    a.Hq = p->num_q_heads;
-    a.Hkv = p->num_kv_heads;
-    a.G = G;
-    a.D = p->head_dim;
-    a.max_seq_len = p->max_seq_len;
-    a.block_size = paged ? p->block_size : 0;
-    a.max_blocks = paged ? p->max_blocks_per_seq : 0;
-    a.num_blocks = paged ? p->num_kv_blocks : 0;
-    a.split_req = p->split_len;
-    a.max_splits = w.max_splits;
-    a.num_sms = dev.sms;
-    a.scale = p->scale;
-    a.phi = p->phi;
-    a.lo = p->lo;
-    a.hi = p->hi;
-    a.mode = p->mode;
-    a.kernel_id = kernel;
+    KernelArgs a = kernel_args(*p, w, workspace, q, k_cache, v_cache, block_table, seq_lens, out,
+                               dev.sms, kernel);
 
     const long long units_max = (long long)p->batch * p->num_kv_heads * w.max_splits;
     cudaStream_t s = (cudaStream_t)stream;
@@ -377,6 +396,130 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     e = launch_combine(a, p->dtype, s);
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, const fdpp_params* p, void* workspace,
+                              size_t workspace_bytes, float* smin_host, float* smax_host,
+                              int32_t* nsplit_host, fdpp_stream stream)
+{
+    fdpp_status st = check_params(p);
+    if (st != FDPP_OK) return st;
+    const bool paged = block_table != nullptr;
+    if (paged && (st = check_paged(p)) != FDPP_OK) return st;
+    if (!q || !k_cache || !seq_lens || !smin_host || !smax_host)
+        return fail(FDPP_ERR_INVALID_ARG, "q, k_cache, seq_lens, smin_host and smax_host must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k_cache, 16))
+        return fail(FDPP_ERR_INVALID_ARG, "q and k_cache must be 16-byte aligned");
+    if (!aligned(seq_lens, 4) || (paged && !aligned(block_table, 4)))
+        return fail(FDPP_ERR_INVALID_ARG, "seq_lens and block_table must be 4-byte aligned");
+    if (!workspace) return fail(FDPP_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(workspace, 256)) return fail(FDPP_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    const WsLayout w = layout_of(*p);
+    if (workspace_bytes < w.total)
+        return fail(FDPP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, w.total);
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != FDPP_OK) return st;
+
+    KernelArgs a = kernel_args(*p, w, workspace, q, k_cache, nullptr, block_table, seq_lens, nullptr,
+                               dev.sms, FDPP_KERNEL_SIMT);
+    const long long units_max = (long long)p->batch * p->num_kv_heads * w.max_splits;
+    const int occ = score_ranges_ctas_per_sm(a, p->dtype);
+    long long grid = (long long)dev.sms * (occ > 0 ? occ : 1);
+    if (grid > units_max) grid = units_max;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_score_ranges(a, p->dtype, (int)grid, s);
+    if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "score range kernel launch: %s", cudaGetErrorString(e));
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return fail(FDPP_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+
+    const size_t B = (size_t)p->batch, Hq = (size_t)p->num_q_heads, ms = (size_t)w.max_splits;
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    std::string nsb(B * 4, '\0');
+    if ((e = cudaMemcpy(&nsb[0], ws + w.nsplit, nsb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(smin_host, ws + w.l_part, B * Hq * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(smax_host, ws + w.m_part, B * Hq * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
+    const int32_t* ns = reinterpret_cast<const int32_t*>(nsb.data());
+    for (size_t b = 0; b < B; ++b) {
+        const size_t n = ns[b] < 0 ? 0 : (ns[b] > (int)ms ? ms : (size_t)ns[b]);
+        for (size_t h = 0; h < Hq; ++h)
+            for (size_t j = n; j < ms; ++j) {
+                smin_host[(b * Hq + h) * ms + j] = NAN;
+                smax_host[(b * Hq + h) * ms + j] = NAN;
+            }
+    }
+    if (nsplit_host) std::memcpy(nsplit_host, ns, B * 4);
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_pick_phi(const float* smin, const float* smax, const int32_t* nsplit, int batch,
+                          int num_q_heads, int max_splits, float lo, float hi, float fallback,
+                          float* phi_out, int32_t* kept_out)
+{
+    if (!smin || !smax || !nsplit || !phi_out)
+        return fail(FDPP_ERR_INVALID_ARG, "smin, smax, nsplit and phi_out must be non-NULL");
+    if (batch < 1 || num_q_heads < 1 || max_splits < 1)
+        return fail(FDPP_ERR_INVALID_ARG, "batch, num_q_heads and max_splits must be >= 1");
+    if (!std::isfinite(lo) || !std::isfinite(hi) || !(lo <= hi) || !std::isfinite(fallback))
+        return fail(FDPP_ERR_INVALID_ARG, "lo <= hi and fallback must be finite");
+    // Sweep per head. The kept count is constant on each distinct endpoint and on each open gap
+    // between two consecutive ones: element 2i is endpoint x_i, element 2i+1 the gap after it. A
+    // split's phi interval [a, b] covers elements 2 idx(a) .. 2 idx(b), counted with a difference
+    // array. The best count's widest run of elements (ties: the first) gives phi (its middle).
+    std::vector<double> a, b, x;
+    std::vector<int> diff;
+    for (int h = 0; h < num_q_heads; ++h) {
+        a.clear();
+        b.clear();
+        for (int s = 0; s < batch; ++s) {
+            const int n = nsplit[s] < 0 ? 0 : (nsplit[s] > max_splits ? max_splits : nsplit[s]);
+            for (int j = 0; j < n; ++j) {
+                const size_t r = ((size_t)s * num_q_heads + h) * (size_t)max_splits + j;
+                const double lo_phi = (double)smax[r] - hi, hi_phi = (double)smin[r] - lo;
+                if (std::isfinite(lo_phi) && std::isfinite(hi_phi) && lo_phi <= hi_phi) {
+                    a.push_back(lo_phi);
+                    b.push_back(hi_phi);
+                }
+            }
+        }
+        if (a.empty()) {
+            phi_out[h] = fallback;
+            if (kept_out) kept_out[h] = 0;
+            continue;
+        }
+        x.assign(a.begin(), a.end());
+        x.insert(x.end(), b.begin(), b.end());
+        std::sort(x.begin(), x.end());
+        x.erase(std::unique(x.begin(), x.end()), x.end());
+        const size_t ne = 2 * x.size() - 1;
+        diff.assign(ne + 1, 0);
+        for (size_t i = 0; i < a.size(); ++i) {
+            const size_t ia = std::lower_bound(x.begin(), x.end(), a[i]) - x.begin();
+            const size_t ib = std::lower_bound(x.begin(), x.end(), b[i]) - x.begin();
+            diff[2 * ia] += 1;
+            diff[2 * ib + 1] -= 1;
+        }
+        int best = 0, run = 0;
+        std::vector<int> cnt(ne);
+        for (size_t e = 0; e < ne; ++e) {
+            run += diff[e];
+            cnt[e] = run;
+            best = std::max(best, run);
+        }
+        double best_w = -1.0, best_mid = 0.0;
+        for (size_t e = 0; e < ne;) {
+            if (cnt[e] != best) { ++e; continue; }
+            size_t f = e;
+            while (f + 1 < ne && cnt[f + 1] == best) ++f;
+            const double left = x[e / 2], right = x[(f + 1) / 2];
+            if (right - left > best_w) { best_w = right - left; best_mid = 0.5 * (left + right); }
+            e = f + 1;
+        }
+        phi_out[h] = (float)best_mid;
+        if (kept_out) kept_out[h] = best;
+    }
     return FDPP_OK;
 }
 

@@ -341,6 +341,12 @@ __device__ __forceinline__ unsigned classify(float x, float lo, float hi)
 }
 
 // exp(m_w - M) with the exact 1 when the frames agree (so phi-frame partials add plainly).
+// Unified max of query head h: its own value when the caller gave one per head.
+__device__ __forceinline__ float phi_of(const KernelArgs& a, int h)
+{
+    return a.phi_heads ? __ldg(a.phi_heads + h) : a.phi;
+}
+
 __device__ __forceinline__ float frame_weight(float m, float M)
 {
     return m == M ? 1.0f : __expf(m - M);

@@ -68,6 +68,7 @@ struct KernelArgs {
     int max_seq_len, block_size, max_blocks, num_blocks;
     int split_req, max_splits, num_sms;
     float scale, phi, lo, hi;
+    const float* phi_heads;       // [Hq] per-head unified max, or nullptr (phi for every head)
     int mode;
     int kernel_id;
     int nstage;                   // tensor kernel: TMA ring depth
@@ -85,6 +86,9 @@ cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStre
 cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s);
 cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
+// Score range of every row-split (least into l_part, greatest into m_part) and the split plan.
+cudaError_t launch_score_ranges(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
+int score_ranges_ctas_per_sm(const KernelArgs& a, int dtype);
 
 // Bytes at the front of a workspace for `p` that must be zero when a call starts.
 size_t workspace_zero_prefix(const fdpp_params& p);

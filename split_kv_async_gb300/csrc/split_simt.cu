@@ -84,9 +84,9 @@ __device__ __forceinline__ long long kv_row(const KernelArgs& a, int b, int t, i
 // softmax; otherwise the phi frame. Results stay in the warp's registers.
 template <typename T, int E, int GM, bool ONLINE>
 __device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int t0, int t1,
-                                          const float (&qr)[GM][E], float (&o)[GM][E],
-                                          float (&l)[GM], float (&m)[GM], unsigned (&fl)[GM],
-                                          bool& bad_block)
+                                          const float (&qr)[GM][E], const float (&ph)[GM],
+                                          float (&o)[GM][E], float (&l)[GM], float (&m)[GM],
+                                          unsigned (&fl)[GM], bool& bad_block)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const T* K = static_cast<const T*>(a.k);
@@ -94,7 +94,7 @@ __device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int
 #pragma unroll
     for (int h = 0; h < GM; ++h) {
         l[h] = 0.f;
-        m[h] = ONLINE ? -INFINITY : a.phi;
+        m[h] = ONLINE ? -INFINITY : ph[h];
         fl[h] = 0u;
 #pragma unroll
         for (int e = 0; e < E; ++e) o[h][e] = 0.f;
@@ -113,7 +113,7 @@ __device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int
             for (int e = 0; e < E; ++e) part = fmaf(qr[h][e], kx[e], part);
             part = warp_sum(part);
             const float s = __fmul_rn(part, a.scale);
-            const float x = __fsub_rn(s, a.phi);
+            const float x = __fsub_rn(s, ph[h]);
             fl[h] |= classify(x, a.lo, a.hi);
             if (ONLINE) {
                 const float mn = fmaxf(m[h], s);
@@ -211,14 +211,17 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(KernelArgs a)
                 for (int e = 0; e < E; ++e) qr[h][e] = 0.f;
             }
         }
+        float ph[GM];                               // each head's unified max
+#pragma unroll
+        for (int h = 0; h < GM; ++h) ph[h] = h < a.G ? phi_of(a, g * a.G + h) : a.phi;
         float o[GM][E], l[GM], m[GM];
         unsigned fl[GM];
         if (a.mode == FDPP_MODE_FORCE_ONLINE) {
-            warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+            warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
             merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, FDPP_FLAG_RECOMPUTED, true);
             continue;
         }
-        warp_pass<T, E, GM, false>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+        warp_pass<T, E, GM, false>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
         merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, 0u, true);
         if (a.mode != FDPP_MODE_NORMAL) continue;
         unsigned redo = 0u;
@@ -226,8 +229,78 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(KernelArgs a)
             if (sh.unit_flags[h] & FDPP_FLAG_OUT) redo |= 1u << h;
         if (!redo) continue;
         // the split left the safe window: read it again with the ordinary online softmax
-        warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, o, l, m, fl, bad_block);
+        warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
         merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, redo, FDPP_FLAG_RECOMPUTED, false);
+    }
+    if (bad_block) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
+}
+
+// Score ranges for choosing phi in advance (opt.ai.kr "FlashDecoding++ async softmax -- theory",
+// s3: phi is set by observing the distribution beforehand): for every unit, the least and greatest
+// scaled score of each of its G heads over the split's tokens, the least into l_part and the
+// greatest into m_part. Only K is read. Same plan and unit walk as the split kernel.
+template <typename T, int E, int GM>
+__global__ void __launch_bounds__(kThreads) score_range_kernel(KernelArgs a)
+{
+    __shared__ long long red[32];
+    __shared__ float s_lo[kWarps][GM], s_hi[kWarps][GM];
+    int S, n_units;
+    block_plan(a, red, S, n_units);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const T* Q = static_cast<const T*>(a.q);
+    const T* K = static_cast<const T*>(a.k);
+    UnitCursor cur;
+    cur.reset();
+    bool bad_block = false;
+    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+        int b, g, j, L;
+        cur.seek(a, S, u, b, g, j, L);
+        const int t0 = j * S, t1 = min(t0 + S, L);
+        float qr[GM][E];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+            if (h < a.G) {
+                Elem<T>::template load<E>(Q + ((long long)b * a.Hq + (long long)g * a.G + h) * a.D + lane * E, qr[h]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) qr[h][e] = 0.f;
+            }
+        }
+        float lo[GM], hi[GM];
+#pragma unroll
+        for (int h = 0; h < GM; ++h) { lo[h] = INFINITY; hi[h] = -INFINITY; }
+        for (int t = t0 + warp; t < t1; t += kWarps) {
+            const long long row = kv_row(a, b, t, g);
+            if (row < 0) { bad_block = true; continue; }
+            float kx[E];
+            Elem<T>::template load<E>(K + row + lane * E, kx);
+#pragma unroll
+            for (int h = 0; h < GM; ++h) {
+                if (h >= a.G) break;
+                float part = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) part = fmaf(qr[h][e], kx[e], part);
+                part = warp_sum(part);
+                const float s = __fmul_rn(part, a.scale);
+                lo[h] = fminf(lo[h], s);
+                hi[h] = fmaxf(hi[h], s);
+            }
+        }
+        __syncthreads();                           // the previous unit's readers are done
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < GM; ++h) { s_lo[warp][h] = lo[h]; s_hi[warp][h] = hi[h]; }
+        }
+        __syncthreads();
+        if (threadIdx.x < a.G) {
+            const int h = threadIdx.x;
+            float mn = s_lo[0][h], mx = s_hi[0][h];
+            for (int w = 1; w < kWarps; ++w) { mn = fminf(mn, s_lo[w][h]); mx = fmaxf(mx, s_hi[w][h]); }
+            const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
+            a.l_part[r] = mn;
+            a.m_part[r] = mx;
+        }
     }
     if (bad_block) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
 }
@@ -276,6 +349,50 @@ cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStre
 int split_simt_ctas_per_sm(const KernelArgs& a, int dtype)
 {
     return dtype == FDPP_F32 ? occ_dtype<float>(a) : occ_dtype<__nv_bfloat16>(a);
+}
+
+namespace {
+
+template <typename T>
+cudaError_t launch_ranges_dtype(const KernelArgs& a, int grid, cudaStream_t s)
+{
+    const bool e4 = (a.D == 128);
+    if (a.G <= 4) {
+        if (e4) score_range_kernel<T, 4, 4><<<grid, kThreads, 0, s>>>(a);
+        else score_range_kernel<T, 2, 4><<<grid, kThreads, 0, s>>>(a);
+    } else {
+        if (e4) score_range_kernel<T, 4, 16><<<grid, kThreads, 0, s>>>(a);
+        else score_range_kernel<T, 2, 16><<<grid, kThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+int ranges_occ_dtype(const KernelArgs& a)
+{
+    int n = 0;
+    const bool e4 = (a.D == 128);
+    cudaError_t e;
+    if (a.G <= 4)
+        e = e4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 4, 4>, kThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 2, 4>, kThreads, 0);
+    else
+        e = e4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 4, 16>, kThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 2, 16>, kThreads, 0);
+    return e == cudaSuccess ? n : 0;
+}
+
+}  // namespace
+
+cudaError_t launch_score_ranges(const KernelArgs& a, int dtype, int grid, cudaStream_t s)
+{
+    return dtype == FDPP_F32 ? launch_ranges_dtype<float>(a, grid, s)
+                             : launch_ranges_dtype<__nv_bfloat16>(a, grid, s);
+}
+
+int score_ranges_ctas_per_sm(const KernelArgs& a, int dtype)
+{
+    return dtype == FDPP_F32 ? ranges_occ_dtype<float>(a) : ranges_occ_dtype<__nv_bfloat16>(a);
 }
 
 }  // namespace fdpp

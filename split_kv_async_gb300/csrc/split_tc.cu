@@ -626,9 +626,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float lsum[2] = {0.f, 0.f};
-        float mrun[2] = {online ? -INFINITY : a.phi, online ? -INFINITY : a.phi};
-        unsigned fl[2] = {0u, 0u};
         const bool hv[2] = {head0 < a.G, head0 + 1 < a.G};
+        // this lane's heads' unified max (their own values when given per head)
+        const float phv[2] = {hv[0] ? phi_of(a, g * a.G + head0) : a.phi,
+                              hv[1] ? phi_of(a, g * a.G + head0 + 1) : a.phi};
+        float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
+        unsigned fl[2] = {0u, 0u};
         const int ntiles = ceil_div_i(t1 - t0, TILE);
         uint32_t held = 0;                         // stage of the last tile: the merge scratch
 
@@ -655,13 +658,13 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             for (int e = 0; e < 4; ++e) {
                 sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
                 valid[e] = hv[e & 1] && (tok_r + 8 * (e >> 1) < nvalid);
-                if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], a.phi), a.lo, a.hi);
+                if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
             }
 
             float p[4];
             if (!online) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], a.phi)) : 0.f;
+                for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], phv[e & 1])) : 0.f;
             } else {
                 float corr[2];
 #pragma unroll

@@ -57,9 +57,29 @@ def oracle_out(inp: W.Inputs, rows=None):
     return out
 
 
-def oracle_flags(inp: W.Inputs, split_len: int, max_splits: int):
+def oracle_flags(inp: W.Inputs, split_len: int, max_splits: int, phi_heads=None):
     return oracle.window_flags(oracle_problem(inp), inp.q, inp.k, inp.seq_lens, split_len,
-                               max_splits, block_table=inp.block_table)
+                               max_splits, block_table=inp.block_table, phi_heads=phi_heads)
+
+
+def oracle_flags_robust(inp: W.Inputs, split_len: int, max_splits: int, phi_heads=None,
+                        eps: float = 1e-3):
+    """Oracle decisions and, per row-split, whether the OUT decision is robust: the same with
+    the window widened and narrowed by eps on both sides (fp32 scores on the GPU may differ from
+    fp64 by far less than eps, so a robust decision must come out the same)."""
+    wl = inp.wl
+    flags, _ = oracle_flags(inp, split_len, max_splits, phi_heads)
+
+    def with_window(lo, hi):
+        prob = oracle_problem(inp)
+        prob.lo, prob.hi = np.float32(lo), np.float32(hi)
+        f, _ = oracle.window_flags(prob, inp.q, inp.k, inp.seq_lens, split_len, max_splits,
+                                   block_table=inp.block_table, phi_heads=phi_heads)
+        return (f & oracle.FLAG_OUT) != 0
+
+    wide = with_window(wl.lo - eps, wl.hi + eps)
+    narrow = with_window(wl.lo + eps, wl.hi - eps)
+    return flags, wide == narrow
 
 
 class DeviceInputs:

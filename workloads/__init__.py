@@ -24,6 +24,11 @@ Recipe (the design notes repeat it):
     seeded position by k = 12 * q_h0 / ||q_h0|| * sqrt(d) (h0 = first query head of the kv
     group, computed in float32 from the rounded query, then rounded to bf16), so that head's
     score is about 12 ||q|| and far above phi + 10.
+  * ``score_shift`` > 0 moves each query head's scores to its own level: per kv head g a seeded
+    unit direction u_g, per query head h a seeded level mu_h uniform in [0, score_shift]; the keys
+    of kv head g gain a * u_g and query h gains (mu_h sqrt(d) / a) * u_g, a = sqrt(score_shift
+    sqrt(d)) (float32, then rounded to bf16), so that head h's scaled scores centre near mu_h.
+    Heads then need a unified max of their own (tests of per-head phi and of its calibration).
 """
 from __future__ import annotations
 
@@ -37,7 +42,7 @@ F32, BF16 = "f32", "bf16"
 _CHUNK = 1 << 24
 
 # stream ids of the per-array generators
-_S_SEQ, _S_Q, _S_K, _S_V, _S_PERM, _S_STRESS = 1, 2, 3, 4, 5, 6
+_S_SEQ, _S_Q, _S_K, _S_V, _S_PERM, _S_STRESS, _S_SHIFT = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclasses.dataclass(frozen=True)
@@ -57,6 +62,7 @@ class Workload:
     lo: float = -30.0
     hi: float = 10.0
     stress_frac: float = 0.0
+    score_shift: float = 0.0                   # > 0: per-head score levels in [0, score_shift]
     seed: int = 0x5EED0000
 
     @property
@@ -182,10 +188,35 @@ def generate(wl: Workload, *, seq_lens: Optional[np.ndarray] = None, poison_tail
                     k[last, L % bs:] = nan_val
                     v[last, L % bs:] = nan_val
 
+    if wl.score_shift > 0:
+        _shift_scores(wl, q, k)
     hot = []
     if wl.stress_frac > 0:
         hot = _inject_hot_keys(wl, sl, q, k, table)
     return Inputs(wl, sl, q, k, v, table, Lmax, mbps, nblk_total, hot)
+
+
+def _shift_scores(wl, q, k):
+    """Per-head score levels (see the module docstring), in place."""
+    rng = _rng(wl.seed, _S_SHIFT)
+    Hkv, G, d = wl.num_kv_heads, wl.group, wl.head_dim
+    u = rng.standard_normal((Hkv, d)).astype(np.float32)
+    u /= np.linalg.norm(u, axis=1, keepdims=True).astype(np.float32)
+    mu = rng.uniform(0.0, wl.score_shift, size=wl.num_q_heads).astype(np.float32)
+    a = np.float32(math.sqrt(wl.score_shift * math.sqrt(d)))
+
+    def widen(x):
+        return x if wl.dtype == F32 else bf16_bits_to_f32(x)
+
+    def narrow(x):
+        return x.astype(np.float32) if wl.dtype == F32 else f32_to_bf16_bits(x)
+
+    for g in range(Hkv):
+        kg = widen(k[..., g, :]) + a * u[g]
+        k[..., g, :] = narrow(kg)
+        for h in range(g * G, (g + 1) * G):
+            qh = widen(q[:, h, :]) + (mu[h] * np.float32(math.sqrt(d)) / a) * u[g]
+            q[:, h, :] = narrow(qh)
 
 
 def _inject_hot_keys(wl, sl, q, k, table):
