@@ -63,6 +63,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="per-head phi chosen from the score ranges of a seeded sample of the "
+                         "workload (another seed), then used for the timed steps")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -352,6 +355,33 @@ def run_fdpp(args, dist: Dist):
                   max_seq_len=inp.max_blocks_per_seq * wl.block_size)
     p = F.make_params(**kw)
     ws = F.alloc_workspace(p, dev)
+    calib = None
+    if args.calibrate:
+        # phi observed in advance: score ranges of a sample drawn with another seed, one phi per
+        # head picked from them on the host; the timed steps then run with those values
+        sample = W.generate(wl.replace(seed=wl.seed + 1))
+        sq = _dev_tensor(sample.q, dev)
+        sk = _dev_tensor(sample.k, dev)
+        ssl = torch.from_numpy(sample.seq_lens).to(dev)
+        sbt = None if sample.block_table is None else torch.from_numpy(sample.block_table).to(dev)
+        pk = dict(kw)
+        if wl.paged:
+            pk.update(max_blocks_per_seq=sample.max_blocks_per_seq,
+                      num_kv_blocks=sample.num_kv_blocks,
+                      max_seq_len=sample.max_blocks_per_seq * wl.block_size)
+        else:
+            pk.update(max_seq_len=sample.max_seq_len)
+        ps = F.make_params(**pk)
+        wss = F.alloc_workspace(ps, dev)
+        smin, smax, ns = F.fdpp_score_ranges(sq, sk, sbt, ssl, ps, wss)
+        phi_np, kept = F.fdpp_pick_phi(smin, smax, ns, wl.lo, wl.hi, fallback=wl.phi)
+        phi_dev = torch.from_numpy(phi_np).to(dev)
+        kw["phi_heads"] = phi_dev
+        p = F.make_params(**kw)
+        calib = {"sample_seed": wl.seed + 1, "sample_row_splits": int(ns.sum()) * wl.num_q_heads,
+                 "kept": int(kept.sum()), "phi_min": float(phi_np.min()),
+                 "phi_max": float(phi_np.max())}
+        del sq, sk, wss
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
@@ -530,6 +560,9 @@ def run_fdpp(args, dist: Dist):
         "clocks": clocks,
         "error_bits": diag["error_bits"],
     }
+    if calib is not None:
+        res["config"]["phi"] = "per head, calibrated"
+        res["calibration"] = calib
     return res
 
 

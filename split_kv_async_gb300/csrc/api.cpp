@@ -109,6 +109,12 @@ fdpp_status check_paged(const fdpp_params* p)
     return FDPP_OK;
 }
 
+// Entries of one fallback list: one per unit, plus one per part for units cut in two.
+size_t redo_capacity(const fdpp_params& p)
+{
+    return (size_t)p.batch * p.num_kv_heads * max_splits_of(p) + TC_MAX_PARTS;
+}
+
 WsLayout layout_of(const fdpp_params& p)
 {
     WsLayout w{};
@@ -120,8 +126,8 @@ WsLayout layout_of(const fdpp_params& p)
     w.nsplit = off;  off = align256(off + (size_t)p.batch * 4);
     w.tstart = off;  off = align256(off + ((size_t)p.batch + 1) * 4);
     // a fallback entry per unit, plus one per part for units cut in two
-    const size_t entries = (size_t)p.batch * p.num_kv_heads * w.max_splits + TC_MAX_PARTS;
-    w.redo = off;    off = align256(off + entries * REDO_WORDS * 8);
+    const size_t entries = redo_capacity(p);
+    w.redo = off;    off = align256(off + REDO_NLISTS * entries * REDO_WORDS * 8);
     w.flags = off;   off = align256(off + slots);
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
@@ -236,6 +242,7 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
     a.tstart = reinterpret_cast<int32_t*>(ws + w.tstart);
     a.redo = reinterpret_cast<long long*>(ws + w.redo);
+    a.redo_cap = (int)redo_capacity(*p);
     a.flags = ws + w.flags;
     a.m_part = reinterpret_cast<float*>(ws + w.m_part);
     a.l_part = reinterpret_cast<float*>(ws + w.l_part);

@@ -65,8 +65,7 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
     const bool live = row < a.B * a.Hq;
     // the split kernel has finished: its fallback-list counters go back to zero for the next call
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        a.hdr[HDR_REDO_COUNT] = 0;
-        a.hdr[HDR_REDO_TAKEN] = 0;
+        for (int i = 0; i < 2 * REDO_NLISTS; ++i) a.hdr[HDR_REDO_LISTS + i] = 0;
     }
     const int b = live ? row / a.Hq : 0;
     const int h = live ? row - b * a.Hq : 0;

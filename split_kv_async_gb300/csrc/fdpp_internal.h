@@ -19,9 +19,9 @@ enum {
     HDR_ERR = 3,        // sticky FDPP_ERRBIT_* (atomicOr)
     HDR_BATCH = 4,      // B of the last call
     HDR_MAXSPLITS = 5,  // partial slots per row
-    HDR_REDO_COUNT = 8, // fallback list: entries pushed (zeroed by the combine kernel)
-    HDR_REDO_TAKEN = 9, // fallback list: entries claimed (zeroed by the combine kernel);
-                        //   words 8 and 9 are read together as one 8-byte word
+    HDR_REDO_LISTS = 16, // fallback lists: words 16 + 2i / 17 + 2i = entries pushed to / claimed
+                         //   from list i (read together as one 8-byte word), i < REDO_NLISTS;
+                         //   zeroed by the combine kernel
     HDR_PARTS = 11,     // tensor kernel: parts P of the tile-balanced partition (0: none)
     HDR_TILES = 12,     // tensor kernel: 64-token tiles T of all units together
     HDR_WORDS = 64
@@ -43,6 +43,9 @@ constexpr int TC_PLAN_SMEM_MAX_B = 1024;
 // Fallback list entry: 4 x int64 = {(b + 1) | (g * max_splits + j) << 32,
 // t0 | t1 << 32 (token range of the segment), dest (-1: split slot j, else extra slot), 0}.
 constexpr int REDO_WORDS = 4;
+// The fallback list is this many lists (CTA c pushes to list c % REDO_NLISTS), each with room for
+// every entry of a call.
+constexpr int REDO_NLISTS = 8;
 
 // Everything a kernel of this library needs about one call. Plain pointers and sizes.
 struct KernelArgs {
@@ -55,7 +58,8 @@ struct KernelArgs {
     int32_t* hdr;
     int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
     int32_t* tstart;              // [B + 1] tile prefix of the sequences (tensor kernel, CTA 0)
-    long long* redo;              // fallback list, REDO_WORDS per entry (tensor kernel)
+    long long* redo;              // fallback lists, REDO_WORDS per entry (tensor kernel)
+    int redo_cap;                 // entries per fallback list
     uint8_t* flags;               // [B][Hq][max_splits]
     float* m_part;                // [B][Hq][max_splits]
     float* l_part;                // [B][Hq][max_splits]

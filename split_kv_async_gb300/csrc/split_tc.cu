@@ -492,16 +492,21 @@ struct Producer {
         if (!ok) return;
 
         if (A.mode == FDPP_MODE_NORMAL) {
-            // the consumers push this CTA's flagged segments before they report the own work done
+            // The consumers push this CTA's flagged segments before they report the own work done.
+            // The list is REDO_NLISTS lists, CTA c pushing to list c % REDO_NLISTS: a CTA drains
+            // its own list first, then the others in turn, so that few CTAs contend for one
+            // list's claim word.
             if (had_own && !ring_wait(rg.own_done, 0u, misc, A)) return;
-            int* cnt = &A.hdr[HDR_REDO_COUNT];
-            int* taken = &A.hdr[HDR_REDO_TAKEN];
+            int li = 0;
             for (;;) {
+                const int list = (int)((blockIdx.x + li) % REDO_NLISTS);
+                int* cnt = &A.hdr[HDR_REDO_LISTS + 2 * list];
+                int* taken = cnt + 1;
                 int k = 0;
                 bool got = false, stop = false;
                 if (lane == 0) {
                     for (;;) {
-                        // count (word HDR_REDO_COUNT) and taken (the next word) in one read
+                        // count and taken (the next word) in one read
                         const unsigned long long both = ld_relaxed_gpu_u64(
                             reinterpret_cast<const unsigned long long*>(cnt));
                         const int c = (int)(unsigned)(both & 0xffffffffull);
@@ -511,14 +516,17 @@ struct Producer {
                     }
                 }
                 stop = __shfl_sync(0xffffffffu, stop, 0);
-                if (stop) break;
+                if (stop) {                              // this list is empty: the next one
+                    if (++li == REDO_NLISTS) break;
+                    continue;
+                }
                 got = __shfl_sync(0xffffffffu, got, 0);
                 k = __shfl_sync(0xffffffffu, k, 0);
                 if (!got) continue;
                 // the pusher reserved entry k before storing it: read it with a bounded wait
                 long long e = 0, rng = 0, dst = 0;
                 if (lane == 0) {
-                    long long* ent = A.redo + (long long)k * REDO_WORDS;
+                    long long* ent = A.redo + ((long long)list * A.redo_cap + k) * REDO_WORDS;
                     const uint64_t t0 = global_ns();
                     while ((e = ld_acquire_gpu(ent)) == 0 && global_ns() - t0 < FDPP_WAIT_NS) {
                     }
@@ -859,8 +867,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
             // thread 0 fills the entry, then publishes its first word with a release store
             if (ctid == 0) {
-                const int k = atomicAdd(&a.hdr[HDR_REDO_COUNT], 1);
-                long long* ent = a.redo + (long long)k * REDO_WORDS;
+                const int list = (int)(blockIdx.x % REDO_NLISTS);
+                const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
+                long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
                 ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
                 ent[2] = dest;
                 st_release_gpu(ent, ((long long)(g * a.max_splits + j) << 32) |

@@ -63,9 +63,12 @@ def test_max_splits_and_workspace_size():
     assert F.fdpp_max_splits(p) == 8
     ws = F.fdpp_workspace_size(p)
     # partials o (d floats), l, m and a flag byte per split slot and per extra slot (G = 4 rows
-    # for each of FDPP_TC_MAX_PARTS parts), plus header, plan and fallback list
+    # for each of FDPP_TC_MAX_PARTS parts), the fallback lists (8 lists of 32-byte entries, one
+    # per unit and per part each), plus header and plan
     slots = 8 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 4
-    assert slots * (128 * 4 + 4 + 4 + 1) <= ws <= slots * (128 * 4 + 4 + 4 + 1) + 64 * 1024
+    lists = 8 * (8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
+    assert fixed <= ws <= fixed + 64 * 1024
     assert ws % 256 == 0
     p0 = _gqa_params(split_len=0)
     assert F.fdpp_max_splits(p0) == 4096 // F.FDPP_AUTO_MIN_SPLIT

@@ -29,6 +29,8 @@ Recipe (the design notes repeat it):
     of kv head g gain a * u_g and query h gains (mu_h sqrt(d) / a) * u_g, a = sqrt(score_shift
     sqrt(d)) (float32, then rounded to bf16), so that head h's scaled scores centre near mu_h.
     Heads then need a unified max of their own (tests of per-head phi and of its calibration).
+    The levels and directions come from ``shift_seed`` alone, like a property of the model's
+    weights, so samples drawn with other seeds share them.
 """
 from __future__ import annotations
 
@@ -63,6 +65,7 @@ class Workload:
     hi: float = 10.0
     stress_frac: float = 0.0
     score_shift: float = 0.0                   # > 0: per-head score levels in [0, score_shift]
+    shift_seed: int = 0x5EED00FF               # the levels and directions (fixed across samples)
     seed: int = 0x5EED0000
 
     @property
@@ -86,7 +89,11 @@ PAGED = Workload("paged_batch", 64, 64, 8, 128, BF16, split_len=512, seq_len_ran
                  paged=True, block_size=16, seed=0x5EED0003)
 STRESS = Workload("fallback_stress", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096,
                   stress_frac=0.02, seed=0x5EED0004)
-ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS)}
+# GQA decode shapes whose query heads score at their own levels in [0, 30]: one scalar phi sends
+# most splits to the fallback; phi chosen per head from a sample keeps them on the fast path.
+SHIFTED = Workload("gqa_head_levels", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096,
+                   score_shift=30.0, seed=0x5EED0005)
+ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED)}
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -198,7 +205,7 @@ def generate(wl: Workload, *, seq_lens: Optional[np.ndarray] = None, poison_tail
 
 def _shift_scores(wl, q, k):
     """Per-head score levels (see the module docstring), in place."""
-    rng = _rng(wl.seed, _S_SHIFT)
+    rng = _rng(wl.shift_seed, _S_SHIFT)
     Hkv, G, d = wl.num_kv_heads, wl.group, wl.head_dim
     u = rng.standard_normal((Hkv, d)).astype(np.float32)
     u /= np.linalg.norm(u, axis=1, keepdims=True).astype(np.float32)
