@@ -497,13 +497,22 @@ struct Producer {
             // its own list first, then the others in turn, so that few CTAs contend for one
             // list's claim word.
             if (had_own && !ring_wait(rg.own_done, 0u, misc, A)) return;
-            int li = 0;
             for (;;) {
-                const int list = (int)((blockIdx.x + li) % REDO_NLISTS);
+                // every list's (count, taken) in one read, a lane per list starting at this CTA's
+                const int my = (int)((blockIdx.x + lane) % REDO_NLISTS);
+                bool pending = false;
+                if (lane < REDO_NLISTS) {
+                    const unsigned long long both = ld_relaxed_gpu_u64(
+                        reinterpret_cast<const unsigned long long*>(&A.hdr[HDR_REDO_LISTS + 2 * my]));
+                    pending = (int)(unsigned)(both >> 32) < (int)(unsigned)(both & 0xffffffffull);
+                }
+                const unsigned lists = __ballot_sync(0xffffffffu, pending);
+                if (lists == 0u) break;
+                const int list = (int)((blockIdx.x + (__ffs(lists) - 1)) % REDO_NLISTS);
                 int* cnt = &A.hdr[HDR_REDO_LISTS + 2 * list];
                 int* taken = cnt + 1;
                 int k = 0;
-                bool got = false, stop = false;
+                bool got = false;
                 if (lane == 0) {
                     for (;;) {
                         // count and taken (the next word) in one read
@@ -511,14 +520,9 @@ struct Producer {
                             reinterpret_cast<const unsigned long long*>(cnt));
                         const int c = (int)(unsigned)(both & 0xffffffffull);
                         const int t = (int)(unsigned)(both >> 32);
-                        if (t >= c) { stop = true; break; }
+                        if (t >= c) break;
                         if (atomicCAS(taken, t, t + 1) == t) { k = t; got = true; break; }
                     }
-                }
-                stop = __shfl_sync(0xffffffffu, stop, 0);
-                if (stop) {                              // this list is empty: the next one
-                    if (++li == REDO_NLISTS) break;
-                    continue;
                 }
                 got = __shfl_sync(0xffffffffu, got, 0);
                 k = __shfl_sync(0xffffffffu, k, 0);
