@@ -17,6 +17,8 @@ the passage of the pages it follows:
 * ``split_method``     -- the method's steps in fp64: phi-frame partials per split, detect,
   online recompute, max-rescaled (plain when nothing fell back) sum.
 * ``split_len`` / ``plan`` -- the split scheduler restated: n_b = ceil(L_b / S).
+* several query tokens per sequence (``make_problem(q_tokens=Tq)``): the last Tq positions,
+  causal (oracle.c, R9); every function above then works on the B*Tq query rows.
 * ``score_ranges`` / ``pick_phi`` -- phi observed in advance (same page, section 3): the score
   range of every row-split on sample inputs, and per head the phi that keeps the most row-splits
   inside the window (the reading is stated in oracle.c, R8).
@@ -67,8 +69,13 @@ class Problem(ctypes.Structure):
         ("max_seq_len", ctypes.c_int), ("block_size", ctypes.c_int),
         ("max_blocks_per_seq", ctypes.c_int),
         ("scale", ctypes.c_float), ("phi", ctypes.c_float), ("lo", ctypes.c_float),
-        ("hi", ctypes.c_float),
+        ("hi", ctypes.c_float), ("q_tokens", ctypes.c_int),
     ]
+
+    @property
+    def query_rows(self) -> int:
+        """B * Tq: q, out, flags and ranges are [B*Tq][Hq][...] (oracle.c, R9)."""
+        return self.batch * max(1, self.q_tokens)
 
 
 def _load():
@@ -122,17 +129,19 @@ def _kv_array(a, dtype):
 
 
 def make_problem(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, scale, phi, lo, hi,
-                 max_seq_len=0, block_size=0, max_blocks_per_seq=0, paged=False) -> Problem:
+                 max_seq_len=0, block_size=0, max_blocks_per_seq=0, paged=False,
+                 q_tokens=1) -> Problem:
     if num_q_heads % num_kv_heads:
         raise ValueError("num_q_heads must be a multiple of num_kv_heads")
     return Problem(batch, num_q_heads, num_kv_heads, head_dim, dtype, 1 if paged else 0,
                    max_seq_len, block_size, max_blocks_per_seq,
-                   np.float32(scale), np.float32(phi), np.float32(lo), np.float32(hi))
+                   np.float32(scale), np.float32(phi), np.float32(lo), np.float32(hi),
+                   max(1, int(q_tokens)))
 
 
 def _rows_arg(prob, rows):
     if rows is None:
-        return None, prob.batch * prob.num_q_heads
+        return None, prob.query_rows * prob.num_q_heads
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
     return r, r.shape[0]
 
@@ -186,8 +195,8 @@ def window_flags(prob, q, k, seq_lens, split_len, max_splits, block_table=None, 
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
     ph = _phi_arg(prob, phi_heads)
-    flags = np.zeros((prob.batch, prob.num_q_heads, max_splits), dtype=np.uint8)
-    margin = np.zeros((prob.batch, prob.num_q_heads), dtype=np.float64)
+    flags = np.zeros((prob.query_rows, prob.num_q_heads, max_splits), dtype=np.uint8)
+    margin = np.zeros((prob.query_rows, prob.num_q_heads), dtype=np.float64)
     lib.or_window_flags(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), split_len,
                         max_splits, _ptr(flags), _ptr(margin), _ptr(ph), n_threads)
     return flags, margin
@@ -200,7 +209,7 @@ def score_ranges(prob, q, k, seq_lens, split_len, max_splits, block_table=None, 
     q, k = (_kv_array(x, prob.dtype) for x in (q, k))
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     bt = None if block_table is None else np.ascontiguousarray(block_table, dtype=np.int32)
-    smin = np.zeros((prob.batch, prob.num_q_heads, max_splits), dtype=np.float64)
+    smin = np.zeros((prob.query_rows, prob.num_q_heads, max_splits), dtype=np.float64)
     smax = np.zeros_like(smin)
     lib.or_score_ranges(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(sl), split_len,
                         max_splits, _ptr(smin), _ptr(smax), n_threads)

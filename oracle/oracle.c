@@ -38,6 +38,10 @@
  *   R8  "phi is set by observing the distribution in advance" ([theory] s3) is read as: on
  *       sample inputs, phi_h is a value that keeps the most row-splits of head h inside the
  *       window; among all values that do, the middle of the widest closed run of them.
+ *   R9  Several query tokens per sequence ([theory] s3 quotes the method for prefill as well as
+ *       decode): the Tq query tokens are the sequence's last Tq positions, so query token i sees
+ *       the keys t < L_b - Tq + 1 + i (causal). The splits stay those of the sequence's keys; a
+ *       query row's last splits may hold fewer of its keys or none. A row with no key is zero.
  *
  * Precision: every value is widened exactly to double (bf16 and fp32 both widen exactly);
  * all arithmetic is double. Threads: rows are independent, and are spread over pthreads.
@@ -70,7 +74,21 @@ typedef struct {
     int block_size;       /* paged only */
     int max_blocks_per_seq; /* paged only: row length of block_table */
     float scale, phi, lo, hi;
+    int q_tokens;         /* Tq >= 1 query tokens per sequence, the last Tq positions (R9) */
 } or_problem;
+
+/* Query rows (R9). q and out are [B][Tq][Hq][d], i.e. [B*Tq][Hq][d]: "query row" bi = b*Tq + i
+ * is query token i of sequence b. It sees the keys t < L_b - Tq + 1 + i (causal within the last
+ * Tq positions; all L_b keys for Tq = 1). */
+static int or_tq(const or_problem* p) { return p->q_tokens > 1 ? p->q_tokens : 1; }
+
+static int or_key_limit(const or_problem* p, const int32_t* seq_lens, int bi)
+{
+    int tq = or_tq(p), L = seq_lens[bi / tq];
+    int lim = L - tq + 1 + bi % tq;
+    if (L <= 0 || lim < 0) return 0;
+    return lim;
+}
 
 /* ----------------------------------------------------------------------------------------- */
 /* element access                                                                            */
@@ -100,12 +118,13 @@ static size_t or_kv_offset(const or_problem* p, const int32_t* table, int b, int
     return (((size_t)blk * (size_t)p->block_size + slot) * hkv + (size_t)g) * d;
 }
 
-/* s_t = scale * sum_i q[b,h,i] * k[b,t,g(h),i]  for t < L, g(h) = floor(h / G)   ([theory] s1) */
+/* s_t = scale * sum_i q[bi,h,i] * k[b,t,g(h),i]  for t < L, g(h) = floor(h / G), b = bi / Tq
+ * ([theory] s1) */
 static void or_scores(const or_problem* p, const void* q, const void* k, const int32_t* table,
-                      int b, int h, int L, double* s)
+                      int bi, int h, int L, double* s)
 {
-    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
-    size_t qoff = ((size_t)b * (size_t)p->num_q_heads + (size_t)h) * (size_t)d;
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G, b = bi / or_tq(p);
+    size_t qoff = ((size_t)bi * (size_t)p->num_q_heads + (size_t)h) * (size_t)d;
     double scale = (double)p->scale;
     for (int t = 0; t < L; ++t) {
         size_t koff = or_kv_offset(p, table, b, t, g);
@@ -189,6 +208,7 @@ typedef struct {
     double phi_override;   /* shift used when use_phi == 2 */
 } or_attn_ctx;
 
+/* Row r -> (query row bi, head h); explicit rows are (bi, h) pairs. */
 static void or_row_bh(const or_problem* p, const int32_t* rows, int r, int* b, int* h)
 {
     if (rows) { *b = rows[2 * r]; *h = rows[2 * r + 1]; }
@@ -199,16 +219,16 @@ static void or_attn_row(void* vctx, int r)
 {
     or_attn_ctx* c = (or_attn_ctx*)vctx;
     const or_problem* p = c->p;
-    int b, h;
-    or_row_bh(p, c->rows, r, &b, &h);
-    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
-    int L = c->seq_lens[b];
+    int bi, h;
+    or_row_bh(p, c->rows, r, &bi, &h);
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G, b = bi / or_tq(p);
+    int L = or_key_limit(p, c->seq_lens, bi);
     double* o = c->out + (size_t)r * (size_t)d;
     for (int i = 0; i < d; ++i) o[i] = 0.0;
     if (L <= 0) return;                                   /* R5 */
 
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
-    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+    or_scores(p, c->q, c->k, c->table, bi, h, L, s);
 
     double shift;
     if (c->use_phi == 1) shift = (double)p->phi;
@@ -335,14 +355,14 @@ static void or_flag_row(void* vctx, int r)
 {
     or_flag_ctx* c = (or_flag_ctx*)vctx;
     const or_problem* p = c->p;
-    int b = r / p->num_q_heads, h = r % p->num_q_heads;
-    int L = c->seq_lens[b];
+    int bi = r / p->num_q_heads, h = r % p->num_q_heads;
+    int L = or_key_limit(p, c->seq_lens, bi);
     uint8_t* f = c->flags + (size_t)r * (size_t)c->max_splits;
     for (int j = 0; j < c->max_splits; ++j) f[j] = 0;
     double margin = INFINITY;
     if (L > 0) {
         double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        or_scores(p, c->q, c->k, c->table, b, h, L, s);
+        or_scores(p, c->q, c->k, c->table, bi, h, L, s);
         double phi = or_phi(p, c->phi_heads, h), lo = (double)p->lo, hi = (double)p->hi;
         for (int t = 0; t < L; ++t) {
             double x = s[t] - phi;
@@ -364,7 +384,7 @@ int or_window_flags(const or_problem* p, const void* q, const void* k,
                     uint8_t* flags, double* row_margin, const float* phi_heads, int n_threads)
 {
     or_flag_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, flags, row_margin, phi_heads };
-    return or_parallel_rows(or_flag_row, &c, p->batch * p->num_q_heads, n_threads);
+    return or_parallel_rows(or_flag_row, &c, p->batch * or_tq(p) * p->num_q_heads, n_threads);
 }
 
 /* ----------------------------------------------------------------------------------------- */
@@ -403,22 +423,24 @@ static void or_split_row(void* vctx, int r)
 {
     or_split_ctx* c = (or_split_ctx*)vctx;
     const or_problem* p = c->p;
-    int b, h;
-    or_row_bh(p, c->rows, r, &b, &h);
-    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G;
-    int L = c->seq_lens[b];
+    int bi, h;
+    or_row_bh(p, c->rows, r, &bi, &h);
+    int d = p->head_dim, G = p->num_q_heads / p->num_kv_heads, g = h / G, b = bi / or_tq(p);
+    /* the splits are the sequence's (n_b = ceil(L_b / S)); this row's keys stop at L (R9), so
+     * its last splits may hold fewer tokens, or none */
+    int Lseq = c->seq_lens[b], L = or_key_limit(p, c->seq_lens, bi);
     double* out = c->out + (size_t)r * (size_t)d;
     for (int i = 0; i < d; ++i) out[i] = 0.0;
-    int n = L > 0 ? (L + c->S - 1) / c->S : 0;
+    int n = Lseq > 0 ? (Lseq + c->S - 1) / c->S : 0;
     if (n > c->max_splits) n = c->max_splits;
-    if (n == 0) return;
+    if (n == 0 || L <= 0) return;
 
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
     double* o = (double*)calloc((size_t)n * (size_t)d, sizeof(double));
     double* l = (double*)calloc((size_t)n, sizeof(double));
     double* m = (double*)calloc((size_t)n, sizeof(double));
     uint8_t* f = (uint8_t*)calloc((size_t)n, 1);
-    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+    or_scores(p, c->q, c->k, c->table, bi, h, L, s);
     double phi = or_phi(p, c->phi_heads, h), lo = (double)p->lo, hi = (double)p->hi;
 
     for (int j = 0; j < n; ++j) {
@@ -512,14 +534,14 @@ static void or_range_row(void* vctx, int r)
 {
     or_range_ctx* c = (or_range_ctx*)vctx;
     const or_problem* p = c->p;
-    int b = r / p->num_q_heads, h = r % p->num_q_heads;
-    int L = c->seq_lens[b];
+    int bi = r / p->num_q_heads, h = r % p->num_q_heads;
+    int L = or_key_limit(p, c->seq_lens, bi);
     double* lo = c->smin + (size_t)r * (size_t)c->max_splits;
     double* hi = c->smax + (size_t)r * (size_t)c->max_splits;
     for (int j = 0; j < c->max_splits; ++j) { lo[j] = NAN; hi[j] = NAN; }
     if (L <= 0) return;
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
-    or_scores(p, c->q, c->k, c->table, b, h, L, s);
+    or_scores(p, c->q, c->k, c->table, bi, h, L, s);
     for (int t = 0; t < L; ++t) {
         int j = t / c->S;
         if (j >= c->max_splits) break;
@@ -536,7 +558,7 @@ int or_score_ranges(const or_problem* p, const void* q, const void* k, const int
                     int n_threads)
 {
     or_range_ctx c = { p, q, k, block_table, seq_lens, S, max_splits, smin, smax };
-    return or_parallel_rows(or_range_row, &c, p->batch * p->num_q_heads, n_threads);
+    return or_parallel_rows(or_range_row, &c, p->batch * or_tq(p) * p->num_q_heads, n_threads);
 }
 
 static int or_cmp_double(const void* a, const void* b)

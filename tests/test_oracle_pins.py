@@ -492,3 +492,65 @@ def test_picked_phi_keeps_exactly_the_counted_splits():
     for h in range(Hq):
         inside = sum(int((f[b, h, j] & oracle.FLAG_OUT) == 0) for b in range(B) for j in range(nb[b]))
         assert inside == kept[h]
+
+
+# ------------------------------------------------------------------------------------------
+# several query tokens per sequence, causal within the last Tq positions (oracle.c, R9)
+# ------------------------------------------------------------------------------------------
+
+def test_query_token_rows_are_decodes_of_shorter_caches():
+    """Query token i of a Tq-token chunk is exactly a single-token decode against the first
+    L_b - Tq + 1 + i keys: two differently shaped computations must agree."""
+    rng = np.random.default_rng(21)
+    B, Tq, Hq, Hkv, d, L = 3, 4, 4, 2, 8, 30
+    q = rng.standard_normal((B, Tq, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    sl = np.array([30, 9, 4], np.int32)
+    prob = _prob(B, Hq, Hkv, d, 0.5, L, q_tokens=Tq)
+    multi, _ = oracle.attention(prob, q.reshape(B * Tq, Hq, d), k, v, sl)
+    multi = multi.reshape(B, Tq, Hq, d)
+    for i in range(Tq):
+        lim = (sl - Tq + 1 + i).astype(np.int32)
+        single, _ = oracle.attention(_prob(B, Hq, Hkv, d, 0.5, L), np.ascontiguousarray(q[:, i]), k,
+                                     v, lim)
+        np.testing.assert_allclose(multi[:, i], single.reshape(B, Hq, d), rtol=0, atol=1e-14)
+
+
+def test_two_query_tokens_closed_form():
+    """L = 2, Tq = 2: the first query token sees key 0 only (out = v_0); the second sees both, a
+    logistic mix with weight sigma(s_1 - s_0) on v_1."""
+    d = 4
+    q = np.array([[[1.0, 0, 0, 0]], [[0.5, 1.0, 0, 0]]], np.float32)      # [Tq][1][d]
+    k = np.array([[[[2.0, 0, 0, 0]], [[0, 3.0, 0, 0]]]], np.float32)       # [1][2][1][d]
+    v = np.array([[[[1.0, 2.0, 3.0, 4.0]], [[-1.0, 0.5, 0.0, 2.0]]]], np.float32)
+    prob = _prob(1, 1, 1, d, 1.0, 2, q_tokens=2)
+    out, _ = oracle.attention(prob, q, k, v, np.array([2], np.int32))
+    np.testing.assert_allclose(out[0], v[0, 0, 0], rtol=0, atol=0)
+    s0, s1 = 0.5 * 2.0, 1.0 * 3.0
+    w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    v64 = v.astype(np.float64)
+    np.testing.assert_allclose(out[1], (1 - w1) * v64[0, 0, 0] + w1 * v64[0, 1, 0], rtol=1e-14)
+
+
+def test_query_tokens_split_method_and_decisions():
+    """The method's steps with Tq query tokens equal the definition, and their decisions equal
+    the window replay, including splits that hold none of an early row's keys. A sequence
+    shorter than Tq leaves its first rows with no key: zero rows."""
+    rng = np.random.default_rng(22)
+    B, Tq, Hq, Hkv, d, L, S = 3, 3, 4, 2, 8, 33, 8
+    q = (rng.standard_normal((B * Tq, Hq, d)) * 2.5).astype(np.float32)
+    k = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    sl = np.array([33, 17, 2], np.int32)                 # 17 = 2 S + 1: an empty last split
+    prob = _prob(B, Hq, Hkv, d, 0.5, L, lo=-4.0, hi=3.0, q_tokens=Tq)
+    ms = -(-L // S)
+    exact, _ = oracle.attention(prob, q, k, v, sl)
+    res = oracle.split_method(prob, q, k, v, sl, S, ms)
+    np.testing.assert_allclose(res["out"], exact, rtol=1e-12, atol=1e-12)
+    f, _ = oracle.window_flags(prob, q, k, sl, S, ms)
+    np.testing.assert_array_equal(res["flags"].reshape(f.shape), f)
+    assert f.any()
+    # sequence 2 has 2 keys for 3 query tokens: its first query row sees none
+    np.testing.assert_array_equal(exact.reshape(B, Tq, Hq, d)[2, 0], 0.0)
+    assert np.abs(exact.reshape(B, Tq, Hq, d)[2, 1]).sum() > 0
