@@ -246,8 +246,10 @@ def oracle_sample_rate(inp, budget_s=None, max_groups=None):
         batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
         head_dim=wl.head_dim, dtype=oracle.F32 if wl.dtype == "f32" else oracle.BF16,
         scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi, max_seq_len=inp.max_seq_len,
-        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq)
+        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
+        q_tokens=wl.q_tokens)
     es = 4 if wl.dtype == "f32" else 2
+    Tq = max(1, wl.q_tokens)
     groups = [(b, g) for b in range(wl.batch) for g in range(wl.num_kv_heads)]
     rng = np.random.default_rng(wl.seed ^ 0xC0FFEE)
     order = rng.permutation(len(groups))
@@ -258,8 +260,9 @@ def oracle_sample_rate(inp, budget_s=None, max_groups=None):
         c_n = chunk if max_groups is None else min(chunk, max_groups - n_groups)
         sel = [groups[order[(i + c) % len(groups)]] for c in range(c_n)]
         i += c_n
-        rows = np.array([(b, g * wl.group + h) for (b, g) in sel for h in range(wl.group)],
-                        np.int32)
+        # every query token of the group: query row b Tq + i, head g G + h
+        rows = np.array([(b * Tq + i, g * wl.group + h) for (b, g) in sel for i in range(Tq)
+                         for h in range(wl.group)], np.int32)
         t0 = time.perf_counter()
         _, used = oracle.attention(prob, inp.q, inp.k, inp.v, inp.seq_lens,
                                    block_table=inp.block_table, rows=rows, n_threads=threads)
@@ -268,7 +271,7 @@ def oracle_sample_rate(inp, budget_s=None, max_groups=None):
         done_bytes += sum(int(inp.seq_lens[b]) * wl.head_dim * 2 * es for (b, g) in sel)
         n_groups += len(sel)
     gbs = done_bytes / done_s / 1e9 if done_s > 0 else 0.0
-    desc = (f"{n_groups} (sequence, kv-head) groups x {wl.group} query heads of {wl.name}, "
+    desc = (f"{n_groups} (sequence, kv-head) groups x {wl.group * Tq} query rows of {wl.name}, "
             f"{done_s:.1f} s of fp64 oracle work on {threads} threads")
     return gbs, threads, desc, done_s, done_bytes
 
@@ -347,7 +350,8 @@ def run_fdpp(args, dist: Dist):
     kw = dict(batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
               head_dim=wl.head_dim, dtype=F.FDPP_F32 if wl.dtype == "f32" else F.FDPP_BF16,
               max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
-              split_len=split_len, mode=args.mode, kernel=args.kernel, tc_stages=args.tc_stages,
+              split_len=split_len, q_tokens=wl.q_tokens, mode=args.mode, kernel=args.kernel,
+              tc_stages=args.tc_stages,
               tc_ctas_per_sm=args.tc_ctas, tc_prefetch=args.tc_prefetch)
     if wl.paged:
         kw.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
@@ -541,6 +545,7 @@ def run_fdpp(args, dist: Dist):
                    "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "seq_len": wl.seq_len if wl.seq_len else list(wl.seq_len_range),
                    "paged": wl.paged, "block_size": wl.block_size if wl.paged else None,
+                   "q_tokens": max(1, wl.q_tokens),
                    "split_len": diag["split_len"], "phi": wl.phi, "window": [wl.lo, wl.hi],
                    "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
                    "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "

@@ -112,6 +112,12 @@ typedef struct fdpp_params {
     const float* phi_heads;  /* DEVICE float32 [Hq], 4-byte aligned: the unified max of each query
                                 head (e.g. from fdpp_pick_phi), used in place of `phi`; NULL = the
                                 scalar `phi` for every head */
+    int q_tokens;            /* Tq query tokens per sequence (0 or 1: one, the decode step): the
+                                sequence's last Tq positions, whose keys are already in the cache,
+                                so query token i sees the keys t < L_b - Tq + 1 + i (a short
+                                prefill chunk or a speculative-decoding step). q and out are then
+                                [B][Tq][Hq][d]. Query rows per kv head, Tq * Hq / Hkv: at most 8
+                                for the tensor kernel, 16 for the SIMT kernel. */
 } fdpp_params;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over
@@ -142,10 +148,10 @@ int fdpp_max_splits(const fdpp_params* p);
 #define FDPP_TC_MAX_PARTS 512
 
 /* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
- * holds the split plan, the per-split partials (o: fp32 [B][Hq][max_splits][d]; l, m: fp32
- * [B][Hq][max_splits]), the flag bytes [B][Hq][max_splits], FDPP_TC_MAX_PARTS extra slots of
- * G = Hq / Hkv rows each (o, l, m and flags, like a split's), the fallback list and a small
- * header. */
+ * holds the split plan, the per-split partials (o: fp32 [B][Tq][Hq][max_splits][d]; l, m: fp32
+ * [B][Tq][Hq][max_splits]), the flag bytes [B][Tq][Hq][max_splits], FDPP_TC_MAX_PARTS extra
+ * slots of Tq * Hq / Hkv rows each (o, l, m and flags, like a split's), the fallback lists and a
+ * small header. */
 fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
 
 /* Zeroes a workspace (stream-ordered). Call once after allocating it; it also clears the
@@ -153,7 +159,7 @@ fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
 fdpp_status fdpp_workspace_init(void* workspace, size_t workspace_bytes, fdpp_stream stream);
 
 /* One decode-attention step for B sequences (enqueued on `stream`).
- *   q           DEVICE [B][Hq][d] of dtype, 16-byte aligned.
+ *   q           DEVICE [B][Tq][Hq][d] of dtype, 16-byte aligned (Tq = q_tokens, 1 by default).
  *   k_cache,    DEVICE, 16-byte aligned, dtype. Contiguous (block_table == NULL):
  *   v_cache       [B][max_seq_len][Hkv][d]. Paged: pools [num_kv_blocks][block_size][Hkv][d];
  *                 token t of sequence b is slot t % block_size of block
@@ -162,7 +168,8 @@ fdpp_status fdpp_workspace_init(void* workspace, size_t workspace_bytes, fdpp_st
  *   seq_lens    DEVICE int32 [B]: L_b, 0 <= L_b <= max_seq_len. L_b == 0 gives a zero row.
  *   workspace   DEVICE, 256-byte aligned, >= fdpp_workspace_size bytes, zeroed once by
  *               fdpp_workspace_init. Not shared by overlapping calls.
- *   out         DEVICE [B][Hq][d] of dtype (rounded to nearest even from fp32).
+ *   out         DEVICE [B][Tq][Hq][d] of dtype (rounded to nearest even from fp32). A query token
+ *               that sees no key (L_b < Tq) gives a zero row.
  * Tokens t >= L_b are never part of a score, a window test or a sum (they may hold anything,
  * NaN included). */
 fdpp_status fdpp_decode_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -205,10 +212,12 @@ fdpp_status fdpp_decode_attn_noalloc(const void* q, const void* k_cache, const v
 /* Score range of every row-split, for choosing phi in advance (opt.ai.kr "FlashDecoding++ async
  * softmax -- theory", section 3: phi is set by observing the score distribution beforehand).
  * On sample inputs laid out as for fdpp_decode_attn (q, k_cache, block_table, seq_lens, p,
- * workspace), writes for each (b, h, j) with j < nsplit[b] the least and greatest scaled score
- * s = scale <q, k_t> over the split's tokens:
- *   smin_host, smax_host  HOST float [B][Hq][max_splits] (NaN past a sequence's splits);
- *   nsplit_host           HOST int32 [B] or NULL.
+ * workspace), writes for each query row (b, i), head h and split j < nsplit[b] the least and
+ * greatest scaled score s = scale <q, k_t> over the split's tokens that row sees:
+ *   smin_host, smax_host  HOST float [B][Tq][Hq][max_splits] (NaN past a sequence's splits, and
+ *                         for a split that holds none of the row's keys);
+ *   nsplit_host           HOST int32 [B][Tq] (each query row's split count, its sequence's) or
+ *                         NULL.
  * V is not read. Enqueues one kernel on `stream` and waits for it (synchronous). Uses the
  * workspace's partial arrays; phi, lo, hi, mode and kernel in p are ignored. */
 fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t* block_table,
@@ -221,16 +230,16 @@ fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t*
  * [smax - hi, smin - lo]. For each head h, phi_out[h] is a value inside the most such intervals
  * of the row-splits j < nsplit[b] over all sequences b; of all values that reach that count, the
  * middle of the widest closed run of them. A head with no split that any phi keeps gets
- * `fallback`. smin, smax: HOST float [B][Hq][max_splits] as written by fdpp_score_ranges;
- * nsplit: HOST int32 [B]; phi_out: HOST float [Hq]; kept_out: HOST int32 [Hq] (the row-splits
- * each phi_out keeps) or NULL. */
+ * `fallback`. smin, smax: HOST float [batch][Hq][max_splits] as written by fdpp_score_ranges
+ * (batch = B * Tq query rows); nsplit: HOST int32 [batch]; phi_out: HOST float [Hq];
+ * kept_out: HOST int32 [Hq] (the row-splits each phi_out keeps) or NULL. */
 fdpp_status fdpp_pick_phi(const float* smin, const float* smax, const int32_t* nsplit, int batch,
                           int num_q_heads, int max_splits, float lo, float hi, float fallback,
                           float* phi_out, int32_t* kept_out);
 
 /* Reads what the last call left in `workspace` (synchronous device-to-host copies; call after
  * that call's stream has been synchronised). diag: HOST, required. flags_host: HOST uint8
- * [B][Hq][max_splits] or NULL. nsplit_host: HOST int32 [B] (splits per sequence) or NULL.
+ * [B][Tq][Hq][max_splits] or NULL. nsplit_host: HOST int32 [B] (splits per sequence) or NULL.
  * Entries with j >= nsplit[b] are stale. */
 fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const fdpp_params* p,
                            fdpp_diag* diag, uint8_t* flags_host, int32_t* nsplit_host);

@@ -57,6 +57,7 @@ class fdpp_params(ctypes.Structure):
         ("split_len", ctypes.c_int), ("mode", ctypes.c_int), ("kernel", ctypes.c_int),
         ("tc_stages", ctypes.c_int), ("tc_ctas_per_sm", ctypes.c_int),
         ("tc_prefetch", ctypes.c_int), ("phi_heads", ctypes.c_void_p),
+        ("q_tokens", ctypes.c_int),
     ]
 
 
@@ -117,12 +118,13 @@ def _check(status: int, where: str) -> None:
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, scale,
                 phi=0.0, lo=-30.0, hi=10.0, split_len=0, block_size=0, max_blocks_per_seq=0,
                 num_kv_blocks=0, mode=FDPP_MODE_NORMAL, kernel=FDPP_KERNEL_AUTO, tc_stages=0,
-                tc_ctas_per_sm=0, tc_prefetch=0, phi_heads=None) -> fdpp_params:
-    """phi_heads: a float32 device tensor [num_q_heads] (or its address), or None."""
+                tc_ctas_per_sm=0, tc_prefetch=0, phi_heads=None, q_tokens=1) -> fdpp_params:
+    """phi_heads: a float32 device tensor [num_q_heads] (or its address), or None. q_tokens:
+    query tokens per sequence (q and out are then [batch][q_tokens][num_q_heads][head_dim])."""
     ph = phi_heads if phi_heads is None or isinstance(phi_heads, int) else phi_heads.data_ptr()
     return fdpp_params(batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, block_size,
                        max_blocks_per_seq, num_kv_blocks, scale, phi, lo, hi, split_len, mode,
-                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch, ph)
+                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch, ph, q_tokens)
 
 
 def fdpp_max_splits(p: fdpp_params) -> int:
@@ -192,12 +194,14 @@ def fdpp_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, p: fdpp
 
 def fdpp_score_ranges(q, k_cache, block_table, seq_lens, p: fdpp_params, workspace, stream=None):
     """Least and greatest score of every row-split on sample inputs (synchronous). Returns
-    (smin, smax float32 numpy [B][Hq][max_splits], NaN past a sequence's splits; nsplit int32)."""
+    (smin, smax float32 numpy [B*Tq][Hq][max_splits], NaN where a query row has no key of the
+    split; nsplit int32 [B*Tq])."""
     import numpy as np
     ms = fdpp_max_splits(p)
-    smin = np.empty((p.batch, p.num_q_heads, ms), np.float32)
+    rows = p.batch * max(1, p.q_tokens)
+    smin = np.empty((rows, p.num_q_heads, ms), np.float32)
     smax = np.empty_like(smin)
-    ns = np.empty(p.batch, np.int32)
+    ns = np.empty(rows, np.int32)
     _check(lib.fdpp_score_ranges(_ptr(q), _ptr(k_cache), _ptr(block_table), _ptr(seq_lens),
                                  ctypes.byref(p), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), smin.ctypes.data,
@@ -225,7 +229,7 @@ def fdpp_read_diag(workspace, p: fdpp_params, want_flags=False, want_nsplit=Fals
     import numpy as np
     d = fdpp_diag()
     ms = fdpp_max_splits(p)
-    flags = np.zeros((p.batch, p.num_q_heads, ms), np.uint8) if want_flags else None
+    flags = np.zeros((p.batch * max(1, p.q_tokens), p.num_q_heads, ms), np.uint8) if want_flags else None
     ns = np.zeros(p.batch, np.int32) if want_nsplit else None
     _check(lib.fdpp_read_diag(_ptr(workspace), workspace.numel() * workspace.element_size(),
                               ctypes.byref(p), ctypes.byref(d),

@@ -44,6 +44,8 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int q_tokens_of(const fdpp_params& p) { return p.q_tokens > 1 ? p.q_tokens : 1; }
+
 int max_splits_of(const fdpp_params& p)
 {
     const long long S = p.split_len > 0 ? p.split_len : FDPP_AUTO_MIN_SPLIT;
@@ -82,12 +84,16 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "tc_prefetch must be -1, 0 or in [1, 32]");
     if (p->phi_heads && ((uintptr_t)p->phi_heads % 4) != 0)
         return fail(FDPP_ERR_INVALID_ARG, "phi_heads must be 4-byte aligned");
+    if (p->q_tokens < 0 || p->q_tokens > 64)
+        return fail(FDPP_ERR_INVALID_ARG, "q_tokens must be in [0, 64] (got %d)", p->q_tokens);
     const int G = p->num_q_heads / p->num_kv_heads;
-    if (G > SIMT_MAX_GROUP)
-        return fail(FDPP_ERR_UNSUPPORTED, "query heads per kv head %d > %d", G, SIMT_MAX_GROUP);
+    const int R = q_tokens_of(*p) * G;
+    if (R > SIMT_MAX_GROUP)
+        return fail(FDPP_ERR_UNSUPPORTED, "query rows per kv head (q_tokens x heads per kv head) %d > %d",
+                    R, SIMT_MAX_GROUP);
     // sizes stay far from overflow: partials below 2^50 bytes, unit indices below 2^31
-    const long double o_bytes = (long double)p->batch * p->num_q_heads * max_splits_of(*p) *
-                                p->head_dim * 4.0L;
+    const long double o_bytes = (long double)p->batch * q_tokens_of(*p) * p->num_q_heads *
+                                max_splits_of(*p) * p->head_dim * 4.0L;
     const long double units = (long double)p->batch * p->num_kv_heads * max_splits_of(*p);
     if (o_bytes > 1e15L || units > 2e9L)
         return fail(FDPP_ERR_INVALID_ARG, "problem too large for one workspace");
@@ -119,7 +125,7 @@ WsLayout layout_of(const fdpp_params& p)
 {
     WsLayout w{};
     w.max_splits = max_splits_of(p);
-    const size_t rows = (size_t)p.batch * p.num_q_heads;
+    const size_t rows = (size_t)p.batch * q_tokens_of(p) * p.num_q_heads;
     const size_t slots = rows * (size_t)w.max_splits;
     size_t off = 0;
     w.header = off;  off = align256(off + HDR_WORDS * 4);
@@ -132,9 +138,9 @@ WsLayout layout_of(const fdpp_params& p)
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
     w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
-    // extra slots of the tensor kernel's parts (G rows each)
-    const size_t G = (size_t)(p.num_q_heads / p.num_kv_heads);
-    const size_t xrows = (size_t)TC_MAX_PARTS * G;
+    // extra slots of the tensor kernel's parts (R = Tq G rows each)
+    const size_t R = (size_t)q_tokens_of(p) * (size_t)(p.num_q_heads / p.num_kv_heads);
+    const size_t xrows = (size_t)TC_MAX_PARTS * R;
     w.xf = off;      off = align256(off + xrows);
     w.xm = off;      off = align256(off + xrows * 4);
     w.xl = off;      off = align256(off + xrows * 4);
@@ -255,6 +261,8 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.Hq = p->num_q_heads;
     a.Hkv = p->num_kv_heads;
     a.G = G;
+    a.Tq = q_tokens_of(*p);
+    a.R = a.Tq * G;
     a.D = p->head_dim;
     a.max_seq_len = p->max_seq_len;
     a.block_size = paged ? p->block_size : 0;
@@ -355,11 +363,11 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         return fail(FDPP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, w.total);
 
     const int G = p->num_q_heads / p->num_kv_heads;
-    const bool tc_ok = p->dtype == FDPP_BF16 && G <= TC_MAX_GROUP;
+    const bool tc_ok = p->dtype == FDPP_BF16 && q_tokens_of(*p) * G <= TC_MAX_GROUP;
     int kernel = p->kernel;
     if (kernel == FDPP_KERNEL_AUTO) kernel = tc_ok ? FDPP_KERNEL_TENSOR : FDPP_KERNEL_SIMT;
     if (kernel == FDPP_KERNEL_TENSOR && !tc_ok)
-        return fail(FDPP_ERR_UNSUPPORTED, "tensor kernel needs bf16 and at most %d query heads per kv head",
+        return fail(FDPP_ERR_UNSUPPORTED, "tensor kernel needs bf16 and at most %d query rows per kv head",
                     TC_MAX_GROUP);
 
     DeviceInfo dev;
@@ -374,7 +382,7 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     if (kernel == FDPP_KERNEL_TENSOR) {
-        const TcPlan plan = split_tc_plan(p->head_dim, G, p->batch, p->tc_stages,
+        const TcPlan plan = split_tc_plan(p->head_dim, q_tokens_of(*p) * G, p->batch, p->tc_stages,
                                           p->tc_ctas_per_sm, dev.smem_per_sm, dev.smem_per_block);
         if (plan.nstage == 0)
             return fail(FDPP_ERR_UNSUPPORTED, "no tensor-kernel geometry fits (stages %d, CTAs/SM %d)",
@@ -441,23 +449,28 @@ fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t*
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
 
-    const size_t B = (size_t)p->batch, Hq = (size_t)p->num_q_heads, ms = (size_t)w.max_splits;
+    const size_t B = (size_t)p->batch, Tq = (size_t)q_tokens_of(*p), Hq = (size_t)p->num_q_heads,
+                 ms = (size_t)w.max_splits, rows = B * Tq * Hq;
     const uint8_t* ws = static_cast<const uint8_t*>(workspace);
     std::string nsb(B * 4, '\0');
     if ((e = cudaMemcpy(&nsb[0], ws + w.nsplit, nsb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess ||
-        (e = cudaMemcpy(smin_host, ws + w.l_part, B * Hq * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
-        (e = cudaMemcpy(smax_host, ws + w.m_part, B * Hq * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        (e = cudaMemcpy(smin_host, ws + w.l_part, rows * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess ||
+        (e = cudaMemcpy(smax_host, ws + w.m_part, rows * ms * 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
     const int32_t* ns = reinterpret_cast<const int32_t*>(nsb.data());
-    for (size_t b = 0; b < B; ++b) {
+    for (size_t r = 0; r < rows; ++r) {
+        const size_t b = r / (Tq * Hq);
         const size_t n = ns[b] < 0 ? 0 : (ns[b] > (int)ms ? ms : (size_t)ns[b]);
-        for (size_t h = 0; h < Hq; ++h)
-            for (size_t j = n; j < ms; ++j) {
-                smin_host[(b * Hq + h) * ms + j] = NAN;
-                smax_host[(b * Hq + h) * ms + j] = NAN;
-            }
+        for (size_t j = 0; j < ms; ++j) {
+            float& lo = smin_host[r * ms + j];
+            float& hi = smax_host[r * ms + j];
+            // past the sequence's splits, or a split holding none of this query row's keys
+            if (j >= n || !std::isfinite(lo) || !std::isfinite(hi)) { lo = NAN; hi = NAN; }
+        }
     }
-    if (nsplit_host) std::memcpy(nsplit_host, ns, B * 4);
+    if (nsplit_host)
+        for (size_t b = 0; b < B; ++b)
+            for (size_t i = 0; i < Tq; ++i) nsplit_host[b * Tq + i] = ns[b];
     return FDPP_OK;
 }
 
@@ -544,9 +557,10 @@ fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const 
     int32_t hdr[HDR_WORDS];
     cudaError_t e = cudaMemcpy(hdr, ws + w.header, sizeof hdr, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
-    const size_t B = (size_t)p->batch, Hq = (size_t)p->num_q_heads, ms = (size_t)w.max_splits;
+    const size_t B = (size_t)p->batch, Tq = (size_t)q_tokens_of(*p), Hq = (size_t)p->num_q_heads,
+                 ms = (size_t)w.max_splits;
     std::string nsb(B * 4, '\0');
-    std::string flb(B * Hq * ms, '\0');
+    std::string flb(B * Tq * Hq * ms, '\0');
     if ((e = cudaMemcpy(&nsb[0], ws + w.nsplit, nsb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess ||
         (e = cudaMemcpy(&flb[0], ws + w.flags, flb.size(), cudaMemcpyDeviceToHost)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaMemcpy: %s", cudaGetErrorString(e));
@@ -564,11 +578,12 @@ fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const 
         for (int j = 0; j < n; ++j) {
             for (size_t g = 0; g < (size_t)p->num_kv_heads; ++g) {
                 bool any = false;
-                for (size_t hh = 0; hh < G; ++hh) {
-                    const uint8_t f = fl[((b * Hq) + g * G + hh) * ms + (size_t)j];
-                    if (f & FDPP_FLAG_OUT) { ++diag->n_flagged_row_splits; any = true; }
-                    if (f & FDPP_FLAG_RECOMPUTED) ++diag->n_recomputed_row_splits;
-                }
+                for (size_t i = 0; i < Tq; ++i)
+                    for (size_t hh = 0; hh < G; ++hh) {
+                        const uint8_t f = fl[(((b * Tq + i) * Hq) + g * G + hh) * ms + (size_t)j];
+                        if (f & FDPP_FLAG_OUT) { ++diag->n_flagged_row_splits; any = true; }
+                        if (f & FDPP_FLAG_RECOMPUTED) ++diag->n_recomputed_row_splits;
+                    }
                 if (any) ++diag->n_flagged_units;
             }
         }

@@ -61,15 +61,16 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rpc = NW / wpr;                       // rows of this CTA, wpr warps each
     const int rl = warp / wpr, wr = warp - rl * wpr;
-    const int row = blockIdx.x * rpc + rl;          // b * Hq + h
-    const bool live = row < a.B * a.Hq;
+    const int row = blockIdx.x * rpc + rl;          // (b Tq + i) Hq + h: head h of query token i
+    const bool live = row < a.B * a.Tq * a.Hq;
     // the split kernel has finished: its fallback-list counters go back to zero for the next call
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int i = 0; i < 2 * REDO_NLISTS; ++i) a.hdr[HDR_REDO_LISTS + i] = 0;
     }
-    const int b = live ? row / a.Hq : 0;
-    const int h = live ? row - b * a.Hq : 0;
-    const int hh = h - h / a.G * a.G;               // head within its group
+    const int bi = live ? row / a.Hq : 0;           // query row of the batch: b Tq + i
+    const int b = bi / a.Tq;
+    const int h = live ? row - bi * a.Hq : 0;
+    const int rr = (bi - b * a.Tq) * a.G + h % a.G;  // the unit's query row (extra-slot row)
     const int n = live ? a.nsplit[b] : 0;
 
     // Parts that may start inside this row's units: the row's kv head owns tiles [W, W + nt).
@@ -95,9 +96,9 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         const int jx = ki / TS;
         return ki == jx * TS ? -1 : jx;
     };
-    const float* xm = a.xm + hh;
-    const float* xl = a.xl + hh;
-    const float* xo = a.xo + (long long)hh * D;
+    const float* xm = a.xm + rr;
+    const float* xl = a.xl + rr;
+    const float* xo = a.xo + (long long)rr * D;
     const long long base = (long long)row * a.max_splits;
     const float* m = a.m_part + base;
     const float* l = a.l_part + base;
@@ -118,13 +119,13 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         const int c = c_lo + (e - n);
         const int jx = extra_split(c);
         if (jx >= 0) {
-            M = fmaxf(M, xm[(long long)c * a.G]);
+            M = fmaxf(M, xm[(long long)c * a.R]);
             // the split's flag byte also covers the extra slot's tokens
             uint8_t* fb = a.flags + (long long)row * a.max_splits + jx;
             const uintptr_t addr = reinterpret_cast<uintptr_t>(fb);
             const unsigned sh = (unsigned)(addr & 3u) * 8u;
             atomicOr(reinterpret_cast<unsigned*>(addr & ~uintptr_t(3)),
-                     (unsigned)a.xf[(long long)c * a.G + hh] << sh);
+                     (unsigned)a.xf[(long long)c * a.R + rr] << sh);
         }
     }
 #pragma unroll
@@ -157,8 +158,8 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
                 } else {
                     const int c = c_lo + (e - n);
                     if (extra_split(c) >= 0) {
-                        pm = xm + (long long)c * a.G; pl = xl + (long long)c * a.G;
-                        po = xo + (long long)c * a.G * D;
+                        pm = xm + (long long)c * a.R; pl = xl + (long long)c * a.R;
+                        po = xo + (long long)c * a.R * D;
                         ok[u] = true;
                     }
                 }
@@ -200,7 +201,8 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
             const int d = lane + 32 * e;
             float total = 0.f;
             for (int w = 0; w < wpr; ++w) total += s_acc[rl * wpr + w][d];
-            store_out<T>(out + d, n > 0 ? __fdiv_rn(total, ltot) : 0.f);
+            // a query row that sees no key (or a sequence without keys) is a zero row
+            store_out<T>(out + d, (n > 0 && ltot != 0.f) ? __fdiv_rn(total, ltot) : 0.f);
         }
     }
 }
@@ -219,7 +221,7 @@ int warps_per_row(long long rows, int num_sms)
 template <typename T, int D>
 cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
 {
-    const long long rows = (long long)a.B * a.Hq;
+    const long long rows = (long long)a.B * a.Tq * a.Hq;
     const int wpr = warps_per_row(rows, a.num_sms);
     const int nw = wpr > CW ? CW_WIDE : CW;
     const int rpc = nw / wpr;

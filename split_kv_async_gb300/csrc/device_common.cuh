@@ -341,6 +341,22 @@ __device__ __forceinline__ unsigned classify(float x, float lo, float hi)
 }
 
 // exp(m_w - M) with the exact 1 when the frames agree (so phi-frame partials add plainly).
+// Partial slot of query row rr of unit (b, g): query token i = rr / G of sequence b, head
+// g G + rr % G, split j. Partial arrays are [B][Tq][Hq][max_splits].
+__device__ __forceinline__ long long unit_row_slot(const KernelArgs& a, int b, int g, int rr, int j)
+{
+    const int i = rr / a.G, hh = rr - i * a.G;
+    return (((long long)b * a.Tq + i) * a.Hq + (long long)g * a.G + hh) * a.max_splits + j;
+}
+
+// Keys query token i of a sequence with L keys sees: t < L - Tq + 1 + i (causal over the last
+// Tq positions; all L keys for Tq = 1).
+__device__ __forceinline__ int key_limit(const KernelArgs& a, int L, int i)
+{
+    const int lim = L - a.Tq + 1 + i;
+    return lim < 0 ? 0 : lim;
+}
+
 // Unified max of query head h: its own value when the caller gave one per head.
 __device__ __forceinline__ float phi_of(const KernelArgs& a, int h)
 {

@@ -60,15 +60,17 @@ struct KernelArgs {
     int32_t* tstart;              // [B + 1] tile prefix of the sequences (tensor kernel, CTA 0)
     long long* redo;              // fallback lists, REDO_WORDS per entry (tensor kernel)
     int redo_cap;                 // entries per fallback list
-    uint8_t* flags;               // [B][Hq][max_splits]
-    float* m_part;                // [B][Hq][max_splits]
-    float* l_part;                // [B][Hq][max_splits]
-    float* o_part;                // [B][Hq][max_splits][D]
-    uint8_t* xf;                  // extra slots [TC_MAX_PARTS][G]: flags,
+    uint8_t* flags;               // [B][Tq][Hq][max_splits]
+    float* m_part;                // [B][Tq][Hq][max_splits]
+    float* l_part;                // [B][Tq][Hq][max_splits]
+    float* o_part;                // [B][Tq][Hq][max_splits][D]
+    uint8_t* xf;                  // extra slots [TC_MAX_PARTS][R]: flags,
     float* xm;                    //   m,
     float* xl;                    //   l,
-    float* xo;                    //   o [TC_MAX_PARTS][G][D]
+    float* xo;                    //   o [TC_MAX_PARTS][R][D]
     int B, Hq, Hkv, G, D;
+    int Tq;                       // query tokens per sequence (the last Tq positions, causal)
+    int R;                        // query rows per kv head and sequence: Tq * G
     int max_seq_len, block_size, max_blocks, num_blocks;
     int split_req, max_splits, num_sms;
     float scale, phi, lo, hi;
@@ -79,8 +81,8 @@ struct KernelArgs {
     int pf_tiles;                 // tensor kernel: L2 prefetch distance in tiles (0 = off)
 };
 
-// Tensor-core kernel shape limits (bf16, G <= 8 so that the hi and lo halves of P fit the
-// 16 rows of one m16n8k16 A tile).
+// Query rows per kv head (R = Tq * G) each kernel handles: the tensor kernel's 8 columns of one
+// m16n8k16 tile, the SIMT kernel's 16 register rows.
 constexpr int TC_MAX_GROUP = 8;
 constexpr int SIMT_MAX_GROUP = 16;
 

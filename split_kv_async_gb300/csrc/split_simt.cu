@@ -85,8 +85,8 @@ __device__ __forceinline__ long long kv_row(const KernelArgs& a, int b, int t, i
 template <typename T, int E, int GM, bool ONLINE>
 __device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int t0, int t1,
                                           const float (&qr)[GM][E], const float (&ph)[GM],
-                                          float (&o)[GM][E], float (&l)[GM], float (&m)[GM],
-                                          unsigned (&fl)[GM], bool& bad_block)
+                                          const int (&lim)[GM], float (&o)[GM][E], float (&l)[GM],
+                                          float (&m)[GM], unsigned (&fl)[GM], bool& bad_block)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const T* K = static_cast<const T*>(a.k);
@@ -107,7 +107,8 @@ __device__ __forceinline__ void warp_pass(const KernelArgs& a, int b, int g, int
         Elem<T>::template load<E>(V + row + lane * E, vx);
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-            if (h >= a.G) break;
+            if (h >= a.R) break;
+            if (t >= lim[h]) continue;             // past this query row's keys (warp-uniform)
             float part = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) part = fmaf(qr[h][e], kx[e], part);
@@ -147,13 +148,13 @@ __device__ __forceinline__ void merge_and_store(const KernelArgs& a, SimtShared<
     __syncthreads();   // previous readers of sh are done
 #pragma unroll
     for (int h = 0; h < GM; ++h) {
-        if (h >= a.G) break;
+        if (h >= a.R) break;
 #pragma unroll
         for (int e = 0; e < E; ++e) sh.o[warp][h][lane * E + e] = o[h][e];
         if (lane == 0) { sh.l[warp][h] = l[h]; sh.m[warp][h] = m[h]; sh.f[warp][h] = fl[h]; }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < a.G * D; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < a.R * D; idx += kThreads) {
         const int h = idx / D, d = idx - h * D;
         if (!((write_mask >> h) & 1u)) continue;
         float M = sh.m[0][h];
@@ -162,17 +163,16 @@ __device__ __forceinline__ void merge_and_store(const KernelArgs& a, SimtShared<
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) acc = fmaf(frame_weight(sh.m[w][h], M), sh.o[w][h][d], acc);
-        const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
-        a.o_part[r * D + d] = acc;
+        a.o_part[unit_row_slot(a, b, g, h, j) * D + d] = acc;
     }
-    if (threadIdx.x < a.G && ((write_mask >> threadIdx.x) & 1u)) {
+    if (threadIdx.x < a.R && ((write_mask >> threadIdx.x) & 1u)) {
         const int h = threadIdx.x;
         float M = sh.m[0][h];
         unsigned f = sh.f[0][h];
         for (int w = 1; w < kWarps; ++w) { M = fmaxf(M, sh.m[w][h]); f |= sh.f[w][h]; }
         float lsum = 0.f;
         for (int w = 0; w < kWarps; ++w) lsum = fmaf(frame_weight(sh.m[w][h], M), sh.l[w][h], lsum);
-        const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
+        const long long r = unit_row_slot(a, b, g, h, j);
         a.l_part[r] = lsum;
         a.m_part[r] = M;
         if (store_flags) a.flags[r] = (uint8_t)(f | extra_flag);
@@ -194,42 +194,45 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(KernelArgs a)
     UnitCursor cur;
     cur.reset();
     bool bad_block = false;
-    const unsigned all_heads = (a.G >= 32) ? 0xffffffffu : ((1u << a.G) - 1u);
+    const unsigned all_heads = (a.R >= 32) ? 0xffffffffu : ((1u << a.R) - 1u);
 
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
         int b, g, j, L;
         cur.seek(a, S, u, b, g, j, L);
         const int t0 = j * S, t1 = min(t0 + S, L);
 
+        // the unit's R = Tq G query rows: row h is head g G + h % G of query token h / G
         float qr[GM][E];
+        float ph[GM];                               // each row's unified max (its head's)
+        int lim[GM];                                // each row's key limit
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-            if (h < a.G) {
-                Elem<T>::template load<E>(Q + ((long long)b * a.Hq + (long long)g * a.G + h) * a.D + lane * E, qr[h]);
+            const int i = h / a.G, hh = h - i * a.G;
+            if (h < a.R) {
+                Elem<T>::template load<E>(Q + (((long long)b * a.Tq + i) * a.Hq + (long long)g * a.G + hh) * a.D + lane * E, qr[h]);
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) qr[h][e] = 0.f;
             }
+            ph[h] = h < a.R ? phi_of(a, g * a.G + hh) : a.phi;
+            lim[h] = h < a.R ? key_limit(a, L, i) : 0;
         }
-        float ph[GM];                               // each head's unified max
-#pragma unroll
-        for (int h = 0; h < GM; ++h) ph[h] = h < a.G ? phi_of(a, g * a.G + h) : a.phi;
         float o[GM][E], l[GM], m[GM];
         unsigned fl[GM];
         if (a.mode == FDPP_MODE_FORCE_ONLINE) {
-            warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
+            warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, lim, o, l, m, fl, bad_block);
             merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, FDPP_FLAG_RECOMPUTED, true);
             continue;
         }
-        warp_pass<T, E, GM, false>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
+        warp_pass<T, E, GM, false>(a, b, g, t0, t1, qr, ph, lim, o, l, m, fl, bad_block);
         merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, all_heads, 0u, true);
         if (a.mode != FDPP_MODE_NORMAL) continue;
         unsigned redo = 0u;
-        for (int h = 0; h < a.G; ++h)
+        for (int h = 0; h < a.R; ++h)
             if (sh.unit_flags[h] & FDPP_FLAG_OUT) redo |= 1u << h;
         if (!redo) continue;
         // the split left the safe window: read it again with the ordinary online softmax
-        warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, o, l, m, fl, bad_block);
+        warp_pass<T, E, GM, true>(a, b, g, t0, t1, qr, ph, lim, o, l, m, fl, bad_block);
         merge_and_store<E, GM>(a, sh, b, g, j, o, l, m, fl, redo, FDPP_FLAG_RECOMPUTED, false);
     }
     if (bad_block) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
@@ -258,14 +261,17 @@ __global__ void __launch_bounds__(kThreads) score_range_kernel(KernelArgs a)
         cur.seek(a, S, u, b, g, j, L);
         const int t0 = j * S, t1 = min(t0 + S, L);
         float qr[GM][E];
+        int lim[GM];
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-            if (h < a.G) {
-                Elem<T>::template load<E>(Q + ((long long)b * a.Hq + (long long)g * a.G + h) * a.D + lane * E, qr[h]);
+            const int i = h / a.G, hh = h - i * a.G;
+            if (h < a.R) {
+                Elem<T>::template load<E>(Q + (((long long)b * a.Tq + i) * a.Hq + (long long)g * a.G + hh) * a.D + lane * E, qr[h]);
             } else {
 #pragma unroll
                 for (int e = 0; e < E; ++e) qr[h][e] = 0.f;
             }
+            lim[h] = h < a.R ? key_limit(a, L, i) : 0;
         }
         float lo[GM], hi[GM];
 #pragma unroll
@@ -277,7 +283,8 @@ __global__ void __launch_bounds__(kThreads) score_range_kernel(KernelArgs a)
             Elem<T>::template load<E>(K + row + lane * E, kx);
 #pragma unroll
             for (int h = 0; h < GM; ++h) {
-                if (h >= a.G) break;
+                if (h >= a.R) break;
+                if (t >= lim[h]) continue;         // past this query row's keys (warp-uniform)
                 float part = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) part = fmaf(qr[h][e], kx[e], part);
@@ -293,11 +300,11 @@ __global__ void __launch_bounds__(kThreads) score_range_kernel(KernelArgs a)
             for (int h = 0; h < GM; ++h) { s_lo[warp][h] = lo[h]; s_hi[warp][h] = hi[h]; }
         }
         __syncthreads();
-        if (threadIdx.x < a.G) {
+        if (threadIdx.x < a.R) {
             const int h = threadIdx.x;
             float mn = s_lo[0][h], mx = s_hi[0][h];
             for (int w = 1; w < kWarps; ++w) { mn = fminf(mn, s_lo[w][h]); mx = fmaxf(mx, s_hi[w][h]); }
-            const long long r = ((long long)b * a.Hq + (long long)g * a.G + h) * a.max_splits + j;
+            const long long r = unit_row_slot(a, b, g, h, j);
             a.l_part[r] = mn;
             a.m_part[r] = mx;
         }
@@ -316,7 +323,7 @@ template <typename T>
 cudaError_t launch_dtype(const KernelArgs& a, int grid, cudaStream_t s)
 {
     const bool e4 = (a.D == 128);
-    if (a.G <= 4) return e4 ? launch_t<T, 4, 4>(a, grid, s) : launch_t<T, 2, 4>(a, grid, s);
+    if (a.R <= 4) return e4 ? launch_t<T, 4, 4>(a, grid, s) : launch_t<T, 2, 4>(a, grid, s);
     return e4 ? launch_t<T, 4, 16>(a, grid, s) : launch_t<T, 2, 16>(a, grid, s);
 }
 
@@ -334,7 +341,7 @@ template <typename T>
 int occ_dtype(const KernelArgs& a)
 {
     const bool e4 = (a.D == 128);
-    if (a.G <= 4) return e4 ? occ_t<T, 4, 4>() : occ_t<T, 2, 4>();
+    if (a.R <= 4) return e4 ? occ_t<T, 4, 4>() : occ_t<T, 2, 4>();
     return e4 ? occ_t<T, 4, 16>() : occ_t<T, 2, 16>();
 }
 
@@ -357,7 +364,7 @@ template <typename T>
 cudaError_t launch_ranges_dtype(const KernelArgs& a, int grid, cudaStream_t s)
 {
     const bool e4 = (a.D == 128);
-    if (a.G <= 4) {
+    if (a.R <= 4) {
         if (e4) score_range_kernel<T, 4, 4><<<grid, kThreads, 0, s>>>(a);
         else score_range_kernel<T, 2, 4><<<grid, kThreads, 0, s>>>(a);
     } else {
@@ -373,7 +380,7 @@ int ranges_occ_dtype(const KernelArgs& a)
     int n = 0;
     const bool e4 = (a.D == 128);
     cudaError_t e;
-    if (a.G <= 4)
+    if (a.R <= 4)
         e = e4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 4, 4>, kThreads, 0)
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_range_kernel<T, 2, 4>, kThreads, 0);
     else

@@ -60,7 +60,7 @@ static_assert(NCW * 8 * (128 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 128 * 2, "
 // unit kinds carried in the Q-ring header
 enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
 // header words
-enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_WORDS };
+enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_L, H_WORDS };
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge
 // scratch of a unit lives in the stage of the unit's last tile (offsets scr_* relative to that
@@ -119,11 +119,6 @@ __device__ __forceinline__ bool consumer_sync(const Ring& rg, uint32_t& parity, 
     const bool ok = ring_wait(rg.cbar, parity, misc, a);
     parity ^= 1u;
     return ok;
-}
-
-__device__ __forceinline__ long long row_slot(const KernelArgs& a, int b, int h, int j)
-{
-    return ((long long)b * a.Hq + h) * a.max_splits + j;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -222,8 +217,8 @@ struct Producer {
                 const int nb = in_smem ? plan[b + 1] - plan[b]
                                        : clamp_len(A.seq_lens[b], A.max_seq_len);
                 if (nb != 0) continue;
-                for (int i = lane; i < A.Hq * A.D; i += 32)
-                    out[(long long)b * A.Hq * A.D + i] = __float2bfloat16_rn(0.f);
+                for (int i = lane; i < A.Tq * A.Hq * A.D; i += 32)
+                    out[(long long)b * A.Tq * A.Hq * A.D + i] = __float2bfloat16_rn(0.f);
             }
         }
         return n_units;
@@ -279,15 +274,18 @@ struct Producer {
             int* hdr = reinterpret_cast<int*>(smp + lay->qring + qs * lay->qslot_bytes);
             hdr[H_KIND] = kind; hdr[H_B] = b; hdr[H_G] = g; hdr[H_J] = j;
             hdr[H_T0] = t0; hdr[H_T1] = t1; hdr[H_DEST] = dest;
-            hdr[H_F0] = hw[0]; hdr[H_F1] = hw[1]; hdr[H_MASK] = hw[2];
+            hdr[H_F0] = hw[0]; hdr[H_F1] = hw[1]; hdr[H_MASK] = hw[2]; hdr[H_L] = L;
             if (kind == KIND_END) {
                 mbar_arrive(rg.qfull + 8 * qs);
             } else {
+                // the unit's R = Tq G query rows: row i G + hh is head g G + hh of query token i
                 const uint32_t bytes = (uint32_t)(A.G * D * 2);
-                const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(A.q) +
-                                           ((long long)b * A.Hq + (long long)g * A.G) * D;
-                mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes);
-                bulk_load(slot + QHDR_BYTES, src, bytes, rg.qfull + 8 * qs);
+                mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes * (uint32_t)A.Tq);
+                for (int i = 0; i < A.Tq; ++i) {
+                    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(A.q) +
+                        (((long long)b * A.Tq + i) * A.Hq + (long long)g * A.G) * D;
+                    bulk_load(slot + QHDR_BYTES + i * bytes, src, bytes, rg.qfull + 8 * qs);
+                }
             }
         }
         ++qiter;
@@ -555,9 +553,9 @@ struct Producer {
                 const int L = clamp_len(A.seq_lens[rb], A.max_seq_len);
                 // flag bytes of the segment's G heads (written by the pushing CTA before its push)
                 int hw[3] = {0, 0, 0};
-                if (lane < A.G) {
-                    const unsigned f = dest < 0 ? __ldcg(A.flags + row_slot(A, rb, rg_ * A.G + lane, rj))
-                                                : __ldcg(A.xf + (long long)dest * A.G + lane);
+                if (lane < A.R) {
+                    const unsigned f = dest < 0 ? __ldcg(A.flags + unit_row_slot(A, rb, rg_, lane, rj))
+                                                : __ldcg(A.xf + (long long)dest * A.R + lane);
                     const unsigned sh = (unsigned)(lane & 3) * 8u;
                     const unsigned w0 = lane < 4 ? (f << sh) : 0u;
                     const unsigned w1 = lane >= 4 ? (f << sh) : 0u;
@@ -597,8 +595,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ctid = threadIdx.x;
     const int r = lane >> 2, qd = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;      // ldmatrix: matrix and row of this lane
-    const bool pack_lo = a.G <= 4;
-    const bool q_ok = r < a.G;                    // this lane supplies Q row (head) r
+    const bool pack_lo = a.R <= 4;
+    const bool q_ok = r < a.R;                    // this lane supplies Q row r
     const uint32_t k_row = warp * TPW + (mi & 1) * 8 + r8;
     const uint32_t v_row = warp * TPW + (mi >> 1) * 8 + r8;
     const int tok_r = warp * TPW + r;             // this lane's tokens: tok_r and tok_r + 8
@@ -615,7 +613,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const int kind = hdr[H_KIND];
         if (kind == KIND_END) return;
         const int b = hdr[H_B], g = hdr[H_G], j = hdr[H_J];
-        const int t0 = hdr[H_T0], t1 = hdr[H_T1], dest = hdr[H_DEST];
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], dest = hdr[H_DEST], seq_len = hdr[H_L];
         const unsigned fw0 = (unsigned)hdr[H_F0], fw1 = (unsigned)hdr[H_F1];
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
         const bool redo = kind == KIND_REDO;
@@ -638,10 +636,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float lsum[2] = {0.f, 0.f};
-        const bool hv[2] = {head0 < a.G, head0 + 1 < a.G};
-        // this lane's heads' unified max (their own values when given per head)
-        const float phv[2] = {hv[0] ? phi_of(a, g * a.G + head0) : a.phi,
-                              hv[1] ? phi_of(a, g * a.G + head0 + 1) : a.phi};
+        // this lane's two query rows head0, head0 + 1: row rr is head g G + rr % G of query token
+        // rr / G, which sees the keys t < L - Tq + 1 + rr / G
+        const bool hv[2] = {head0 < a.R, head0 + 1 < a.R};
+        const float phv[2] = {hv[0] ? phi_of(a, g * a.G + head0 % a.G) : a.phi,
+                              hv[1] ? phi_of(a, g * a.G + (head0 + 1) % a.G) : a.phi};
+        const int klim[2] = {key_limit(a, seq_len, head0 / a.G), key_limit(a, seq_len, (head0 + 1) / a.G)};
         float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
         const int ntiles = ceil_div_i(t1 - t0, TILE);
@@ -669,7 +669,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
-                valid[e] = hv[e & 1] && (tok_r + 8 * (e >> 1) < nvalid);
+                const int tok = tok_r + 8 * (e >> 1);
+                valid[e] = hv[e & 1] && (tok < nvalid) && (t0 + i * TILE + tok < klim[e & 1]);
                 if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
             }
 
@@ -783,48 +784,47 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             if (!hv[c] || (pack_lo && qd >= 2)) continue;
-            float* row = scr_o + (warp * a.G + head0 + c) * lay.scr_row;
+            float* row = scr_o + (warp * a.R + head0 + c) * lay.scr_row;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 row[16 * mt + r] = o[mt][c];
                 row[16 * mt + r + 8] = o[mt][c + 2];
             }
             if (r == 0) {
-                scr_l[warp * a.G + head0 + c] = lsum[c];
-                scr_m[warp * a.G + head0 + c] = mrun[c];
-                scr_f[warp * a.G + head0 + c] = fl[c];
+                scr_l[warp * a.R + head0 + c] = lsum[c];
+                scr_m[warp * a.R + head0 + c] = mrun[c];
+                scr_f[warp * a.R + head0 + c] = fl[c];
             }
         }
         if (!consumer_sync(rg, cpar, misc, a)) return;
         const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
         // The four warp partials of each head, summed in warp order. In the phi frame every
         // warp's m is phi and each weight is exactly 1, so the sum needs no exponentials.
-        // Destination: the split's own slot (heads max_splits slots apart) or the extra slot of
-        // a part that began inside the unit (heads adjacent).
-        float* o_dst = dest < 0 ? a.o_part + row_slot(a, b, g * a.G, j) * D
-                                : a.xo + (long long)dest * a.G * D;
-        const long long o_hstride = dest < 0 ? (long long)a.max_splits * D : (long long)D;
+        // Destination: the split's own slot of each query row, or the extra slot of a part that
+        // began inside the unit (rows adjacent).
         {
-            constexpr int HPP = NCT / D;           // heads per pass of the 128 threads
+            constexpr int HPP = NCT / D;           // rows per pass of the 128 threads
             const int d = ctid % D, hsub = ctid / D;
 #pragma unroll
             for (int k = 0; k < TC_MAX_GROUP / HPP; ++k) {
-                const int hh = k * HPP + hsub;
-                if (hh < a.G && ((write_mask >> hh) & 1u)) {
+                const int hh = k * HPP + hsub;     // query row
+                if (hh < a.R && ((write_mask >> hh) & 1u)) {
                     float acc = 0.f;
                     if (!online) {
 #pragma unroll
-                        for (int w = 0; w < NCW; ++w) acc += scr_o[(w * a.G + hh) * lay.scr_row + d];
+                        for (int w = 0; w < NCW; ++w) acc += scr_o[(w * a.R + hh) * lay.scr_row + d];
                     } else {
                         float M = scr_m[hh];
 #pragma unroll
-                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
+                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
 #pragma unroll
                         for (int w = 0; w < NCW; ++w)
-                            acc = fmaf(frame_weight(scr_m[w * a.G + hh], M),
-                                       scr_o[(w * a.G + hh) * lay.scr_row + d], acc);
+                            acc = fmaf(frame_weight(scr_m[w * a.R + hh], M),
+                                       scr_o[(w * a.R + hh) * lay.scr_row + d], acc);
                     }
-                    o_dst[hh * o_hstride + d] = acc;
+                    float* o_dst = dest < 0 ? a.o_part + unit_row_slot(a, b, g, hh, j) * D
+                                            : a.xo + ((long long)dest * a.R + hh) * D;
+                    o_dst[d] = acc;
                 }
             }
         }
@@ -834,20 +834,20 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             const int hh = lane;
             unsigned f = 0u;
             float M = 0.f, lam = 0.f;
-            if (hh < a.G) {
+            if (hh < a.R) {
 #pragma unroll
-                for (int w = 0; w < NCW; ++w) f |= scr_f[w * a.G + hh];
+                for (int w = 0; w < NCW; ++w) f |= scr_f[w * a.R + hh];
                 M = scr_m[hh];
 #pragma unroll
-                for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.G + hh]);
+                for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
 #pragma unroll
                 for (int w = 0; w < NCW; ++w)
-                    lam = online ? fmaf(frame_weight(scr_m[w * a.G + hh], M), scr_l[w * a.G + hh], lam)
-                                 : lam + scr_l[w * a.G + hh];
+                    lam = online ? fmaf(frame_weight(scr_m[w * a.R + hh], M), scr_l[w * a.R + hh], lam)
+                                 : lam + scr_l[w * a.R + hh];
             }
-            unit_out = __ballot_sync(0xffffffffu, hh < a.G && (f & FDPP_FLAG_OUT));
-            if (hh < a.G && ((write_mask >> hh) & 1u)) {
-                const long long r = dest < 0 ? row_slot(a, b, g * a.G + hh, j) : (long long)dest * a.G + hh;
+            unit_out = __ballot_sync(0xffffffffu, hh < a.R && (f & FDPP_FLAG_OUT));
+            if (hh < a.R && ((write_mask >> hh) & 1u)) {
+                const long long r = dest < 0 ? unit_row_slot(a, b, g, hh, j) : (long long)dest * a.R + hh;
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
                 uint8_t* fp = dest < 0 ? a.flags : a.xf;
@@ -898,7 +898,7 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    const TcLayout lay(D, a.G, a.nstage, a.B);
+    const TcLayout lay(D, a.R, a.nstage, a.B);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* misc = reinterpret_cast<volatile int*>(sm + lay.misc);   // [0] abort, [1] last
     Ring rg;

@@ -48,7 +48,8 @@ def oracle_problem(inp: W.Inputs):
         batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
         head_dim=wl.head_dim, dtype=oracle.F32 if wl.dtype == W.F32 else oracle.BF16,
         scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi, max_seq_len=inp.max_seq_len,
-        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq)
+        paged=wl.paged, block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
+        q_tokens=wl.q_tokens)
 
 
 def oracle_out(inp: W.Inputs, rows=None):
@@ -110,7 +111,7 @@ def params_for(inp: W.Inputs, **kw):
     base = dict(batch=wl.batch, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
                 head_dim=wl.head_dim, dtype=F.FDPP_F32 if wl.dtype == W.F32 else F.FDPP_BF16,
                 max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
-                split_len=wl.split_len)
+                split_len=wl.split_len, q_tokens=wl.q_tokens)
     if wl.paged:
         base.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
                     num_kv_blocks=inp.num_kv_blocks,

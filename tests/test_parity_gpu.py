@@ -40,6 +40,16 @@ SMALL = {
     "paged_bs128": (_wl(W.PAGED, name="paged_bs128", batch=3, block_size=128,
                         seq_len_range=(100, 1100), split_len=256), None),
     "tiny": (W.TINY, None),
+    # several query tokens per sequence (the last Tq positions, causal): 8 query rows per kv head
+    # on the tensor kernel, 16 on the SIMT kernel only; sequences shorter than Tq included
+    "tq2_gqa": (_wl(W.GQA, name="tq2_gqa", batch=3, num_q_heads=8, num_kv_heads=2, q_tokens=2,
+                    split_len=256), [700, 65, 1]),
+    "tq8_mha": (_wl(W.GQA, name="tq8_mha", batch=3, num_q_heads=4, num_kv_heads=4, head_dim=64,
+                    q_tokens=8, split_len=64), [300, 9, 5]),
+    "tq2_g8_simt": (_wl(W.GQA, name="tq2_g8", batch=2, num_q_heads=16, num_kv_heads=2, q_tokens=2,
+                        split_len=128), [400, 130]),
+    "tq4_paged": (_wl(W.PAGED, name="tq4_paged", batch=4, num_q_heads=4, num_kv_heads=2,
+                      q_tokens=4, seq_len_range=(3, 700), split_len=128), None),
 }
 
 
@@ -58,7 +68,7 @@ def _inputs(name, poison=False):
 
 def _kernels(inp):
     ks = [F.FDPP_KERNEL_SIMT]
-    if inp.wl.dtype == W.BF16 and inp.wl.group <= 8:
+    if inp.wl.dtype == W.BF16 and inp.wl.group * inp.wl.q_tokens <= 8:
         ks.insert(0, F.FDPP_KERNEL_TENSOR)
     return ks
 
@@ -82,7 +92,7 @@ def test_small_parity(name):
         assert diag["n_flagged_row_splits"] == 0 and (flags & F.FDPP_FLAG_OUT).sum() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny"])
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny", "tq4_paged"])
 def test_nan_past_seq_len_is_never_read_into_results(name):
     inp, dinp = _inputs(name, poison=True)
     ref = H.oracle_out(inp)

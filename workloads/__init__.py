@@ -65,6 +65,7 @@ class Workload:
     hi: float = 10.0
     stress_frac: float = 0.0
     score_shift: float = 0.0                   # > 0: per-head score levels in [0, score_shift]
+    q_tokens: int = 1                          # query tokens per sequence (the last positions)
     shift_seed: int = 0x5EED00FF               # the levels and directions (fixed across samples)
     seed: int = 0x5EED0000
 
@@ -93,7 +94,11 @@ STRESS = Workload("fallback_stress", 8, 32, 8, 128, BF16, split_len=512, seq_len
 # most splits to the fallback; phi chosen per head from a sample keeps them on the fast path.
 SHIFTED = Workload("gqa_head_levels", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096,
                    score_shift=30.0, seed=0x5EED0005)
-ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED)}
+# A speculative-decoding step on gqa_decode shapes: two query tokens per sequence (the last two
+# positions, causal), 8 query rows per kv head.
+SPEC = Workload("spec_decode_tq2", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=2,
+                seed=0x5EED0006)
+ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED, SPEC)}
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -127,7 +132,7 @@ class Inputs:
     """Host arrays of one workload instance (bf16 as uint16 bit patterns)."""
     wl: Workload
     seq_lens: np.ndarray            # int32 [B]
-    q: np.ndarray                   # [B][Hq][d]
+    q: np.ndarray                   # [B][Hq][d], or [B][Tq][Hq][d] for several query tokens
     k: np.ndarray                   # contiguous [B][Lmax][Hkv][d] or paged [N][bs][Hkv][d]
     v: np.ndarray
     block_table: Optional[np.ndarray]   # int32 [B][max_blocks_per_seq] or None
@@ -158,7 +163,9 @@ def generate(wl: Workload, *, seq_lens: Optional[np.ndarray] = None, poison_tail
     sl = make_seq_lens(wl) if seq_lens is None else np.asarray(seq_lens, dtype=np.int32)
     assert sl.shape == (B,)
     Lmax = max(1, int(sl.max()))
-    q = _normals(_rng(wl.seed, _S_Q), B * Hq * d, wl.dtype).reshape(B, Hq, d)
+    Tq = max(1, wl.q_tokens)
+    q = _normals(_rng(wl.seed, _S_Q), B * Tq * Hq * d, wl.dtype)
+    q = q.reshape(B, Hq, d) if Tq == 1 else q.reshape(B, Tq, Hq, d)
     nan_val = np.float32(np.nan) if wl.dtype == F32 else np.uint16(0x7FC0)
 
     table = None
@@ -199,6 +206,7 @@ def generate(wl: Workload, *, seq_lens: Optional[np.ndarray] = None, poison_tail
         _shift_scores(wl, q, k)
     hot = []
     if wl.stress_frac > 0:
+        assert Tq == 1, "hot keys are placed for one query token per sequence"
         hot = _inject_hot_keys(wl, sl, q, k, table)
     return Inputs(wl, sl, q, k, v, table, Lmax, mbps, nblk_total, hot)
 
@@ -222,8 +230,8 @@ def _shift_scores(wl, q, k):
         kg = widen(k[..., g, :]) + a * u[g]
         k[..., g, :] = narrow(kg)
         for h in range(g * G, (g + 1) * G):
-            qh = widen(q[:, h, :]) + (mu[h] * np.float32(math.sqrt(d)) / a) * u[g]
-            q[:, h, :] = narrow(qh)
+            qh = widen(q[..., h, :]) + (mu[h] * np.float32(math.sqrt(d)) / a) * u[g]
+            q[..., h, :] = narrow(qh)
 
 
 def _inject_hot_keys(wl, sl, q, k, table):
