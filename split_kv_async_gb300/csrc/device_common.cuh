@@ -340,7 +340,6 @@ __device__ __forceinline__ unsigned classify(float x, float lo, float hi)
     return x > hi ? (FDPP_FLAG_OUT | FDPP_FLAG_ABOVE) : (FDPP_FLAG_OUT | FDPP_FLAG_BELOW);
 }
 
-// exp(m_w - M) with the exact 1 when the frames agree (so phi-frame partials add plainly).
 // Partial slot of query row rr of unit (b, g): query token i = rr / G of sequence b, head
 // g G + rr % G, split j. Partial arrays are [B][Tq][Hq][max_splits].
 __device__ __forceinline__ long long unit_row_slot(const KernelArgs& a, int b, int g, int rr, int j)
@@ -363,6 +362,7 @@ __device__ __forceinline__ float phi_of(const KernelArgs& a, int h)
     return a.phi_heads ? __ldg(a.phi_heads + h) : a.phi;
 }
 
+// exp(m_w - M) with the exact 1 when the frames agree (so phi-frame partials add plainly).
 __device__ __forceinline__ float frame_weight(float m, float M)
 {
     return m == M ? 1.0f : __expf(m - M);

@@ -579,7 +579,7 @@ struct Producer {
 // ------------------------------------------------------------------------------------------
 // consumer warps
 // ------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool MQ>
 __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay, uint8_t* sm,
                                         uint32_t sbase, const Ring& rg, volatile int* misc)
 {
@@ -641,7 +641,13 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const bool hv[2] = {head0 < a.R, head0 + 1 < a.R};
         const float phv[2] = {hv[0] ? phi_of(a, g * a.G + head0 % a.G) : a.phi,
                               hv[1] ? phi_of(a, g * a.G + (head0 + 1) % a.G) : a.phi};
-        const int klim[2] = {key_limit(a, seq_len, head0 / a.G), key_limit(a, seq_len, (head0 + 1) / a.G)};
+        // several query tokens: keys of the segment each row sees, counted from t0 (none for a
+        // lane without a row); one query token sees every key of the segment
+        int kseg[2] = {0, 0};
+        if constexpr (MQ) {
+            kseg[0] = hv[0] ? key_limit(a, seq_len, head0 / a.G) - t0 : 0;
+            kseg[1] = hv[1] ? key_limit(a, seq_len, (head0 + 1) / a.G) - t0 : 0;
+        }
         float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
         const int ntiles = ceil_div_i(t1 - t0, TILE);
@@ -670,7 +676,10 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             for (int e = 0; e < 4; ++e) {
                 sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
                 const int tok = tok_r + 8 * (e >> 1);
-                valid[e] = hv[e & 1] && (tok < nvalid) && (t0 + i * TILE + tok < klim[e & 1]);
+                if constexpr (MQ)
+                    valid[e] = tok < min(nvalid, kseg[e & 1] - i * TILE);   // the row's tokens of the tile
+                else
+                    valid[e] = hv[e & 1] && tok < nvalid;
                 if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
             }
 
@@ -805,9 +814,31 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         {
             constexpr int HPP = NCT / D;           // rows per pass of the 128 threads
             const int d = ctid % D, hsub = ctid / D;
+            // Row hh = i G + h2 (query token i, head g G + h2): consecutive rows are hstride apart,
+            // plus `wrap` more where the next query token starts (one query token: rows are
+            // plainly hstride apart).
+            const long long hstride = dest < 0 ? (long long)a.max_splits * D : (long long)D;
+            float* o_dst = dest < 0 ? a.o_part + unit_row_slot(a, b, g, 0, j) * D
+                                    : a.xo + (long long)dest * a.R * D;
+            [[maybe_unused]] const long long wrap = dest < 0 ? (long long)(a.Hq - a.G) * a.max_splits * D : 0;
+            [[maybe_unused]] int h2 = 0;
+            [[maybe_unused]] float* o_row = o_dst;
+            auto next_row = [&]() {
+                o_row += hstride;
+                if (++h2 == a.G) { h2 = 0; o_row += wrap; }
+            };
+            if constexpr (MQ) {
+                if (hsub) next_row();
+            }
 #pragma unroll
             for (int k = 0; k < TC_MAX_GROUP / HPP; ++k) {
                 const int hh = k * HPP + hsub;     // query row
+                if constexpr (MQ) {
+                    if (k > 0) {
+#pragma unroll
+                        for (int s = 0; s < HPP; ++s) next_row();
+                    }
+                }
                 if (hh < a.R && ((write_mask >> hh) & 1u)) {
                     float acc = 0.f;
                     if (!online) {
@@ -822,9 +853,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                             acc = fmaf(frame_weight(scr_m[w * a.R + hh], M),
                                        scr_o[(w * a.R + hh) * lay.scr_row + d], acc);
                     }
-                    float* o_dst = dest < 0 ? a.o_part + unit_row_slot(a, b, g, hh, j) * D
-                                            : a.xo + ((long long)dest * a.R + hh) * D;
-                    o_dst[d] = acc;
+                    if constexpr (MQ) o_row[d] = acc;
+                    else o_dst[hh * hstride + d] = acc;
                 }
             }
         }
@@ -847,7 +877,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             }
             unit_out = __ballot_sync(0xffffffffu, hh < a.R && (f & FDPP_FLAG_OUT));
             if (hh < a.R && ((write_mask >> hh) & 1u)) {
-                const long long r = dest < 0 ? unit_row_slot(a, b, g, hh, j) : (long long)dest * a.R + hh;
+                const long long r = dest >= 0 ? (long long)dest * a.R + hh
+                                    : MQ ? unit_row_slot(a, b, g, hh, j)
+                                         : ((long long)b * a.Hq + g * a.G + hh) * a.max_splits + j;
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
                 uint8_t* fp = dest < 0 ? a.flags : a.xf;
@@ -889,8 +921,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 // ------------------------------------------------------------------------------------------
 // MINB = CTAs per SM the build is register-limited for: 2 caps a thread at 168 registers (two
 // 5-warp CTAs, warps allocated in pairs), 1 leaves the compiler free (~240) and pairs with a
-// deeper TMA ring.
-template <int D, bool PAGED, int MINB>
+// deeper TMA ring. MQ: several query tokens per sequence (rows R = Tq G with causal key limits);
+// the one-token build keeps the plain row addressing.
+template <int D, bool PAGED, int MINB, bool MQ>
 __global__ void __launch_bounds__(NTHREADS, MINB)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const KernelArgs a)
@@ -940,7 +973,7 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
         pr.run<D, PAGED>();
         if (pr.bad_block && lane == 0) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
     } else {
-        consume<D>(a, lay, sm, sbase, rg, misc);
+        consume<D, MQ>(a, lay, sm, sbase, rg, misc);
     }
     __syncthreads();
     if (warp == NCW && lane == 0) {
@@ -967,7 +1000,9 @@ template <int D, bool PAGED>
 cudaError_t launch_t(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                      int smem, int ctas_per_sm, cudaStream_t s)
 {
-    auto kern = ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2> : split_tc_kernel<D, PAGED, 1>;
+    // several query tokens per sequence take their own build (causal row limits, row addressing)
+    auto kern = a.Tq > 1 ? (ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2, true> : split_tc_kernel<D, PAGED, 1, true>)
+                         : (ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2, false> : split_tc_kernel<D, PAGED, 1, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // a programmatic dependent of the previous kernel on the stream (the previous call's combine
