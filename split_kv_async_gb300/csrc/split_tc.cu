@@ -830,9 +830,32 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             if constexpr (MQ) {
                 if (hsub) next_row();
             }
+            // every row's sum is read from the scratch before any store, so the loads are not held
+            // behind the global stores
+            constexpr int NK = TC_MAX_GROUP / HPP;
+            float acc[NK];
 #pragma unroll
-            for (int k = 0; k < TC_MAX_GROUP / HPP; ++k) {
+            for (int k = 0; k < NK; ++k) {
                 const int hh = k * HPP + hsub;     // query row
+                acc[k] = 0.f;
+                if (hh < a.R) {
+                    if (!online) {
+#pragma unroll
+                        for (int w = 0; w < NCW; ++w) acc[k] += scr_o[(w * a.R + hh) * lay.scr_row + d];
+                    } else {
+                        float M = scr_m[hh];
+#pragma unroll
+                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
+#pragma unroll
+                        for (int w = 0; w < NCW; ++w)
+                            acc[k] = fmaf(frame_weight(scr_m[w * a.R + hh], M),
+                                          scr_o[(w * a.R + hh) * lay.scr_row + d], acc[k]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < NK; ++k) {
+                const int hh = k * HPP + hsub;
                 if constexpr (MQ) {
                     if (k > 0) {
 #pragma unroll
@@ -840,21 +863,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     }
                 }
                 if (hh < a.R && ((write_mask >> hh) & 1u)) {
-                    float acc = 0.f;
-                    if (!online) {
-#pragma unroll
-                        for (int w = 0; w < NCW; ++w) acc += scr_o[(w * a.R + hh) * lay.scr_row + d];
-                    } else {
-                        float M = scr_m[hh];
-#pragma unroll
-                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
-#pragma unroll
-                        for (int w = 0; w < NCW; ++w)
-                            acc = fmaf(frame_weight(scr_m[w * a.R + hh], M),
-                                       scr_o[(w * a.R + hh) * lay.scr_row + d], acc);
-                    }
-                    if constexpr (MQ) o_row[d] = acc;
-                    else o_dst[hh * hstride + d] = acc;
+                    if constexpr (MQ) o_row[d] = acc[k];
+                    else o_dst[hh * hstride + d] = acc[k];
                 }
             }
         }
