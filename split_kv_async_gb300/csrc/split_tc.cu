@@ -40,6 +40,8 @@
 // combine, more than the TMA ring can hide.)
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace fdpp {
@@ -49,50 +51,47 @@ constexpr int NCW = 4;                  // consumer warps
 constexpr int TPW = 16;                 // tokens per consumer warp and tile
 constexpr int TILE = NCW * TPW;         // tokens per tile
 constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int NCT = NCW * 32;           // consumer threads
 constexpr int PLAN_SMEM_MAX_B = TC_PLAN_SMEM_MAX_B;
 constexpr int QHDR_BYTES = 64;          // unit header at the start of each Q-ring slot
 static_assert(TILE == TC_TILE_TOKENS, "tile height is part of the tensor-map contract");
-// the merge scratch (4 warps x G <= 8 rows x (d + 8) floats, plus l, m, flags) fits in a stage
-static_assert(NCW * 8 * (64 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 64 * 2, "scratch (d=64)");
-static_assert(NCW * 8 * (128 + 8) * 4 + 3 * NCW * 8 * 4 <= 2 * TILE * 128 * 2, "scratch (d=128)");
 
 // unit kinds carried in the Q-ring header
 enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
 // header words
 enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_L, H_WORDS };
 
-// Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge
-// scratch of a unit lives in the stage of the unit's last tile (offsets scr_* relative to that
-// stage), which is released to the producer only after the merge.
+// Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge has
+// scratch of its own, so a unit's last stage goes back to the producer like any other:
+//   xchg: two slots of one warp's O^T fragments (d/16 float4 per lane) for the warp-sum tree;
+//   xrow: l, m and flag word per consumer warp and query row, two buffers (by unit parity).
 struct TcLayout {
-    int stage_bytes, kv_bytes, qslot_bytes, scr_row;
-    int stages, qring, scr_o, scr_l, scr_m, scr_f, plan, bars, misc, total;
+    int stage_bytes, kv_bytes, qslot_bytes;
+    int stages, qring, xchg, xrow, plan, bars, misc, total;
 
     __host__ __device__ static constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
     __host__ __device__ TcLayout(int D, int G, int nstage, int B)
         : stage_bytes(2 * TILE * D * 2), kv_bytes(TILE * D * 2),
-          qslot_bytes(round_up(QHDR_BYTES + G * D * 2, 128)), scr_row(D + 8), stages(0), qring(0),
-          scr_o(0), scr_l(0), scr_m(0), scr_f(0), plan(0), bars(0), misc(0), total(0)
+          qslot_bytes(round_up(QHDR_BYTES + G * D * 2, 128)), stages(0), qring(0), xchg(0),
+          xrow(0), plan(0), bars(0), misc(0), total(0)
     {
         qring = stages + nstage * stage_bytes;
-        scr_o = 0;
-        scr_l = scr_o + NCW * G * scr_row * 4;
-        scr_m = scr_l + NCW * G * 4;
-        scr_f = scr_m + NCW * G * 4;
-        plan = qring + 2 * qslot_bytes;
-        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 3 * B + 2 : 0) + 1;
+        xchg = qring + 2 * qslot_bytes;
+        xrow = xchg + 2 * (D / 16) * 32 * 16;
+        plan = xrow + 2 * 3 * NCW * TC_MAX_GROUP * 4;
+        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 2 * B + 1 : 0) + 1;
         bars = round_up(plan + plan_ints * 4, 8);
-        misc = bars + (2 * nstage + 6) * 8;
+        misc = bars + (2 * nstage + 8) * 8;
         total = misc + 16;
     }
 };
 
 struct Ring {
     uint32_t full, empty, qfull, qempty;   // shared addresses of the barrier arrays
-    uint32_t cbar;                         // consumer-warps barrier (128 arrivals per phase)
+    uint32_t cbar;                         // merge: every consumer warp wrote its partial (4 arrivals)
     uint32_t own_done;                     // consumers finished the CTA's own units
+    uint32_t mhand;                        // merge: warp 1's sum is in exchange slot 1
+    uint32_t mdone;                        // merge: warp 0 has read both exchange slots
     int nstage;
 };
 
@@ -106,18 +105,6 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatil
         misc[0] = 1;
         set_error(a, FDPP_ERRBIT_TIMEOUT);
     }
-    return ok;
-}
-
-// Barrier of the 4 consumer warps with a bounded wait (a bar.sync could not give up). One
-// arrival per warp after __syncwarp; the arrive releases and the wait acquires at CTA scope.
-__device__ __forceinline__ bool consumer_sync(const Ring& rg, uint32_t& parity, volatile int* misc,
-                                              const KernelArgs& a)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(rg.cbar);
-    const bool ok = ring_wait(rg.cbar, parity, misc, a);
-    parity ^= 1u;
     return ok;
 }
 
@@ -138,9 +125,8 @@ struct Producer {
     uint32_t sbase;
     uint8_t* smp;              // generic pointer to the same shared-memory base
     volatile int* misc;
-    int* plan;                 // smem (B <= PLAN_SMEM_MAX_B): prefix of n_b [B + 1],
-    int* tplan;                //   prefix of the tiles of each sequence [B + 1],
-    int* lplan;                //   clamped L_b [B]
+    int* tplan;                // smem (B <= PLAN_SMEM_MAX_B): prefix of the tiles of each sequence [B + 1],
+    int* lplan;                //   clamped L_b [B] (n_b = min(ceil(L_b / S), max_splits))
     int S = 0, TS = 0;         // split length, tiles of a full split
     uint32_t stage = 0, phase = 0, qiter = 0;
     bool bad_block = false;
@@ -189,14 +175,14 @@ struct Producer {
             __syncwarp();
             if (b < A.B) {
                 const int tfirst = (int)(trun + tincl - nt);
-                if (in_smem) { plan[b] = run + incl - nb; tplan[b] = tfirst; }
+                if (in_smem) tplan[b] = tfirst;
                 if (blockIdx.x == 0) { A.nsplit[b] = nb; A.tstart[b] = tfirst; }
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
             trun += __shfl_sync(0xffffffffu, tincl, 31);
         }
         if (lane == 0) {
-            if (in_smem) { plan[A.B] = run; tplan[A.B] = (int)trun; }
+            if (in_smem) tplan[A.B] = (int)trun;
             if (blockIdx.x == 0) A.tstart[A.B] = (int)trun;
         }
         __syncwarp();
@@ -214,9 +200,8 @@ struct Producer {
             // rows of empty sequences are zero (no unit will write them)
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(A.out);
             for (int b = 0; b < A.B; ++b) {
-                const int nb = in_smem ? plan[b + 1] - plan[b]
-                                       : clamp_len(A.seq_lens[b], A.max_seq_len);
-                if (nb != 0) continue;
+                const int Lc = in_smem ? lplan[b] : clamp_len(A.seq_lens[b], A.max_seq_len);
+                if (Lc != 0) continue;
                 for (int i = lane; i < A.Tq * A.Hq * A.D; i += 32)
                     out[(long long)b * A.Tq * A.Hq * A.D + i] = __float2bfloat16_rn(0.f);
             }
@@ -403,8 +388,8 @@ struct Producer {
             const int k = r - s.g * ntb;             // tile of sequence cb, head s.g
             s.j = k / TS;
             const int ilo = k - s.j * TS;
-            const int nb = plan[cb + 1] - plan[cb];
             s.L = lplan[cb];
+            const int nb = min(ceil_div_i(s.L, S), A.max_splits);
             const int nu = (s.j < nb - 1) ? TS : ntb - (nb - 1) * TS;
             const int ihi = (int)min((long long)nu, ilo + (te - t));
             s.t0 = s.j * S + ilo * TILE;
@@ -592,7 +577,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     // columns 4..7 (unused otherwise), so P.V costs d/16 MMAs; for G > 4 hi and lo go through
     // two MMAs into the same accumulator.
     constexpr int KS = D / 16;           // k-steps of S^T, and m-tiles of O^T
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ctid = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, qd = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;      // ldmatrix: matrix and row of this lane
     const bool pack_lo = a.R <= 4;
@@ -602,7 +587,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const int tok_r = warp * TPW + r;             // this lane's tokens: tok_r and tok_r + 8
     const int tok_q = warp * TPW + 2 * qd;        // tokens of this lane's V^T fragment columns
     const int head0 = 2 * qd;                     // this lane's heads: head0, head0 + 1
-    uint32_t stage = 0, phase = 0, qiter = 0, cpar = 0;
+    uint32_t stage = 0, phase = 0, qiter = 0, un = 0;   // un: units merged so far
 
     for (;;) {
         // ---- next unit from the producer ----
@@ -651,129 +636,125 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
         const int ntiles = ceil_div_i(t1 - t0, TILE);
-        uint32_t held = 0;                         // stage of the last tile: the merge scratch
 
-        for (int i = 0; i < ntiles; ++i) {
-            const int nvalid = min(TILE, t1 - (t0 + i * TILE));
-            if (!ring_wait(rg.full + 8 * stage, phase, misc, a)) return;
-            const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
-            const uint32_t vb = kb + lay.kv_bytes;
+        // The tile loop, built once for the phi frame and once for the running max (fallback
+        // segments and forced online mode), so the hot phi-frame loop stays compact.
+        auto run_tiles = [&](auto online_c) -> bool {
+            constexpr bool ONLINE = decltype(online_c)::value;
+            for (int i = 0; i < ntiles; ++i) {
+                const int nvalid = min(TILE, t1 - (t0 + i * TILE));
+                if (!ring_wait(rg.full + 8 * stage, phase, misc, a)) return false;
+                const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
+                const uint32_t vb = kb + lay.kv_bytes;
 
-            // S^T = K Q^T for this warp's 16 tokens, two accumulation chains
-            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int chunk = 2 * ks + (mi >> 1);
-                const uint32_t addr = kb + (chunk >> 3) * (TILE * 128) + k_row * 128 + (((chunk & 7) ^ r8) << 4);
-                uint32_t k0, k1, k2, k3;
-                ldsm_x4(addr, k0, k1, k2, k3);
-                mma_16816(sa[ks & 1], k0, k1, k2, k3, qb[ks][0], qb[ks][1]);
-            }
-            // element e of sa: token tok_r + 8 (e >> 1), head head0 + (e & 1)
-            float sv[4];
-            bool valid[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
-                const int tok = tok_r + 8 * (e >> 1);
-                if constexpr (MQ)
-                    valid[e] = tok < min(nvalid, kseg[e & 1] - i * TILE);   // the row's tokens of the tile
-                else
-                    valid[e] = hv[e & 1] && tok < nvalid;
-                if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
-            }
-
-            float p[4];
-            if (!online) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], phv[e & 1])) : 0.f;
-            } else {
-                float corr[2];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float tmax = -INFINITY;
-                    if (valid[c]) tmax = sv[c];
-                    if (valid[c + 2]) tmax = fmaxf(tmax, sv[c + 2]);
-                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-                    const float mnew = fmaxf(mrun[c], tmax);
-                    corr[c] = (mrun[c] == mnew) ? 1.f : (mrun[c] == -INFINITY ? 0.f : __expf(mrun[c] - mnew));
-                    mrun[c] = mnew;
-                    lsum[c] *= corr[c];
-                    p[c] = valid[c] ? __expf(sv[c] - mnew) : 0.f;
-                    p[c + 2] = valid[c + 2] ? __expf(sv[c + 2] - mnew) : 0.f;
+                // S^T = K Q^T for this warp's 16 tokens, two accumulation chains
+                float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    #pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int chunk = 2 * ks + (mi >> 1);
+                    const uint32_t addr = kb + (chunk >> 3) * (TILE * 128) + k_row * 128 + (((chunk & 7) ^ r8) << 4);
+                    uint32_t k0, k1, k2, k3;
+                    ldsm_x4(addr, k0, k1, k2, k3);
+                    mma_16816(sa[ks & 1], k0, k1, k2, k3, qb[ks][0], qb[ks][1]);
                 }
-                // columns 4..7 of lanes qd >= 2 hold the lo part of heads 0..3 (G <= 4)
-                float oc[2] = {corr[0], corr[1]};
-                if (pack_lo) {
-                    const float x0 = __shfl_xor_sync(0xffffffffu, corr[0], 2);
-                    const float x1 = __shfl_xor_sync(0xffffffffu, corr[1], 2);
-                    if (qd >= 2) { oc[0] = x0; oc[1] = x1; }
+                // element e of sa: token tok_r + 8 (e >> 1), head head0 + (e & 1)
+                float sv[4];
+                bool valid[4];
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
+                    const int tok = tok_r + 8 * (e >> 1);
+                    if constexpr (MQ)
+                        valid[e] = tok < min(nvalid, kseg[e & 1] - i * TILE);   // the row's tokens of the tile
+                    else
+                        valid[e] = hv[e & 1] && tok < nvalid;
+                    if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
                 }
-                if (oc[0] != 1.f || oc[1] != 1.f) {
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        o[mt][0] *= oc[0]; o[mt][2] *= oc[0];
-                        o[mt][1] *= oc[1]; o[mt][3] *= oc[1];
+
+                float p[4];
+                if constexpr (!ONLINE) {
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], phv[e & 1])) : 0.f;
+                } else {
+                    float corr[2];
+    #pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        float tmax = -INFINITY;
+                        if (valid[c]) tmax = sv[c];
+                        if (valid[c + 2]) tmax = fmaxf(tmax, sv[c + 2]);
+                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                        const float mnew = fmaxf(mrun[c], tmax);
+                        corr[c] = (mrun[c] == mnew) ? 1.f : (mrun[c] == -INFINITY ? 0.f : __expf(mrun[c] - mnew));
+                        mrun[c] = mnew;
+                        lsum[c] *= corr[c];
+                        p[c] = valid[c] ? __expf(sv[c] - mnew) : 0.f;
+                        p[c + 2] = valid[c + 2] ? __expf(sv[c + 2] - mnew) : 0.f;
+                    }
+                    // columns 4..7 of lanes qd >= 2 hold the lo part of heads 0..3 (G <= 4)
+                    float oc[2] = {corr[0], corr[1]};
+                    if (pack_lo) {
+                        const float x0 = __shfl_xor_sync(0xffffffffu, corr[0], 2);
+                        const float x1 = __shfl_xor_sync(0xffffffffu, corr[1], 2);
+                        if (qd >= 2) { oc[0] = x0; oc[1] = x1; }
+                    }
+                    if (oc[0] != 1.f || oc[1] != 1.f) {
+    #pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            o[mt][0] *= oc[0]; o[mt][2] *= oc[0];
+                            o[mt][1] *= oc[1]; o[mt][3] *= oc[1];
+                        }
                     }
                 }
-            }
-            lsum[0] += p[0] + p[2];
-            lsum[1] += p[1] + p[3];
+                lsum[0] += p[0] + p[2];
+                lsum[1] += p[1] + p[3];
 
-            // P^T as the B operand of O^T += V^T P^T (tokens x heads), hi and lo bf16 parts
-            const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
-            const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
-            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-            uint32_t x_hi0 = *reinterpret_cast<const uint32_t*>(&h01);
-            uint32_t x_hi1 = *reinterpret_cast<const uint32_t*>(&h23);
-            const uint32_t x_lo0 = pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
-            const uint32_t x_lo1 = pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
-            uint32_t b_hi0, b_hi1, b_lo0 = 0u, b_lo1 = 0u;
-            if (pack_lo) {
-                const uint32_t y0 = __shfl_xor_sync(0xffffffffu, x_lo0, 2);
-                const uint32_t y1 = __shfl_xor_sync(0xffffffffu, x_lo1, 2);
-                if (qd >= 2) { x_hi0 = y0; x_hi1 = y1; }
-                b_hi0 = movmatrix_trans(x_hi0);
-                b_hi1 = movmatrix_trans(x_hi1);
-            } else {
-                b_hi0 = movmatrix_trans(x_hi0);
-                b_hi1 = movmatrix_trans(x_hi1);
-                b_lo0 = movmatrix_trans(x_lo0);
-                b_lo1 = movmatrix_trans(x_lo1);
-            }
+                // P^T as the B operand of O^T += V^T P^T (tokens x heads), hi and lo bf16 parts
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                uint32_t x_hi0 = *reinterpret_cast<const uint32_t*>(&h01);
+                uint32_t x_hi1 = *reinterpret_cast<const uint32_t*>(&h23);
+                const uint32_t x_lo0 = pack_bf16x2(p[0] - f01.x, p[1] - f01.y);
+                const uint32_t x_lo1 = pack_bf16x2(p[2] - f23.x, p[3] - f23.y);
+                uint32_t b_hi0, b_hi1, b_lo0 = 0u, b_lo1 = 0u;
+                if (pack_lo) {
+                    const uint32_t y0 = __shfl_xor_sync(0xffffffffu, x_lo0, 2);
+                    const uint32_t y1 = __shfl_xor_sync(0xffffffffu, x_lo1, 2);
+                    if (qd >= 2) { x_hi0 = y0; x_hi1 = y1; }
+                    b_hi0 = movmatrix_trans(x_hi0);
+                    b_hi1 = movmatrix_trans(x_hi1);
+                } else {
+                    b_hi0 = movmatrix_trans(x_hi0);
+                    b_hi1 = movmatrix_trans(x_hi1);
+                    b_lo0 = movmatrix_trans(x_lo0);
+                    b_lo1 = movmatrix_trans(x_lo1);
+                }
 
-            // V rows past the valid tokens may hold anything (NaN included): mask them to zero
-            uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-            if (nvalid < TILE) {
-                vm_lo = (tok_q < nvalid ? 0x0000ffffu : 0u) | (tok_q + 1 < nvalid ? 0xffff0000u : 0u);
-                vm_hi = (tok_q + 8 < nvalid ? 0x0000ffffu : 0u) | (tok_q + 9 < nvalid ? 0xffff0000u : 0u);
-            }
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                const int chunk = 2 * mt + (mi & 1);
-                const uint32_t addr = vb + (chunk >> 3) * (TILE * 128) + v_row * 128 + (((chunk & 7) ^ r8) << 4);
-                uint32_t v0, v1, v2, v3;
-                ldsm_x4_t(addr, v0, v1, v2, v3);
-                v0 &= vm_lo; v1 &= vm_lo; v2 &= vm_hi; v3 &= vm_hi;
-                mma_16816(o[mt], v0, v1, v2, v3, b_hi0, b_hi1);
-                if (!pack_lo) mma_16816(o[mt], v0, v1, v2, v3, b_lo0, b_lo1);
-            }
-            if (i + 1 < ntiles) {
+                // V rows past the valid tokens may hold anything (NaN included): mask them to zero
+                uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+                if (nvalid < TILE) {
+                    vm_lo = (tok_q < nvalid ? 0x0000ffffu : 0u) | (tok_q + 1 < nvalid ? 0xffff0000u : 0u);
+                    vm_hi = (tok_q + 8 < nvalid ? 0x0000ffffu : 0u) | (tok_q + 9 < nvalid ? 0xffff0000u : 0u);
+                }
+    #pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int chunk = 2 * mt + (mi & 1);
+                    const uint32_t addr = vb + (chunk >> 3) * (TILE * 128) + v_row * 128 + (((chunk & 7) ^ r8) << 4);
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_t(addr, v0, v1, v2, v3);
+                    v0 &= vm_lo; v1 &= vm_lo; v2 &= vm_hi; v3 &= vm_hi;
+                    mma_16816(o[mt], v0, v1, v2, v3, b_hi0, b_hi1);
+                    if (!pack_lo) mma_16816(o[mt], v0, v1, v2, v3, b_lo0, b_lo1);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rg.empty + 8 * stage);
-            } else {
-                held = stage;
+                if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
             }
-            if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
-        }
-        uint8_t* scr = sm + lay.stages + held * lay.stage_bytes;
-        float* scr_o = reinterpret_cast<float*>(scr + lay.scr_o);
-        float* scr_l = reinterpret_cast<float*>(scr + lay.scr_l);
-        float* scr_m = reinterpret_cast<float*>(scr + lay.scr_m);
-        unsigned* scr_f = reinterpret_cast<unsigned*>(scr + lay.scr_f);
-
+            return true;
+        };
+        if (!(online ? run_tiles(std::true_type{}) : run_tiles(std::false_type{}))) return;
         // ---- this warp's partial: reduce over its 16 tokens (lanes r), fold in the lo part ----
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -789,101 +770,96 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
                 for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(0xffffffffu, o[mt][e], 2);
         }
-        if (!consumer_sync(rg, cpar, misc, a)) return;   // every warp is done with the last tile
+
+        // ---- merge of the four warp partials: (w0 + w2) + (w1 + w3) ----
+        // Warps 2 and 3 leave their O^T fragments in exchange slots 0 and 1 (after warp 0 has read
+        // the previous unit's), every warp its rows' l, m and flags; warps 0 and 1 add the slot
+        // of their partner, warp 1 hands its sum to warp 0 through slot 1, and warp 0 writes the
+        // row's partial. In the phi frame every warp's m is phi and each weight is exactly 1, so
+        // the sums need no exponentials.
+        const uint32_t upar = un & 1u;
+        float4* xs = reinterpret_cast<float4*>(sm + lay.xchg);
+        float* xl_s = reinterpret_cast<float*>(sm + lay.xrow) + upar * 3 * NCW * TC_MAX_GROUP;
+        float* xm_s = xl_s + NCW * TC_MAX_GROUP;
+        unsigned* xf_s = reinterpret_cast<unsigned*>(xm_s + NCW * TC_MAX_GROUP);
+        if (warp >= 2) {
+            if (un > 0 && !ring_wait(rg.mdone, upar ^ 1u, misc, a)) return;
+            float4* slot = xs + (warp - 2) * KS * 32;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (!hv[c] || (pack_lo && qd >= 2)) continue;
-            float* row = scr_o + (warp * a.R + head0 + c) * lay.scr_row;
+            for (int mt = 0; mt < KS; ++mt) slot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (!hv[c]) continue;
+                xl_s[warp * TC_MAX_GROUP + head0 + c] = lsum[c];
+                xm_s[warp * TC_MAX_GROUP + head0 + c] = mrun[c];
+                xf_s[warp * TC_MAX_GROUP + head0 + c] = fl[c];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rg.cbar);
+        ++un;
+        if (warp >= 2) continue;                   // warps 2 and 3 go on to the next unit
+        if (!ring_wait(rg.cbar, upar, misc, a)) return;
+
+        // this warp and its partner (warp + 2), each weighted into the rows' common frame
+        {
+            float ws[2] = {1.f, 1.f}, wp[2] = {1.f, 1.f};
+            if (online) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    if (!hv[c]) continue;
+                    const int hh = head0 + c;
+                    float M = xm_s[hh];
+#pragma unroll
+                    for (int w = 1; w < NCW; ++w) M = fmaxf(M, xm_s[w * TC_MAX_GROUP + hh]);
+                    ws[c] = frame_weight(xm_s[warp * TC_MAX_GROUP + hh], M);
+                    wp[c] = frame_weight(xm_s[(warp + 2) * TC_MAX_GROUP + hh], M);
+                }
+            }
+            const float4* slot = xs + warp * KS * 32;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                row[16 * mt + r] = o[mt][c];
-                row[16 * mt + r + 8] = o[mt][c + 2];
-            }
-            if (r == 0) {
-                scr_l[warp * a.R + head0 + c] = lsum[c];
-                scr_m[warp * a.R + head0 + c] = mrun[c];
-                scr_f[warp * a.R + head0 + c] = fl[c];
+                const float4 v = slot[mt * 32 + lane];
+                if (!online) {
+                    o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
+                } else {
+                    o[mt][0] = fmaf(wp[0], v.x, ws[0] * o[mt][0]);
+                    o[mt][1] = fmaf(wp[1], v.y, ws[1] * o[mt][1]);
+                    o[mt][2] = fmaf(wp[0], v.z, ws[0] * o[mt][2]);
+                    o[mt][3] = fmaf(wp[1], v.w, ws[1] * o[mt][3]);
+                }
             }
         }
-        if (!consumer_sync(rg, cpar, misc, a)) return;
+        if (warp == 1) {
+            // warp 1 has read slot 1 (warp 3's); its own sum takes the slot for warp 0
+            float4* slot = xs + KS * 32;
+            __syncwarp();
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) slot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rg.mhand);
+            continue;
+        }
+
+        // ---- warp 0: l, m and the flag byte of every row (lane hh for row hh) ----
         const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
-        // The four warp partials of each head, summed in warp order. In the phi frame every
-        // warp's m is phi and each weight is exactly 1, so the sum needs no exponentials.
-        // Destination: the split's own slot of each query row, or the extra slot of a part that
-        // began inside the unit (rows adjacent).
+        unsigned unit_out = 0u;                    // rows of this segment outside the window
         {
-            constexpr int HPP = NCT / D;           // rows per pass of the 128 threads
-            const int d = ctid % D, hsub = ctid / D;
-            // Row hh = i G + h2 (query token i, head g G + h2): consecutive rows are hstride apart,
-            // plus `wrap` more where the next query token starts (one query token: rows are
-            // plainly hstride apart).
-            const long long hstride = dest < 0 ? (long long)a.max_splits * D : (long long)D;
-            float* o_dst = dest < 0 ? a.o_part + unit_row_slot(a, b, g, 0, j) * D
-                                    : a.xo + (long long)dest * a.R * D;
-            [[maybe_unused]] const long long wrap = dest < 0 ? (long long)(a.Hq - a.G) * a.max_splits * D : 0;
-            [[maybe_unused]] int h2 = 0;
-            [[maybe_unused]] float* o_row = o_dst;
-            auto next_row = [&]() {
-                o_row += hstride;
-                if (++h2 == a.G) { h2 = 0; o_row += wrap; }
-            };
-            if constexpr (MQ) {
-                if (hsub) next_row();
-            }
-            // every row's sum is read from the scratch before any store, so the loads are not held
-            // behind the global stores
-            constexpr int NK = TC_MAX_GROUP / HPP;
-            float acc[NK];
-#pragma unroll
-            for (int k = 0; k < NK; ++k) {
-                const int hh = k * HPP + hsub;     // query row
-                acc[k] = 0.f;
-                if (hh < a.R) {
-                    if (!online) {
-#pragma unroll
-                        for (int w = 0; w < NCW; ++w) acc[k] += scr_o[(w * a.R + hh) * lay.scr_row + d];
-                    } else {
-                        float M = scr_m[hh];
-#pragma unroll
-                        for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
-#pragma unroll
-                        for (int w = 0; w < NCW; ++w)
-                            acc[k] = fmaf(frame_weight(scr_m[w * a.R + hh], M),
-                                          scr_o[(w * a.R + hh) * lay.scr_row + d], acc[k]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < NK; ++k) {
-                const int hh = k * HPP + hsub;
-                if constexpr (MQ) {
-                    if (k > 0) {
-#pragma unroll
-                        for (int s = 0; s < HPP; ++s) next_row();
-                    }
-                }
-                if (hh < a.R && ((write_mask >> hh) & 1u)) {
-                    if constexpr (MQ) o_row[d] = acc[k];
-                    else o_dst[hh * hstride + d] = acc[k];
-                }
-            }
-        }
-        // l, m and the flag byte: lane hh of warp 0 for head hh
-        unsigned unit_out = 0u;                   // heads of this segment outside the window
-        if (warp == 0) {
             const int hh = lane;
             unsigned f = 0u;
             float M = 0.f, lam = 0.f;
             if (hh < a.R) {
 #pragma unroll
-                for (int w = 0; w < NCW; ++w) f |= scr_f[w * a.R + hh];
-                M = scr_m[hh];
+                for (int w = 0; w < NCW; ++w) f |= xf_s[w * TC_MAX_GROUP + hh];
+                M = xm_s[hh];
 #pragma unroll
-                for (int w = 1; w < NCW; ++w) M = fmaxf(M, scr_m[w * a.R + hh]);
+                for (int w = 1; w < NCW; ++w) M = fmaxf(M, xm_s[w * TC_MAX_GROUP + hh]);
 #pragma unroll
                 for (int w = 0; w < NCW; ++w)
-                    lam = online ? fmaf(frame_weight(scr_m[w * a.R + hh], M), scr_l[w * a.R + hh], lam)
-                                 : lam + scr_l[w * a.R + hh];
+                    lam = online ? fmaf(frame_weight(xm_s[w * TC_MAX_GROUP + hh], M), xl_s[w * TC_MAX_GROUP + hh], lam)
+                                 : lam + xl_s[w * TC_MAX_GROUP + hh];
             }
             unit_out = __ballot_sync(0xffffffffu, hh < a.R && (f & FDPP_FLAG_OUT));
             if (hh < a.R && ((write_mask >> hh) & 1u)) {
@@ -903,26 +879,49 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 }
             }
         }
-        // every warp has read the scratch: the stage goes back to the producer (its generic-proxy
-        // scratch writes are ordered before the TMA writes that will refill it). The barrier also
-        // orders every thread's flag stores before the fallback push below.
-        fence_proxy_async_smem();
-        if (!consumer_sync(rg, cpar, misc, a)) return;
-        if (lane == 0) mbar_arrive(rg.empty + 8 * held);
-        // ---- a segment with a head outside the window goes on the device-wide fallback list ----
-        if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL) {
-            // thread 0 fills the entry, then publishes its first word with a release store
-            if (ctid == 0) {
-                const int list = (int)(blockIdx.x % REDO_NLISTS);
-                const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
-                long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
-                ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
-                ent[2] = dest;
-                st_release_gpu(ent, ((long long)(g * a.max_splits + j) << 32) |
-                                        (long long)(unsigned)(b + 1));
+        // the partial rows of this lane: head0 and head0 + 1, the split's own slot or the extra
+        // slot of a part that began inside the unit
+        float* orow[2] = {nullptr, nullptr};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int hh = head0 + c;
+            if (!hv[c] || !((write_mask >> hh) & 1u)) continue;
+            orow[c] = dest >= 0 ? a.xo + ((long long)dest * a.R + hh) * D
+                                : a.o_part + (MQ ? unit_row_slot(a, b, g, hh, j)
+                                                 : ((long long)b * a.Hq + g * a.G + hh) * a.max_splits + j) * D;
+        }
+        if (!ring_wait(rg.mhand, upar, misc, a)) return;
+        {
+            const float4* slot = xs + KS * 32;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const float4 v = slot[mt * 32 + lane];
+                o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
             }
         }
-        if (ctid == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rg.mdone);      // both slots read: warps 2 and 3 may refill them
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            if (orow[c] == nullptr) continue;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                orow[c][16 * mt + r] = o[mt][c];
+                orow[c][16 * mt + r + 8] = o[mt][c + 2];
+            }
+        }
+        // ---- a segment with a row outside the window goes on the device-wide fallback list ----
+        // (warp 0's flag stores are ordered before the release store that publishes the entry)
+        __syncwarp();
+        if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL && lane == 0) {
+            const int list = (int)(blockIdx.x % REDO_NLISTS);
+            const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
+            long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
+            ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
+            ent[2] = dest;
+            st_release_gpu(ent, ((long long)(g * a.max_splits + j) << 32) | (long long)(unsigned)(b + 1));
+        }
+        if (lane == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
     }
 }
 
@@ -952,6 +951,8 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     rg.qempty = rg.qfull + 16;
     rg.cbar = rg.qempty + 16;
     rg.own_done = rg.cbar + 8;
+    rg.mhand = rg.own_done + 8;
+    rg.mdone = rg.mhand + 8;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.nstage; ++s) {
@@ -964,6 +965,8 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
         }
         mbar_init(rg.cbar, NCW);
         mbar_init(rg.own_done, 1);
+        mbar_init(rg.mhand, 1);
+        mbar_init(rg.mdone, 1);
         misc[0] = 0;
         misc[1] = 0;
         fence_mbar_init();
@@ -974,7 +977,7 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     grid_dependency_wait();
 
     int* plan = reinterpret_cast<int*>(sm + lay.plan);
-    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1), plan + 2 * (a.B + 1)};
+    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1)};
     if (warp == NCW) {
         if (lane == 0) {
             prefetch_tensormap(&tmK);
