@@ -109,6 +109,9 @@ def _load():
             lib.or_plan.argtypes = [ip, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ip, ip]
             lib.or_plan.restype = ctypes.c_longlong
+            lib.or_flat_gemm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         vp, vp, ip, ctypes.c_int, vp, ctypes.c_int]
+            lib.or_flat_gemm.restype = ctypes.c_int
             lib.or_default_threads.argtypes = []
             lib.or_default_threads.restype = ctypes.c_int
             _lib = lib
@@ -271,3 +274,29 @@ def plan(seq_lens, num_kv_heads, max_seq_len, S):
     off = np.zeros(B + 1, dtype=np.int32)
     n_units = lib.or_plan(_ptr(sl), B, num_kv_heads, max_seq_len, S, _ptr(nsplit), _ptr(off))
     return nsplit, off, int(n_units)
+
+
+def flat_gemm(x, w, entries=None, dtype=BF16, n_threads=0):
+    """C = x W^T in float64 on the widened inputs (oracle.c, R10).
+
+    x: [M][K], w: [N][K], uint16 bf16 bit patterns (dtype BF16) or float32 (dtype F32).
+    entries: None for the whole [M][N] product, or an int array of (m, n) pairs, giving
+    float64 [len(entries)]."""
+    lib = _load()
+    x = _kv_array(x, dtype)
+    w = _kv_array(w, dtype)
+    if x.ndim != 2 or w.ndim != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"shapes {x.shape} and {w.shape} do not make x W^T")
+    M, K = x.shape
+    N = w.shape[0]
+    if entries is None:
+        out = np.empty((M, N), np.float64)
+        e, ne = None, 0
+    else:
+        e = np.ascontiguousarray(np.asarray(entries, np.int32).reshape(-1, 2))
+        ne = e.shape[0]
+        out = np.empty(ne, np.float64)
+    used = lib.or_flat_gemm(M, N, K, dtype, _ptr(x), _ptr(w), _ptr(e), ne, _ptr(out), n_threads)
+    if used < 0:
+        raise ValueError("or_flat_gemm rejected its arguments")
+    return out

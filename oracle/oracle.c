@@ -42,6 +42,11 @@
  *       decode): the Tq query tokens are the sequence's last Tq positions, so query token i sees
  *       the keys t < L_b - Tq + 1 + i (causal). The splits stay those of the sequence's keys; a
  *       query row's last splits may hold fewer of its keys or none. A row with no key is zero.
+ *   R10 The flat GEMM of [theory] s2 (2) and s4 is a decode-time linear layer: a few rows of
+ *       activations (M, the batch of query tokens) times a weight matrix that does not change
+ *       (N x K). Read as y = x W^T with x [M][K] and W [N][K] row-major (a linear layer's weight
+ *       as stored), C[m][n] = sum_k x[m][k] W[n][k]. The pages give no layout or dtype; bf16 in,
+ *       as for the cache.
  *
  * Precision: every value is widened exactly to double (bf16 and fp32 both widen exactly);
  * all arithmetic is double. Threads: rows are independent, and are spread over pthreads.
@@ -634,6 +639,58 @@ int or_pick_phi(const double* smin, const double* smax, const int32_t* nsplit, i
     }
     free(a); free(bb); free(x); free(cnt);
     return 0;
+}
+
+/* ----------------------------------------------------------------------------------------- */
+/* 5. flat GEMM of a decode-time linear layer ([theory] s2 (2), s4; R10)                      */
+/* ----------------------------------------------------------------------------------------- */
+
+typedef struct {
+    int M, N, K, dtype;
+    const void* x;            /* [M][K] */
+    const void* w;            /* [N][K] */
+    const int32_t* entries;   /* (m, n) pairs, or NULL for every (m, n) */
+    double* out;              /* [n_entries] or [M][N] */
+} or_gemm_ctx;
+
+/* One output row of work: entry r, or row m = r of the full product. */
+static void or_gemm_row(void* vctx, int r)
+{
+    const or_gemm_ctx* c = (const or_gemm_ctx*)vctx;
+    if (c->entries) {
+        const int m = c->entries[2 * r], n = c->entries[2 * r + 1];
+        double acc = 0.0;
+        for (int k = 0; k < c->K; ++k)
+            acc += or_widen(c->x, c->dtype, (size_t)m * c->K + k) *
+                   or_widen(c->w, c->dtype, (size_t)n * c->K + k);
+        c->out[r] = acc;
+        return;
+    }
+    for (int n = 0; n < c->N; ++n) {
+        double acc = 0.0;
+        for (int k = 0; k < c->K; ++k)
+            acc += or_widen(c->x, c->dtype, (size_t)r * c->K + k) *
+                   or_widen(c->w, c->dtype, (size_t)n * c->K + k);
+        c->out[(size_t)r * c->N + n] = acc;
+    }
+}
+
+/* C[m][n] = sum_k x[m][k] * W[n][k] in double, k ascending, on the widened inputs (R10). With
+ * entries == NULL, out is the whole [M][N] product; otherwise out[i] is entry i's (m, n).
+ * Returns the thread count used, or -1 on a bad argument. */
+int or_flat_gemm(int M, int N, int K, int dtype, const void* x, const void* w,
+                 const int32_t* entries, int n_entries, double* out, int n_threads)
+{
+    if (M < 0 || N < 0 || K < 0 || !out || (M > 0 && K > 0 && !x) || (N > 0 && K > 0 && !w))
+        return -1;
+    if (entries) {
+        for (int i = 0; i < n_entries; ++i)
+            if (entries[2 * i] < 0 || entries[2 * i] >= M || entries[2 * i + 1] < 0 ||
+                entries[2 * i + 1] >= N)
+                return -1;
+    }
+    or_gemm_ctx c = {M, N, K, dtype, x, w, entries, out};
+    return or_parallel_rows(or_gemm_row, &c, entries ? n_entries : M, n_threads);
 }
 
 /* Number of threads or_* calls use for n_threads == 0 (the host's online CPUs). */
