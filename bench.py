@@ -60,6 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--tc-ctas", type=int, default=0)
     ap.add_argument("--tc-prefetch", type=int, default=0)
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
+    ap.add_argument("--split-k", type=int, default=0, help="flat GEMM configs: split_k (0 = auto)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -208,6 +209,14 @@ def split_kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def gemm_kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("flat_gemm.cu", "device_common.cuh", "fdpp_internal.h"):
+        with open(os.path.join(ROOT, "split_kv_async_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(config_name: str, kernel_name: str):
     """DRAM bytes per split-kernel launch from the committed ncu summary, when it was taken on
     the current kernel sources (else None)."""
@@ -217,7 +226,8 @@ def recorded_traffic(config_name: str, kernel_name: str):
     with open(path) as f:
         d = json.load(f)
     e = d.get(f"{config_name}/{kernel_name}")
-    if not e or e.get("source_hash") != split_kernel_source_hash():
+    want = gemm_kernel_source_hash() if kernel_name == "flat_gemm" else split_kernel_source_hash()
+    if not e or e.get("source_hash") != want:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -571,6 +581,149 @@ def run_fdpp(args, dist: Dist):
     return res
 
 
+GEMM_METRIC = "flat-GEMM (decode linear layer y = x W^T) bytes GB/s and µs/call at 1 GB300"
+
+
+def gemm_oracle_rate(x, w, budget_s):
+    """The oracle's rate on sampled entries of the product, as bytes of the whole call per
+    second (time per entry x M x N for the whole product)."""
+    import numpy as np
+    import oracle
+    M, K = x.shape
+    N = w.shape[0]
+    rng = np.random.default_rng(1)
+    threads = oracle.default_threads()
+    done, t_sum, n = 0, 0.0, 4 * threads
+    while t_sum < budget_s:
+        ent = np.stack([rng.integers(0, M, n), rng.integers(0, N, n)], axis=1)
+        t0 = time.perf_counter()
+        oracle.flat_gemm(x, w, entries=ent, n_threads=threads)
+        t_sum += time.perf_counter() - t0
+        done += n
+        n = min(n * 2, 1 << 20)
+    per_entry = t_sum / done
+    call_bytes = (N * K + M * K + M * N) * 2
+    return call_bytes / (per_entry * M * N) / 1e9, threads, (
+        f"{done} sampled entries of the {M}x{N}x{K} product, {t_sum:.1f} s of fp64 oracle work on "
+        f"{threads} threads, scaled to the whole product")
+
+
+def run_gemm(args, dist: Dist):
+    import numpy as np
+    import torch
+
+    import split_kv_async_gb300 as F
+    import workloads as W
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    wl = W.GEMM[args.config]
+    if dist.world > 1:
+        wl = wl.replace(seed=wl.seed + 1000 * dist.rank)
+    x_np, w_np = W.gemm_inputs(wl)
+    M, N, K = wl.M, wl.N, wl.K
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
+    w_bytes = w_np.nbytes
+    R = max(1, min(64, math.ceil(4 * l2 / w_bytes)))
+    x = _dev_tensor(x_np, dev)
+    ws_ = [_dev_tensor(w_np, dev)]
+    for _ in range(R - 1):
+        ws_.append(ws_[0].clone())
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    # the heuristic dataflow's table, measured offline on this GPU model (gemm_lut.py)
+    from split_kv_async_gb300 import gemm_lut
+    lut_rows = gemm_lut.apply() if args.split_k == 0 else 0
+    split = F.fdpp_flat_gemm_split_k(M, N, K, args.split_k)
+    work = F.alloc_flat_gemm_workspace(M, N, K, split, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    call = F.lib.fdpp_flat_gemm
+    wsb = work.numel()
+
+    def step(i):
+        st = call(x.data_ptr(), ws_[i % R].data_ptr(), y.data_ptr(), M, N, K, split, work.data_ptr(),
+                  wsb, sh)
+        if st != 0:
+            raise F.FdppError(st, "fdpp_flat_gemm", F.fdpp_last_error())
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    Ksteps = args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0,
+                           enabled=not args.no_clocks and dist.local_rank == 0)
+    time.sleep(0.25 if sampler.proc else 0.0)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(Ksteps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    call_bytes = (N * K + M * K + M * N) * 2
+    _, t_max, value = aggregate(call_bytes * Ksteps, total_ms / 1e3, dist)
+    us = t_max * 1e6 / Ksteps
+    peak, peak_kind = measured_peaks()
+    achieved = call_bytes / (total_ms / 1e3 / Ksteps) / 1e9
+    err = F.fdpp_flat_gemm_read_error(work)
+
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step(i):
+            x.copy_(hx, non_blocking=True)
+            step(i)
+            hy.copy_(y, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(3):
+            e2e_step(i)
+        n = max(1, args.e2e_steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _, t_e2e, v_e2e = aggregate(call_bytes * n, e0.elapsed_time(e1) / 1e3, dist)
+        e2e = {"value": v_e2e, "unit": "GB/s", "h2d_bytes_per_step": int(x_np.nbytes),
+               "d2h_bytes_per_step": int(M * N * 2), "us_per_step": t_e2e * 1e6 / n, "mode": "eager"}
+
+    cpu = None
+    if not args.no_cpu and dist.rank == 0:
+        gbs, threads, desc = gemm_oracle_rate(x_np, w_np, args.cpu_budget_s)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+    if dist.rank != 0:
+        return None
+    return {
+        "metric": GEMM_METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": Ksteps,
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "us_per_step": us, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12 * dist.world,
+        "config": {"workload": wl.name, "M": M, "N": N, "K": K, "split_k": split,
+                   "split_k_from": ("request" if args.split_k else
+                                    "lookup table" if lut_rows else "heuristic"),
+                   "bytes_per_call": call_bytes,
+                   "l2_policy": f"rotate {R} weight copies ({R * w_bytes / 2**20:.0f} MiB >= 4x L2 "
+                                f"{l2 / 2**20:.0f} MiB); no flush",
+                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": recorded_traffic(wl.name, "flat_gemm"), "kernel": "flat_gemm_kernel",
+                     "kernel_us": us},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": Ksteps, "clocks": clocks, "error_bits": err,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist(args.gpus)
@@ -583,7 +736,7 @@ def main(argv=None):
                 __graft_entry__.build()
             dist.barrier()
             __graft_entry__.build()
-            res = run_fdpp(args, dist)
+            res = run_gemm(args, dist) if args.config.startswith("gemm_") else run_fdpp(args, dist)
         if res is not None and dist.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

@@ -28,10 +28,13 @@ FDPP_FLAG_OUT, FDPP_FLAG_ABOVE, FDPP_FLAG_BELOW, FDPP_FLAG_NAN, FDPP_FLAG_RECOMP
 FDPP_ERRBIT_SEQ_LEN, FDPP_ERRBIT_BLOCK_TABLE, FDPP_ERRBIT_TIMEOUT = 1, 2, 4
 FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 
-# Names every build of the library exports (the C ABI of include/fdpp.h).
+# Names every build of the library exports (the C ABI of include/fdpp.h and include/fdpp_gemm.h).
 EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fdpp_decode_attn",
             "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_score_ranges",
-            "fdpp_pick_phi", "fdpp_read_diag", "fdpp_status_str", "fdpp_last_error")
+            "fdpp_pick_phi", "fdpp_read_diag", "fdpp_status_str", "fdpp_last_error",
+            "fdpp_flat_gemm_split_k", "fdpp_flat_gemm_workspace_size", "fdpp_flat_gemm",
+            "fdpp_flat_gemm_set_lut", "fdpp_flat_gemm_read_error")
+FDPP_GEMM_MAX_M = 128
 FDPP_NOALLOC_WORKSPACE_BYTES = 16 << 20
 FDPP_TC_MAX_PARTS = 512
 
@@ -104,6 +107,17 @@ def _load() -> ctypes.CDLL:
     lib.fdpp_status_str.restype = ctypes.c_char_p
     lib.fdpp_last_error.argtypes = []
     lib.fdpp_last_error.restype = ctypes.c_char_p
+    ci = ctypes.c_int
+    lib.fdpp_flat_gemm_split_k.argtypes = [ci, ci, ci, ci]
+    lib.fdpp_flat_gemm_split_k.restype = ci
+    lib.fdpp_flat_gemm_workspace_size.argtypes = [ci, ci, ci, ci]
+    lib.fdpp_flat_gemm_workspace_size.restype = ctypes.c_size_t
+    lib.fdpp_flat_gemm.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
+    lib.fdpp_flat_gemm.restype = ci
+    lib.fdpp_flat_gemm_set_lut.argtypes = [vp, ci]
+    lib.fdpp_flat_gemm_set_lut.restype = ci
+    lib.fdpp_flat_gemm_read_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.fdpp_flat_gemm_read_error.restype = ci
     return lib
 
 
@@ -244,3 +258,49 @@ def fdpp_status_str(status: int) -> str:
 
 def fdpp_last_error() -> str:
     return lib.fdpp_last_error().decode()
+
+
+# ---- flat GEMM (include/fdpp_gemm.h) --------------------------------------------------------
+
+def fdpp_flat_gemm_split_k(M: int, N: int, K: int, split_k: int = 0) -> int:
+    """split_k fdpp_flat_gemm uses on the current device (0: the shape is invalid)."""
+    return int(lib.fdpp_flat_gemm_split_k(M, N, K, split_k))
+
+
+def fdpp_flat_gemm_workspace_size(M: int, N: int, K: int, split_k: int = 0) -> int:
+    return int(lib.fdpp_flat_gemm_workspace_size(M, N, K, split_k))
+
+
+def alloc_flat_gemm_workspace(M: int, N: int, K: int, split_k: int = 0, device="cuda"):
+    """A zeroed uint8 device tensor large enough for fdpp_flat_gemm(M, N, K, split_k)."""
+    import torch
+    n = fdpp_flat_gemm_workspace_size(M, N, K, split_k)
+    if n == 0:
+        raise FdppError(FDPP_ERR_INVALID_ARG, "fdpp_flat_gemm_workspace_size",
+                        f"invalid shape M={M} N={N} K={K}")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def fdpp_flat_gemm(x, w, y, workspace, split_k: int = 0, stream=None) -> None:
+    """y = x W^T: x [M][K], w [N][K], y [M][N], bf16 device tensors (or addresses with shapes
+    given by the tensors)."""
+    M, K = int(x.shape[0]), int(x.shape[1])
+    N = int(w.shape[0])
+    _check(lib.fdpp_flat_gemm(_ptr(x), _ptr(w), _ptr(y), M, N, K, split_k, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream)), "fdpp_flat_gemm")
+
+
+def fdpp_flat_gemm_set_lut(entries) -> None:
+    """entries: rows of (m_max, N, K, split_k); an empty list clears the table."""
+    import numpy as np
+    e = np.ascontiguousarray(np.asarray(entries, np.int32).reshape(-1, 4))
+    _check(lib.fdpp_flat_gemm_set_lut(e.ctypes.data if len(e) else None, len(e)),
+           "fdpp_flat_gemm_set_lut")
+
+
+def fdpp_flat_gemm_read_error(workspace) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(lib.fdpp_flat_gemm_read_error(_ptr(workspace), ctypes.byref(bits)),
+           "fdpp_flat_gemm_read_error")
+    return int(bits.value)

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfdpp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cpp", "split_tc.cu", "split_simt.cu", "combine.cu", "no_alloc.cu"]
+SOURCES = ["api.cpp", "split_tc.cu", "split_simt.cu", "combine.cu", "no_alloc.cu", "flat_gemm.cu"]
 HEADERS = ["fdpp_internal.h", "device_common.cuh"]
 
 
@@ -33,6 +33,7 @@ def _nvcc() -> str:
 def _newest_input() -> float:
     paths = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
     paths.append(os.path.join(INCLUDE, "fdpp.h"))
+    paths.append(os.path.join(INCLUDE, "fdpp_gemm.h"))
     paths.append(os.path.abspath(__file__))
     return max(os.path.getmtime(p) for p in paths)
 

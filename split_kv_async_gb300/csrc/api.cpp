@@ -284,6 +284,22 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
 }  // namespace
 
 namespace fdpp {
+
+fdpp_status query_device(int* sms, int* smem_per_sm, int* smem_per_block)
+{
+    DeviceInfo d;
+    const fdpp_status st = device_info(d);
+    if (st != FDPP_OK) return st;
+    if (sms) *sms = d.sms;
+    if (smem_per_sm) *smem_per_sm = d.smem_per_sm;
+    if (smem_per_block) *smem_per_block = d.smem_per_block;
+    return FDPP_OK;
+}
+
+fdpp_status get_tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn)
+{
+    return tensor_map_encoder(*fn);
+}
 // Bytes at the start of a workspace for `p` that hold the state which must be zero before a call:
 // header, plan and the fallback list (everything before the flag bytes).
 size_t workspace_zero_prefix(const fdpp_params& p) { return layout_of(p).flags; }

@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "fdpp.h"
@@ -95,6 +96,11 @@ cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
 // Score range of every row-split (least into l_part, greatest into m_part) and the split plan.
 cudaError_t launch_score_ranges(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
 int score_ranges_ctas_per_sm(const KernelArgs& a, int dtype);
+
+// The current device's SM count and shared-memory limits (sm_103a checked; cached per device).
+fdpp_status query_device(int* sms, int* smem_per_sm, int* smem_per_block);
+// The driver's cuTensorMapEncodeTiled (looked up once).
+fdpp_status get_tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
 
 // Bytes at the front of a workspace for `p` that must be zero when a call starts.
 size_t workspace_zero_prefix(const fdpp_params& p);

@@ -10,13 +10,18 @@ import pytest
 
 import split_kv_async_gb300 as F
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "fdpp.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+HEADER = os.path.join(INCLUDE, "fdpp.h")
+GEMM_HEADER = os.path.join(INCLUDE, "fdpp_gemm.h")
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fdpp_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(fdpp_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_names():
@@ -49,6 +54,8 @@ def test_binding_constants_match_header_defines():
     for name in ("FDPP_AUTO_UNITS_PER_SM", "FDPP_AUTO_GRANULE", "FDPP_AUTO_MIN_SPLIT",
                  "FDPP_TC_MAX_PARTS", "FDPP_NOALLOC_WORKSPACE_BYTES"):
         assert getattr(F, name) == defines[name], name
+    gemm = dict((n, int(v)) for n, v in re.findall(r"#define (FDPP_\w+) (\d+)", open(GEMM_HEADER).read()))
+    assert F.FDPP_GEMM_MAX_M == gemm["FDPP_GEMM_MAX_M"]
 
 
 def _gqa_params(**kw):
@@ -164,3 +171,38 @@ def test_no_gpu_gives_cuda_error_not_a_crash():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _call(_gqa_params()) == F.FDPP_ERR_CUDA
+
+
+# ---- flat GEMM: argument errors before any CUDA call ----------------------------------------
+
+def _gemm_status(x=16, w=16, y=16, M=8, N=256, K=512, split_k=0, ws=256, ws_bytes=1 << 20):
+    return F.lib.fdpp_flat_gemm(x, w, y, M, N, K, split_k, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [dict(M=0), dict(M=129), dict(N=0), dict(K=4), dict(K=100),
+                                dict(x=None), dict(w=None), dict(y=None), dict(x=24),
+                                dict(w=8), dict(split_k=-1), dict(split_k=9), dict(K=4096, split_k=9)])
+def test_flat_gemm_rejects_bad_arguments(kw):
+    assert _gemm_status(**kw) == F.FDPP_ERR_INVALID_ARG
+    assert F.fdpp_last_error()
+
+
+def test_flat_gemm_rejects_a_misaligned_workspace():
+    assert _gemm_status(ws=256 + 64) == F.FDPP_ERR_WORKSPACE
+
+
+def test_flat_gemm_split_k_and_size_reject_bad_shapes():
+    assert F.fdpp_flat_gemm_split_k(0, 128, 64) == 0
+    assert F.fdpp_flat_gemm_split_k(8, 128, 63) == 0
+    assert F.fdpp_flat_gemm_workspace_size(8, 0, 64) == 0
+
+
+@pytest.mark.parametrize("rows", [[(0, 128, 64, 1)], [(8, 128, 4, 1)], [(8, 128, 64, 0)]])
+def test_flat_gemm_lut_rejects_bad_entries(rows):
+    with pytest.raises(F.FdppError):
+        F.fdpp_flat_gemm_set_lut(rows)
+
+
+def test_flat_gemm_lut_accepts_and_clears():
+    F.fdpp_flat_gemm_set_lut([(16, 4096, 4096, 10)])
+    F.fdpp_flat_gemm_set_lut([])

@@ -1,4 +1,4 @@
-"""Seeded synthetic decode-attention workloads.
+"""Seeded synthetic decode-attention workloads (and the decode-time linear layers' GEMMs).
 
 This module only builds inputs: shapes, seeded random draws, bf16 rounding and cache layout. It
 holds none of the attention arithmetic, and both the CUDA path (through its tests and the bench)
@@ -99,6 +99,43 @@ SHIFTED = Workload("gqa_head_levels", 8, 32, 8, 128, BF16, split_len=512, seq_le
 SPEC = Workload("spec_decode_tq2", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=2,
                 seed=0x5EED0006)
 ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED, SPEC)}
+
+
+@dataclasses.dataclass(frozen=True)
+class GemmWorkload:
+    """A decode-time linear layer y = x W^T: x [M][K] activations, W [N][K] weight, both bf16
+    standard normals (W scaled by 1/sqrt(K), as an initialised layer's weight)."""
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+
+    def replace(self, **kw) -> "GemmWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# The four linear layers of a decoder block with the attention workloads' geometry (hidden
+# 4096 = 32 query heads x 128, 8 kv heads, FFN width 14336 with gate and up fused), at the batch of
+# gqa_decode (M = 8) and of paged_batch (M = 64).
+_LAYERS = (("qkv", 6144, 4096), ("o_proj", 4096, 4096), ("gate_up", 28672, 4096),
+           ("down", 4096, 14336))
+GEMM = {f"gemm_{n}_m{m}": GemmWorkload(f"gemm_{n}_m{m}", m, N, K, seed=0x5EEDA000 + 16 * i + m)
+        for i, (n, N, K) in enumerate(_LAYERS) for m in (8, 64)}
+
+_S_GX, _S_GW = 11, 12
+
+
+def gemm_inputs(wl: GemmWorkload):
+    """(x, w) as uint16 bf16 bit patterns, [M][K] and [N][K]."""
+    x = _normals(_rng(wl.seed, _S_GX), wl.M * wl.K, BF16).reshape(wl.M, wl.K)
+    rng = _rng(wl.seed, _S_GW)
+    scale = np.float32(1.0 / math.sqrt(wl.K))
+    w = np.empty(wl.N * wl.K, np.uint16)
+    for i in range(0, w.size, _CHUNK):
+        n = min(_CHUNK, w.size - i)
+        w[i:i + n] = f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32) * scale)
+    return x, w.reshape(wl.N, wl.K)
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
