@@ -134,6 +134,7 @@ WsLayout layout_of(const fdpp_params& p)
     // a fallback entry per unit, plus one per part for units cut in two
     const size_t entries = redo_capacity(p);
     w.redo = off;    off = align256(off + REDO_NLISTS * entries * REDO_WORDS * 8);
+    w.hint = off;    off = align256(off + (size_t)TC_MAX_PARTS * HINT_WORDS * 4);
     w.flags = off;   off = align256(off + slots);
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
@@ -248,6 +249,7 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.nsplit = reinterpret_cast<int32_t*>(ws + w.nsplit);
     a.tstart = reinterpret_cast<int32_t*>(ws + w.tstart);
     a.redo = reinterpret_cast<long long*>(ws + w.redo);
+    a.hint = reinterpret_cast<int32_t*>(ws + w.hint);
     a.redo_cap = (int)redo_capacity(*p);
     a.flags = ws + w.flags;
     a.m_part = reinterpret_cast<float*>(ws + w.m_part);

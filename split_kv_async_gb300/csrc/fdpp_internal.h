@@ -30,7 +30,7 @@ enum {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-    size_t header, nsplit, tstart, redo, flags, m_part, l_part, o_part, xf, xm, xl, xo, total;
+    size_t header, nsplit, tstart, redo, hint, flags, m_part, l_part, o_part, xf, xm, xl, xo, total;
     int max_splits;
 };
 
@@ -47,6 +47,11 @@ constexpr int REDO_WORDS = 4;
 // The fallback list is this many lists (CTA c pushes to list c % REDO_NLISTS), each with room for
 // every entry of a call.
 constexpr int REDO_NLISTS = 8;
+// Start-up hint of the tensor kernel (contiguous caches): per CTA, the TMA coordinates (x, y, z)
+// of the first HINT_TILES tiles it streamed in the last call, after a count; prefetched into L2
+// before the kernel waits for the previous one. HINT_WORDS int32 per CTA.
+constexpr int HINT_TILES = 3;
+constexpr int HINT_WORDS = 16;
 
 // Everything a kernel of this library needs about one call. Plain pointers and sizes.
 struct KernelArgs {
@@ -60,6 +65,7 @@ struct KernelArgs {
     int32_t* nsplit;              // [B], written by CTA 0 of the split kernel
     int32_t* tstart;              // [B + 1] tile prefix of the sequences (tensor kernel, CTA 0)
     long long* redo;              // fallback lists, REDO_WORDS per entry (tensor kernel)
+    int32_t* hint;                // [TC_MAX_PARTS][HINT_WORDS] start-up hint (tensor kernel)
     int redo_cap;                 // entries per fallback list
     uint8_t* flags;               // [B][Tq][Hq][max_splits]
     float* m_part;                // [B][Tq][Hq][max_splits]

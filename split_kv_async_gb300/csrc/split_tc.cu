@@ -129,6 +129,7 @@ struct Producer {
     int* lplan;                //   clamped L_b [B] (n_b = min(ceil(L_b / S), max_splits))
     int S = 0, TS = 0;         // split length, tiles of a full split
     uint32_t stage = 0, phase = 0, qiter = 0;
+    int hint_n = 0;            // tiles recorded in this CTA's start-up hint
     bool bad_block = false;
 
     // Split plan: S, the n_b and tile prefixes in smem (or a global walk for large batches),
@@ -307,6 +308,14 @@ struct Producer {
                     const int hv = lane >> 1;
                     tma_load_3d(((lane & 1) ? vdst : kdst) + hv * TILE * 128, (lane & 1) ? tmV : tmK,
                                 g * D + hv * 64, tt, b, fb);
+                }
+                // the first tiles of this call are the next call's start-up hint
+                if (lane == 0 && hint_n < HINT_TILES && kind != KIND_REDO && blockIdx.x < TC_MAX_PARTS) {
+                    int* h = A.hint + (long long)blockIdx.x * HINT_WORDS;
+                    h[1 + 3 * hint_n] = g * D;
+                    h[2 + 3 * hint_n] = tt;
+                    h[3 + 3 * hint_n] = b;
+                    h[0] = ++hint_n;
                 }
             } else {
                 const int lb0 = tt / bs;
@@ -972,8 +981,26 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
         fence_mbar_init();
     }
     __syncthreads();
-    // launched as a programmatic dependent: no global memory is read or written before the
-    // previous kernel on the stream has completed
+    // Launched as a programmatic dependent: nothing is read into the CTA or written before the
+    // previous kernel on the stream has completed. Before that, while it finishes, the tiles this
+    // CTA streamed first in the last call (contiguous caches) are prefetched into L2: the split
+    // plan changes little from one decode step to the next. A stale hint costs a useless
+    // prefetch only (L2 is where the previous kernel's writes land).
+    if (!PAGED && warp == NCW && lane == 0 && blockIdx.x < TC_MAX_PARTS) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        const volatile int* h = a.hint + (long long)blockIdx.x * HINT_WORDS;
+        const int n = min(max(h[0], 0), HINT_TILES);
+        for (int i = 0; i < n; ++i) {
+            const int x = h[1 + 3 * i], y = h[2 + 3 * i], z = h[3 + 3 * i];
+            if (x < 0 || (x & 63) != 0) continue;
+#pragma unroll
+            for (int hv = 0; hv < D / 64; ++hv) {
+                tma_prefetch_3d(&tmK, x + 64 * hv, y, z);
+                tma_prefetch_3d(&tmV, x + 64 * hv, y, z);
+            }
+        }
+    }
     grid_dependency_wait();
 
     int* plan = reinterpret_cast<int*>(sm + lay.plan);
