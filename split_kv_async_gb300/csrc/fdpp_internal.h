@@ -50,7 +50,7 @@ constexpr int REDO_NLISTS = 8;
 // Start-up hint of the tensor kernel (contiguous caches): per CTA, the TMA coordinates (x, y, z)
 // of the first HINT_TILES tiles it streamed in the last call, after a count; prefetched into L2
 // before the kernel waits for the previous one. HINT_WORDS int32 per CTA.
-constexpr int HINT_TILES = 3;
+constexpr int HINT_TILES = 5;
 constexpr int HINT_WORDS = 16;
 
 // Everything a kernel of this library needs about one call. Plain pointers and sizes.
