@@ -30,10 +30,16 @@
 //                                    K byte read from HBM feeds all G heads once;
 //             P = exp(S - phi), window test;
 //             O^T += V^T P^T         P carried as bf16 hi + lo parts (~16 mantissa bits).
-//             The four warps merge their fp32 partials through shared memory (a plain sum in
-//             the phi frame) and write o, l, m and the flag byte of each head.
+//             The four warps merge their fp32 partials through shared memory of their own, as a
+//             tree (w0 + w2) + (w1 + w3) (a plain sum in the phi frame), and warp 0 writes o, l,
+//             m and the flag byte of each query row; every stage goes back to the producer as
+//             soon as its tile is read.
 // When a CTA starts its last own segment it allows the dependent combine launch to begin
-// (programmatic dependent launch), so that launch overlaps the tail of this one.
+// (programmatic dependent launch), so that launch overlaps the tail of this one. This kernel is
+// a programmatic dependent too: before it waits for the previous kernel, each CTA prefetches
+// into L2 the tiles it streamed first in the previous call (a hint kept in the workspace).
+// Several query tokens per sequence (MQ builds): R = Tq G query rows per kv head, each with its
+// causal key limit.
 // Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT and the CTA stops.
 // (A fused last-arriver combine was measured here and removed: under full HBM load its
 // latency-bound reads of the partials stalled the consumer warps for several microseconds per
@@ -658,7 +664,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 
                 // S^T = K Q^T for this warp's 16 tokens, two accumulation chains
                 float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    #pragma unroll
+#pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     const int chunk = 2 * ks + (mi >> 1);
                     const uint32_t addr = kb + (chunk >> 3) * (TILE * 128) + k_row * 128 + (((chunk & 7) ^ r8) << 4);
@@ -669,7 +675,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 // element e of sa: token tok_r + 8 (e >> 1), head head0 + (e & 1)
                 float sv[4];
                 bool valid[4];
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
                     const int tok = tok_r + 8 * (e >> 1);
@@ -682,11 +688,11 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 
                 float p[4];
                 if constexpr (!ONLINE) {
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 4; ++e) p[e] = valid[e] ? __expf(__fsub_rn(sv[e], phv[e & 1])) : 0.f;
                 } else {
                     float corr[2];
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         float tmax = -INFINITY;
                         if (valid[c]) tmax = sv[c];
@@ -709,7 +715,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                         if (qd >= 2) { oc[0] = x0; oc[1] = x1; }
                     }
                     if (oc[0] != 1.f || oc[1] != 1.f) {
-    #pragma unroll
+#pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
                             o[mt][0] *= oc[0]; o[mt][2] *= oc[0];
                             o[mt][1] *= oc[1]; o[mt][3] *= oc[1];
@@ -747,7 +753,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     vm_lo = (tok_q < nvalid ? 0x0000ffffu : 0u) | (tok_q + 1 < nvalid ? 0xffff0000u : 0u);
                     vm_hi = (tok_q + 8 < nvalid ? 0x0000ffffu : 0u) | (tok_q + 9 < nvalid ? 0xffff0000u : 0u);
                 }
-    #pragma unroll
+#pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     const int chunk = 2 * mt + (mi & 1);
                     const uint32_t addr = vb + (chunk >> 3) * (TILE * 128) + v_row * 128 + (((chunk & 7) ^ r8) << 4);
