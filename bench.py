@@ -33,6 +33,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -145,7 +146,9 @@ class ClockSampler:
         if not enabled:
             return
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out")
+            # raw samples (the JSON line carries their summary): FDPP_BENCH_LOG_DIR, else the
+            # system temporary directory
+            out_dir = os.environ.get("FDPP_BENCH_LOG_DIR") or tempfile.gettempdir()
             os.makedirs(out_dir, exist_ok=True)
             self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
