@@ -1,5 +1,5 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (default
-kernel choice and pipeline geometry):
+kernel choice and pipeline geometry), including two query tokens per sequence (spec_decode_tq2):
   * sampled output rows against the fp64 oracle (computed one row at a time);
   * every output finite; the split plan equal to the oracle's scheduler;
   * window decisions: none for the N(0,1) workloads; for the fallback-stress workload every
@@ -18,8 +18,9 @@ N_SAMPLE_ROWS = 64
 
 
 def _sample_rows(inp, n, seed):
+    """(query row b Tq + i, head h) pairs; Tq = 1 for the decode step."""
     rng = np.random.default_rng(seed)
-    B, Hq = inp.wl.batch, inp.wl.num_q_heads
+    B, Hq = inp.wl.batch * max(1, inp.wl.q_tokens), inp.wl.num_q_heads
     flat = rng.choice(B * Hq, size=min(n, B * Hq), replace=False)
     rows = np.stack([flat // Hq, flat % Hq], axis=1).astype(np.int32)
     if inp.hot:                                  # always include the hot-key rows
@@ -28,7 +29,7 @@ def _sample_rows(inp, n, seed):
     return rows
 
 
-@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS, W.SPEC], ids=lambda w: w.name)
 def test_full_size(wl):
     import split_kv_async_gb300 as F
     inp = W.generate(wl)
@@ -42,7 +43,7 @@ def test_full_size(wl):
     assert diag["n_units"] == o_units
     rows = _sample_rows(inp, N_SAMPLE_ROWS, wl.seed)
     ref = H.oracle_out(inp, rows=rows)
-    g = got.reshape(wl.batch, wl.num_q_heads, wl.head_dim)[rows[:, 0], rows[:, 1]]
+    g = got.reshape(wl.batch * max(1, wl.q_tokens), wl.num_q_heads, wl.head_dim)[rows[:, 0], rows[:, 1]]
     # the stated bound, verbatim, on every row whose output stays below 0.5 in magnitude (all
     # rows of the N(0,1) workloads); rows dominated by an injected hot key carry a single V row
     # (|o| up to ~4), where the bf16 output's own rounding can exceed 2e-3
