@@ -88,9 +88,9 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "q_tokens must be in [0, 64] (got %d)", p->q_tokens);
     const int G = p->num_q_heads / p->num_kv_heads;
     const int R = q_tokens_of(*p) * G;
-    if (R > SIMT_MAX_GROUP)
+    if (R > TC_MAX_ROWS)
         return fail(FDPP_ERR_UNSUPPORTED, "query rows per kv head (q_tokens x heads per kv head) %d > %d",
-                    R, SIMT_MAX_GROUP);
+                    R, TC_MAX_ROWS);
     // sizes stay far from overflow: partials below 2^50 bytes, unit indices below 2^31
     const long double o_bytes = (long double)p->batch * q_tokens_of(*p) * p->num_q_heads *
                                 max_splits_of(*p) * p->head_dim * 4.0L;
@@ -116,9 +116,16 @@ fdpp_status check_paged(const fdpp_params* p)
 }
 
 // Entries of one fallback list: one per unit, plus one per part for units cut in two.
+// Row groups of the tensor kernel: each (kv head, group of up to 8 query rows) is a unit head.
+int row_groups_of(const fdpp_params& p)
+{
+    const int R = q_tokens_of(p) * (p.num_q_heads / p.num_kv_heads);
+    return (R + TC_MAX_GROUP - 1) / TC_MAX_GROUP;
+}
+
 size_t redo_capacity(const fdpp_params& p)
 {
-    return (size_t)p.batch * p.num_kv_heads * max_splits_of(p) + TC_MAX_PARTS;
+    return (size_t)p.batch * p.num_kv_heads * row_groups_of(p) * max_splits_of(p) + TC_MAX_PARTS;
 }
 
 WsLayout layout_of(const fdpp_params& p)
@@ -139,9 +146,9 @@ WsLayout layout_of(const fdpp_params& p)
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
     w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
-    // extra slots of the tensor kernel's parts (R = Tq G rows each)
+    // extra slots of the tensor kernel's parts (one row group, min(R, 8) rows, each)
     const size_t R = (size_t)q_tokens_of(p) * (size_t)(p.num_q_heads / p.num_kv_heads);
-    const size_t xrows = (size_t)TC_MAX_PARTS * R;
+    const size_t xrows = (size_t)TC_MAX_PARTS * (R < TC_MAX_GROUP ? R : TC_MAX_GROUP);
     w.xf = off;      off = align256(off + xrows);
     w.xm = off;      off = align256(off + xrows * 4);
     w.xl = off;      off = align256(off + xrows * 4);
@@ -265,6 +272,9 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.G = G;
     a.Tq = q_tokens_of(*p);
     a.R = a.Tq * G;
+    a.NRG = row_groups_of(*p);
+    a.Rg = a.R < TC_MAX_GROUP ? a.R : TC_MAX_GROUP;
+    a.Hv = p->num_kv_heads * a.NRG;
     a.D = p->head_dim;
     a.max_seq_len = p->max_seq_len;
     a.block_size = paged ? p->block_size : 0;
@@ -381,12 +391,16 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         return fail(FDPP_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, w.total);
 
     const int G = p->num_q_heads / p->num_kv_heads;
-    const bool tc_ok = p->dtype == FDPP_BF16 && q_tokens_of(*p) * G <= TC_MAX_GROUP;
+    const int R = q_tokens_of(*p) * G;
+    const bool tc_ok = p->dtype == FDPP_BF16 && R <= TC_MAX_ROWS;
     int kernel = p->kernel;
     if (kernel == FDPP_KERNEL_AUTO) kernel = tc_ok ? FDPP_KERNEL_TENSOR : FDPP_KERNEL_SIMT;
+    if (kernel == FDPP_KERNEL_SIMT && R > SIMT_MAX_GROUP)
+        return fail(FDPP_ERR_UNSUPPORTED, "SIMT kernel needs at most %d query rows per kv head (got %d)",
+                    SIMT_MAX_GROUP, R);
     if (kernel == FDPP_KERNEL_TENSOR && !tc_ok)
         return fail(FDPP_ERR_UNSUPPORTED, "tensor kernel needs bf16 and at most %d query rows per kv head",
-                    TC_MAX_GROUP);
+                    TC_MAX_ROWS);
 
     DeviceInfo dev;
     if ((st = device_info(dev)) != FDPP_OK) return st;
@@ -400,7 +414,7 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     if (kernel == FDPP_KERNEL_TENSOR) {
-        const TcPlan plan = split_tc_plan(p->head_dim, q_tokens_of(*p) * G, p->batch, p->tc_stages,
+        const TcPlan plan = split_tc_plan(p->head_dim, R < TC_MAX_GROUP ? R : TC_MAX_GROUP, p->batch, p->tc_stages,
                                           p->tc_ctas_per_sm, dev.smem_per_sm, dev.smem_per_block);
         if (plan.nstage == 0)
             return fail(FDPP_ERR_UNSUPPORTED, "no tensor-kernel geometry fits (stages %d, CTAs/SM %d)",
@@ -416,7 +430,8 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         // TC_MAX_PARTS); larger ones are dealt out as whole units, no more CTAs than units.
         long long grid = (long long)dev.sms * plan.ctas_per_sm;
         if (grid > TC_MAX_PARTS) grid = TC_MAX_PARTS;
-        if (p->batch > TC_PLAN_SMEM_MAX_B && grid > units_max) grid = units_max;
+        const long long vunits = units_max * row_groups_of(*p);
+        if (p->batch > TC_PLAN_SMEM_MAX_B && grid > vunits) grid = vunits;
         e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, plan.ctas_per_sm, s);
     } else {
         const int occ = split_simt_ctas_per_sm(a, p->dtype);
@@ -439,6 +454,8 @@ fdpp_status fdpp_score_ranges(const void* q, const void* k_cache, const int32_t*
 {
     fdpp_status st = check_params(p);
     if (st != FDPP_OK) return st;
+    if (q_tokens_of(*p) * (p->num_q_heads / p->num_kv_heads) > SIMT_MAX_GROUP)
+        return fail(FDPP_ERR_UNSUPPORTED, "score ranges take at most %d query rows per kv head", SIMT_MAX_GROUP);
     const bool paged = block_table != nullptr;
     if (paged && (st = check_paged(p)) != FDPP_OK) return st;
     if (!q || !k_cache || !seq_lens || !smin_host || !smax_host)

@@ -70,7 +70,11 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
     const int bi = live ? row / a.Hq : 0;           // query row of the batch: b Tq + i
     const int b = bi / a.Tq;
     const int h = live ? row - bi * a.Hq : 0;
-    const int rr = (bi - b * a.Tq) * a.G + h % a.G;  // the unit's query row (extra-slot row)
+    // the row's place in the tensor kernel's units: kv-head row rr, in row group rr / 8 (the
+    // virtual head kvh NRG + group) as row rr % 8 (the extra-slot row)
+    const int rr = (bi - b * a.Tq) * a.G + h % a.G;
+    const int grp = a.NRG == 1 ? 0 : rr / TC_MAX_GROUP;
+    const int rr8 = rr - grp * TC_MAX_GROUP;
     const int n = live ? a.nsplit[b] : 0;
 
     // Parts that may start inside this row's units: the row's kv head owns tiles [W, W + nt).
@@ -81,7 +85,7 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         tiles = a.hdr[HDR_TILES];
         TS = (a.hdr[HDR_SPLIT] + 63) / 64;
         nt = a.tstart[b + 1] - a.tstart[b];
-        W = (long long)a.Hkv * a.tstart[b] + (long long)(h / a.G) * nt;
+        W = (long long)a.Hv * a.tstart[b] + (long long)((h / a.G) * a.NRG + grp) * nt;
         c_lo = (int)(((W + 1) * P + tiles - 1) / tiles);   // first part starting after tile W
         c_hi = (int)(((W + nt) * P - 1) / tiles);           // last part starting before W + nt
     }
@@ -96,9 +100,9 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         const int jx = ki / TS;
         return ki == jx * TS ? -1 : jx;
     };
-    const float* xm = a.xm + rr;
-    const float* xl = a.xl + rr;
-    const float* xo = a.xo + (long long)rr * D;
+    const float* xm = a.xm + rr8;
+    const float* xl = a.xl + rr8;
+    const float* xo = a.xo + (long long)rr8 * D;
     const long long base = (long long)row * a.max_splits;
     const float* m = a.m_part + base;
     const float* l = a.l_part + base;
@@ -119,13 +123,13 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         const int c = c_lo + (e - n);
         const int jx = extra_split(c);
         if (jx >= 0) {
-            M = fmaxf(M, xm[(long long)c * a.R]);
+            M = fmaxf(M, xm[(long long)c * a.Rg]);
             // the split's flag byte also covers the extra slot's tokens
             uint8_t* fb = a.flags + (long long)row * a.max_splits + jx;
             const uintptr_t addr = reinterpret_cast<uintptr_t>(fb);
             const unsigned sh = (unsigned)(addr & 3u) * 8u;
             atomicOr(reinterpret_cast<unsigned*>(addr & ~uintptr_t(3)),
-                     (unsigned)a.xf[(long long)c * a.R + rr] << sh);
+                     (unsigned)a.xf[(long long)c * a.Rg + rr8] << sh);
         }
     }
 #pragma unroll
@@ -158,8 +162,8 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
                 } else {
                     const int c = c_lo + (e - n);
                     if (extra_split(c) >= 0) {
-                        pm = xm + (long long)c * a.R; pl = xl + (long long)c * a.R;
-                        po = xo + (long long)c * a.R * D;
+                        pm = xm + (long long)c * a.Rg; pl = xl + (long long)c * a.Rg;
+                        po = xo + (long long)c * a.Rg * D;
                         ok[u] = true;
                     }
                 }

@@ -114,11 +114,12 @@ struct UnitCursor {
 
     __device__ __forceinline__ void reset() { b = -1; nb = 0; base = 0; }
 
-    __device__ __forceinline__ void seek(const KernelArgs& a, int S, long long u, int& ub, int& ug,
-                                         int& uj, int& L)
+    // heads: the heads of a sequence's units (Hkv, or the tensor kernel's virtual heads Hv)
+    __device__ __forceinline__ void seek(const KernelArgs& a, int heads, int S, long long u, int& ub,
+                                         int& ug, int& uj, int& L)
     {
-        while (b < 0 || u >= base + (long long)a.Hkv * nb) {
-            if (b >= 0) base += (long long)a.Hkv * nb;
+        while (b < 0 || u >= base + (long long)heads * nb) {
+            if (b >= 0) base += (long long)heads * nb;
             ++b;
             int n = ceil_div_i(clamp_len(a.seq_lens[b], a.max_seq_len), S);
             nb = n > a.max_splits ? a.max_splits : n;

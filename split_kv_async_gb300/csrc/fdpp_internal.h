@@ -78,6 +78,9 @@ struct KernelArgs {
     int B, Hq, Hkv, G, D;
     int Tq;                       // query tokens per sequence (the last Tq positions, causal)
     int R;                        // query rows per kv head and sequence: Tq * G
+    // Tensor kernel: the R rows of a kv head are cut into NRG groups of up to Rg = min(R, 8)
+    // rows; each (kv head, group) is a virtual head of the plan, Hv = Hkv * NRG of them.
+    int NRG, Rg, Hv;
     int max_seq_len, block_size, max_blocks, num_blocks;
     int split_req, max_splits, num_sms;
     float scale, phi, lo, hi;
@@ -88,9 +91,10 @@ struct KernelArgs {
     int pf_tiles;                 // tensor kernel: L2 prefetch distance in tiles (0 = off)
 };
 
-// Query rows per kv head (R = Tq * G) each kernel handles: the tensor kernel's 8 columns of one
-// m16n8k16 tile, the SIMT kernel's 16 register rows.
+// Query rows per kv head (R = Tq * G): the tensor kernel takes 8 rows per unit (the columns of one
+// m16n8k16 tile) and up to TC_MAX_ROWS in groups of 8; the SIMT kernel holds 16 register rows.
 constexpr int TC_MAX_GROUP = 8;
+constexpr int TC_MAX_ROWS = 64;
 constexpr int SIMT_MAX_GROUP = 16;
 
 // Launchers (each returns the launch status). `grid` is the persistent CTA count. Either split

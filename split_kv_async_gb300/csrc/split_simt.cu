@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) split_simt_kernel(KernelArgs a)
 
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
         int b, g, j, L;
-        cur.seek(a, S, u, b, g, j, L);
+        cur.seek(a, a.Hkv, S, u, b, g, j, L);
         const int t0 = j * S, t1 = min(t0 + S, L);
 
         // the unit's R = Tq G query rows: row h is head g G + h % G of query token h / G
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) score_range_kernel(KernelArgs a)
     bool bad_block = false;
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
         int b, g, j, L;
-        cur.seek(a, S, u, b, g, j, L);
+        cur.seek(a, a.Hkv, S, u, b, g, j, L);
         const int t0 = j * S, t1 = min(t0 + S, L);
         float qr[GM][E];
         int lim[GM];

@@ -122,6 +122,9 @@ struct NextUnit {
     int valid, b, g, t0, t1, win_base, ent;
 };
 
+// RG: row-group build (R > 8 rows per kv head): each unit head is a virtual head g = kvh NRG +
+// group. Other builds fold heads() to Hkv and kv_head(g) to g.
+template <bool RG>
 struct Producer {
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
@@ -137,6 +140,9 @@ struct Producer {
     uint32_t stage = 0, phase = 0, qiter = 0;
     int hint_n = 0;            // tiles recorded in this CTA's start-up hint
     bool bad_block = false;
+
+    __device__ __forceinline__ int heads() const { if constexpr (RG) return a->Hv; else return a->Hkv; }
+    __device__ __forceinline__ int kv_head(int g) const { if constexpr (RG) return g / a->NRG; else return g; }
 
     // Split plan: S, the n_b and tile prefixes in smem (or a global walk for large batches),
     // the unit count; T = 64-token tiles of all units.
@@ -193,12 +199,14 @@ struct Producer {
             if (blockIdx.x == 0) A.tstart[A.B] = (int)trun;
         }
         __syncwarp();
-        T = trun * A.Hkv;
-        const int n_units = run * A.Hkv;
+        // units and tiles over the virtual heads (kv head, row group); the diag reports the
+        // (b, g, j) units
+        T = trun * heads();
+        const int n_units = run * heads();
         if (blockIdx.x == 0) {
             if (lane == 0) {
                 A.hdr[HDR_SPLIT] = S;
-                A.hdr[HDR_UNITS] = n_units;
+                A.hdr[HDR_UNITS] = run * A.Hkv;
                 A.hdr[HDR_KERNEL] = A.kernel_id;
                 A.hdr[HDR_BATCH] = A.B;
                 A.hdr[HDR_MAXSPLITS] = A.max_splits;
@@ -231,7 +239,7 @@ struct Producer {
         if (!PAGED) {
             if (lane < PER_BLK) {
                 const int hv = lane >> 1;
-                tma_prefetch_3d((lane & 1) ? tmV : tmK, g * D + hv * 64, tt, b);
+                tma_prefetch_3d((lane & 1) ? tmV : tmK, kv_head(g) * D + hv * 64, tt, b);
             }
         } else {
             const int bs = A.block_size;
@@ -241,7 +249,8 @@ struct Producer {
             const int k = min(lane / PER_BLK, TILE / 16 - 1), r = lane % PER_BLK, hv = r >> 1;
             const int e = __shfl_sync(0xffffffffu, ent, min(lb0 + k - win_base, 31));
             if (lane < nbk * PER_BLK && e >= 0 && e < A.num_blocks)
-                tma_prefetch_3d((r & 1) ? tmV : tmK, g * D + hv * 64, (bs <= TILE) ? 0 : (tt % bs), e);
+                tma_prefetch_3d((r & 1) ? tmV : tmK, kv_head(g) * D + hv * 64,
+                                (bs <= TILE) ? 0 : (tt % bs), e);
         }
     }
 
@@ -270,19 +279,36 @@ struct Producer {
             if (kind == KIND_END) {
                 mbar_arrive(rg.qfull + 8 * qs);
             } else {
-                // the unit's R = Tq G query rows: row i G + hh is head g G + hh of query token i
-                const uint32_t bytes = (uint32_t)(A.G * D * 2);
-                mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes * (uint32_t)A.Tq);
-                for (int i = 0; i < A.Tq; ++i) {
-                    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(A.q) +
-                        (((long long)b * A.Tq + i) * A.Hq + (long long)g * A.G) * D;
-                    bulk_load(slot + QHDR_BYTES + i * bytes, src, bytes, rg.qfull + 8 * qs);
+                // The unit's query rows: row rr of the kv head's R = Tq G rows is head
+                // kvh G + rr % G of query token rr / G. Virtual head g = kvh NRG + group takes
+                // rows group * 8 .. (up to Rg of them).
+                const int kvh = kv_head(g);
+                const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(A.q);
+                if constexpr (!RG) {
+                    const uint32_t bytes = (uint32_t)(A.G * D * 2);
+                    mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes * (uint32_t)A.Tq);
+                    for (int i = 0; i < A.Tq; ++i)
+                        bulk_load(slot + QHDR_BYTES + i * bytes,
+                                  q + (((long long)b * A.Tq + i) * A.Hq + (long long)kvh * A.G) * D, bytes,
+                                  rg.qfull + 8 * qs);
+                } else {
+                    const int rbase = (g - kvh * A.NRG) * TC_MAX_GROUP;
+                    const int nrow = min(A.Rg, A.R - rbase);
+                    const uint32_t bytes = (uint32_t)(D * 2);
+                    mbar_arrive_expect_tx(rg.qfull + 8 * qs, bytes * (uint32_t)nrow);
+                    for (int rr = 0; rr < nrow; ++rr) {
+                        const int row = rbase + rr, i = row / A.G;
+                        bulk_load(slot + QHDR_BYTES + rr * bytes,
+                                  q + (((long long)b * A.Tq + i) * A.Hq + (long long)kvh * A.G + (row - i * A.G)) * D,
+                                  bytes, rg.qfull + 8 * qs);
+                    }
                 }
             }
         }
         ++qiter;
         if (kind == KIND_END) return true;
 
+        const int gk = kv_head(g);
         const int bs = PAGED ? A.block_size : TILE;
         const int rows_box = bs < TILE ? bs : TILE;
         const uint32_t box_bytes = 128u * (uint32_t)rows_box;
@@ -313,12 +339,12 @@ struct Producer {
                 if (lane < PER_BLK) {
                     const int hv = lane >> 1;
                     tma_load_3d(((lane & 1) ? vdst : kdst) + hv * TILE * 128, (lane & 1) ? tmV : tmK,
-                                g * D + hv * 64, tt, b, fb);
+                                gk * D + hv * 64, tt, b, fb);
                 }
                 // the first tiles of this call are the next call's start-up hint
                 if (lane == 0 && hint_n < HINT_TILES && kind != KIND_REDO && blockIdx.x < TC_MAX_PARTS) {
                     int* h = A.hint + (long long)blockIdx.x * HINT_WORDS;
-                    h[1 + 3 * hint_n] = g * D;
+                    h[1 + 3 * hint_n] = gk * D;
                     h[2 + 3 * hint_n] = tt;
                     h[3 + 3 * hint_n] = b;
                     h[0] = ++hint_n;
@@ -348,7 +374,7 @@ struct Producer {
                 if (lane < nbk * PER_BLK && e >= 0 && e < A.num_blocks) {
                     const int y = (bs <= TILE) ? 0 : (tt % bs);
                     const uint32_t off = hv * TILE * 128 + k * rows_box * 128;
-                    tma_load_3d(((r & 1) ? vdst : kdst) + off, (r & 1) ? tmV : tmK, g * D + hv * 64, y,
+                    tma_load_3d(((r & 1) ? vdst : kdst) + off, (r & 1) ? tmV : tmK, gk * D + hv * 64, y,
                                 e, fb);
                 }
             }
@@ -395,9 +421,9 @@ struct Producer {
         struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
         int cb = 0;
         auto seg_at = [&](long long t, Seg& s) {
-            while ((long long)A.Hkv * tplan[cb + 1] <= t) ++cb;
+            while ((long long)heads() * tplan[cb + 1] <= t) ++cb;
             const int ntb = tplan[cb + 1] - tplan[cb];
-            const int r = (int)(t - (long long)A.Hkv * tplan[cb]);
+            const int r = (int)(t - (long long)heads() * tplan[cb]);
             s.b = cb;
             s.g = r / ntb;
             const int k = r - s.g * ntb;             // tile of sequence cb, head s.g
@@ -460,7 +486,7 @@ struct Producer {
         cur.reset();
         for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
             int b, g, j, L;
-            cur.seek(A, S, u, b, g, j, L);
+            cur.seek(A, heads(), S, u, b, g, j, L);
             const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
             if (kind == KIND_LAST_OWN) grid_launch_dependents();
             const int t0 = j * S, t1 = min(t0 + S, L);
@@ -553,9 +579,12 @@ struct Producer {
                 const int L = clamp_len(A.seq_lens[rb], A.max_seq_len);
                 // flag bytes of the segment's G heads (written by the pushing CTA before its push)
                 int hw[3] = {0, 0, 0};
-                if (lane < A.R) {
-                    const unsigned f = dest < 0 ? __ldcg(A.flags + unit_row_slot(A, rb, rg_, lane, rj))
-                                                : __ldcg(A.xf + (long long)dest * A.R + lane);
+                const int rkvh = kv_head(rg_);
+                const int rrow = RG ? (rg_ - rkvh * A.NRG) * TC_MAX_GROUP + lane : lane;
+                const int rows = RG ? A.Rg : A.R;        // rows of a unit (extra-slot stride)
+                if (lane < rows && rrow < A.R) {
+                    const unsigned f = dest < 0 ? __ldcg(A.flags + unit_row_slot(A, rb, rkvh, rrow, rj))
+                                                : __ldcg(A.xf + (long long)dest * rows + lane);
                     const unsigned sh = (unsigned)(lane & 3) * 8u;
                     const unsigned w0 = lane < 4 ? (f << sh) : 0u;
                     const unsigned w1 = lane >= 4 ? (f << sh) : 0u;
@@ -579,7 +608,7 @@ struct Producer {
 // ------------------------------------------------------------------------------------------
 // consumer warps
 // ------------------------------------------------------------------------------------------
-template <int D, bool MQ>
+template <int D, bool MQ, bool RG>
 __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay, uint8_t* sm,
                                         uint32_t sbase, const Ring& rg, volatile int* misc)
 {
@@ -596,7 +625,6 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const int r = lane >> 2, qd = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;      // ldmatrix: matrix and row of this lane
     const bool pack_lo = a.R <= 4;
-    const bool q_ok = r < a.R;                    // this lane supplies Q row r
     const uint32_t k_row = warp * TPW + (mi & 1) * 8 + r8;
     const uint32_t v_row = warp * TPW + (mi >> 1) * 8 + r8;
     const int tok_r = warp * TPW + r;             // this lane's tokens: tok_r and tok_r + 8
@@ -618,6 +646,14 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
         const bool redo = kind == KIND_REDO;
         const bool online = redo || (a.mode == FDPP_MODE_FORCE_ONLINE);
+        // RG builds: virtual head g = kv head kvh, row group of rows rbase .. rbase + nrow() - 1
+        // of the kv head (rows() = the unit's row stride in the extra slots); else g is the kv
+        // head. Both are read at each use: a kernel parameter holds no register between uses.
+        const int kvh = RG ? g / a.NRG : g;
+        const int rbase = RG ? (g - kvh * a.NRG) * TC_MAX_GROUP : 0;
+        auto nrow = [&]() { return RG ? min(a.Rg, a.R - rbase) : a.R; };
+        auto rows = [&]() { return RG ? a.Rg : a.R; };
+        const bool q_ok = r < nrow();              // this lane supplies Q row r of the group
 
         uint32_t qb[KS][2];                        // B operand of S^T: Q^T, column r = head r
         {
@@ -636,17 +672,18 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float lsum[2] = {0.f, 0.f};
-        // this lane's two query rows head0, head0 + 1: row rr is head g G + rr % G of query token
-        // rr / G, which sees the keys t < L - Tq + 1 + rr / G
-        const bool hv[2] = {head0 < a.R, head0 + 1 < a.R};
-        const float phv[2] = {hv[0] ? phi_of(a, g * a.G + head0 % a.G) : a.phi,
-                              hv[1] ? phi_of(a, g * a.G + (head0 + 1) % a.G) : a.phi};
+        // this lane's two query rows head0, head0 + 1 of the group: kv-head row rr = rbase + head0
+        // (+ 1) is head kvh G + rr % G of query token rr / G, which sees the keys
+        // t < L - Tq + 1 + rr / G
+        const bool hv[2] = {head0 < nrow(), head0 + 1 < nrow()};
+        const float phv[2] = {hv[0] ? phi_of(a, kvh * a.G + (rbase + head0) % a.G) : a.phi,
+                              hv[1] ? phi_of(a, kvh * a.G + (rbase + head0 + 1) % a.G) : a.phi};
         // several query tokens: keys of the segment each row sees, counted from t0 (none for a
         // lane without a row); one query token sees every key of the segment
         int kseg[2] = {0, 0};
         if constexpr (MQ) {
-            kseg[0] = hv[0] ? key_limit(a, seq_len, head0 / a.G) - t0 : 0;
-            kseg[1] = hv[1] ? key_limit(a, seq_len, (head0 + 1) / a.G) - t0 : 0;
+            kseg[0] = hv[0] ? key_limit(a, seq_len, (rbase + head0) / a.G) - t0 : 0;
+            kseg[1] = hv[1] ? key_limit(a, seq_len, (rbase + head0 + 1) / a.G) - t0 : 0;
         }
         float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
@@ -865,7 +902,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             const int hh = lane;
             unsigned f = 0u;
             float M = 0.f, lam = 0.f;
-            if (hh < a.R) {
+            if (hh < nrow()) {
 #pragma unroll
                 for (int w = 0; w < NCW; ++w) f |= xf_s[w * TC_MAX_GROUP + hh];
                 M = xm_s[hh];
@@ -876,11 +913,11 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     lam = online ? fmaf(frame_weight(xm_s[w * TC_MAX_GROUP + hh], M), xl_s[w * TC_MAX_GROUP + hh], lam)
                                  : lam + xl_s[w * TC_MAX_GROUP + hh];
             }
-            unit_out = __ballot_sync(0xffffffffu, hh < a.R && (f & FDPP_FLAG_OUT));
-            if (hh < a.R && ((write_mask >> hh) & 1u)) {
-                const long long r = dest >= 0 ? (long long)dest * a.R + hh
-                                    : MQ ? unit_row_slot(a, b, g, hh, j)
-                                         : ((long long)b * a.Hq + g * a.G + hh) * a.max_splits + j;
+            unit_out = __ballot_sync(0xffffffffu, hh < nrow() && (f & FDPP_FLAG_OUT));
+            if (hh < nrow() && ((write_mask >> hh) & 1u)) {
+                const long long r = dest >= 0 ? (long long)dest * rows() + hh
+                                    : MQ ? unit_row_slot(a, b, kvh, rbase + hh, j)
+                                         : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j;
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
                 uint8_t* fp = dest < 0 ? a.flags : a.xf;
@@ -901,9 +938,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         for (int c = 0; c < 2; ++c) {
             const int hh = head0 + c;
             if (!hv[c] || !((write_mask >> hh) & 1u)) continue;
-            orow[c] = dest >= 0 ? a.xo + ((long long)dest * a.R + hh) * D
-                                : a.o_part + (MQ ? unit_row_slot(a, b, g, hh, j)
-                                                 : ((long long)b * a.Hq + g * a.G + hh) * a.max_splits + j) * D;
+            orow[c] = dest >= 0 ? a.xo + ((long long)dest * rows() + hh) * D
+                                : a.o_part + (MQ ? unit_row_slot(a, b, kvh, rbase + hh, j)
+                                                 : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j) * D;
         }
         if (!ring_wait(rg.mhand, upar, misc, a)) return;
         {
@@ -946,8 +983,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 // MINB = CTAs per SM the build is register-limited for: 2 caps a thread at 168 registers (two
 // 5-warp CTAs, warps allocated in pairs), 1 leaves the compiler free (~240) and pairs with a
 // deeper TMA ring. MQ: several query tokens per sequence (rows R = Tq G with causal key limits);
-// the one-token build keeps the plain row addressing.
-template <int D, bool PAGED, int MINB, bool MQ>
+// the one-token build keeps the plain row addressing. RG (with MQ): more than 8 rows per kv head,
+// taken as row groups of 8 by virtual heads.
+template <int D, bool PAGED, int MINB, bool MQ, bool RG>
 __global__ void __launch_bounds__(NTHREADS, MINB)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const KernelArgs a)
@@ -955,7 +993,7 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    const TcLayout lay(D, a.R, a.nstage, a.B);
+    const TcLayout lay(D, RG ? a.Rg : a.R, a.nstage, a.B);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* misc = reinterpret_cast<volatile int*>(sm + lay.misc);   // [0] abort, [1] last
     Ring rg;
@@ -1010,16 +1048,16 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     grid_dependency_wait();
 
     int* plan = reinterpret_cast<int*>(sm + lay.plan);
-    Producer pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1)};
+    Producer<RG> pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1)};
     if (warp == NCW) {
         if (lane == 0) {
             prefetch_tensormap(&tmK);
             prefetch_tensormap(&tmV);
         }
-        pr.run<D, PAGED>();
+        pr.template run<D, PAGED>();
         if (pr.bad_block && lane == 0) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
     } else {
-        consume<D, MQ>(a, lay, sm, sbase, rg, misc);
+        consume<D, MQ, RG>(a, lay, sm, sbase, rg, misc);
     }
     __syncthreads();
     if (warp == NCW && lane == 0) {
@@ -1046,9 +1084,12 @@ template <int D, bool PAGED>
 cudaError_t launch_t(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                      int smem, int ctas_per_sm, cudaStream_t s)
 {
-    // several query tokens per sequence take their own build (causal row limits, row addressing)
-    auto kern = a.Tq > 1 ? (ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2, true> : split_tc_kernel<D, PAGED, 1, true>)
-                         : (ctas_per_sm >= 2 ? split_tc_kernel<D, PAGED, 2, false> : split_tc_kernel<D, PAGED, 1, false>);
+    // several query tokens per sequence take their own build (causal row limits, row addressing),
+    // and more than 8 rows per kv head another (row groups)
+    const bool two = ctas_per_sm >= 2;
+    auto kern = a.NRG > 1 ? (two ? split_tc_kernel<D, PAGED, 2, true, true> : split_tc_kernel<D, PAGED, 1, true, true>)
+              : a.Tq > 1  ? (two ? split_tc_kernel<D, PAGED, 2, true, false> : split_tc_kernel<D, PAGED, 1, true, false>)
+                          : (two ? split_tc_kernel<D, PAGED, 2, false, false> : split_tc_kernel<D, PAGED, 1, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // a programmatic dependent of the previous kernel on the stream (the previous call's combine

@@ -114,7 +114,7 @@ def test_bad_params_are_rejected_on_the_host(field, value, status):
 
 
 def test_group_too_large_is_unsupported():
-    p = _gqa_params(num_q_heads=64 * 8, num_kv_heads=8)     # G = 64
+    p = _gqa_params(num_q_heads=128 * 8, num_kv_heads=8)    # G = 128 > 64 query rows per kv head
     n = ctypes.c_size_t(0)
     assert F.lib.fdpp_workspace_size(ctypes.byref(p), ctypes.byref(n)) == F.FDPP_ERR_UNSUPPORTED
 
@@ -159,8 +159,10 @@ def test_paged_contract_errors():
 def test_tensor_kernel_limits():
     fp32 = _gqa_params(dtype=F.FDPP_F32, kernel=F.FDPP_KERNEL_TENSOR)
     assert _call(fp32) == F.FDPP_ERR_UNSUPPORTED
-    big_group = _gqa_params(num_q_heads=128, num_kv_heads=8, kernel=F.FDPP_KERNEL_TENSOR)
-    assert _call(big_group) == F.FDPP_ERR_UNSUPPORTED
+    too_many_rows = _gqa_params(num_q_heads=128, num_kv_heads=1, kernel=F.FDPP_KERNEL_TENSOR)
+    assert _call(too_many_rows, ws_bytes=1 << 30) == F.FDPP_ERR_UNSUPPORTED   # 128 rows > 64
+    simt_rows = _gqa_params(num_q_heads=64, num_kv_heads=2, kernel=F.FDPP_KERNEL_SIMT)
+    assert _call(simt_rows) == F.FDPP_ERR_UNSUPPORTED              # 32 rows > the SIMT kernel's 16
 
 
 def test_status_strings():

@@ -48,6 +48,15 @@ SMALL = {
                     q_tokens=8, split_len=64), [300, 9, 5]),
     "tq2_g8_simt": (_wl(W.GQA, name="tq2_g8", batch=2, num_q_heads=16, num_kv_heads=2, q_tokens=2,
                         split_len=128), [400, 130]),
+    # more than 8 query rows per kv head: the tensor kernel takes them in groups of 8
+    "tq16_g4": (_wl(W.GQA, name="tq16_g4", batch=3, num_q_heads=8, num_kv_heads=2, q_tokens=16,
+                    split_len=256), [900, 300, 40]),
+    "tq3_g4": (_wl(W.GQA, name="tq3_g4", batch=2, num_q_heads=8, num_kv_heads=2, q_tokens=3,
+                   split_len=128), [700, 129]),
+    "g16": (_wl(W.GQA, name="g16", batch=2, num_q_heads=32, num_kv_heads=2, split_len=256),
+            [1000, 333]),
+    "tq8_paged_g2": (_wl(W.PAGED, name="tq8_paged_g2", batch=3, num_q_heads=4, num_kv_heads=2,
+                         q_tokens=8, seq_len_range=(40, 1200), split_len=256), None),
     "tq4_paged": (_wl(W.PAGED, name="tq4_paged", batch=4, num_q_heads=4, num_kv_heads=2,
                       q_tokens=4, seq_len_range=(3, 700), split_len=128), None),
 }
@@ -67,8 +76,9 @@ def _inputs(name, poison=False):
 
 
 def _kernels(inp):
-    ks = [F.FDPP_KERNEL_SIMT]
-    if inp.wl.dtype == W.BF16 and inp.wl.group * inp.wl.q_tokens <= 8:
+    R = inp.wl.group * max(1, inp.wl.q_tokens)
+    ks = [F.FDPP_KERNEL_SIMT] if R <= 16 else []
+    if inp.wl.dtype == W.BF16 and R <= 64:
         ks.insert(0, F.FDPP_KERNEL_TENSOR)
     return ks
 
@@ -191,6 +201,22 @@ def test_fallback_decisions_and_results(kernel):
     np.testing.assert_array_equal((flags & F.FDPP_FLAG_RECOMPUTED) != 0, hot_rows)
     assert diag["n_flagged_row_splits"] == hot_rows.sum()
     H.assert_parity(got, ref, f"stress {kernel}")
+
+
+def test_fallback_with_row_groups():
+    """Four query tokens of four heads per kv head: 16 rows, two row groups of the tensor kernel.
+    Hot keys send segments of either group to the fallback lists; decisions and results as for
+    one group."""
+    inp, oflags = _stress_inputs(batch=4, seq_len=1024, split_len=256, frac=0.1, num_q_heads=16,
+                                 num_kv_heads=4, q_tokens=4)
+    dinp = H.DeviceInputs(inp)
+    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    np.testing.assert_array_equal(flags & 0x0F, oflags)
+    hot_rows = (oflags & oracle.FLAG_OUT) != 0
+    assert hot_rows.sum() >= len(inp.hot)
+    np.testing.assert_array_equal((flags & F.FDPP_FLAG_RECOMPUTED) != 0, hot_rows)
+    assert diag["error_bits"] == 0
+    H.assert_parity(got, H.oracle_out(inp), "stress, row groups")
 
 
 def _check_fallback(inp, oflags, what):

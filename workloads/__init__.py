@@ -98,7 +98,11 @@ SHIFTED = Workload("gqa_head_levels", 8, 32, 8, 128, BF16, split_len=512, seq_le
 # positions, causal), 8 query rows per kv head.
 SPEC = Workload("spec_decode_tq2", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=2,
                 seed=0x5EED0006)
-ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED, SPEC)}
+# A 16-token prefill chunk against gqa_decode's caches: 64 query rows per kv head, which the
+# tensor kernel takes in 8 groups of 8.
+CHUNK = Workload("prefill_chunk_tq16", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=16,
+                 seed=0x5EED0007)
+ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED, SPEC, CHUNK)}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -243,7 +247,6 @@ def generate(wl: Workload, *, seq_lens: Optional[np.ndarray] = None, poison_tail
         _shift_scores(wl, q, k)
     hot = []
     if wl.stress_frac > 0:
-        assert Tq == 1, "hot keys are placed for one query token per sequence"
         hot = _inject_hot_keys(wl, sl, q, k, table)
     return Inputs(wl, sl, q, k, v, table, Lmax, mbps, nblk_total, hot)
 
@@ -285,7 +288,8 @@ def _inject_hot_keys(wl, sl, q, k, table):
         t0, t1 = j * S, min((j + 1) * S, int(sl[b]))
         t = int(rng.integers(t0, t1))
         h0 = g * G
-        qv = q[b, h0].astype(np.float32) if wl.dtype == F32 else bf16_bits_to_f32(q[b, h0])
+        qrow = q[b, h0] if q.ndim == 3 else q[b, 0, h0]     # several query tokens: the first
+        qv = qrow.astype(np.float32) if wl.dtype == F32 else bf16_bits_to_f32(qrow)
         kv = (np.float32(12.0) * qv / np.float32(np.linalg.norm(qv))
               * np.float32(math.sqrt(d))).astype(np.float32)
         row = kv if wl.dtype == F32 else f32_to_bf16_bits(kv)
