@@ -116,8 +116,11 @@ typedef struct fdpp_params {
                                 sequence's last Tq positions, whose keys are already in the cache,
                                 so query token i sees the keys t < L_b - Tq + 1 + i (a short
                                 prefill chunk or a speculative-decoding step). q and out are then
-                                [B][Tq][Hq][d]. Query rows per kv head, Tq * Hq / Hkv: at most 8
-                                for the tensor kernel, 16 for the SIMT kernel. */
+                                [B][Tq][Hq][d]. Query rows per kv head, R = Tq * Hq / Hkv: at
+                                most 64 for the tensor kernel (more than 8 go in groups of 8,
+                                each streaming the kv head's K/V; the groups' reads of a tile
+                                mostly meet in L2), at most 16 for the SIMT kernel and for
+                                fdpp_score_ranges; more is FDPP_ERR_UNSUPPORTED. */
 } fdpp_params;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over
@@ -150,7 +153,7 @@ int fdpp_max_splits(const fdpp_params* p);
 /* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
  * holds the split plan, the per-split partials (o: fp32 [B][Tq][Hq][max_splits][d]; l, m: fp32
  * [B][Tq][Hq][max_splits]), the flag bytes [B][Tq][Hq][max_splits], FDPP_TC_MAX_PARTS extra
- * slots of Tq * Hq / Hkv rows each (o, l, m and flags, like a split's), the fallback lists and a
+ * slots of min(Tq * Hq / Hkv, 8) rows each (o, l, m and flags, like a split's), the fallback lists and a
  * small header. */
 fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
 

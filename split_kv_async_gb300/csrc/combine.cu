@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
     const int rr8 = rr - grp * TC_MAX_GROUP;
     const int n = live ? a.nsplit[b] : 0;
 
-    // Parts that may start inside this row's units: the row's kv head owns tiles [W, W + nt).
+    // Parts that may start inside this row's units: the row's kv head (and row group) owns tiles
+    // [W, W + nt). The split kernel orders its tiles (row group, b, kv head, j).
     const int P = a.hdr[HDR_PARTS];
     long long W = 0, tiles = 1;
     int nt = 0, TS = 1, c_lo = 0, c_hi = -1;
@@ -85,7 +86,8 @@ __global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(Kern
         tiles = a.hdr[HDR_TILES];
         TS = (a.hdr[HDR_SPLIT] + 63) / 64;
         nt = a.tstart[b + 1] - a.tstart[b];
-        W = (long long)a.Hv * a.tstart[b] + (long long)((h / a.G) * a.NRG + grp) * nt;
+        W = (long long)grp * a.Hkv * a.tstart[a.B] + (long long)a.Hkv * a.tstart[b] +
+            (long long)(h / a.G) * nt;
         c_lo = (int)(((W + 1) * P + tiles - 1) / tiles);   // first part starting after tile W
         c_hi = (int)(((W + nt) * P - 1) / tiles);           // last part starting before W + nt
     }

@@ -78,9 +78,6 @@ struct KernelArgs {
     int B, Hq, Hkv, G, D;
     int Tq;                       // query tokens per sequence (the last Tq positions, causal)
     int R;                        // query rows per kv head and sequence: Tq * G
-    // Tensor kernel: the R rows of a kv head are cut into NRG groups of up to Rg = min(R, 8)
-    // rows; each (kv head, group) is a virtual head of the plan, Hv = Hkv * NRG of them.
-    int NRG, Rg, Hv;
     int max_seq_len, block_size, max_blocks, num_blocks;
     int split_req, max_splits, num_sms;
     float scale, phi, lo, hi;
@@ -89,6 +86,11 @@ struct KernelArgs {
     int kernel_id;
     int nstage;                   // tensor kernel: TMA ring depth
     int pf_tiles;                 // tensor kernel: L2 prefetch distance in tiles (0 = off)
+    // Tensor kernel: the R rows of a kv head are cut into NRG groups of up to Rg = min(R, 8)
+    // rows; each (kv head, group) is a virtual head of the plan, Hv = Hkv * NRG of them. (Kept
+    // last: fields added in the middle move the others' parameter offsets and change the
+    // kernels' code.)
+    int NRG, Rg, Hv;
 };
 
 // Query rows per kv head (R = Tq * G): the tensor kernel takes 8 rows per unit (the columns of one

@@ -39,7 +39,10 @@
 // a programmatic dependent too: before it waits for the previous kernel, each CTA prefetches
 // into L2 the tiles it streamed first in the previous call (a hint kept in the workspace).
 // Several query tokens per sequence (MQ builds): R = Tq G query rows per kv head, each with its
-// causal key limit.
+// causal key limit. More than 8 rows (RG builds, a prefill chunk): the rows are cut into groups
+// of 8, each (kv head, group) a virtual head with its own units, and the tiles are ordered
+// group-major so that the groups' reads of one K/V tile fall at about the same time and all but
+// the first hit L2. The one-group builds compile exactly as without row groups.
 // Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT and the CTA stops.
 // (A fused last-arriver combine was measured here and removed: under full HBM load its
 // latency-bound reads of the partials stalled the consumer warps for several microseconds per
@@ -406,6 +409,9 @@ struct Producer {
     // equal parts and CTA c streams part c, [c T / P, (c + 1) T / P). A part that starts inside
     // a unit writes that unit's partial of its tiles to extra slot c; every other segment
     // writes the split's own slot.
+    // RG builds order the tiles group-major, (row group, b, kv head, j): the groups' ranges
+    // have the same shape, so parts c, c + P / NRG, ... read the same K/V tiles at about the
+    // same time and all but the first find them in L2.
     template <int D, bool PAGED>
     __device__ __forceinline__ bool run_parts(long long T, int P, bool& had_own)
     {
@@ -419,14 +425,23 @@ struct Producer {
         const long long te = (long long)(c + 1) * q + ((c + 1) * r) / P;
         const int zero3[3] = {0, 0, 0};
         struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
-        int cb = 0;
+        int cb = 0, cgrp = 0;
         auto seg_at = [&](long long t, Seg& s) {
-            while ((long long)heads() * tplan[cb + 1] <= t) ++cb;
+            long long tg = t;                        // tile index within the row group
+            int grp = 0;
+            if constexpr (RG) {
+                const long long TG = (long long)A.Hkv * tplan[A.B];
+                grp = (int)(t / TG);
+                tg = t - grp * TG;
+                if (grp != cgrp) { cgrp = grp; cb = 0; }
+            }
+            while ((long long)A.Hkv * tplan[cb + 1] <= tg) ++cb;
             const int ntb = tplan[cb + 1] - tplan[cb];
-            const int r = (int)(t - (long long)heads() * tplan[cb]);
+            const int r = (int)(tg - (long long)A.Hkv * tplan[cb]);
             s.b = cb;
-            s.g = r / ntb;
-            const int k = r - s.g * ntb;             // tile of sequence cb, head s.g
+            const int kvh = r / ntb;
+            s.g = RG ? kvh * A.NRG + grp : kvh;
+            const int k = r - kvh * ntb;             // tile of sequence cb, kv head kvh
             s.j = k / TS;
             const int ilo = k - s.j * TS;
             s.L = lplan[cb];
