@@ -1,5 +1,6 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (default
-kernel choice and pipeline geometry), including two query tokens per sequence (spec_decode_tq2):
+kernel choice and pipeline geometry), including two query tokens per sequence (spec_decode_tq2)
+and a 16-token prefill chunk (prefill_chunk_tq16: 64 rows per kv head, eight row groups):
   * sampled output rows against the fp64 oracle (computed one row at a time);
   * every output finite; the split plan equal to the oracle's scheduler;
   * window decisions: none for the N(0,1) workloads; for the fallback-stress workload every
@@ -29,7 +30,8 @@ def _sample_rows(inp, n, seed):
     return rows
 
 
-@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS, W.SPEC], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS, W.SPEC, W.CHUNK],
+                         ids=lambda w: w.name)
 def test_full_size(wl):
     import split_kv_async_gb300 as F
     inp = W.generate(wl)

@@ -252,6 +252,16 @@ def test_batch_beyond_the_shared_memory_plan():
     assert diag["n_units"] == 1100 * 2 * 2
 
 
+def test_batch_beyond_the_shared_memory_plan_with_row_groups():
+    """The whole-unit path with row groups: five query tokens of four heads per kv head are 20
+    rows, three groups of 8, 8 and 4. Units are dealt out per (sequence, row group, split); the
+    reported unit count stays per kv head."""
+    inp, oflags = _stress_inputs(batch=1100, seq_len=256, split_len=128, frac=0.01,
+                                 num_q_heads=8, num_kv_heads=2, head_dim=64, q_tokens=5)
+    diag = _check_fallback(inp, oflags, "batch 1100, row groups")
+    assert diag["n_units"] == 1100 * 2 * 2
+
+
 def test_many_rows_share_combine_blocks():
     """735 softmax rows: the combine gives a row fewer than 8 warps when the rows would not fit
     on the GPU at once, and packs several rows into one block (the last block has a row to
