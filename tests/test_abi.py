@@ -83,6 +83,25 @@ def test_max_splits_and_workspace_size():
     assert F.fdpp_max_splits(p1) == 5
 
 
+def test_workspace_size_with_row_groups():
+    # 16 query tokens of 4 heads per kv head: R = 64 rows, 8 row groups of the tensor kernel.
+    # Partials per (query row, split); a part's extra slot holds one segment, so one group's 8
+    # rows; the fallback lists hold an entry per (sequence, kv head, row group, split) and per part
+    p = _gqa_params(q_tokens=16)
+    ws = F.fdpp_workspace_size(p)
+    slots = 8 * 16 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 8
+    lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
+    assert fixed <= ws <= fixed + 64 * 1024
+    # 12 rows: two groups (8 + 4); extra slots still 8 rows, lists twice the one-group count
+    p12 = _gqa_params(q_tokens=3)
+    ws12 = F.fdpp_workspace_size(p12)
+    slots = 8 * 3 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 8
+    lists = 8 * (8 * 8 * 2 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
+    assert fixed <= ws12 <= fixed + 64 * 1024
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("batch", 0, F.FDPP_ERR_INVALID_ARG),
     ("num_q_heads", 30, F.FDPP_ERR_INVALID_ARG),        # not a multiple of 8 kv heads
