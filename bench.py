@@ -4,9 +4,10 @@ test, fallback recompute, combine) through libfdpp's C ABI on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl fdpp|reference]
 
-Prints ONE JSON line (rank 0). The default workload is GQA decode: batch 8, 32 query / 8 kv heads,
-head_dim 128, 4096 tokens each, bf16, split 512, phi 0, window [-30, 10]. `--config` names one of
-workloads.ALL.
+Prints ONE JSON line (rank 0). The default workload is the paged continuous batch, the largest
+single-GPU one: batch 64, 64 query / 8 kv heads, head_dim 128, seq_lens uniform in [512, 16384],
+paged bf16 cache (block 16, permuted block table), split 512, phi 0, window [-30, 10]. `--config`
+names one of workloads.ALL (e.g. long_context, gqa_decode, fallback_stress).
 
   value      KV-read GB/s: algorithmic K+V bytes of all ranks' steps (tokens t < L_b only) over the
              max-over-ranks device time of the K timed steps (CUDA events, inputs resident in HBM).
@@ -15,9 +16,12 @@ workloads.ALL.
   e2e        the same metric through the C ABI with HOST buffers: each step copies q, seq_lens
              (and the block table) host->device from pinned memory, runs the step, copies the
              output back and synchronises. The K/V cache is resident device state.
-  roofline   split kernel alone (CUDA events recorded around it by fdpp_decode_attn_timed):
-             algorithmic KV bytes per launch / mean launch time, against the measured HBM copy
-             bandwidth of MEASURED_PEAKS.json.
+  roofline   the split kernel: algorithmic KV bytes per launch over its launch time, against the
+             measured HBM copy bandwidth of MEASURED_PEAKS.json. The launch time is the median of
+             a separate pass after the timed region, CUDA events recorded right around each
+             split kernel by fdpp_decode_attn_timed (>= 50 launches). Such events keep the launch
+             from overlapping the previous kernel, so where that median exceeds the whole step's
+             time (small steps) the step time is used instead, and `kernel_time_from` says so.
   cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the same workload.
 
 With --gpus N > 1 (torchrun) every rank runs its own seeded batch (weak scaling, no collective on
@@ -51,9 +55,11 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="gqa_decode")
+    ap.add_argument("--config", default="paged_batch")
     ap.add_argument("--impl", default="fdpp", choices=["fdpp", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--split-samples", type=int, default=100,
+                    help="launches of the split-kernel timing pass (at least 50)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--kernel", type=int, default=0, help="fdpp_kernel (0 auto, 1 tensor, 2 simt)")
     ap.add_argument("--mode", type=int, default=0, help="fdpp_mode (0 normal, 1 fast, 2 online)")
@@ -62,6 +68,9 @@ def parse_args(argv=None):
     ap.add_argument("--tc-prefetch", type=int, default=0)
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
     ap.add_argument("--split-k", type=int, default=0, help="flat GEMM configs: split_k (0 = auto)")
+    ap.add_argument("--noalloc", action="store_true",
+                    help="time fdpp_decode_attn_noalloc (the library's static scratch) in the "
+                         "timed region instead of fdpp_decode_attn with a workspace")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -71,6 +80,7 @@ def parse_args(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    args.split_samples = max(50, args.split_samples)
     return args
 
 
@@ -410,7 +420,15 @@ def run_fdpp(args, dist: Dist):
                 None if bt is None else bt.data_ptr(), sl.data_ptr(), pp, ws.data_ptr(), ws_bytes,
                 out.data_ptr(), sh) for i in range(R)]
 
+    noalloc = F.lib.fdpp_decode_attn_noalloc
+
     def step(i, eb=None, ee=None):
+        if args.noalloc and eb is None:
+            a_ = argsets[i % R]
+            st = noalloc(a_[0], a_[1], a_[2], a_[3], a_[4], pp, a_[8], sh)
+            if st != 0:
+                raise F.FdppError(st, "fdpp_decode_attn_noalloc", F.fdpp_last_error())
+            return
         st = call(*argsets[i % R], eb, ee)
         if st != 0:
             raise F.FdppError(st, "fdpp_decode_attn_timed", F.fdpp_last_error())
@@ -418,21 +436,10 @@ def run_fdpp(args, dist: Dist):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    diag, _, _ = F.fdpp_read_diag(ws, p)
+    diag, _, _ = F.fdpp_read_diag_noalloc(p) if args.noalloc else F.fdpp_read_diag(ws, p)
     kernel_name = {1: "tensor", 2: "simt"}.get(diag["kernel"], "?")
 
     K = args.steps
-    # The split kernel is timed on every SAMPLE_EVERY-th step of the timed region (events around
-    # it sit between the two kernels of a step and cost that step its launch overlap, so they
-    # are not put on every step). torch creates an event's CUDA handle on its first record:
-    # record each once here so the raw handles handed to fdpp_decode_attn_timed exist.
-    SAMPLE_EVERY = 16
-    n_samp = (K + SAMPLE_EVERY - 1) // SAMPLE_EVERY
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_samp)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_samp)]
-    for ev in ev_b + ev_e:
-        ev.record(stream)
-    torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if dev.index is not None else 0,
@@ -442,25 +449,46 @@ def run_fdpp(args, dist: Dist):
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(K):
-        if i % SAMPLE_EVERY == 0:
-            k = i // SAMPLE_EVERY
-            step(i, ev_b[k].cuda_event, ev_e[k].cuda_event)
-        else:
-            step(i)
+        step(i)
     t_end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
-    split_ms = [ev_b[k].elapsed_time(ev_e[k]) for k in range(n_samp)]
-    diag, _, _ = F.fdpp_read_diag(ws, p)
+    diag, _, _ = F.fdpp_read_diag_noalloc(p) if args.noalloc else F.fdpp_read_diag(ws, p)
+
+    # The split kernel alone, in a pass of its own after the timed region: events right around
+    # it (fdpp_decode_attn_timed) and around the whole call, on every launch. torch creates an
+    # event's CUDA handle on its first record: record each once first so that the raw handles
+    # handed to the C call exist.
+    n_samp = args.split_samples
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_samp)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_samp)]
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_samp)]
+    for ev in ev_b + ev_e + ev_s:
+        ev.record(stream)
+    torch.cuda.synchronize()
+    for k in range(n_samp):
+        step(K + k, ev_b[k].cuda_event, ev_e[k].cuda_event)
+        ev_s[k].record(stream)
+    torch.cuda.synchronize()
+    split_ms = sorted(ev_b[k].elapsed_time(ev_e[k]) for k in range(n_samp))
+    alone_ms = sorted(ev_b[k].elapsed_time(ev_s[k]) for k in range(n_samp))
+
+    def pct(xs, f):
+        return xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
 
     kv_bytes = inp.kv_bytes
     tot_bytes, t_max, value = aggregate(kv_bytes * K, total_ms / 1e3, dist)
     ms_per_step = t_max * 1e3 / K
-    split_mean_ms = sum(split_ms) / n_samp
+    split_med_ms = statistics.median(split_ms)
     peak, peak_kind = measured_peaks()
-    achieved = kv_bytes / (split_mean_ms / 1e3) / 1e9
+    # the kernel cannot take longer than the step it is part of: events around a launch cost it
+    # the overlap with the kernel before it, which matters only for short steps
+    kernel_ms, kernel_from = split_med_ms, "split-kernel events, median of the separate pass"
+    if split_med_ms > total_ms / K:
+        kernel_ms, kernel_from = total_ms / K, "whole step (split-kernel median exceeded it)"
+    achieved = kv_bytes / (kernel_ms / 1e3) / 1e9
 
     # End to end through the C ABI with host buffers: every step sends that step's inputs (q,
     # seq_lens and, paged, the block table), packed in one pinned host buffer, with one
@@ -563,15 +591,24 @@ def run_fdpp(args, dist: Dist):
                    "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
                    "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "
                                 f"4x L2 {l2 / 2**20:.0f} MiB); no flush",
-                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single"},
+                   "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single",
+                   "entry_point": "fdpp_decode_attn_noalloc" if args.noalloc else "fdpp_decode_attn"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": traffic, "kernel": f"split_{kernel_name}",
-                     "split_kernel_us": split_mean_ms * 1e3,
+                     "kernel_us": kernel_ms * 1e3, "kernel_time_from": kernel_from,
+                     "split_kernel_us": {"median": split_med_ms * 1e3, "p10": pct(split_ms, 0.1) * 1e3,
+                                         "p90": pct(split_ms, 0.9) * 1e3},
                      "timed_launches": n_samp},
+        "step_alone_us": {"median": statistics.median(alone_ms) * 1e3,
+                          "p10": pct(alone_ms, 0.1) * 1e3, "p90": pct(alone_ms, 0.9) * 1e3,
+                          "about": "one call with events around it (no overlap with the step "
+                                   "before), same pass as split_kernel_us"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * K,
+        "traffic_note": None if traffic is not None else
+        "no ncu capture at the current kernel sources for this workload",
         "fallback": {"flagged_row_splits": diag["n_flagged_row_splits"],
                      "flagged_units": diag["n_flagged_units"], "units": diag["n_units"],
                      "unit_rate": diag["n_flagged_units"] / max(1, diag["n_units"])},

@@ -202,15 +202,29 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
  * exits. It allocates nothing and frees nothing. Arguments are those of fdpp_decode_attn.
  *   - Problems whose fdpp_workspace_size exceeds FDPP_NOALLOC_WORKSPACE_BYTES are rejected
  *     with FDPP_ERR_WORKSPACE before anything is enqueued (fdpp_last_error() says by how much).
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     on the host; make that first call before any stream capture on that device.
- *   - Each call clears, on `stream`, the part of the array that must start at zero, then runs
- *     the same kernels as fdpp_decode_attn. All calls share the array and it keeps the last
- *     call's contents: calls that overlap on the GPU (unordered streams or threads) race on it
- *     and produce wrong results. Calls ordered on one stream are safe. */
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, on the host). The first call on a device also loads the array
+ *     there, so make that first call before any stream capture on that device.
+ *   - Each call clears, on `stream`, the array's header, split plan and fallback lists, then
+ *     runs the same kernels as fdpp_decode_attn on the same inputs, with the same results bit
+ *     for bit. All calls share the array and it keeps the last call's contents: calls that
+ *     overlap on the GPU (unordered streams or threads) race on it and produce wrong results.
+ *     Calls ordered on one stream are safe, whatever shapes they have.
+ *   - What the last call found on the device (error bits, fallback flags, the split plan) is
+ *     read with fdpp_read_diag_noalloc, after that call's stream has been synchronised; the
+ *     error bits there are that call's alone, not sticky across calls. */
 fdpp_status fdpp_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_table, const int32_t* seq_lens,
                                      const fdpp_params* p, void* out, fdpp_stream stream);
+
+/* fdpp_read_diag for the array behind fdpp_decode_attn_noalloc on the current device: what the
+ * last no-alloc call with parameters `p` left there (synchronous device-to-host copies; call after
+ * that call's stream has been synchronised). Arguments and results as for fdpp_read_diag.
+ * Problems beyond FDPP_NOALLOC_WORKSPACE_BYTES are rejected with FDPP_ERR_WORKSPACE. This reader
+ * has no counterpart in the pages either; it exists so that a caller of the no-alloc step can see
+ * device-side problems (FDPP_ERRBIT_*) and the fallback decisions, as a workspace caller can. */
+fdpp_status fdpp_read_diag_noalloc(const fdpp_params* p, fdpp_diag* diag, uint8_t* flags_host,
+                                   int32_t* nsplit_host);
 
 /* Score range of every row-split, for choosing phi in advance (opt.ai.kr "FlashDecoding++ async
  * softmax -- theory", section 3: phi is set by observing the score distribution beforehand).

@@ -20,7 +20,7 @@
  *   [3dgen]   hwan-h-heo.github.io, "Optimizing sparse 3D generation inference", section 2.2:
  *             softmax rows sum to one, so value rows that are all equal to v0 give v0.
  *
- * Readings where the pages leave a step open (each is also listed in the design notes):
+ * Readings where the pages leave a step open:
  *   R1  The windowed quantity x is the scaled score s = scale * <q, k> (the softmax input of
  *       [theory] s3), in the same units as phi.
  *   R2  A score is in the window iff lo <= s - phi <= hi (closed). The pages name only the

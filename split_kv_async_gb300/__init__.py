@@ -31,7 +31,8 @@ FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 # Names every build of the library exports (the C ABI of include/fdpp.h and include/fdpp_gemm.h).
 EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fdpp_decode_attn",
             "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_score_ranges",
-            "fdpp_pick_phi", "fdpp_read_diag", "fdpp_status_str", "fdpp_last_error",
+            "fdpp_pick_phi", "fdpp_read_diag", "fdpp_read_diag_noalloc", "fdpp_status_str",
+            "fdpp_last_error",
             "fdpp_flat_gemm_split_k", "fdpp_flat_gemm_workspace_size", "fdpp_flat_gemm",
             "fdpp_flat_gemm_set_lut", "fdpp_flat_gemm_read_error")
 FDPP_GEMM_MAX_M = 128
@@ -103,6 +104,8 @@ def _load() -> ctypes.CDLL:
     lib.fdpp_pick_phi.restype = ctypes.c_int
     lib.fdpp_read_diag.argtypes = [vp, ctypes.c_size_t, P, ctypes.POINTER(fdpp_diag), vp, vp]
     lib.fdpp_read_diag.restype = ctypes.c_int
+    lib.fdpp_read_diag_noalloc.argtypes = [P, ctypes.POINTER(fdpp_diag), vp, vp]
+    lib.fdpp_read_diag_noalloc.restype = ctypes.c_int
     lib.fdpp_status_str.argtypes = [ctypes.c_int]
     lib.fdpp_status_str.restype = ctypes.c_char_p
     lib.fdpp_last_error.argtypes = []
@@ -249,6 +252,20 @@ def fdpp_read_diag(workspace, p: fdpp_params, want_flags=False, want_nsplit=Fals
                               ctypes.byref(p), ctypes.byref(d),
                               None if flags is None else flags.ctypes.data,
                               None if ns is None else ns.ctypes.data), "fdpp_read_diag")
+    return d.as_dict(), flags, ns
+
+
+def fdpp_read_diag_noalloc(p: fdpp_params, want_flags=False, want_nsplit=False):
+    """fdpp_read_diag for the no-alloc entry point's static array on the current device."""
+    import numpy as np
+    d = fdpp_diag()
+    ms = fdpp_max_splits(p)
+    flags = np.zeros((p.batch * max(1, p.q_tokens), p.num_q_heads, ms), np.uint8) if want_flags else None
+    ns = np.zeros(p.batch, np.int32) if want_nsplit else None
+    _check(lib.fdpp_read_diag_noalloc(ctypes.byref(p), ctypes.byref(d),
+                                      None if flags is None else flags.ctypes.data,
+                                      None if ns is None else ns.ctypes.data),
+           "fdpp_read_diag_noalloc")
     return d.as_dict(), flags, ns
 
 

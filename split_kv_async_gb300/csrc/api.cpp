@@ -315,6 +315,9 @@ fdpp_status get_tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn)
 // Bytes at the start of a workspace for `p` that hold the state which must be zero before a call:
 // header, plan and the fallback list (everything before the flag bytes).
 size_t workspace_zero_prefix(const fdpp_params& p) { return layout_of(p).flags; }
+// Offset of the start-up hint region: everything before it (header, plan, fallback lists) is
+// the state that a call must find zeroed or written by the call before it.
+size_t workspace_hint_offset(const fdpp_params& p) { return layout_of(p).hint; }
 // Sets the reason fdpp_last_error() reports on this thread.
 void set_last_error(const char* what) { g_last_error = what; }
 }  // namespace fdpp

@@ -116,6 +116,8 @@ fdpp_status get_tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
 
 // Bytes at the front of a workspace for `p` that must be zero when a call starts.
 size_t workspace_zero_prefix(const fdpp_params& p);
+// Offset of the start-up hint region (the zero prefix minus the hint, which may stay stale).
+size_t workspace_hint_offset(const fdpp_params& p);
 // Sets the reason fdpp_last_error() reports on this thread.
 void set_last_error(const char* what);
 

@@ -25,6 +25,17 @@ REL_FLOOR = 1e-3
 BF16_RESOLUTION = 2.0 ** -8
 
 
+def no_fake_pointer_calls_on_a_gpu():
+    """Skips the calling test where a GPU is present. Tests of host-side argument checks pass
+    made-up device addresses that a correct check rejects before any launch; if a check ever
+    regressed on a machine with a GPU, the call would launch a kernel on those addresses. They
+    run only where nothing can be launched."""
+    import pytest
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("passes made-up device pointers: run only without a GPU")
+
+
 def errors(got, ref):
     err = np.abs(got - ref)
     rel = err / np.maximum(np.abs(ref), REL_FLOOR)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import split_kv_async_gb300 as F
+from fdpp_harness import no_fake_pointer_calls_on_a_gpu
 
 INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 HEADER = os.path.join(INCLUDE, "fdpp.h")
@@ -126,6 +127,7 @@ def test_bad_params_are_rejected_on_the_host(field, value, status):
     n = ctypes.c_size_t(0)
     assert F.lib.fdpp_workspace_size(ctypes.byref(p), ctypes.byref(n)) == status
     assert F.fdpp_last_error()
+    no_fake_pointer_calls_on_a_gpu()
     fake = 1 << 20                                          # never dereferenced
     st = F.lib.fdpp_decode_attn(fake, fake, fake, None, fake, ctypes.byref(p), fake * 256,
                                 1 << 30, fake, None)
@@ -140,6 +142,8 @@ def test_group_too_large_is_unsupported():
 
 def _call(p, q=1 << 20, k=1 << 20, v=1 << 20, bt=None, sl=1 << 20, ws=1 << 28, ws_bytes=None,
           out=1 << 20):
+    # made-up device addresses: only where no kernel can be launched on them
+    no_fake_pointer_calls_on_a_gpu()
     if ws_bytes is None:
         ws_bytes = F.fdpp_workspace_size(p)
     return F.lib.fdpp_decode_attn(q, k, v, bt, sl, ctypes.byref(p), ws, ws_bytes, out, None)
@@ -167,12 +171,8 @@ def test_paged_contract_errors():
     assert _call(_gqa_params(**dict(base, num_kv_blocks=0)), bt=bt) == F.FDPP_ERR_INVALID_ARG
     assert _call(_gqa_params(split_len=520, **base), bt=bt) == F.FDPP_ERR_INVALID_ARG
     # The same parameters without a block table are a contiguous cache: the host checks ignore
-    # the block fields. With a GPU present that call would pass the checks and launch on the
-    # fake pointers, so it is made only where there is no device to launch on (it then stops at
-    # the device query).
-    import torch
-    if not torch.cuda.is_available():
-        assert _call(_gqa_params(**dict(base, block_size=24))) == F.FDPP_ERR_CUDA
+    # the block fields, and with no device the call stops at the device query.
+    assert _call(_gqa_params(**dict(base, block_size=24))) == F.FDPP_ERR_CUDA
 
 
 def test_tensor_kernel_limits():
@@ -191,15 +191,13 @@ def test_status_strings():
 
 
 def test_no_gpu_gives_cuda_error_not_a_crash():
-    import torch
-    if torch.cuda.is_available():
-        pytest.skip("a GPU is present")
     assert _call(_gqa_params()) == F.FDPP_ERR_CUDA
 
 
 # ---- flat GEMM: argument errors before any CUDA call ----------------------------------------
 
 def _gemm_status(x=16, w=16, y=16, M=8, N=256, K=512, split_k=0, ws=256, ws_bytes=1 << 20):
+    no_fake_pointer_calls_on_a_gpu()
     return F.lib.fdpp_flat_gemm(x, w, y, M, N, K, split_k, ws, ws_bytes, None)
 
 

@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 import split_kv_async_gb300 as F
+from fdpp_harness import no_fake_pointer_calls_on_a_gpu
 
 
 def _random_ranges(seed, B=5, Hq=6, ms=7):
@@ -66,6 +67,7 @@ def test_calibration_argument_errors():
     assert st == F.FDPP_ERR_INVALID_ARG                 # lo > hi
     p = F.make_params(batch=1, num_q_heads=4, num_kv_heads=1, head_dim=64, dtype=F.FDPP_F32,
                       max_seq_len=256, scale=0.125, split_len=64)
+    no_fake_pointer_calls_on_a_gpu()
     fake = vp(1 << 20)                                  # never dereferenced: rejected first
     st = F.lib.fdpp_score_ranges(None, fake, None, fake, ctypes.byref(p), fake, 1 << 30,
                                  buf.ctypes.data, buf.ctypes.data, None, None)

@@ -9,7 +9,7 @@ section 1: one query token per sequence against a long K/V cache. The shapes bel
 decode workloads this library is measured on (tiny MHA, GQA decode, long context, paged
 continuous batch, fallback stress).
 
-Recipe (the design notes repeat it):
+Recipe:
   * every array has its own numpy ``Generator(PCG64)`` seeded with ``[seed, stream_id]``, so
     changing one array's size does not shift another array's draws;
   * values are float32 standard normals; bf16 inputs are the float32 draws rounded to nearest
