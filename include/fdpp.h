@@ -75,7 +75,9 @@ enum {
     FDPP_FLAG_ABOVE = 2,         /* ... above phi + hi (the overflow side) */
     FDPP_FLAG_BELOW = 4,         /* ... below phi + lo */
     FDPP_FLAG_NAN = 8,           /* ... was NaN */
-    FDPP_FLAG_RECOMPUTED = 16    /* the partial of this row-split came from online softmax */
+    FDPP_FLAG_RECOMPUTED = 16,   /* the partial of this row-split came from online softmax */
+    FDPP_FLAG_SLOT = 32          /* tensor kernel: this row-split's own partial slot holds a
+                                    recomputed piece (its run's phi-frame partial left it out) */
 };
 
 /* Sticky device error bits (cleared by fdpp_workspace_init). */
@@ -146,15 +148,17 @@ typedef struct fdpp_diag {
 int fdpp_max_splits(const fdpp_params* p);
 
 /* The tensor kernel cuts the 64-token tiles of all (b, g, j) units into at most this many
- * equal parts, one per CTA, so that every CTA streams the same number of bytes. A part that
- * begins inside a split leaves its share of that split in one extra slot of the workspace. */
+ * equal parts, one per CTA, so that every CTA streams the same number of bytes. A part's share
+ * of one sequence's kv head is a run, which leaves one partial (in the phi frame, summed across
+ * its splits) in a run slot of the workspace; window decisions stay per split. */
 #define FDPP_TC_MAX_PARTS 512
 
 /* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
  * holds the split plan, the per-split partials (o: fp32 [B][Tq][Hq][max_splits][d]; l, m: fp32
- * [B][Tq][Hq][max_splits]), the flag bytes [B][Tq][Hq][max_splits], FDPP_TC_MAX_PARTS extra
- * slots of min(Tq * Hq / Hkv, 8) rows each (o, l, m and flags, like a split's), the fallback lists and a
- * small header. */
+ * [B][Tq][Hq][max_splits]), the flag bytes [B][Tq][Hq][max_splits], the tensor kernel's run
+ * slots (FDPP_TC_MAX_PARTS + B * Hkv * ceil(Tq * Hq / Hkv / 8) of them, min(Tq * Hq / Hkv, 8)
+ * rows each: o, l, m and edge flags, like a split's; a run is one CTA's share of one sequence's
+ * kv head, across split boundaries), the fallback lists and a small header. */
 fdpp_status fdpp_workspace_size(const fdpp_params* p, size_t* bytes);
 
 /* Zeroes a workspace (stream-ordered). Call once after allocating it; it also clears the

@@ -25,6 +25,7 @@ FDPP_F32, FDPP_BF16 = 0, 1
 FDPP_MODE_NORMAL, FDPP_MODE_FORCE_FAST, FDPP_MODE_FORCE_ONLINE = 0, 1, 2
 FDPP_KERNEL_AUTO, FDPP_KERNEL_TENSOR, FDPP_KERNEL_SIMT = 0, 1, 2
 FDPP_FLAG_OUT, FDPP_FLAG_ABOVE, FDPP_FLAG_BELOW, FDPP_FLAG_NAN, FDPP_FLAG_RECOMPUTED = 1, 2, 4, 8, 16
+FDPP_FLAG_SLOT = 32
 FDPP_ERRBIT_SEQ_LEN, FDPP_ERRBIT_BLOCK_TABLE, FDPP_ERRBIT_TIMEOUT = 1, 2, 4
 FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 

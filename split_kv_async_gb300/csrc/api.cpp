@@ -146,9 +146,12 @@ WsLayout layout_of(const fdpp_params& p)
     w.m_part = off;  off = align256(off + slots * 4);
     w.l_part = off;  off = align256(off + slots * 4);
     w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
-    // extra slots of the tensor kernel's parts (one row group, min(R, 8) rows, each)
+    // run slots of the tensor kernel: a run is a part's share of one (row group, sequence, kv
+    // head), so there are fewer than parts + (row groups x sequences x kv heads) of them, each
+    // of min(R, 8) rows
     const size_t R = (size_t)q_tokens_of(p) * (size_t)(p.num_q_heads / p.num_kv_heads);
-    const size_t xrows = (size_t)TC_MAX_PARTS * (R < TC_MAX_GROUP ? R : TC_MAX_GROUP);
+    const size_t runs = (size_t)TC_MAX_PARTS + (size_t)p.batch * p.num_kv_heads * row_groups_of(p);
+    const size_t xrows = runs * (R < TC_MAX_GROUP ? R : TC_MAX_GROUP);
     w.xf = off;      off = align256(off + xrows);
     w.xm = off;      off = align256(off + xrows * 4);
     w.xl = off;      off = align256(off + xrows * 4);
@@ -414,6 +417,7 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     const long long units_max = (long long)p->batch * p->num_kv_heads * w.max_splits;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
+    int split_grid = 0;
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     if (kernel == FDPP_KERNEL_TENSOR) {
@@ -435,17 +439,19 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
         if (grid > TC_MAX_PARTS) grid = TC_MAX_PARTS;
         const long long vunits = units_max * row_groups_of(*p);
         if (p->batch > TC_PLAN_SMEM_MAX_B && grid > vunits) grid = vunits;
+        split_grid = (int)grid;
         e = launch_split_tc(a, tk, tv, (int)grid, plan.smem_bytes, plan.ctas_per_sm, s);
     } else {
         const int occ = split_simt_ctas_per_sm(a, p->dtype);
         long long grid = (long long)dev.sms * (occ > 0 ? occ : 1);
         if (grid > units_max) grid = units_max;
+        split_grid = (int)grid;
         e = launch_split_simt(a, p->dtype, (int)grid, s);
     }
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "split kernel launch: %s", cudaGetErrorString(e));
     if (ev_split_end && (e = cudaEventRecord((cudaEvent_t)ev_split_end, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
-    e = launch_combine(a, p->dtype, s);
+    e = launch_combine(a, p->dtype, split_grid, s);
     if (e != cudaSuccess) return fail(FDPP_ERR_CUDA, "combine kernel launch: %s", cudaGetErrorString(e));
     return FDPP_OK;
 }

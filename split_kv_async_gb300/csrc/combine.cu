@@ -1,4 +1,5 @@
-// combine.cu -- cross-split combine: one CTA (8 warps) per softmax row (sequence b, query head h).
+// combine.cu -- cross-split combine: for every softmax row (sequence b, query head h) the sum of
+// its split partials.
 //
 // opt.ai.kr "FlashDecoding++ async softmax -- theory", s3: with a unified max every split's
 // partial (o_j, l_j) is already in the same frame, so only a plain sum remains. A split that
@@ -7,19 +8,24 @@
 // with w_j = 1 exactly when m_j == M: if no split of the row fell back (all m_j = phi) this is
 // exactly the plain sum.
 //
-// The row's partials (its n_b splits, then its extra slots) are divided into contiguous ranges,
-// one per warp of the row (each lane owns 4 or 2 output columns), read 4 at a time per lane; the
-// warp sums are then added in warp order. A row gets up to 32 warps while the rows fit on the
-// GPU at that width, and fewer when there are many rows, so that all rows are in flight. The
-// order is fixed, so results are deterministic. The result is rounded to nearest even into the
-// output dtype.
+// Entries of a row. A split kernel that cut its work into parts (the tensor kernel, header
+// HDR_PARTS = P > 0) leaves one partial per run: part c's share of one (row group, sequence,
+// kv head) u, in run slot c + u. A run covers whole splits and pieces of splits in the phi frame;
+// its rows whose scores left the window in one of its splits hold an empty partial there, and the
+// fallback rewrote those rows piece by piece: a first piece that starts inside a split into the
+// run slot, every other piece into its split's own slot, marked FDPP_FLAG_SLOT. So the row's
+// entries are its head's run slots (the parts overlapping its tiles) and the own slots of its
+// splits marked FDPP_FLAG_SLOT. A run that starts inside a split also carries that piece's window
+// decisions (edge flags), which are ORed into the split's flag byte. A split kernel without parts
+// (P = 0: the SIMT kernel, and very large batches) leaves one partial per split in its own slot.
 //
-// Extra slots. The tensor kernel cuts the 64-token tiles of all units (order b, g, j) into P
-// equal parts, part c = tiles [floor(c T / P), floor((c + 1) T / P)). A part that starts inside
-// a split (not on its first tile) computed that split's partial over its own tiles only and left
-// it in extra slot c, in the phi frame or, if recomputed, in its own max frame. Partials of
-// disjoint token sets of one split add up like those of different splits, so the combine adds
-// each extra slot in with the same weights, and ORs its flag byte into the split's flag byte.
+// One pass. A warp owns a row (or, with ES warps per row for rows with many runs, a contiguous
+// share of its runs and splits); each lane owns D/32 output columns, and the warp reads up to U
+// entries at a time (each entry's columns in one coalesced load per lane, with its m and l),
+// keeping a running max that is the same in every lane (the sums are rescaled only when the max
+// grows, so phi-frame partials add with weight 1). The flag bytes are scanned 32 at a time. The
+// slices of a row are added in warp order through shared memory. Every order is fixed, so results
+// are deterministic. The result is rounded to nearest even into the output dtype.
 //
 // Launched as a programmatic dependent of the split kernel: it may start while the split kernel
 // finishes, and waits (griddepcontrol.wait) before touching the partials. It lets the kernel
@@ -31,8 +37,8 @@
 namespace fdpp {
 namespace {
 
-constexpr int CW = 8;                 // warps per CTA of the many-rows build
-constexpr int CW_WIDE = 32;           // warps per CTA when a few long rows take 16 or 32 warps each
+constexpr int NWC = 8;                // warps per CTA
+constexpr int U = 8;                  // entries in flight per warp
 
 template <typename T>
 __device__ __forceinline__ void store_out(T* p, float x);
@@ -46,194 +52,219 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* p, float
     *p = __float2bfloat16_rn(x);
 }
 
-template <typename T, int D, int NW>
-__global__ void __launch_bounds__(NW * 32, NW == CW ? 3 : 1) combine_kernel(KernelArgs a, int wpr)
+// Running sums of one warp: acc (this lane's columns) and lam, in the frame of the max mrun.
+template <int E>
+struct Sums {
+    float acc[E];
+    float lam, mrun;
+
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = 0.f;
+        lam = 0.f;
+        mrun = -INFINITY;
+    }
+    __device__ __forceinline__ void add(float mv, float lv, const float (&ov)[E])
+    {
+        if (mv > mrun) {                             // a larger max: earlier sums shrink
+            const float r = mrun == -INFINITY ? 0.f : __expf(mrun - mv);
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] *= r;
+            lam *= r;
+            mrun = mv;
+        }
+        const float w = frame_weight(mv, mrun);
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = fmaf(w, ov[c], acc[c]);
+        lam = fmaf(w, lv, lam);
+    }
+};
+
+template <int E>
+__device__ __forceinline__ void load_cols(const float* oj, float (&ov)[E])
 {
+    if constexpr (E == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(oj));
+        ov[0] = v.x; ov[1] = v.y; ov[2] = v.z; ov[3] = v.w;
+    } else {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(oj));
+        ov[0] = v.x; ov[1] = v.y;
+    }
+}
+
+// ES warps per row, NWC / ES rows per CTA.
+template <typename T, int D, int ES>
+__global__ void __launch_bounds__(NWC * 32) combine_kernel(KernelArgs a)
+{
+    constexpr int RPC = NWC / ES;
     constexpr int E = D / 32;                       // output columns per lane
-    __shared__ float s_acc[NW][D];
-    __shared__ float s_lam[NW];
-    __shared__ float s_max[NW];
+    __shared__ float s_acc[ES > 1 ? NWC : 1][D];
+    __shared__ float s_lam[NWC];
+    __shared__ float s_max[NWC];
     // the next call's split kernel may launch now; it waits for this grid to complete before
     // it touches global memory
     grid_launch_dependents();
     grid_dependency_wait();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rpc = NW / wpr;                       // rows of this CTA, wpr warps each
-    const int rl = warp / wpr, wr = warp - rl * wpr;
-    const int row = blockIdx.x * rpc + rl;          // (b Tq + i) Hq + h: head h of query token i
-    const bool live = row < a.B * a.Tq * a.Hq;
+    const int rw = warp / ES, slice = warp - rw * ES;
     // the split kernel has finished: its fallback-list counters go back to zero for the next call
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int i = 0; i < 2 * REDO_NLISTS; ++i) a.hdr[HDR_REDO_LISTS + i] = 0;
     }
-    const int bi = live ? row / a.Hq : 0;           // query row of the batch: b Tq + i
+    const long long rows = (long long)a.B * a.Tq * a.Hq;
+    const long long row_ll = (long long)blockIdx.x * RPC + rw;
+    const bool live = row_ll < rows;
+    const int row = live ? (int)row_ll : 0;         // (b Tq + i) Hq + h: head h of query token i
+    const int bi = row / a.Hq;                      // query row of the batch: b Tq + i
     const int b = bi / a.Tq;
-    const int h = live ? row - bi * a.Hq : 0;
+    const int h = row - bi * a.Hq;
     // the row's place in the tensor kernel's units: kv-head row rr, in row group rr / 8 (the
-    // virtual head kvh NRG + group) as row rr % 8 (the extra-slot row)
+    // virtual head kvh NRG + group) as row rr % 8 (the run-slot row)
     const int rr = (bi - b * a.Tq) * a.G + h % a.G;
     const int grp = a.NRG == 1 ? 0 : rr / TC_MAX_GROUP;
     const int rr8 = rr - grp * TC_MAX_GROUP;
+    const int kvh = h / a.G;
     const int n = live ? a.nsplit[b] : 0;
+    const long long fbase = (long long)row * a.max_splits;   // the row's flag bytes and split slots
 
-    // Parts that may start inside this row's units: the row's kv head (and row group) owns tiles
-    // [W, W + nt). The split kernel orders its tiles (row group, b, kv head, j).
+    // Runs of the row's head u = (grp, b, kvh): it owns tiles [W, W + nt) of the split kernel's
+    // order (row group, b, kv head, j); part c = tiles [floor(c T / P), floor((c + 1) T / P)).
     const int P = a.hdr[HDR_PARTS];
     long long W = 0, tiles = 1;
-    int nt = 0, TS = 1, c_lo = 0, c_hi = -1;
+    int nt = 0, TS = 1, c_first = 0, n_r = 0, u = 0;
     if (P > 0 && n > 0) {
         tiles = a.hdr[HDR_TILES];
         TS = (a.hdr[HDR_SPLIT] + 63) / 64;
         nt = a.tstart[b + 1] - a.tstart[b];
-        W = (long long)grp * a.Hkv * a.tstart[a.B] + (long long)a.Hkv * a.tstart[b] +
-            (long long)(h / a.G) * nt;
-        c_lo = (int)(((W + 1) * P + tiles - 1) / tiles);   // first part starting after tile W
-        c_hi = (int)(((W + nt) * P - 1) / tiles);           // last part starting before W + nt
+        W = (long long)grp * a.Hkv * a.tstart[a.B] + (long long)a.Hkv * a.tstart[b] + (long long)kvh * nt;
+        u = (grp * a.B + b) * a.Hkv + kvh;
+        // the parts holding tiles W and W + nt - 1
+        c_first = (int)(((W + 1) * P - 1) / tiles);
+        n_r = (int)(((W + nt) * P - 1) / tiles) - c_first + 1;
     }
-    // extra slot of part c belongs to split jx of this row, or c left none here. Part c starts at
-    // floor(c tiles / P) = c q + floor(c r / P) with tiles = q P + r (32-bit arithmetic per part).
     const long long q_p = P > 0 ? tiles / P : 0;
     const int r_p = P > 0 ? (int)(tiles - q_p * P) : 0;
-    auto extra_split = [&](int c) -> int {
-        const long long k = (long long)c * q_p + (c * r_p) / P - W;
-        if (k <= 0 || k >= nt) return -1;
-        const int ki = (int)k;
-        const int jx = ki / TS;
-        return ki == jx * TS ? -1 : jx;
-    };
-    const float* xm = a.xm + rr8;
-    const float* xl = a.xl + rr8;
-    const float* xo = a.xo + (long long)rr8 * D;
-    const long long base = (long long)row * a.max_splits;
-    const float* m = a.m_part + base;
-    const float* l = a.l_part + base;
-    const float* o = a.o_part + base * D;
 
-    // The row's entries: its n splits, then the candidate extra slots c_lo .. c_hi (those that
-    // are not extra slots of this row are skipped). Entry e < n is split e.
-    const int n_c = c_hi >= c_lo ? c_hi - c_lo + 1 : 0;
-    const int n_e = n + n_c;
-
-    // M = max over the row's partials; the extra slots' flag bytes are ORed into their splits'
-    float M = -INFINITY;
-    for (int e = wr * 32 + lane; e < n_e; e += wpr * 32) {
-        if (e < n) {
-            M = fmaxf(M, m[e]);
-            continue;
-        }
-        const int c = c_lo + (e - n);
-        const int jx = extra_split(c);
-        if (jx >= 0) {
-            M = fmaxf(M, xm[(long long)c * a.Rg]);
-            // the split's flag byte also covers the extra slot's tokens
-            uint8_t* fb = a.flags + (long long)row * a.max_splits + jx;
-            const uintptr_t addr = reinterpret_cast<uintptr_t>(fb);
-            const unsigned sh = (unsigned)(addr & 3u) * 8u;
-            atomicOr(reinterpret_cast<unsigned*>(addr & ~uintptr_t(3)),
-                     (unsigned)a.xf[(long long)c * a.Rg + rr8] << sh);
-        }
-    }
+    Sums<E> sm;
+    sm.zero();
+    // the slice's splits j_lo .. j_hi - 1; the first 32 flag bytes are read together with the runs
+    const int jper = (n + ES - 1) / ES;
+    const int j_lo = slice * jper, j_hi = min(n, j_lo + jper);
+    const unsigned f_first = (P > 0 && j_lo + lane < j_hi) ? __ldg(a.flags + fbase + j_lo + lane) : 0u;
+    // the slice's runs, U at a time
+    {
+        const int per = (n_r + ES - 1) / ES;
+        const int e_lo = slice * per, e_hi = min(n_r, e_lo + per);
+        for (int eb = e_lo; eb < e_hi; eb += U) {
+            float mv[U], lv[U], ov[U][E];
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-    if (lane == 0) s_max[warp] = M;
-    __syncthreads();
-    M = s_max[rl * wpr];
-    for (int w = 1; w < wpr; ++w) M = fmaxf(M, s_max[rl * wpr + w]);
-
-    // this warp's contiguous range of the row's entries, ascending, U loads in flight per lane
-    const int per = (n_e + wpr - 1) / wpr;
-    const int e0 = wr * per, e1 = min(n_e, e0 + per);
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    float lam = 0.f;
-    constexpr int U = 4;
-    for (int eb = e0; eb < e1; eb += U) {
-        float mv[U], lv[U], ov[U][E];
-        bool ok[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = eb + u;
-            ok[u] = false;
-            const float *pm = m, *pl = l, *po = o;
-            if (e < e1) {
-                if (e < n) {
-                    pm = m + e; pl = l + e; po = o + (long long)e * D;
-                    ok[u] = true;
-                } else {
-                    const int c = c_lo + (e - n);
-                    if (extra_split(c) >= 0) {
-                        pm = xm + (long long)c * a.Rg; pl = xl + (long long)c * a.Rg;
-                        po = xo + (long long)c * a.Rg * D;
-                        ok[u] = true;
+            for (int k = 0; k < U; ++k) {
+                if (eb + k >= e_hi) continue;
+                const int c = c_first + eb + k;
+                const long long rs = (long long)(c + u) * a.Rg + rr8;
+                mv[k] = __ldg(a.xm + rs);
+                lv[k] = __ldg(a.xl + rs);
+                load_cols<E>(a.xo + rs * D + lane * E, ov[k]);
+                // a run that starts inside a split: its edge flags go into the split's byte
+                if (lane == 0) {
+                    const long long ks = (long long)c * q_p + (c * r_p) / P - W;   // part start
+                    if (ks > 0 && ks < nt) {
+                        const int kt = (int)ks, jx = kt / TS;
+                        if (kt != jx * TS) {
+                            uint8_t* fb = a.flags + fbase + jx;
+                            const uintptr_t addr = reinterpret_cast<uintptr_t>(fb);
+                            const unsigned sh = (unsigned)(addr & 3u) * 8u;
+                            atomicOr(reinterpret_cast<unsigned*>(addr & ~uintptr_t(3)),
+                                     (unsigned)a.xf[rs] << sh);
+                        }
                     }
                 }
             }
-            if (ok[u]) {
-                mv[u] = *pm;
-                lv[u] = *pl;
-                const float* oj = po + lane * E;
-                if constexpr (E == 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(oj);
-                    ov[u][0] = v.x; ov[u][1] = v.y; ov[u][2] = v.z; ov[u][3] = v.w;
-                } else {
-                    const float2 v = *reinterpret_cast<const float2*>(oj);
-                    ov[u][0] = v.x; ov[u][1] = v.y;
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (eb + k < e_hi) sm.add(mv[k], lv[k], ov[k]);
+        }
+    }
+    // the slice's splits: with parts, only those whose own slot holds a recomputed piece
+    {
+        for (int jb = j_lo; jb < j_hi; jb += 32) {
+            const int j = jb + lane;
+            bool take = false;
+            if (j < j_hi)
+                take = P == 0 || ((jb == j_lo ? f_first : (unsigned)__ldg(a.flags + fbase + j)) & FDPP_FLAG_SLOT);
+            unsigned mask = __ballot_sync(0xffffffffu, take);
+            while (mask != 0u) {
+                float mv[U], lv[U], ov[U][E];
+                int cnt = 0;
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    if (mask == 0u) continue;
+                    const int jj = jb + __ffs(mask) - 1;
+                    mask &= mask - 1u;
+                    mv[k] = __ldg(a.m_part + fbase + jj);
+                    lv[k] = __ldg(a.l_part + fbase + jj);
+                    load_cols<E>(a.o_part + (fbase + jj) * D + lane * E, ov[k]);
+                    cnt = k + 1;
                 }
-            }
-        }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (ok[u]) {
-                const float w = frame_weight(mv[u], M);
-#pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] = fmaf(w, ov[u][e], acc[e]);
-                lam = fmaf(w, lv[u], lam);
+                for (int k = 0; k < U; ++k)
+                    if (k < cnt) sm.add(mv[k], lv[k], ov[k]);
             }
         }
     }
+    if constexpr (ES > 1) {
+        // the row's slices in warp order, each weighted to the row's max
 #pragma unroll
-    for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
-    if (lane == 0) s_lam[warp] = lam;
-    __syncthreads();
-    // the row's warp sums in warp order; the first warp of the row writes the output
-    if (live && wr == 0) {
-        T* out = static_cast<T*>(a.out) + (long long)row * D;
-        float ltot = 0.f;
-        for (int w = 0; w < wpr; ++w) ltot += s_lam[rl * wpr + w];
+        for (int c = 0; c < E; ++c) s_acc[warp][lane * E + c] = sm.acc[c];
+        if (lane == 0) { s_lam[warp] = sm.lam; s_max[warp] = sm.mrun; }
+        __syncthreads();
+        if (slice != 0) return;
+        const int w0 = rw * ES;
+        float Mr = s_max[w0];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int d = lane + 32 * e;
-            float total = 0.f;
-            for (int w = 0; w < wpr; ++w) total += s_acc[rl * wpr + w][d];
-            // a query row that sees no key (or a sequence without keys) is a zero row
-            store_out<T>(out + d, (n > 0 && ltot != 0.f) ? __fdiv_rn(total, ltot) : 0.f);
+        for (int w = 1; w < ES; ++w) Mr = fmaxf(Mr, s_max[w0 + w]);
+        sm.zero();
+#pragma unroll
+        for (int w = 0; w < ES; ++w) {
+            const float wt = frame_weight(s_max[w0 + w], Mr);
+#pragma unroll
+            for (int c = 0; c < E; ++c) sm.acc[c] = fmaf(wt, s_acc[w0 + w][lane * E + c], sm.acc[c]);
+            sm.lam = fmaf(wt, s_lam[w0 + w], sm.lam);
         }
+    }
+    if (live) {
+        // a query row that sees no key (or a sequence without keys) is a zero row
+        T* out = static_cast<T*>(a.out) + (long long)row * D + lane * E;
+#pragma unroll
+        for (int c = 0; c < E; ++c)
+            store_out<T>(out + c, (n > 0 && sm.lam != 0.f) ? __fdiv_rn(sm.acc[c], sm.lam) : 0.f);
     }
 }
 
-// Warps per row: up to 32 while the rows fit on the GPU at that width (a long row's partials
-// are then read by many warps at once), fewer for many rows, so that all rows are in flight
-// together.
-int warps_per_row(long long rows, int num_sms)
+// Warps per row: enough that a warp reads about U entries of a row at once. With parts a head's
+// runs number about P / (its share of the heads) + 1 (the split kernel's grid bounds P; heads of
+// equal length share the tiles evenly); without, a row has up to max_splits entries.
+int slices_for(const KernelArgs& a, int split_grid)
 {
-    const long long resident = (long long)num_sms * 3 * CW;     // 3 CTAs of 8 warps per SM
-    int w = CW_WIDE;
-    while (w > 1 && rows * w > resident) w >>= 1;
-    return w;
+    long long entries = a.max_splits;
+    if (a.kernel_id == FDPP_KERNEL_TENSOR && a.B <= TC_PLAN_SMEM_MAX_B) {
+        const long long heads = (long long)a.B * a.Hkv * a.NRG;
+        entries = split_grid / heads + 2;
+    }
+    int es = 1;
+    while (es < NWC && entries > (long long)U * es) es *= 2;
+    return es;
 }
 
-template <typename T, int D>
-cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
+template <typename T, int D, int ES>
+cudaError_t launch_es(const KernelArgs& a, cudaStream_t s)
 {
     const long long rows = (long long)a.B * a.Tq * a.Hq;
-    const int wpr = warps_per_row(rows, a.num_sms);
-    const int nw = wpr > CW ? CW_WIDE : CW;
-    const int rpc = nw / wpr;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((rows + rpc - 1) / rpc));
-    cfg.blockDim = dim3((unsigned)(nw * 32));
+    cfg.gridDim = dim3((unsigned)((rows + NWC / ES - 1) / (NWC / ES)));
+    cfg.blockDim = dim3(NWC * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -241,19 +272,30 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (nw == CW_WIDE) return cudaLaunchKernelEx(&cfg, combine_kernel<T, D, CW_WIDE>, a, wpr);
-    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D, CW>, a, wpr);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<T, D, ES>, a);
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const KernelArgs& a, int split_grid, cudaStream_t s)
+{
+    switch (slices_for(a, split_grid)) {
+    case 1: return launch_es<T, D, 1>(a, s);
+    case 2: return launch_es<T, D, 2>(a, s);
+    case 4: return launch_es<T, D, 4>(a, s);
+    default: return launch_es<T, D, 8>(a, s);
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s)
+cudaError_t launch_combine(const KernelArgs& a, int dtype, int split_grid, cudaStream_t s)
 {
     cudaError_t e;
     if (dtype == FDPP_F32)
-        e = a.D == 128 ? launch_t<float, 128>(a, s) : launch_t<float, 64>(a, s);
+        e = a.D == 128 ? launch_t<float, 128>(a, split_grid, s) : launch_t<float, 64>(a, split_grid, s);
     else
-        e = a.D == 128 ? launch_t<__nv_bfloat16, 128>(a, s) : launch_t<__nv_bfloat16, 64>(a, s);
+        e = a.D == 128 ? launch_t<__nv_bfloat16, 128>(a, split_grid, s)
+                       : launch_t<__nv_bfloat16, 64>(a, split_grid, s);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -35,14 +35,15 @@ struct WsLayout {
 };
 
 // The tensor kernel cuts the tiles of all units into at most this many equal parts, one per
-// CTA. A part that starts inside a unit leaves that unit's partial of its own tiles in an
-// extra slot (one per part), which the combine adds in.
+// CTA. A part's share of one (row group, sequence, kv head) is a run, which leaves one partial
+// in its run slot c + u (u: that head's index in tile order), which the combine adds in.
 constexpr int TC_MAX_PARTS = FDPP_TC_MAX_PARTS;
 // Batches up to this size keep their split plan in the tensor kernel's shared memory (and are
 // cut into parts); larger batches are dealt out to the CTAs as whole units.
 constexpr int TC_PLAN_SMEM_MAX_B = 1024;
 // Fallback list entry: 4 x int64 = {(b + 1) | (g * max_splits + j) << 32,
-// t0 | t1 << 32 (token range of the segment), dest (-1: split slot j, else extra slot), 0}.
+// t0 | t1 << 32 (token range of the segment), dest (-1: split slot j, else run slot), the
+// segment's rows whose scores left the window (one bit per row of its row group)}.
 constexpr int REDO_WORDS = 4;
 // The fallback list is this many lists (CTA c pushes to list c % REDO_NLISTS), each with room for
 // every entry of a call.
@@ -71,10 +72,10 @@ struct KernelArgs {
     float* m_part;                // [B][Tq][Hq][max_splits]
     float* l_part;                // [B][Tq][Hq][max_splits]
     float* o_part;                // [B][Tq][Hq][max_splits][D]
-    uint8_t* xf;                  // extra slots [TC_MAX_PARTS][R]: flags,
+    uint8_t* xf;                  // run slots [TC_MAX_PARTS + B Hkv NRG][min(R, 8)]: edge flags,
     float* xm;                    //   m,
     float* xl;                    //   l,
-    float* xo;                    //   o [TC_MAX_PARTS][R][D]
+    float* xo;                    //   o [..][min(R, 8)][D]
     int B, Hq, Hkv, G, D;
     int Tq;                       // query tokens per sequence (the last Tq positions, causal)
     int R;                        // query rows per kv head and sequence: Tq * G
@@ -96,6 +97,9 @@ struct KernelArgs {
 // Query rows per kv head (R = Tq * G): the tensor kernel takes 8 rows per unit (the columns of one
 // m16n8k16 tile) and up to TC_MAX_ROWS in groups of 8; the SIMT kernel holds 16 register rows.
 constexpr int TC_MAX_GROUP = 8;
+// Window decisions of split pieces in flight in one CTA of the tensor kernel (a power of two
+// above the deepest TMA ring: no consumer warp runs more pieces ahead of another).
+constexpr int TC_FSLOTS = 16;
 constexpr int TC_MAX_ROWS = 64;
 constexpr int SIMT_MAX_GROUP = 16;
 
@@ -104,7 +108,8 @@ constexpr int SIMT_MAX_GROUP = 16;
 cudaError_t launch_split_simt(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
 cudaError_t launch_split_tc(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                             int grid, int smem_bytes, int ctas_per_sm, cudaStream_t s);
-cudaError_t launch_combine(const KernelArgs& a, int dtype, cudaStream_t s);
+// split_grid: CTAs of the split kernel before it (bounds the tensor kernel's runs per row).
+cudaError_t launch_combine(const KernelArgs& a, int dtype, int split_grid, cudaStream_t s);
 // Score range of every row-split (least into l_part, greatest into m_part) and the split plan.
 cudaError_t launch_score_ranges(const KernelArgs& a, int dtype, int grid, cudaStream_t s);
 int score_ranges_ctas_per_sm(const KernelArgs& a, int dtype);

@@ -14,8 +14,10 @@
 //   work      the 64-token tiles of all units, in unit order (b, g, j), are cut into P equal
 //             parts, one per CTA, so every CTA streams the same bytes whatever the unit count
 //             (whole units dealt round-robin would leave a last wave of few CTAs). A part is a
-//             run of segments, each the part's tiles of one unit. A segment that is not the
-//             unit's first writes its partial to the part's extra slot; combine.cu adds it in.
+//             run of segments, each the part's share of one (sequence, kv head): a segment may
+//             span several splits and begin or end inside one. Its phi-frame sums run across
+//             the splits into one partial (a run slot, which combine.cu adds in), while the
+//             window decisions are taken split by split.
 //   producer  plans the splits in shared memory (prefixes of n_b = ceil(L_b / S) and of the
 //             tiles per sequence), then for each segment writes a small header into a Q-ring
 //             slot and bulk-copies the unit's G query rows there (this slot is also how
@@ -66,28 +68,35 @@ static_assert(TILE == TC_TILE_TOKENS, "tile height is part of the tensor-map con
 
 // unit kinds carried in the Q-ring header
 enum { KIND_OWN = 0, KIND_LAST_OWN = 1, KIND_REDO = 2, KIND_END = 3 };
-// header words
-enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_L, H_WORDS };
+// header words: a segment is tokens [T0, T1) of sequence B, virtual head G, starting in split J
+// (split length S); DEST is its partial slot (a run slot, or -1: the split's own slot J). A
+// redo segment lies in one split: F0/F1 carry its rows' flag bytes (four per word), MASK the rows
+// it rewrites, ONL the rows it recomputes with online softmax (the others stay in the phi frame).
+enum { H_KIND = 0, H_B, H_G, H_J, H_T0, H_T1, H_DEST, H_F0, H_F1, H_MASK, H_L, H_S, H_ONL, H_WORDS };
+static_assert(H_WORDS * 4 <= QHDR_BYTES, "segment header fits its slot");
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-byte aligned base). The merge has
 // scratch of its own, so a unit's last stage goes back to the producer like any other:
 //   xchg: two slots of one warp's O^T fragments (d/16 float4 per lane) for the warp-sum tree;
-//   xrow: l, m and flag word per consumer warp and query row, two buffers (by unit parity).
+//   xrow: l, m and flag word per consumer warp and query row, two buffers (by unit parity);
+//   fslot: the window decisions of split pieces (TC_FSLOTS 64-bit words), then the taint words of
+//   two segments (by parity).
 struct TcLayout {
     int stage_bytes, kv_bytes, qslot_bytes;
-    int stages, qring, xchg, xrow, plan, bars, misc, total;
+    int stages, qring, xchg, xrow, fslot, plan, bars, misc, total;
 
     __host__ __device__ static constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
     __host__ __device__ TcLayout(int D, int G, int nstage, int B)
         : stage_bytes(2 * TILE * D * 2), kv_bytes(TILE * D * 2),
           qslot_bytes(round_up(QHDR_BYTES + G * D * 2, 128)), stages(0), qring(0), xchg(0),
-          xrow(0), plan(0), bars(0), misc(0), total(0)
+          xrow(0), fslot(0), plan(0), bars(0), misc(0), total(0)
     {
         qring = stages + nstage * stage_bytes;
         xchg = qring + 2 * qslot_bytes;
         xrow = xchg + 2 * (D / 16) * 32 * 16;
-        plan = xrow + 2 * 3 * NCW * TC_MAX_GROUP * 4;
+        fslot = xrow + 2 * 3 * NCW * TC_MAX_GROUP * 4;
+        plan = fslot + TC_FSLOTS * 8 + 16;
         const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 2 * B + 1 : 0) + 1;
         bars = round_up(plan + plan_ints * 4, 8);
         misc = bars + (2 * nstage + 8) * 8;
@@ -257,14 +266,15 @@ struct Producer {
         }
     }
 
-    // Emits one segment: tokens [t0, t1) of unit (b, g, j), whose partial goes to `dest` (-1:
-    // the split's own slot, else extra slot `dest`). Header + Q rows go into the Q ring, then
+    // Emits one segment: tokens [t0, t1) of sequence b, virtual head g, starting in split j,
+    // whose partial goes to `dest` (-1: split j's own slot, else run slot `dest`); hw: a redo
+    // piece's flag words, rewritten rows and online rows. Header + Q rows go into the Q ring, then
     // the K/V tiles into the stage ring, prefetching into L2 the tile `pf` places ahead (in this
     // segment, or in `nx`, the next one).
     // pre_base/pre_ent: a block-table window (entries pre_base + lane) loaded ahead of time.
     template <int D, bool PAGED>
     __device__ __forceinline__ bool emit(int kind, int b, int g, int j, int t0, int t1, int L,
-                                         int dest, const int (&hw)[3], int pre_base = -(1 << 30),
+                                         int dest, const int (&hw)[4], int pre_base = -(1 << 30),
                                          int pre_ent = -1, const NextUnit* nx = nullptr,
                                          bool first = false)
     {
@@ -279,6 +289,7 @@ struct Producer {
             hdr[H_KIND] = kind; hdr[H_B] = b; hdr[H_G] = g; hdr[H_J] = j;
             hdr[H_T0] = t0; hdr[H_T1] = t1; hdr[H_DEST] = dest;
             hdr[H_F0] = hw[0]; hdr[H_F1] = hw[1]; hdr[H_MASK] = hw[2]; hdr[H_L] = L;
+            hdr[H_S] = S; hdr[H_ONL] = hw[3];
             if (kind == KIND_END) {
                 mbar_arrive(rg.qfull + 8 * qs);
             } else {
@@ -315,7 +326,15 @@ struct Producer {
         const int bs = PAGED ? A.block_size : TILE;
         const int rows_box = bs < TILE ? bs : TILE;
         const uint32_t box_bytes = 128u * (uint32_t)rows_box;
-        const int ntiles = ceil_div_i(t1 - t0, TILE);
+        // 64-token tiles of the segment, never across a split boundary (counted only for the
+        // L2 prefetch, which is off by default)
+        int ntiles = 0;
+        if (A.pf_tiles > 0)
+            for (int x = t0; x < t1;) {
+                const int e = min((x / S + 1) * S, t1);
+                ntiles += ceil_div_i(e - x, TILE);
+                x = e;
+            }
         int win_base = pre_base, ent = pre_ent;    // paged: 32 block-table entries per window
         const int nblk_seq = PAGED ? ceil_div_i(L, bs) : 0;
         constexpr int PER_BLK = 2 * HALVES;        // boxes per block: K and V, each half
@@ -328,9 +347,10 @@ struct Producer {
         if (first && pf > 0)                       // the CTA's first segment: nothing prefetched
             for (int ti = 1; ti <= pf && ti < ntiles; ++ti)
                 prefetch_tile<D, PAGED>(b, g, t0 + ti * TILE, t1, win_base, ent);
-        for (int i = 0; i < ntiles; ++i) {
-            const int tt = t0 + i * TILE;
-            const int nvalid = min(TILE, t1 - tt);
+        int tt = t0, se = (t0 / S + 1) * S;        // tile start, end of its split
+        for (int i = 0; tt < t1; ++i) {
+            const int tend = min(min(tt + TILE, se), t1);
+            const int nvalid = tend - tt;
             if (!ring_wait(rg.empty + 8 * stage, phase ^ 1u, misc, A)) return false;
             const uint32_t kdst = sbase + lay->stages + stage * lay->stage_bytes;
             const uint32_t vdst = kdst + lay->kv_bytes;
@@ -391,6 +411,8 @@ struct Producer {
                 }
             }
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
+            tt = tend;
+            if (tt == se) se += S;
         }
         return true;
     }
@@ -406,9 +428,11 @@ struct Producer {
     }
 
     // Own work, tile-balanced: the T tiles of all units (in unit order b, g, j) are cut into P
-    // equal parts and CTA c streams part c, [c T / P, (c + 1) T / P). A part that starts inside
-    // a unit writes that unit's partial of its tiles to extra slot c; every other segment
-    // writes the split's own slot.
+    // equal parts and CTA c streams part c, [c T / P, (c + 1) T / P). A part is a sequence of
+    // runs, one per (sequence, virtual head) it touches; a run may cover several splits and
+    // begin or end inside one. Each run leaves one phi-frame partial, in run slot c + u (u: the
+    // index of the (row group, sequence, kv head) in tile order; the slots of all runs are
+    // distinct), and the flag bytes split by split.
     // RG builds order the tiles group-major, (row group, b, kv head, j): the groups' ranges
     // have the same shape, so parts c, c + P / NRG, ... read the same K/V tiles at about the
     // same time and all but the first find them in L2.
@@ -423,8 +447,9 @@ struct Producer {
         const int r = (int)(T - q * P);
         const long long tb = (long long)c * q + (c * r) / P;
         const long long te = (long long)(c + 1) * q + ((c + 1) * r) / P;
-        const int zero3[3] = {0, 0, 0};
+        const int zero4[4] = {0, 0, 0, 0};
         struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
+        const int nseq = A.B;
         int cb = 0, cgrp = 0;
         auto seg_at = [&](long long t, Seg& s) {
             long long tg = t;                        // tile index within the row group
@@ -442,16 +467,20 @@ struct Producer {
             const int kvh = r / ntb;
             s.g = RG ? kvh * A.NRG + grp : kvh;
             const int k = r - kvh * ntb;             // tile of sequence cb, kv head kvh
+            // the run: tiles k .. kend - 1 of the sequence's ntb (split j has tiles j TS .. j TS +
+            // TS - 1, the last split fewer), tokens t0 .. t1
+            const int kend = (int)min((long long)ntb, k + (te - t));
             s.j = k / TS;
-            const int ilo = k - s.j * TS;
             s.L = lplan[cb];
-            const int nb = min(ceil_div_i(s.L, S), A.max_splits);
-            const int nu = (s.j < nb - 1) ? TS : ntb - (nb - 1) * TS;
-            const int ihi = (int)min((long long)nu, ilo + (te - t));
-            s.t0 = s.j * S + ilo * TILE;
-            s.t1 = min(s.j * S + ihi * TILE, min((s.j + 1) * S, s.L));
-            s.ntile = ihi - ilo;
-            s.dest = ilo == 0 ? -1 : c;
+            s.t0 = s.j * S + (k - s.j * TS) * TILE;
+            if (kend >= ntb) {
+                s.t1 = s.L;
+            } else {
+                const int je = kend / TS;
+                s.t1 = je * S + (kend - je * TS) * TILE;
+            }
+            s.ntile = kend - k;
+            s.dest = c + (grp * nseq + cb) * A.Hkv + kvh;
         };
         Seg cur, nxt;
         long long t = tb;
@@ -474,7 +503,7 @@ struct Producer {
             }
             if (last) grid_launch_dependents();
             if (!emit<D, PAGED>(last ? KIND_LAST_OWN : KIND_OWN, cur.b, cur.g, cur.j, cur.t0, cur.t1,
-                                cur.L, cur.dest, zero3,
+                                cur.L, cur.dest, zero4,
                                 PAGED ? cur.t0 / A.block_size : -(1 << 30), cur_ent, &nx, !had_own))
                 return false;
             had_own = true;
@@ -496,7 +525,7 @@ struct Producer {
     __device__ __forceinline__ bool run_units(int n_units, bool& had_own)
     {
         const KernelArgs& A = *a;
-        const int zero3[3] = {0, 0, 0};
+        const int zero4[4] = {0, 0, 0, 0};
         UnitCursor cur;
         cur.reset();
         for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -505,7 +534,7 @@ struct Producer {
             const int kind = (u + gridDim.x >= n_units) ? KIND_LAST_OWN : KIND_OWN;
             if (kind == KIND_LAST_OWN) grid_launch_dependents();
             const int t0 = j * S, t1 = min(t0 + S, L);
-            if (!emit<D, PAGED>(kind, b, g, j, t0, t1, L, -1, zero3, -(1 << 30), -1, nullptr, !had_own))
+            if (!emit<D, PAGED>(kind, b, g, j, t0, t1, L, -1, zero4, -(1 << 30), -1, nullptr, !had_own))
                 return false;
             had_own = true;
         }
@@ -567,7 +596,7 @@ struct Producer {
                 k = __shfl_sync(0xffffffffu, k, 0);
                 if (!got) continue;
                 // the pusher reserved entry k before storing it: read it with a bounded wait
-                long long e = 0, rng = 0, dst = 0;
+                long long e = 0, rng = 0, dst = 0, tnt = 0;
                 if (lane == 0) {
                     long long* ent = A.redo + ((long long)list * A.redo_cap + k) * REDO_WORDS;
                     const uint64_t t0 = global_ns();
@@ -576,46 +605,58 @@ struct Producer {
                     if (e != 0) {
                         rng = __ldcg(ent + 1);
                         dst = __ldcg(ent + 2);
+                        tnt = __ldcg(ent + 3);
                         ent[0] = 0;                    // leave the list zeroed for the next call
                     }
                 }
                 e = __shfl_sync(0xffffffffu, e, 0);
                 rng = __shfl_sync(0xffffffffu, rng, 0);
                 dst = __shfl_sync(0xffffffffu, dst, 0);
+                tnt = __shfl_sync(0xffffffffu, tnt, 0);
                 if (e == 0) {
                     if (lane == 0) { misc[0] = 1; set_error(A, FDPP_ERRBIT_TIMEOUT); }
                     return;
                 }
                 const int rb = (int)(e & 0xffffffffll) - 1;
                 const int gj = (int)(e >> 32);
-                const int rg_ = gj / A.max_splits, rj = gj % A.max_splits;
+                const int rg_ = gj / A.max_splits;
                 const int st0 = (int)(rng & 0xffffffffll), st1 = (int)(rng >> 32);
                 const int dest = (int)dst;
+                const unsigned taint = (unsigned)tnt;     // the run's rows to recompute
                 const int L = clamp_len(A.seq_lens[rb], A.max_seq_len);
-                // flag bytes of the segment's G heads (written by the pushing CTA before its push)
-                int hw[3] = {0, 0, 0};
                 const int rkvh = kv_head(rg_);
                 const int rrow = RG ? (rg_ - rkvh * A.NRG) * TC_MAX_GROUP + lane : lane;
-                const int rows = RG ? A.Rg : A.R;        // rows of a unit (extra-slot stride)
-                if (lane < rows && rrow < A.R) {
-                    const unsigned f = dest < 0 ? __ldcg(A.flags + unit_row_slot(A, rb, rkvh, rrow, rj))
-                                                : __ldcg(A.xf + (long long)dest * rows + lane);
-                    const unsigned sh = (unsigned)(lane & 3) * 8u;
-                    const unsigned w0 = lane < 4 ? (f << sh) : 0u;
-                    const unsigned w1 = lane >= 4 ? (f << sh) : 0u;
-                    const unsigned m = (f & FDPP_FLAG_OUT) ? (1u << lane) : 0u;
-                    hw[0] = (int)w0; hw[1] = (int)w1; hw[2] = (int)m;
-                }
+                const int rows = RG ? A.Rg : A.R;        // rows of a unit (run-slot stride)
+                // The tainted run again, split by split: each piece's tainted rows are rewritten,
+                // with online softmax where that split's scores left the window (its own flag
+                // bytes, written by the pushing CTA before its push), else in the phi frame. A
+                // first piece that starts inside a split goes back to the run slot (its flags are
+                // the slot's edge flags); every other piece to its split's own slot.
+                for (int tp0 = st0; tp0 < st1;) {
+                    const int rj = tp0 / S;
+                    const int tp1 = min((rj + 1) * S, st1);
+                    const int dp = (tp0 == st0 && dest >= 0 && tp0 != rj * S) ? dest : -1;
+                    int hw[4] = {0, 0, (int)taint, 0};
+                    if (lane < rows && rrow < A.R) {
+                        const unsigned f = dp < 0 ? __ldcg(A.flags + unit_row_slot(A, rb, rkvh, rrow, rj))
+                                                  : __ldcg(A.xf + (long long)dp * rows + lane);
+                        const unsigned sh = (unsigned)(lane & 3) * 8u;
+                        hw[0] = (int)(lane < 4 ? (f << sh) : 0u);
+                        hw[1] = (int)(lane >= 4 ? (f << sh) : 0u);
+                        hw[3] = (int)(((f & FDPP_FLAG_OUT) && ((taint >> lane) & 1u)) ? (1u << lane) : 0u);
+                    }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    hw[0] |= __shfl_xor_sync(0xffffffffu, hw[0], o);
-                    hw[1] |= __shfl_xor_sync(0xffffffffu, hw[1], o);
-                    hw[2] |= __shfl_xor_sync(0xffffffffu, hw[2], o);
+                    for (int o = 16; o > 0; o >>= 1) {
+                        hw[0] |= __shfl_xor_sync(0xffffffffu, hw[0], o);
+                        hw[1] |= __shfl_xor_sync(0xffffffffu, hw[1], o);
+                        hw[3] |= __shfl_xor_sync(0xffffffffu, hw[3], o);
+                    }
+                    if (!emit<D, PAGED>(KIND_REDO, rb, rg_, rj, tp0, tp1, L, dp, hw)) return;
+                    tp0 = tp1;
                 }
-                if (!emit<D, PAGED>(KIND_REDO, rb, rg_, rj, st0, st1, L, dest, hw)) return;
             }
         }
-        const int zeros[3] = {0, 0, 0};
+        const int zeros[4] = {0, 0, 0, 0};
         emit<D, PAGED>(KIND_END, 0, 0, 0, 0, 0, 0, -1, zeros);
     }
 };
@@ -635,6 +676,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     // with movmatrix.trans. P is carried as bf16 hi + lo: for G <= 4 the lo part rides in head
     // columns 4..7 (unused otherwise), so P.V costs d/16 MMAs; for G > 4 hi and lo go through
     // two MMAs into the same accumulator.
+    // A segment is a run of tiles of one (sequence, virtual head) that may cover several splits:
+    // the phi-frame sums run across them, and the window decisions are taken split by split.
     constexpr int KS = D / 16;           // k-steps of S^T, and m-tiles of O^T
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane >> 2, qd = lane & 3;
@@ -645,24 +688,31 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     const int tok_r = warp * TPW + r;             // this lane's tokens: tok_r and tok_r + 8
     const int tok_q = warp * TPW + 2 * qd;        // tokens of this lane's V^T fragment columns
     const int head0 = 2 * qd;                     // this lane's heads: head0, head0 + 1
-    uint32_t stage = 0, phase = 0, qiter = 0, un = 0;   // un: units merged so far
+    uint32_t stage = 0, phase = 0, qiter = 0, un = 0;   // un: segments merged so far
+    uint32_t portion = 0;                         // split pieces of own segments finished
+    unsigned long long* fslot = reinterpret_cast<unsigned long long*>(sm + lay.fslot);
+    unsigned* taint_s = reinterpret_cast<unsigned*>(sm + lay.fslot + TC_FSLOTS * 8);
 
     for (;;) {
-        // ---- next unit from the producer ----
+        // ---- next segment from the producer ----
         const uint32_t qs = qiter & 1u;
         if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) return;
         const uint8_t* slot = sm + lay.qring + qs * lay.qslot_bytes;
         const int* hdr = reinterpret_cast<const int*>(slot);
         const int kind = hdr[H_KIND];
         if (kind == KIND_END) return;
-        const int b = hdr[H_B], g = hdr[H_G], j = hdr[H_J];
+        const int b = hdr[H_B], g = hdr[H_G], j0 = hdr[H_J];
         const int t0 = hdr[H_T0], t1 = hdr[H_T1], dest = hdr[H_DEST], seq_len = hdr[H_L];
+        const int S = hdr[H_S];
         const unsigned fw0 = (unsigned)hdr[H_F0], fw1 = (unsigned)hdr[H_F1];
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
+        const unsigned onl_mask = (unsigned)hdr[H_ONL];
         const bool redo = kind == KIND_REDO;
-        const bool online = redo || (a.mode == FDPP_MODE_FORCE_ONLINE);
+        // a redo piece keeps the phi frame for rows whose own split stayed in the window
+        const bool online = (redo && onl_mask != 0u) || (a.mode == FDPP_MODE_FORCE_ONLINE);
+        const uint32_t upar = un & 1u;
         // RG builds: virtual head g = kv head kvh, row group of rows rbase .. rbase + nrow() - 1
-        // of the kv head (rows() = the unit's row stride in the extra slots); else g is the kv
+        // of the kv head (rows() = the unit's row stride in the run slots); else g is the kv
         // head. Both are read at each use: a kernel parameter holds no register between uses.
         const int kvh = RG ? g / a.NRG : g;
         const int rbase = RG ? (g - kvh * a.NRG) * TC_MAX_GROUP : 0;
@@ -700,16 +750,64 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             kseg[0] = hv[0] ? key_limit(a, seq_len, (rbase + head0) / a.G) - t0 : 0;
             kseg[1] = hv[1] ? key_limit(a, seq_len, (rbase + head0 + 1) / a.G) - t0 : 0;
         }
-        float mrun[2] = {online ? -INFINITY : phv[0], online ? -INFINITY : phv[1]};
+        // rows kept in the phi frame inside an online segment (a redo piece's clean rows)
+        const bool frz[2] = {redo && !((onl_mask >> head0) & 1u), redo && !((onl_mask >> (head0 + 1)) & 1u)};
+        float mrun[2] = {online && !frz[0] ? -INFINITY : phv[0], online && !frz[1] ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
-        const int ntiles = ceil_div_i(t1 - t0, TILE);
 
-        // The tile loop, built once for the phi frame and once for the running max (fallback
-        // segments and forced online mode), so the hot phi-frame loop stays compact.
+        // End of one split piece of an own segment: the four warps' window decisions for it,
+        // combined by whichever warp arrives last (one atomic OR on a 64-bit shared word: 4 bits
+        // per row, an arrival bit per warp), which writes the rows' flag bytes (the split's own,
+        // or the run slot's edge byte for a first piece that starts inside a split) and marks
+        // the rows with a score outside the window as the segment's taint. Pieces cycle through
+        // TC_FSLOTS words: no warp runs more than a ring's depth of tiles ahead of another.
+        auto finish_piece = [&](int jp, bool first_piece) {
+            unsigned f0 = fl[0], f1 = fl[1];
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) {
+                f0 |= __shfl_xor_sync(0xffffffffu, f0, sh);
+                f1 |= __shfl_xor_sync(0xffffffffu, f1, sh);
+            }
+            fl[0] = fl[1] = 0u;
+            if (redo) return;                      // a redo piece's flag bytes come with it
+            unsigned word = ((f0 & 15u) << (8 * qd)) | ((f1 & 15u) << (8 * qd + 4));
+            word |= __shfl_xor_sync(0xffffffffu, word, 1);
+            word |= __shfl_xor_sync(0xffffffffu, word, 2);
+            const uint32_t ks = portion++ & (uint32_t)(TC_FSLOTS - 1);
+            unsigned long long old = 0ull;
+            if (lane == 0) old = atomicOr(&fslot[ks], (1ull << (32 + warp)) | (unsigned long long)word);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if ((((unsigned)(old >> 32)) | (1u << warp)) != (1u << NCW) - 1u) return;
+            const unsigned full = (unsigned)old | word;
+            if (lane == 0) {
+                fslot[ks] = 0ull;
+                unsigned out_rows = 0u;
+#pragma unroll
+                for (int hh = 0; hh < TC_MAX_GROUP; ++hh)
+                    if ((full >> (4 * hh)) & FDPP_FLAG_OUT) out_rows |= 1u << hh;
+                if (out_rows) atomicOr(&taint_s[upar], out_rows);
+            }
+            if (lane < nrow()) {
+                const uint8_t fb = (uint8_t)(((full >> (4 * lane)) & 15u) |
+                                             (a.mode == FDPP_MODE_FORCE_ONLINE ? FDPP_FLAG_RECOMPUTED : 0u));
+                if (first_piece && dest >= 0 && t0 != jp * S)
+                    a.xf[(long long)dest * rows() + lane] = fb;
+                else
+                    a.flags[MQ ? unit_row_slot(a, b, kvh, rbase + lane, jp)
+                               : ((long long)b * a.Hq + kvh * a.G + rbase + lane) * a.max_splits + jp] = fb;
+            }
+        };
+
+        // The tile loop, built once for the phi frame and once for the running max (redo pieces
+        // and forced online mode), so the hot phi-frame loop stays compact. Tiles are 64 tokens
+        // and never cross a split boundary.
         auto run_tiles = [&](auto online_c) -> bool {
             constexpr bool ONLINE = decltype(online_c)::value;
-            for (int i = 0; i < ntiles; ++i) {
-                const int nvalid = min(TILE, t1 - (t0 + i * TILE));
+            int tt = t0, se = (t0 / S + 1) * S, jp = j0;
+            bool first_piece = true;
+            while (tt < t1) {
+                const int tend = min(min(tt + TILE, se), t1);
+                const int nvalid = tend - tt;
                 if (!ring_wait(rg.full + 8 * stage, phase, misc, a)) return false;
                 const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
                 const uint32_t vb = kb + lay.kv_bytes;
@@ -732,7 +830,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     sv[e] = __fmul_rn(sa[0][e] + sa[1][e], a.scale);
                     const int tok = tok_r + 8 * (e >> 1);
                     if constexpr (MQ)
-                        valid[e] = tok < min(nvalid, kseg[e & 1] - i * TILE);   // the row's tokens of the tile
+                        valid[e] = tok < min(nvalid, kseg[e & 1] - (tt - t0));   // the row's tokens of the tile
                     else
                         valid[e] = hv[e & 1] && tok < nvalid;
                     if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
@@ -752,7 +850,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
                         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
                         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-                        const float mnew = fmaxf(mrun[c], tmax);
+                        const float mnew = frz[c] ? mrun[c] : fmaxf(mrun[c], tmax);
                         corr[c] = (mrun[c] == mnew) ? 1.f : (mrun[c] == -INFINITY ? 0.f : __expf(mrun[c] - mnew));
                         mrun[c] = mnew;
                         lsum[c] *= corr[c];
@@ -818,6 +916,13 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rg.empty + 8 * stage);
                 if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
+                tt = tend;
+                if (tt == se || tt == t1) {            // a split piece ends here
+                    finish_piece(jp, first_piece);
+                    first_piece = false;
+                    ++jp;
+                    se += S;
+                }
             }
             return true;
         };
@@ -826,10 +931,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int sh = 4; sh < 32; sh <<= 1) {
-                lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], sh);
-                fl[c] |= __shfl_xor_sync(0xffffffffu, fl[c], sh);
-            }
+            for (int sh = 4; sh < 32; sh <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], sh);
         }
         if (pack_lo) {
 #pragma unroll
@@ -840,20 +942,18 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 
         // ---- merge of the four warp partials: (w0 + w2) + (w1 + w3) ----
         // Warps 2 and 3 leave their O^T fragments in exchange slots 0 and 1 (after warp 0 has read
-        // the previous unit's), every warp its rows' l, m and flags; warps 0 and 1 add the slot
-        // of their partner, warp 1 hands its sum to warp 0 through slot 1, and warp 0 writes the
-        // row's partial. In the phi frame every warp's m is phi and each weight is exactly 1, so
+        // the previous segment's), every warp its rows' l and m; warps 0 and 1 add the slot of
+        // their partner, warp 1 hands its sum to warp 0 through slot 1, and warp 0 writes the
+        // rows' partial. In the phi frame every warp's m is phi and each weight is exactly 1, so
         // the sums need no exponentials.
-        const uint32_t upar = un & 1u;
         float4* xs = reinterpret_cast<float4*>(sm + lay.xchg);
         float* xl_s = reinterpret_cast<float*>(sm + lay.xrow) + upar * 3 * NCW * TC_MAX_GROUP;
         float* xm_s = xl_s + NCW * TC_MAX_GROUP;
-        unsigned* xf_s = reinterpret_cast<unsigned*>(xm_s + NCW * TC_MAX_GROUP);
         if (warp >= 2) {
             if (un > 0 && !ring_wait(rg.mdone, upar ^ 1u, misc, a)) return;
-            float4* slot = xs + (warp - 2) * KS * 32;
+            float4* xslot = xs + (warp - 2) * KS * 32;
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) slot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+            for (int mt = 0; mt < KS; ++mt) xslot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
         }
         if (r == 0) {
 #pragma unroll
@@ -861,13 +961,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 if (!hv[c]) continue;
                 xl_s[warp * TC_MAX_GROUP + head0 + c] = lsum[c];
                 xm_s[warp * TC_MAX_GROUP + head0 + c] = mrun[c];
-                xf_s[warp * TC_MAX_GROUP + head0 + c] = fl[c];
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(rg.cbar);
         ++un;
-        if (warp >= 2) continue;                   // warps 2 and 3 go on to the next unit
+        if (warp >= 2) continue;                   // warps 2 and 3 go on to the next segment
         if (!ring_wait(rg.cbar, upar, misc, a)) return;
 
         // this warp and its partner (warp + 2), each weighted into the rows' common frame
@@ -885,10 +984,10 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     wp[c] = frame_weight(xm_s[(warp + 2) * TC_MAX_GROUP + hh], M);
                 }
             }
-            const float4* slot = xs + warp * KS * 32;
+            const float4* xslot = xs + warp * KS * 32;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                const float4 v = slot[mt * 32 + lane];
+                const float4 v = xslot[mt * 32 + lane];
                 if (!online) {
                     o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
                 } else {
@@ -901,25 +1000,27 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         }
         if (warp == 1) {
             // warp 1 has read slot 1 (warp 3's); its own sum takes the slot for warp 0
-            float4* slot = xs + KS * 32;
+            float4* xslot = xs + KS * 32;
             __syncwarp();
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) slot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+            for (int mt = 0; mt < KS; ++mt) xslot[mt * 32 + lane] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
             __syncwarp();
             if (lane == 0) mbar_arrive(rg.mhand);
             continue;
         }
 
-        // ---- warp 0: l, m and the flag byte of every row (lane hh for row hh) ----
+        // ---- warp 0: l and m of every row (lane hh for row hh) ----
+        // Rows whose scores left the window in some split of an own segment (its taint, complete
+        // once all four warps have merged) get an empty partial here in normal mode: the fallback
+        // recomputes them piece by piece. A redo piece rewrites its tainted rows only and writes
+        // their flag bytes.
         const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
-        unsigned unit_out = 0u;                    // rows of this segment outside the window
+        const unsigned taint = redo ? 0u : taint_s[upar];
+        const bool refill = !redo && a.mode == FDPP_MODE_NORMAL;
         {
             const int hh = lane;
-            unsigned f = 0u;
             float M = 0.f, lam = 0.f;
             if (hh < nrow()) {
-#pragma unroll
-                for (int w = 0; w < NCW; ++w) f |= xf_s[w * TC_MAX_GROUP + hh];
                 M = xm_s[hh];
 #pragma unroll
                 for (int w = 1; w < NCW; ++w) M = fmaxf(M, xm_s[w * TC_MAX_GROUP + hh]);
@@ -928,41 +1029,42 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     lam = online ? fmaf(frame_weight(xm_s[w * TC_MAX_GROUP + hh], M), xl_s[w * TC_MAX_GROUP + hh], lam)
                                  : lam + xl_s[w * TC_MAX_GROUP + hh];
             }
-            unit_out = __ballot_sync(0xffffffffu, hh < nrow() && (f & FDPP_FLAG_OUT));
             if (hh < nrow() && ((write_mask >> hh) & 1u)) {
-                const long long r = dest >= 0 ? (long long)dest * rows() + hh
-                                    : MQ ? unit_row_slot(a, b, kvh, rbase + hh, j)
-                                         : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j;
+                const long long rs = dest >= 0 ? (long long)dest * rows() + hh
+                                     : MQ ? unit_row_slot(a, b, kvh, rbase + hh, j0)
+                                          : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j0;
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
-                uint8_t* fp = dest < 0 ? a.flags : a.xf;
-                lp[r] = lam;
-                mp[r] = M;
+                const bool empty = refill && ((taint >> hh) & 1u);
+                lp[rs] = empty ? 0.f : lam;
+                mp[rs] = empty ? -INFINITY : M;
                 if (redo) {
                     const unsigned f0 = ((hh < 4 ? fw0 : fw1) >> ((hh & 3) * 8)) & 0xffu;
-                    fp[r] = (uint8_t)(f0 | FDPP_FLAG_RECOMPUTED);
-                } else {
-                    fp[r] = (uint8_t)(f | (online ? FDPP_FLAG_RECOMPUTED : 0u));
+                    const unsigned rc = ((onl_mask >> hh) & 1u) ? FDPP_FLAG_RECOMPUTED : 0u;
+                    if (dest < 0) a.flags[rs] = (uint8_t)(f0 | rc | FDPP_FLAG_SLOT);
+                    else a.xf[rs] = (uint8_t)(f0 | rc);
                 }
             }
         }
-        // the partial rows of this lane: head0 and head0 + 1, the split's own slot or the extra
-        // slot of a part that began inside the unit
+        if (!redo && lane == 0) taint_s[upar] = 0u;   // ready for the segment after next
+        // the partial rows of this lane: head0 and head0 + 1, the run slot or the split's own
         float* orow[2] = {nullptr, nullptr};
+        bool oempty[2] = {false, false};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int hh = head0 + c;
             if (!hv[c] || !((write_mask >> hh) & 1u)) continue;
+            oempty[c] = refill && ((taint >> hh) & 1u);
             orow[c] = dest >= 0 ? a.xo + ((long long)dest * rows() + hh) * D
-                                : a.o_part + (MQ ? unit_row_slot(a, b, kvh, rbase + hh, j)
-                                                 : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j) * D;
+                                : a.o_part + (MQ ? unit_row_slot(a, b, kvh, rbase + hh, j0)
+                                                 : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j0) * D;
         }
         if (!ring_wait(rg.mhand, upar, misc, a)) return;
         {
-            const float4* slot = xs + KS * 32;
+            const float4* xslot = xs + KS * 32;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                const float4 v = slot[mt * 32 + lane];
+                const float4 v = xslot[mt * 32 + lane];
                 o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
             }
         }
@@ -973,20 +1075,22 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             if (orow[c] == nullptr) continue;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                orow[c][16 * mt + r] = o[mt][c];
-                orow[c][16 * mt + r + 8] = o[mt][c + 2];
+                orow[c][16 * mt + r] = oempty[c] ? 0.f : o[mt][c];
+                orow[c][16 * mt + r + 8] = oempty[c] ? 0.f : o[mt][c + 2];
             }
         }
-        // ---- a segment with a row outside the window goes on the device-wide fallback list ----
-        // (warp 0's flag stores are ordered before the release store that publishes the entry)
+        // ---- a segment with rows outside the window goes on the device-wide fallback list ----
+        // (every flag byte of its pieces, and warp 0's stores, are ordered before the release
+        // store that publishes the entry)
         __syncwarp();
-        if (!redo && unit_out != 0u && a.mode == FDPP_MODE_NORMAL && lane == 0) {
+        if (!redo && taint != 0u && a.mode == FDPP_MODE_NORMAL && lane == 0) {
             const int list = (int)(blockIdx.x % REDO_NLISTS);
             const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
             long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
             ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
             ent[2] = dest;
-            st_release_gpu(ent, ((long long)(g * a.max_splits + j) << 32) | (long long)(unsigned)(b + 1));
+            ent[3] = (long long)taint;
+            st_release_gpu(ent, ((long long)(g * a.max_splits + j0) << 32) | (long long)(unsigned)(b + 1));
         }
         if (lane == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
     }
@@ -1037,6 +1141,8 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
         mbar_init(rg.mdone, 1);
         misc[0] = 0;
         misc[1] = 0;
+        unsigned long long* fs = reinterpret_cast<unsigned long long*>(sm + lay.fslot);
+        for (int i = 0; i < TC_FSLOTS + 2; ++i) fs[i] = 0ull;
         fence_mbar_init();
     }
     __syncthreads();

@@ -70,10 +70,10 @@ def test_max_splits_and_workspace_size():
     p = _gqa_params()
     assert F.fdpp_max_splits(p) == 8
     ws = F.fdpp_workspace_size(p)
-    # partials o (d floats), l, m and a flag byte per split slot and per extra slot (G = 4 rows
-    # for each of FDPP_TC_MAX_PARTS parts), the fallback lists (8 lists of 32-byte entries, one
-    # per unit and per part each), plus header and plan
-    slots = 8 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 4
+    # partials o (d floats), l, m and a flag byte per split slot and per run slot (G = 4 rows
+    # for each of FDPP_TC_MAX_PARTS parts plus one per (sequence, kv head)), the fallback lists
+    # (8 lists of 32-byte entries, one per unit and per part each), plus header and plan
+    slots = 8 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8) * 4
     lists = 8 * (8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws <= fixed + 64 * 1024
@@ -86,18 +86,19 @@ def test_max_splits_and_workspace_size():
 
 def test_workspace_size_with_row_groups():
     # 16 query tokens of 4 heads per kv head: R = 64 rows, 8 row groups of the tensor kernel.
-    # Partials per (query row, split); a part's extra slot holds one segment, so one group's 8
-    # rows; the fallback lists hold an entry per (sequence, kv head, row group, split) and per part
+    # Partials per (query row, split); a run slot holds one run of one row group, so 8 rows, one
+    # per part plus one per (sequence, kv head, row group); the fallback lists hold an entry per
+    # (sequence, kv head, row group, split) and per part
     p = _gqa_params(q_tokens=16)
     ws = F.fdpp_workspace_size(p)
-    slots = 8 * 16 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 8
+    slots = 8 * 16 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 8
     lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws <= fixed + 64 * 1024
-    # 12 rows: two groups (8 + 4); extra slots still 8 rows, lists twice the one-group count
+    # 12 rows: two groups (8 + 4); run slots still 8 rows, lists twice the one-group count
     p12 = _gqa_params(q_tokens=3)
     ws12 = F.fdpp_workspace_size(p12)
-    slots = 8 * 3 * 32 * 8 + F.FDPP_TC_MAX_PARTS * 8
+    slots = 8 * 3 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 8
     lists = 8 * (8 * 8 * 2 * 8 + F.FDPP_TC_MAX_PARTS) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws12 <= fixed + 64 * 1024
