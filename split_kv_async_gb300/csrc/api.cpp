@@ -115,7 +115,7 @@ fdpp_status check_paged(const fdpp_params* p)
     return FDPP_OK;
 }
 
-// Entries of one fallback list: one per unit, plus one per part for units cut in two.
+// Entries of one fallback list: one per split piece a run may push.
 // Row groups of the tensor kernel: each (kv head, group of up to 8 query rows) is a unit head.
 int row_groups_of(const fdpp_params& p)
 {
@@ -125,7 +125,9 @@ int row_groups_of(const fdpp_params& p)
 
 size_t redo_capacity(const fdpp_params& p)
 {
-    return (size_t)p.batch * p.num_kv_heads * row_groups_of(p) * max_splits_of(p) + TC_MAX_PARTS;
+    // split pieces: every split once, plus one more per run boundary (parts + heads)
+    const size_t heads = (size_t)p.batch * p.num_kv_heads * row_groups_of(p);
+    return heads * max_splits_of(p) + TC_MAX_PARTS + heads;
 }
 
 WsLayout layout_of(const fdpp_params& p)

@@ -48,6 +48,9 @@ constexpr int REDO_WORDS = 4;
 // The fallback list is this many lists (CTA c pushes to list c % REDO_NLISTS), each with room for
 // every entry of a call.
 constexpr int REDO_NLISTS = 8;
+// A claimed fallback entry that spans several splits is cut into one entry per split, shared
+// by the free CTAs, while fewer than this many entries wait to be claimed.
+constexpr int REDO_SPLIT_BELOW = 64;
 // Start-up hint of the tensor kernel (contiguous caches): per CTA, the TMA coordinates (x, y, z)
 // of the first HINT_TILES tiles it streamed in the last call, after a count; prefetched into L2
 // before the kernel waits for the previous one. HINT_WORDS int32 per CTA.

@@ -569,11 +569,14 @@ struct Producer {
                 // every list's (count, taken) in one read, a lane per list starting at this CTA's
                 const int my = (int)((blockIdx.x + lane) % REDO_NLISTS);
                 bool pending = false;
+                int waiting = 0;
                 if (lane < REDO_NLISTS) {
                     const unsigned long long both = ld_relaxed_gpu_u64(
                         reinterpret_cast<const unsigned long long*>(&A.hdr[HDR_REDO_LISTS + 2 * my]));
-                    pending = (int)(unsigned)(both >> 32) < (int)(unsigned)(both & 0xffffffffull);
+                    waiting = (int)(unsigned)(both & 0xffffffffull) - (int)(unsigned)(both >> 32);
+                    pending = waiting > 0;
                 }
+                waiting = warp_sum(max(waiting, 0));      // entries not yet claimed, all lists
                 const unsigned lists = __ballot_sync(0xffffffffu, pending);
                 if (lists == 0u) break;
                 const int list = (int)((blockIdx.x + (__ffs(lists) - 1)) % REDO_NLISTS);
@@ -631,10 +634,31 @@ struct Producer {
                 // with online softmax where that split's scores left the window (its own flag
                 // bytes, written by the pushing CTA before its push), else in the phi frame. A
                 // first piece that starts inside a split goes back to the run slot (its flags are
-                // the slot's edge flags); every other piece to its split's own slot.
-                for (int tp0 = st0; tp0 < st1;) {
+                // the slot's edge flags); every other piece to its split's own slot. An entry of
+                // several pieces keeps its first piece here and goes back on this CTA's list for
+                // the rest, which another free CTA cuts again (while fewer than REDO_SPLIT_BELOW
+                // entries wait).
+                int st1_own = st1;
+                {
+                    const int pe = min((st0 / S + 1) * S, st1);   // end of the first piece
+                    // only while few entries wait: with many, every free CTA has one already
+                    if (pe < st1 && waiting < REDO_SPLIT_BELOW) {
+                        st1_own = pe;
+                        if (lane == 0) {
+                            const int ml = (int)(blockIdx.x % REDO_NLISTS);
+                            const int kk = atomicAdd(&A.hdr[HDR_REDO_LISTS + 2 * ml], 1);
+                            long long* ent = A.redo + ((long long)ml * A.redo_cap + kk) * REDO_WORDS;
+                            ent[1] = (long long)(unsigned)pe | ((long long)(unsigned)st1 << 32);
+                            ent[2] = -1;
+                            ent[3] = (long long)taint;
+                            st_release_gpu(ent, ((long long)(rg_ * A.max_splits + pe / S) << 32) |
+                                                    (long long)(unsigned)(rb + 1));
+                        }
+                    }
+                }
+                for (int tp0 = st0; tp0 < st1_own;) {
                     const int rj = tp0 / S;
-                    const int tp1 = min((rj + 1) * S, st1);
+                    const int tp1 = min((rj + 1) * S, st1_own);
                     const int dp = (tp0 == st0 && dest >= 0 && tp0 != rj * S) ? dest : -1;
                     int hw[4] = {0, 0, (int)taint, 0};
                     if (lane < rows && rrow < A.R) {
@@ -645,7 +669,7 @@ struct Producer {
                         hw[1] = (int)(lane >= 4 ? (f << sh) : 0u);
                         hw[3] = (int)(((f & FDPP_FLAG_OUT) && ((taint >> lane) & 1u)) ? (1u << lane) : 0u);
                     }
-#pragma unroll
+    #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
                         hw[0] |= __shfl_xor_sync(0xffffffffu, hw[0], o);
                         hw[1] |= __shfl_xor_sync(0xffffffffu, hw[1], o);

@@ -72,9 +72,10 @@ def test_max_splits_and_workspace_size():
     ws = F.fdpp_workspace_size(p)
     # partials o (d floats), l, m and a flag byte per split slot and per run slot (G = 4 rows
     # for each of FDPP_TC_MAX_PARTS parts plus one per (sequence, kv head)), the fallback lists
-    # (8 lists of 32-byte entries, one per unit and per part each), plus header and plan
+    # (8 lists of 32-byte entries, one per split piece: units, parts and (sequence, kv head)
+    # pairs), plus header and plan
     slots = 8 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8) * 4
-    lists = 8 * (8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    lists = 8 * (8 * 8 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws <= fixed + 64 * 1024
     assert ws % 256 == 0
@@ -92,14 +93,14 @@ def test_workspace_size_with_row_groups():
     p = _gqa_params(q_tokens=16)
     ws = F.fdpp_workspace_size(p)
     slots = 8 * 16 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 8
-    lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws <= fixed + 64 * 1024
     # 12 rows: two groups (8 + 4); run slots still 8 rows, lists twice the one-group count
     p12 = _gqa_params(q_tokens=3)
     ws12 = F.fdpp_workspace_size(p12)
     slots = 8 * 3 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 8
-    lists = 8 * (8 * 8 * 2 * 8 + F.FDPP_TC_MAX_PARTS) * 32
+    lists = 8 * (8 * 8 * 2 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws12 <= fixed + 64 * 1024
 
