@@ -354,6 +354,10 @@ def run_fdpp(args, dist: Dist):
     wl = W.ALL[args.config]
     if dist.world > 1:
         wl = wl.replace(seed=wl.seed + 1000 * dist.rank)      # each rank its own batch
+    # the heuristic dataflow's table, measured offline on this GPU model (attn_lut.py): kernel
+    # choice for kernel 0, split scheduler targets for split_len 0
+    from split_kv_async_gb300 import attn_lut
+    lut_rows = attn_lut.apply()
     inp = W.generate(wl)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
@@ -587,7 +591,10 @@ def run_fdpp(args, dist: Dist):
                    "seq_len": wl.seq_len if wl.seq_len else list(wl.seq_len_range),
                    "paged": wl.paged, "block_size": wl.block_size if wl.paged else None,
                    "q_tokens": max(1, wl.q_tokens),
-                   "split_len": diag["split_len"], "phi": wl.phi, "window": [wl.lo, wl.hi],
+                   "split_len": diag["split_len"],
+                   "split_len_from": ("lookup table" if lut_rows and split_len == 0 else
+                                      "scheduler defaults" if split_len == 0 else "workload"),
+                   "phi": wl.phi, "window": [wl.lo, wl.hi],
                    "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
                    "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "
                                 f"4x L2 {l2 / 2**20:.0f} MiB); no flush",

@@ -125,12 +125,29 @@ typedef struct fdpp_params {
                                 fdpp_score_ranges; more is FDPP_ERR_UNSUPPORTED. */
 } fdpp_params;
 
-/* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over
- * FDPP_AUTO_UNITS_PER_SM * num_sms units, round up to a multiple of FDPP_AUTO_GRANULE (or of
- * block_size when larger), clamp to [FDPP_AUTO_MIN_SPLIT, max_seq_len rounded up]. */
+/* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over units_per_sm * num_sms
+ * units, round up to a multiple of FDPP_AUTO_GRANULE (or of block_size when larger), clamp to
+ * [min_split, max_seq_len rounded up]. units_per_sm and min_split come from the dataflow table
+ * (fdpp_attn_set_lut) for the call's shape, else FDPP_AUTO_UNITS_PER_SM and FDPP_AUTO_MIN_SPLIT. */
 #define FDPP_AUTO_UNITS_PER_SM 4
 #define FDPP_AUTO_GRANULE 64
 #define FDPP_AUTO_MIN_SPLIT 256
+
+/* One row of the heuristic dataflow table for decode attention (opt.ai.kr "FlashDecoding++
+ * async softmax -- theory", sections 2(3) and 4: the configuration is taken per shape range
+ * from a table measured offline, instead of one static choice for every shape). A call uses the
+ * first row whose ranges hold its shape: batch <= max_batch, max_seq_len <= max_seq_len and
+ * rows per kv head (q_tokens * Hq / Hkv) <= max_rows. */
+typedef struct fdpp_attn_lut_row {
+    int max_batch;           /* >= 1 */
+    int max_seq_len;         /* >= 1 */
+    int max_rows;            /* >= 1 */
+    int kernel;              /* fdpp_kernel for calls with kernel == FDPP_KERNEL_AUTO; AUTO keeps
+                                the default rule, and a kernel that cannot take the call too */
+    int units_per_sm;        /* split_len == 0: units per SM the split length aims at, in [1, 64] */
+    int min_split;           /* split_len == 0: least split length, a multiple of
+                                FDPP_AUTO_GRANULE in [FDPP_AUTO_MIN_SPLIT, 1 << 20] */
+} fdpp_attn_lut_row;
 
 typedef struct fdpp_diag {
     int32_t split_len;            /* S used by the last call on this workspace */
@@ -229,6 +246,17 @@ fdpp_status fdpp_decode_attn_noalloc(const void* q, const void* k_cache, const v
  * device-side problems (FDPP_ERRBIT_*) and the fallback decisions, as a workspace caller can. */
 fdpp_status fdpp_read_diag_noalloc(const fdpp_params* p, fdpp_diag* diag, uint8_t* flags_host,
                                    int32_t* nsplit_host);
+
+/* Installs the dataflow table (copied; process-wide, for every device; n == 0 removes it, and
+ * the defaults apply again). Host only, no CUDA call. FDPP_ERR_INVALID_ARG for a row outside the
+ * ranges documented in fdpp_attn_lut_row (the table is then left as it was). */
+fdpp_status fdpp_attn_set_lut(const fdpp_attn_lut_row* rows, int n);
+
+/* What a call with `p` would use (host only, no CUDA call): the kernel (FDPP_KERNEL_TENSOR or
+ * FDPP_KERNEL_SIMT, after the table and the default rule), and the units_per_sm and min_split of
+ * the split scheduler (used when p->split_len == 0). Any output pointer may be NULL. */
+fdpp_status fdpp_attn_auto_choice(const fdpp_params* p, int* kernel, int* units_per_sm,
+                                  int* min_split);
 
 /* Score range of every row-split, for choosing phi in advance (opt.ai.kr "FlashDecoding++ async
  * softmax -- theory", section 3: phi is set by observing the score distribution beforehand).

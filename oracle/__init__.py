@@ -265,6 +265,27 @@ def split_len(seq_lens, num_kv_heads, max_seq_len, split_len_req, num_sms, units
                             num_sms, units_per_sm, granule, min_split)
 
 
+def dataflow_choice(rows, batch, max_seq_len, rows_per_kv_head, bf16,
+                    default_units=4, default_min_split=256):
+    """The heuristic dataflow table's choice for one call shape (opt.ai.kr "FlashDecoding++
+    async softmax -- theory", s4: the configuration comes from a table measured in advance, per
+    shape range). rows: (max_batch, max_seq_len, max_rows, kernel, units_per_sm, min_split); the
+    first row whose ranges hold (batch, max_seq_len, rows_per_kv_head) applies. Kernel ids: 0 no
+    preference, 1 tensor cores (bf16, at most 64 rows per kv head), 2 CUDA cores (at most 16);
+    without a usable preference the tensor kernel is taken where it applies, else CUDA cores.
+    Returns (kernel, units_per_sm, min_split)."""
+    kernel, units, min_split = 0, default_units, default_min_split
+    for (mb, ml, mr, k, u, m) in rows:
+        if batch <= mb and max_seq_len <= ml and rows_per_kv_head <= mr:
+            kernel, units, min_split = k, u, m
+            break
+    tensor_ok = bf16 and rows_per_kv_head <= 64
+    simt_ok = rows_per_kv_head <= 16
+    if not ((kernel == 1 and tensor_ok) or (kernel == 2 and simt_ok)):
+        kernel = 1 if tensor_ok else 2
+    return kernel, units, min_split
+
+
 def plan(seq_lens, num_kv_heads, max_seq_len, S):
     """Returns (nsplit int32 [B], split_off int32 [B+1], n_units)."""
     lib = _load()

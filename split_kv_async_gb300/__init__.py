@@ -33,7 +33,7 @@ FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT = 4, 64, 256
 EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fdpp_decode_attn",
             "fdpp_decode_attn_timed", "fdpp_decode_attn_noalloc", "fdpp_score_ranges",
             "fdpp_pick_phi", "fdpp_read_diag", "fdpp_read_diag_noalloc", "fdpp_status_str",
-            "fdpp_last_error",
+            "fdpp_last_error", "fdpp_attn_set_lut", "fdpp_attn_auto_choice",
             "fdpp_flat_gemm_split_k", "fdpp_flat_gemm_workspace_size", "fdpp_flat_gemm",
             "fdpp_flat_gemm_set_lut", "fdpp_flat_gemm_read_error")
 FDPP_GEMM_MAX_M = 128
@@ -78,6 +78,11 @@ class fdpp_diag(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class fdpp_attn_lut_row(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in ("max_batch", "max_seq_len", "max_rows", "kernel",
+                                                  "units_per_sm", "min_split")]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -107,6 +112,11 @@ def _load() -> ctypes.CDLL:
     lib.fdpp_read_diag.restype = ctypes.c_int
     lib.fdpp_read_diag_noalloc.argtypes = [P, ctypes.POINTER(fdpp_diag), vp, vp]
     lib.fdpp_read_diag_noalloc.restype = ctypes.c_int
+    lib.fdpp_attn_set_lut.argtypes = [ctypes.POINTER(fdpp_attn_lut_row), ctypes.c_int]
+    lib.fdpp_attn_set_lut.restype = ctypes.c_int
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.fdpp_attn_auto_choice.argtypes = [P, ip, ip, ip]
+    lib.fdpp_attn_auto_choice.restype = ctypes.c_int
     lib.fdpp_status_str.argtypes = [ctypes.c_int]
     lib.fdpp_status_str.restype = ctypes.c_char_p
     lib.fdpp_last_error.argtypes = []
@@ -268,6 +278,23 @@ def fdpp_read_diag_noalloc(p: fdpp_params, want_flags=False, want_nsplit=False):
                                       None if ns is None else ns.ctypes.data),
            "fdpp_read_diag_noalloc")
     return d.as_dict(), flags, ns
+
+
+def fdpp_attn_set_lut(rows) -> None:
+    """rows: (max_batch, max_seq_len, max_rows, kernel, units_per_sm, min_split) tuples, first
+    match wins; an empty list removes the table."""
+    arr = (fdpp_attn_lut_row * max(1, len(rows)))()
+    for i, r in enumerate(rows):
+        arr[i] = fdpp_attn_lut_row(*[int(x) for x in r])
+    _check(lib.fdpp_attn_set_lut(arr if rows else None, len(rows)), "fdpp_attn_set_lut")
+
+
+def fdpp_attn_auto_choice(p: fdpp_params):
+    """(kernel, units_per_sm, min_split) a call with `p` uses (host only)."""
+    k, u, m = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.fdpp_attn_auto_choice(ctypes.byref(p), ctypes.byref(k), ctypes.byref(u),
+                                     ctypes.byref(m)), "fdpp_attn_auto_choice")
+    return k.value, u.value, m.value
 
 
 def fdpp_status_str(status: int) -> str:

@@ -164,6 +164,44 @@ WsLayout layout_of(const fdpp_params& p)
 
 bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
+// The heuristic dataflow table of decode attention (fdpp_attn_set_lut): process-wide, copied in.
+std::mutex g_lut_mutex;
+std::vector<fdpp_attn_lut_row> g_lut;
+
+struct AutoChoice {
+    int kernel, units, min_split;
+};
+
+// The kernel and split-scheduler parameters a call with `p` uses: the first table row whose
+// ranges hold the shape, else the defaults; a kernel named by the table that cannot take the
+// call (dtype, rows per kv head) leaves the default rule.
+AutoChoice auto_choice(const fdpp_params& p)
+{
+    const int R = q_tokens_of(p) * (p.num_q_heads / p.num_kv_heads);
+    const bool tc_ok = p.dtype == FDPP_BF16 && R <= TC_MAX_ROWS;
+    const bool simt_ok = R <= SIMT_MAX_GROUP;
+    AutoChoice c{p.kernel, FDPP_AUTO_UNITS_PER_SM, FDPP_AUTO_MIN_SPLIT};
+    int lut_kernel = FDPP_KERNEL_AUTO;
+    {
+        std::lock_guard<std::mutex> lk(g_lut_mutex);
+        for (const fdpp_attn_lut_row& r : g_lut) {
+            if (p.batch <= r.max_batch && p.max_seq_len <= r.max_seq_len && R <= r.max_rows) {
+                lut_kernel = r.kernel;
+                c.units = r.units_per_sm;
+                c.min_split = r.min_split;
+                break;
+            }
+        }
+    }
+    if (c.kernel == FDPP_KERNEL_AUTO) {
+        if ((lut_kernel == FDPP_KERNEL_TENSOR && tc_ok) || (lut_kernel == FDPP_KERNEL_SIMT && simt_ok))
+            c.kernel = lut_kernel;
+        else
+            c.kernel = tc_ok ? FDPP_KERNEL_TENSOR : FDPP_KERNEL_SIMT;
+    }
+    return c;
+}
+
 struct DeviceInfo {
     bool valid = false;
     int sms = 0, smem_per_sm = 0, smem_per_block = 0;
@@ -295,6 +333,9 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.hi = p->hi;
     a.mode = p->mode;
     a.kernel_id = kernel;
+    const AutoChoice ch = auto_choice(*p);
+    a.auto_units = ch.units;
+    a.auto_min = ch.min_split;
     return a;
 }
 
@@ -342,6 +383,39 @@ const char* fdpp_status_str(fdpp_status s)
 }
 
 const char* fdpp_last_error(void) { return g_last_error.c_str(); }
+
+fdpp_status fdpp_attn_set_lut(const fdpp_attn_lut_row* rows, int n)
+{
+    if (n < 0 || (n > 0 && !rows)) return fail(FDPP_ERR_INVALID_ARG, "rows is NULL or n < 0");
+    if (n > 4096) return fail(FDPP_ERR_INVALID_ARG, "at most 4096 table rows (got %d)", n);
+    for (int i = 0; i < n; ++i) {
+        const fdpp_attn_lut_row& r = rows[i];
+        if (r.max_batch < 1 || r.max_seq_len < 1 || r.max_rows < 1)
+            return fail(FDPP_ERR_INVALID_ARG, "table row %d: ranges must be >= 1", i);
+        if (r.kernel < FDPP_KERNEL_AUTO || r.kernel > FDPP_KERNEL_SIMT)
+            return fail(FDPP_ERR_INVALID_ARG, "table row %d: unknown kernel %d", i, r.kernel);
+        if (r.units_per_sm < 1 || r.units_per_sm > 64)
+            return fail(FDPP_ERR_INVALID_ARG, "table row %d: units_per_sm must be in [1, 64]", i);
+        if (r.min_split < FDPP_AUTO_MIN_SPLIT || r.min_split > (1 << 20) || r.min_split % FDPP_AUTO_GRANULE)
+            return fail(FDPP_ERR_INVALID_ARG,
+                        "table row %d: min_split must be a multiple of %d in [%d, %d]", i,
+                        FDPP_AUTO_GRANULE, FDPP_AUTO_MIN_SPLIT, 1 << 20);
+    }
+    std::lock_guard<std::mutex> lk(g_lut_mutex);
+    g_lut.assign(rows, rows + n);
+    return FDPP_OK;
+}
+
+fdpp_status fdpp_attn_auto_choice(const fdpp_params* p, int* kernel, int* units_per_sm, int* min_split)
+{
+    const fdpp_status st = check_params(p);
+    if (st != FDPP_OK) return st;
+    const AutoChoice c = auto_choice(*p);
+    if (kernel) *kernel = c.kernel;
+    if (units_per_sm) *units_per_sm = c.units;
+    if (min_split) *min_split = c.min_split;
+    return FDPP_OK;
+}
 
 int fdpp_max_splits(const fdpp_params* p)
 {
@@ -401,8 +475,7 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     const int G = p->num_q_heads / p->num_kv_heads;
     const int R = q_tokens_of(*p) * G;
     const bool tc_ok = p->dtype == FDPP_BF16 && R <= TC_MAX_ROWS;
-    int kernel = p->kernel;
-    if (kernel == FDPP_KERNEL_AUTO) kernel = tc_ok ? FDPP_KERNEL_TENSOR : FDPP_KERNEL_SIMT;
+    const int kernel = auto_choice(*p).kernel;
     if (kernel == FDPP_KERNEL_SIMT && R > SIMT_MAX_GROUP)
         return fail(FDPP_ERR_UNSUPPORTED, "SIMT kernel needs at most %d query rows per kv head (got %d)",
                     SIMT_MAX_GROUP, R);

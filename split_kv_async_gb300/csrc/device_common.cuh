@@ -29,12 +29,12 @@ __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
 // Split length: the caller's S when > 0, otherwise spread sum_b L_b * Hkv over
-// FDPP_AUTO_UNITS_PER_SM * num_sms units, rounded up to the granule and clamped to
-// [FDPP_AUTO_MIN_SPLIT, max_seq_len rounded up].
+// auto_units * num_sms units, rounded up to the granule and clamped to [auto_min, max_seq_len
+// rounded up] (auto_units and auto_min from the dataflow table, else the defaults).
 __device__ __forceinline__ int auto_split_len(long long total_tokens, const KernelArgs& a)
 {
     if (a.split_req > 0) return a.split_req;
-    long long units = (long long)FDPP_AUTO_UNITS_PER_SM * (long long)a.num_sms;
+    long long units = (long long)a.auto_units * (long long)a.num_sms;
     if (units < 1) units = 1;
     long long gran = FDPP_AUTO_GRANULE;
     if (a.block_table && a.block_size > gran) gran = a.block_size;
@@ -42,8 +42,9 @@ __device__ __forceinline__ int auto_split_len(long long total_tokens, const Kern
     long long S = (pairs + units - 1) / units;
     S = (S + gran - 1) / gran * gran;
     long long hi = ((long long)a.max_seq_len + gran - 1) / gran * gran;
-    if (hi < FDPP_AUTO_MIN_SPLIT) hi = FDPP_AUTO_MIN_SPLIT;
-    if (S < FDPP_AUTO_MIN_SPLIT) S = FDPP_AUTO_MIN_SPLIT;
+    const long long lo = a.auto_min;
+    if (hi < lo) hi = lo;
+    if (S < lo) S = lo;
     if (S > hi) S = hi;
     return (int)S;
 }

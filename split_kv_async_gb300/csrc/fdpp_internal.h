@@ -95,6 +95,8 @@ struct KernelArgs {
     // last: fields added in the middle move the others' parameter offsets and change the
     // kernels' code.)
     int NRG, Rg, Hv;
+    // split_len == 0: the split scheduler's units per SM and least split length (dataflow table)
+    int auto_units, auto_min;
 };
 
 // Query rows per kv head (R = Tq * G): the tensor kernel takes 8 rows per unit (the columns of one

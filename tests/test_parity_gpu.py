@@ -345,6 +345,46 @@ def test_auto_split_len_matches_replay(name):
         H.assert_parity(got, ref, f"{name} auto split kernel {kernel}")
 
 
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny"])
+def test_dataflow_table_sets_kernel_and_split_as_replayed(name):
+    """split_len = 0 and kernel AUTO with the heuristic dataflow table installed: the kernel,
+    units per SM and least split the table gives for the shape (replayed by the oracle's table
+    rule) set the split length, which the device's plan must equal bit for bit, and the result
+    still matches the oracle. Three tables: the one measured on GB300, and two that force each
+    kernel with other split targets."""
+    import json
+    import torch
+    from split_kv_async_gb300 import attn_lut
+    inp, dinp = _inputs(name)
+    ref = H.oracle_out(inp)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with open(attn_lut.DEFAULT_TABLE) as f:
+        measured = [tuple(r) for r in json.load(f)["rows"]]
+    open_ = 1 << 30
+    tables = [measured, [(open_, open_, 64, F.FDPP_KERNEL_SIMT, 16, 320)],
+              [(open_, open_, 64, F.FDPP_KERNEL_TENSOR, 1, 512)]]
+    try:
+        for rows in tables:
+            F.fdpp_attn_set_lut(rows)
+            p = H.params_for(inp, split_len=0)
+            R = inp.wl.group * max(1, inp.wl.q_tokens)
+            kern, units, min_split = oracle.dataflow_choice(
+                rows, p.batch, p.max_seq_len, R, inp.wl.dtype == W.BF16,
+                F.FDPP_AUTO_UNITS_PER_SM, F.FDPP_AUTO_MIN_SPLIT)
+            got, diag, _, ns, _ = H.run(dinp, split_len=0)
+            assert diag["kernel"] == kern
+            gran = max(F.FDPP_AUTO_GRANULE, inp.wl.block_size if inp.wl.paged else 0)
+            S = oracle.split_len(inp.seq_lens, inp.wl.num_kv_heads, p.max_seq_len, 0, sms,
+                                 units, gran, min_split)
+            assert diag["split_len"] == S
+            o_ns, _, o_units = oracle.plan(inp.seq_lens, inp.wl.num_kv_heads, p.max_seq_len, S)
+            np.testing.assert_array_equal(ns, o_ns)
+            assert diag["n_units"] == o_units
+            H.assert_parity(got, ref, f"{name} table {rows[:1]}")
+    finally:
+        F.fdpp_attn_set_lut([])
+
+
 @pytest.mark.parametrize("name,stages,ctas", [("paged_bs16", 2, 1), ("paged_bs16", 3, 2),
                                                ("paged_bs16", 6, 1), ("gqa_ragged", 2, 2),
                                                ("gqa_ragged", 6, 1), ("gqa_d64", 12, 1),
