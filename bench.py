@@ -66,6 +66,8 @@ def parse_args(argv=None):
     ap.add_argument("--tc-stages", type=int, default=0)
     ap.add_argument("--tc-ctas", type=int, default=0)
     ap.add_argument("--tc-prefetch", type=int, default=0)
+    ap.add_argument("--tc-mma", type=int, default=0,
+                    help="tensor kernel build for > 8 rows per kv head (0 auto, 1 mma.sync, 2 tcgen05)")
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
     ap.add_argument("--split-k", type=int, default=0, help="flat GEMM configs: split_k (0 = auto)")
     ap.add_argument("--noalloc", action="store_true",
@@ -215,8 +217,8 @@ def measured_peaks():
 
 def split_kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("split_tc.cu", "split_simt.cu", "combine.cu", "device_common.cuh",
-                 "fdpp_internal.h"):
+    for name in ("split_tc.cu", "split_um.cu", "split_tc_common.cuh", "split_simt.cu", "combine.cu",
+                 "device_common.cuh", "tcgen05.cuh", "fdpp_internal.h"):
         with open(os.path.join(ROOT, "split_kv_async_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -224,7 +226,7 @@ def split_kernel_source_hash():
 
 def gemm_kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("flat_gemm.cu", "device_common.cuh", "fdpp_internal.h"):
+    for name in ("flat_gemm.cu", "device_common.cuh", "tcgen05.cuh", "fdpp_internal.h"):
         with open(os.path.join(ROOT, "split_kv_async_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -379,7 +381,7 @@ def run_fdpp(args, dist: Dist):
               max_seq_len=inp.max_seq_len, scale=wl.scale, phi=wl.phi, lo=wl.lo, hi=wl.hi,
               split_len=split_len, q_tokens=wl.q_tokens, mode=args.mode, kernel=args.kernel,
               tc_stages=args.tc_stages,
-              tc_ctas_per_sm=args.tc_ctas, tc_prefetch=args.tc_prefetch)
+              tc_ctas_per_sm=args.tc_ctas, tc_prefetch=args.tc_prefetch, tc_mma=args.tc_mma)
     if wl.paged:
         kw.update(block_size=wl.block_size, max_blocks_per_seq=inp.max_blocks_per_seq,
                   num_kv_blocks=inp.num_kv_blocks,
@@ -596,6 +598,7 @@ def run_fdpp(args, dist: Dist):
                                       "scheduler defaults" if split_len == 0 else "workload"),
                    "phi": wl.phi, "window": [wl.lo, wl.hi],
                    "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
+                   "tensor_build": {0: None, 1: "mma.sync", 2: "tcgen05"}.get(diag.get("tc_build", 0)),
                    "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "
                                 f"4x L2 {l2 / 2**20:.0f} MiB); no flush",
                    "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single",

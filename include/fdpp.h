@@ -100,7 +100,7 @@ typedef struct fdpp_params {
     int block_size;          /* paged only: tokens per block, a power of two in [16, 256] */
     int max_blocks_per_seq;  /* paged only: row length of block_table */
     int num_kv_blocks;       /* paged only: number of blocks in the K (and V) pool */
-    float scale;             /* score scale, usually 1/sqrt(d) */
+    float scale;             /* score scale, positive and finite, usually 1/sqrt(d) */
     float phi;               /* unified max, in units of the scaled score s */
     float lo, hi;            /* safe window: a score is inside iff lo <= s - phi <= hi */
     int split_len;           /* S > 0: tokens per split (paged: a multiple of block_size).
@@ -119,11 +119,23 @@ typedef struct fdpp_params {
                                 so query token i sees the keys t < L_b - Tq + 1 + i (a short
                                 prefill chunk or a speculative-decoding step). q and out are then
                                 [B][Tq][Hq][d]. Query rows per kv head, R = Tq * Hq / Hkv: at
-                                most 64 for the tensor kernel (more than 8 go in groups of 8,
-                                each streaming the kv head's K/V; the groups' reads of a tile
-                                mostly meet in L2), at most 16 for the SIMT kernel and for
-                                fdpp_score_ranges; more is FDPP_ERR_UNSUPPORTED. */
+                                most 64 for the tensor kernel, at most 16 for the SIMT kernel and
+                                for fdpp_score_ranges; more is FDPP_ERR_UNSUPPORTED. */
+    int tc_mma;              /* tensor kernel with more than 8 query rows per kv head (fdpp_tc_mma):
+                                which build takes them */
 } fdpp_params;
+
+/* Builds of the tensor kernel for more than 8 query rows per kv head. */
+typedef enum fdpp_tc_mma {
+    FDPP_TC_MMA_AUTO = 0,        /* TCGEN05 where it applies (bf16, d = 128, tc_ctas_per_sm 0 or
+                                    1), else MMA_SYNC */
+    FDPP_TC_MMA_SYNC = 1,        /* mma.sync m16n8k16: the rows in groups of 8, each group a unit
+                                    that streams the kv head's K/V (the groups' reads of a tile
+                                    mostly meet in L2); two CTAs per SM */
+    FDPP_TC_MMA_TCGEN05 = 2      /* tcgen05 tensor cores, accumulators in tensor memory: all R
+                                    rows in one unit, K/V streamed once; one CTA per SM; bf16 and
+                                    d = 128 only (else FDPP_ERR_UNSUPPORTED) */
+} fdpp_tc_mma;
 
 /* Split length chosen by split_len == 0: spread sum_b L_b * Hkv over units_per_sm * num_sms
  * units, round up to a multiple of FDPP_AUTO_GRANULE (or of block_size when larger), clamp to
@@ -158,6 +170,8 @@ typedef struct fdpp_diag {
     int64_t n_recomputed_row_splits; /* (b, h, j) with FDPP_FLAG_RECOMPUTED */
     uint32_t error_bits;          /* FDPP_ERRBIT_* since the last fdpp_workspace_init */
     int32_t kernel;               /* fdpp_kernel that ran last (1 tensor, 2 SIMT) */
+    int32_t tc_build;             /* tensor kernel: the build that ran (FDPP_TC_MMA_SYNC, or
+                                     FDPP_TC_MMA_TCGEN05); 0 for the SIMT kernel */
 } fdpp_diag;
 
 /* Partial slots per (b, h) that a workspace for `p` holds: ceil(max_seq_len / S) for a fixed
@@ -169,6 +183,11 @@ int fdpp_max_splits(const fdpp_params* p);
  * of one sequence's kv head is a run, which leaves one partial (in the phi frame, summed across
  * its splits) in a run slot of the workspace; window decisions stay per split. */
 #define FDPP_TC_MAX_PARTS 512
+
+/* The tensor kernel's tcgen05 build (more than 8 query rows per kv head, bf16, d = 128) runs at
+ * most this many CTAs, one per SM, so at most this many parts; its run slots hold all R rows of a
+ * kv head. */
+#define FDPP_TC_UM_MAX_CTAS 256
 
 /* Bytes of device workspace fdpp_decode_attn needs for `p` (written to *bytes). The workspace
  * holds the split plan, the per-split partials (o: fp32 [B][Tq][Hq][max_splits][d]; l, m: fp32

@@ -24,6 +24,7 @@ FDPP_OK, FDPP_ERR_INVALID_ARG, FDPP_ERR_UNSUPPORTED, FDPP_ERR_WORKSPACE, FDPP_ER
 FDPP_F32, FDPP_BF16 = 0, 1
 FDPP_MODE_NORMAL, FDPP_MODE_FORCE_FAST, FDPP_MODE_FORCE_ONLINE = 0, 1, 2
 FDPP_KERNEL_AUTO, FDPP_KERNEL_TENSOR, FDPP_KERNEL_SIMT = 0, 1, 2
+FDPP_TC_MMA_AUTO, FDPP_TC_MMA_SYNC, FDPP_TC_MMA_TCGEN05 = 0, 1, 2
 FDPP_FLAG_OUT, FDPP_FLAG_ABOVE, FDPP_FLAG_BELOW, FDPP_FLAG_NAN, FDPP_FLAG_RECOMPUTED = 1, 2, 4, 8, 16
 FDPP_FLAG_SLOT = 32
 FDPP_ERRBIT_SEQ_LEN, FDPP_ERRBIT_BLOCK_TABLE, FDPP_ERRBIT_TIMEOUT = 1, 2, 4
@@ -39,6 +40,7 @@ EXPORTED = ("fdpp_max_splits", "fdpp_workspace_size", "fdpp_workspace_init", "fd
 FDPP_GEMM_MAX_M = 128
 FDPP_NOALLOC_WORKSPACE_BYTES = 16 << 20
 FDPP_TC_MAX_PARTS = 512
+FDPP_TC_UM_MAX_CTAS = 256
 
 
 class FdppError(RuntimeError):
@@ -62,7 +64,7 @@ class fdpp_params(ctypes.Structure):
         ("split_len", ctypes.c_int), ("mode", ctypes.c_int), ("kernel", ctypes.c_int),
         ("tc_stages", ctypes.c_int), ("tc_ctas_per_sm", ctypes.c_int),
         ("tc_prefetch", ctypes.c_int), ("phi_heads", ctypes.c_void_p),
-        ("q_tokens", ctypes.c_int),
+        ("q_tokens", ctypes.c_int), ("tc_mma", ctypes.c_int),
     ]
 
 
@@ -72,6 +74,7 @@ class fdpp_diag(ctypes.Structure):
         ("n_units", ctypes.c_int64), ("n_flagged_row_splits", ctypes.c_int64),
         ("n_flagged_units", ctypes.c_int64), ("n_recomputed_row_splits", ctypes.c_int64),
         ("error_bits", ctypes.c_uint32), ("kernel", ctypes.c_int32),
+        ("tc_build", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:
@@ -146,13 +149,15 @@ def _check(status: int, where: str) -> None:
 def make_params(*, batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, scale,
                 phi=0.0, lo=-30.0, hi=10.0, split_len=0, block_size=0, max_blocks_per_seq=0,
                 num_kv_blocks=0, mode=FDPP_MODE_NORMAL, kernel=FDPP_KERNEL_AUTO, tc_stages=0,
-                tc_ctas_per_sm=0, tc_prefetch=0, phi_heads=None, q_tokens=1) -> fdpp_params:
+                tc_ctas_per_sm=0, tc_prefetch=0, phi_heads=None, q_tokens=1,
+                tc_mma=FDPP_TC_MMA_AUTO) -> fdpp_params:
     """phi_heads: a float32 device tensor [num_q_heads] (or its address), or None. q_tokens:
-    query tokens per sequence (q and out are then [batch][q_tokens][num_q_heads][head_dim])."""
+    query tokens per sequence (q and out are then [batch][q_tokens][num_q_heads][head_dim]).
+    tc_mma: the tensor kernel's build for more than 8 query rows per kv head."""
     ph = phi_heads if phi_heads is None or isinstance(phi_heads, int) else phi_heads.data_ptr()
     return fdpp_params(batch, num_q_heads, num_kv_heads, head_dim, dtype, max_seq_len, block_size,
                        max_blocks_per_seq, num_kv_blocks, scale, phi, lo, hi, split_len, mode,
-                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch, ph, q_tokens)
+                       kernel, tc_stages, tc_ctas_per_sm, tc_prefetch, ph, q_tokens, tc_mma)
 
 
 def fdpp_max_splits(p: fdpp_params) -> int:

@@ -19,8 +19,9 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfdpp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cpp", "split_tc.cu", "split_simt.cu", "combine.cu", "no_alloc.cu", "flat_gemm.cu"]
-HEADERS = ["fdpp_internal.h", "device_common.cuh"]
+SOURCES = ["api.cpp", "split_tc.cu", "split_um.cu", "split_simt.cu", "combine.cu", "no_alloc.cu",
+           "flat_gemm.cu"]
+HEADERS = ["fdpp_internal.h", "device_common.cuh", "split_tc_common.cuh", "tcgen05.cuh"]
 
 
 def _nvcc() -> str:

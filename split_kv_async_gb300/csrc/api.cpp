@@ -72,6 +72,7 @@ fdpp_status check_params(const fdpp_params* p)
         !std::isfinite(p->hi))
         return fail(FDPP_ERR_INVALID_ARG, "scale, phi, lo and hi must be finite");
     if (!(p->lo <= p->hi)) return fail(FDPP_ERR_INVALID_ARG, "window needs lo <= hi");
+    if (!(p->scale > 0.f)) return fail(FDPP_ERR_INVALID_ARG, "scale must be positive (got %g)", (double)p->scale);
     if (p->mode < FDPP_MODE_NORMAL || p->mode > FDPP_MODE_FORCE_ONLINE)
         return fail(FDPP_ERR_INVALID_ARG, "unknown mode %d", p->mode);
     if (p->kernel < FDPP_KERNEL_AUTO || p->kernel > FDPP_KERNEL_SIMT)
@@ -86,6 +87,8 @@ fdpp_status check_params(const fdpp_params* p)
         return fail(FDPP_ERR_INVALID_ARG, "phi_heads must be 4-byte aligned");
     if (p->q_tokens < 0 || p->q_tokens > 64)
         return fail(FDPP_ERR_INVALID_ARG, "q_tokens must be in [0, 64] (got %d)", p->q_tokens);
+    if (p->tc_mma < FDPP_TC_MMA_AUTO || p->tc_mma > FDPP_TC_MMA_TCGEN05)
+        return fail(FDPP_ERR_INVALID_ARG, "unknown tc_mma %d", p->tc_mma);
     const int G = p->num_q_heads / p->num_kv_heads;
     const int R = q_tokens_of(*p) * G;
     if (R > TC_MAX_ROWS)
@@ -123,6 +126,20 @@ int row_groups_of(const fdpp_params& p)
     return (R + TC_MAX_GROUP - 1) / TC_MAX_GROUP;
 }
 
+// The tcgen05 build can take the call: bf16, d = 128, more than 8 query rows per kv head.
+bool um_applies(const fdpp_params& p)
+{
+    const int R = q_tokens_of(p) * (p.num_q_heads / p.num_kv_heads);
+    return p.dtype == FDPP_BF16 && p.head_dim == 128 && R > TC_MAX_GROUP && R <= TC_MAX_ROWS;
+}
+
+// The tensor kernel of this call is the tcgen05 build (tc_mma, and the geometry asked for).
+bool um_selected(const fdpp_params& p)
+{
+    if (!um_applies(p) || p.tc_mma == FDPP_TC_MMA_SYNC) return false;
+    return p.tc_mma == FDPP_TC_MMA_TCGEN05 || p.tc_ctas_per_sm <= 1;
+}
+
 size_t redo_capacity(const fdpp_params& p)
 {
     // split pieces: every split once, plus one more per run boundary (parts + heads)
@@ -150,10 +167,15 @@ WsLayout layout_of(const fdpp_params& p)
     w.o_part = off;  off = align256(off + slots * (size_t)p.head_dim * 4);
     // run slots of the tensor kernel: a run is a part's share of one (row group, sequence, kv
     // head), so there are fewer than parts + (row groups x sequences x kv heads) of them, each
-    // of min(R, 8) rows
+    // of min(R, 8) rows; the tcgen05 build's runs hold all R rows, with at most TC_UM_MAX_CTAS
+    // parts
     const size_t R = (size_t)q_tokens_of(p) * (size_t)(p.num_q_heads / p.num_kv_heads);
     const size_t runs = (size_t)TC_MAX_PARTS + (size_t)p.batch * p.num_kv_heads * row_groups_of(p);
-    const size_t xrows = runs * (R < TC_MAX_GROUP ? R : TC_MAX_GROUP);
+    size_t xrows = runs * (R < TC_MAX_GROUP ? R : TC_MAX_GROUP);
+    if (um_applies(p)) {
+        const size_t um_rows = ((size_t)TC_UM_MAX_CTAS + (size_t)p.batch * p.num_kv_heads) * R;
+        if (um_rows > xrows) xrows = um_rows;
+    }
     w.xf = off;      off = align256(off + xrows);
     w.xm = off;      off = align256(off + xrows * 4);
     w.xl = off;      off = align256(off + xrows * 4);
@@ -278,11 +300,32 @@ fdpp_status encode_kv_map(CUtensorMap* map, const void* base, const fdpp_params&
     return FDPP_OK;
 }
 
+// 4-D bf16 tensor map over q for the tcgen05 build: dims {d, Hq, Tq, B}, box {64, G, Tq, 1}, so
+// one load lands the R = Tq G query rows of a kv head (row i G + h = head g G + h of query token
+// i) as R rows of 128 bytes, 128-byte swizzled: the K-major B operand of S^T = K Q^T.
+fdpp_status encode_q_map(CUtensorMap* map, const void* q, const fdpp_params& p)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    fdpp_status st = tensor_map_encoder(enc);
+    if (st != FDPP_OK) return st;
+    const cuuint64_t D = (cuuint64_t)p.head_dim, Hq = (cuuint64_t)p.num_q_heads;
+    const cuuint64_t Tq = (cuuint64_t)q_tokens_of(p);
+    cuuint64_t dims[4] = {D, Hq, Tq, (cuuint64_t)p.batch};
+    cuuint64_t strides[3] = {D * 2, Hq * D * 2, Tq * Hq * D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)(p.num_q_heads / p.num_kv_heads), (cuuint32_t)Tq, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FDPP_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (%d)", (int)r);
+    return FDPP_OK;
+}
+
 // Everything the kernels of one call need: pointers into the caller's buffers and workspace,
 // and the shape.
 KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace, const void* q,
                        const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       const int32_t* seq_lens, void* out, int num_sms, int kernel)
+                       const int32_t* seq_lens, void* out, int num_sms, int kernel, bool um = false)
 {
     const fdpp_params* p = &P;
     const bool paged = block_table != nullptr;
@@ -315,8 +358,9 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     a.G = G;
     a.Tq = q_tokens_of(*p);
     a.R = a.Tq * G;
-    a.NRG = row_groups_of(*p);
-    a.Rg = a.R < TC_MAX_GROUP ? a.R : TC_MAX_GROUP;
+    // the tcgen05 build takes all R rows of a kv head in one unit: one row group of R rows
+    a.NRG = um ? 1 : row_groups_of(*p);
+    a.Rg = um ? a.R : (a.R < TC_MAX_GROUP ? a.R : TC_MAX_GROUP);
     a.Hv = p->num_kv_heads * a.NRG;
     a.D = p->head_dim;
     a.max_seq_len = p->max_seq_len;
@@ -482,12 +526,18 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (kernel == FDPP_KERNEL_TENSOR && !tc_ok)
         return fail(FDPP_ERR_UNSUPPORTED, "tensor kernel needs bf16 and at most %d query rows per kv head",
                     TC_MAX_ROWS);
+    if (kernel == FDPP_KERNEL_TENSOR && p->tc_mma == FDPP_TC_MMA_TCGEN05 && !um_applies(*p))
+        return fail(FDPP_ERR_UNSUPPORTED,
+                    "tcgen05 build needs bf16, head_dim 128 and 9..%d query rows per kv head", TC_MAX_ROWS);
+    if (kernel == FDPP_KERNEL_TENSOR && p->tc_mma == FDPP_TC_MMA_TCGEN05 && p->tc_ctas_per_sm > 1)
+        return fail(FDPP_ERR_UNSUPPORTED, "tcgen05 build runs one CTA per SM");
+    const bool um = kernel == FDPP_KERNEL_TENSOR && um_selected(*p);
 
     DeviceInfo dev;
     if ((st = device_info(dev)) != FDPP_OK) return st;
 
     KernelArgs a = kernel_args(*p, w, workspace, q, k_cache, v_cache, block_table, seq_lens, out,
-                               dev.sms, kernel);
+                               dev.sms, kernel, um);
 
     const long long units_max = (long long)p->batch * p->num_kv_heads * w.max_splits;
     cudaStream_t s = (cudaStream_t)stream;
@@ -495,7 +545,24 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     int split_grid = 0;
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
-    if (kernel == FDPP_KERNEL_TENSOR) {
+    if (um) {
+        // tcgen05 build: one CTA per SM with the deepest ring that fits (or the one asked for)
+        const int budget = std::min(dev.smem_per_block, dev.smem_per_sm - 1024);
+        int ns = p->tc_stages > 0 ? p->tc_stages : 8;
+        while (ns >= 2 && split_um_smem_bytes(R, ns, p->batch) > budget) --ns;
+        if (ns < 2 || (p->tc_stages > 0 && ns != p->tc_stages))
+            return fail(FDPP_ERR_UNSUPPORTED, "no tcgen05 geometry fits (stages %d)", p->tc_stages);
+        a.nstage = ns;
+        a.pf_tiles = p->tc_prefetch > 0 ? p->tc_prefetch : 0;
+        CUtensorMap tk, tv, tq;
+        if ((st = encode_kv_map(&tk, k_cache, *p, paged)) != FDPP_OK) return st;
+        if ((st = encode_kv_map(&tv, v_cache, *p, paged)) != FDPP_OK) return st;
+        if ((st = encode_q_map(&tq, q, *p)) != FDPP_OK) return st;
+        long long grid = std::min<long long>(dev.sms, TC_UM_MAX_CTAS);
+        if (p->batch > TC_PLAN_SMEM_MAX_B && grid > units_max) grid = units_max;
+        split_grid = (int)grid;
+        e = launch_split_um(a, tk, tv, tq, (int)grid, split_um_smem_bytes(R, ns, p->batch), s);
+    } else if (kernel == FDPP_KERNEL_TENSOR) {
         const TcPlan plan = split_tc_plan(p->head_dim, R < TC_MAX_GROUP ? R : TC_MAX_GROUP, p->batch, p->tc_stages,
                                           p->tc_ctas_per_sm, dev.smem_per_sm, dev.smem_per_block);
         if (plan.nstage == 0)
@@ -691,6 +758,7 @@ fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const 
     diag->n_units = hdr[HDR_UNITS];
     diag->error_bits = (uint32_t)hdr[HDR_ERR];
     diag->kernel = hdr[HDR_KERNEL];
+    diag->tc_build = hdr[HDR_KERNEL] == FDPP_KERNEL_TENSOR ? hdr[HDR_TC_BUILD] : 0;
     const size_t G = Hq / (size_t)p->num_kv_heads;
     for (size_t b = 0; b < B; ++b) {
         const int n = ns[b] < 0 ? 0 : (ns[b] > (int)ms ? (int)ms : ns[b]);

@@ -25,6 +25,7 @@ enum {
                          //   zeroed by the combine kernel
     HDR_PARTS = 11,     // tensor kernel: parts P of the tile-balanced partition (0: none)
     HDR_TILES = 12,     // tensor kernel: 64-token tiles T of all units together
+    HDR_TC_BUILD = 13,  // tensor kernel build that ran: 1 mma.sync, 2 tcgen05 (split_um.cu)
     HDR_WORDS = 64
 };
 
@@ -146,5 +147,16 @@ TcPlan split_tc_plan(int head_dim, int group, int batch, int req_stages, int req
                      int smem_per_sm, int smem_per_block);
 // Tokens per TMA tile of the tensor-core kernel (box height of the contiguous tensor maps).
 constexpr int TC_TILE_TOKENS = 64;
+
+// tcgen05 build of the tensor kernel (split_um.cu): bf16, d = 128, more than 8 and at most
+// TC_MAX_ROWS query rows per kv head, all of them in one unit; one CTA per SM, at most
+// TC_UM_MAX_CTAS CTAs (so at most that many parts), rows padded to split_um_rows_padded(R).
+constexpr int TC_UM_MAX_CTAS = FDPP_TC_UM_MAX_CTAS;
+int split_um_rows_padded(int R);
+// Dynamic shared memory of one CTA with an `nstage`-deep ring (alignment slack included).
+int split_um_smem_bytes(int R, int nstage, int batch);
+// tq: the query tensor map ({d, Hq, Tq, B} bf16, box {64, G, Tq, 1}, 128-byte swizzle).
+cudaError_t launch_split_um(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tq, int grid, int smem_bytes, cudaStream_t s);
 
 }  // namespace fdpp

@@ -31,6 +31,7 @@
 
 #include "device_common.cuh"
 #include "fdpp_gemm.h"
+#include "tcgen05.cuh"
 
 namespace fdpp {
 namespace {
@@ -49,67 +50,6 @@ struct GemmArgs {
     int split_k, kb_total, n_tiles, nstage;
     uint32_t idesc;                      // tcgen05 instruction descriptor
 };
-
-// ---- tcgen05 ------------------------------------------------------------------------------
-
-// Shared-memory matrix descriptor of a K-major operand stored as TMA writes it with 128-byte
-// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), the leading
-// byte offset unused for swizzled K-major layouts (1), version 1, swizzle mode 2 (128 B).
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
-           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The mbarrier gets one arrival when every tcgen05 operation this thread issued before has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 16 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) ..).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar)
 {
@@ -545,7 +485,7 @@ fdpp_status fdpp_flat_gemm(const void* x, const void* w, void* y, int M, int N, 
     g.nstage = nstage;
     // kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1), both K-major,
     // N = Mp (bits 17-22 = N / 8), M = 128 (bits 24-28 = M / 16)
-    g.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(g.Mp >> 3) << 17) | ((uint32_t)(GB_N >> 4) << 24);
+    g.idesc = umma_idesc_bf16(GB_N, g.Mp, false);
 
     CUtensorMap tw, tx;
     if ((st = encode_2d(&tw, w, N, K, GB_N)) != FDPP_OK) return st;

@@ -1,0 +1,792 @@
+// split_um.cu -- per-split kernel for many query rows per kv head (a prefill chunk, a
+// speculative-decoding step, a wide GQA group: up to 64 rows) with bf16 K/V and d = 128, on the
+// tcgen05 tensor cores with the accumulators in tensor memory. combine.cu then sums the partials.
+//
+// What it computes is what split_tc.cu computes (opt.ai.kr "FlashDecoding++ async softmax --
+// theory", s1 and s3): for one unit (sequence b, kv head g, split j) and its R = Tq G query rows,
+//     s = scale <q_r, k_t>, p = exp(s - phi_r), l = sum p, o = sum p v_t      (fast pass)
+// in the unified-max frame, each score tested against lo <= s - phi <= hi, and a segment with a
+// row outside the window goes on the device-wide fallback list, whose pieces are computed again
+// in the rows' own max frame. Query token i of a sequence with L keys sees the keys
+// t < L - Tq + 1 + i. The partial of a segment (a part's share of one (sequence, kv head), see
+// split_tc_common.cuh) goes to a run slot or to the split's own slot, exactly as in split_tc.cu,
+// with all R rows of the kv head in one unit.
+//
+// Why another kernel. At R = 64 every 512 bytes of K and V read from HBM carry 49,152 FLOP
+// (q.K^T, and P.V with P split into bf16 hi and lo parts): 0.64 PFLOP/s at the copy rate, beyond
+// what m16n8k16 mma.sync issue keeps up with, well inside the tcgen05 rate.
+//
+// How. One CTA per SM, six warps:
+//   warp 4    the producer of split_tc_common.cuh: split plan, tile-balanced parts, 64-token K/V
+//             tiles by TMA into a ring of stages (128-byte swizzle), fallback-list drain. The
+//             unit's R query rows arrive by one 4-D TMA load per 64-wide half of d.
+//   warp 5    one thread issues the MMAs, the warp owns the tensor memory:
+//               S^T = K Q^T      M = 64 tokens, N = NP (R rounded up to 16, 32 or 64), K = d;
+//               O^T += V^T P^T   M = d = 128, N = NP, K = 64 tokens, P as bf16 hi and lo (two
+//                                MMAs per 16 tokens into one accumulator, ~16 mantissa bits);
+//             V^T is read MN-major straight from the TMA-landed V tile. S^T has two buffers in
+//             tensor memory (tile parity), O^T two (segment parity). tcgen05.commit arrives on
+//             mbarriers that release the K/V stage, the P buffer and the Q slot and wake the
+//             softmax warps. Inside a segment the P.V of tile i is issued after the q.K^T of
+//             tile i + 1, so the tensor core works on the next tile while the softmax warps finish
+//             this one.
+//   warps 0-3 softmax: warp w holds tokens 16w .. 16w + 15 of a tile (the 64-row accumulator
+//             puts token t in tensor-memory lane (t mod 16) + 32 floor(t / 16)); tcgen05.ld
+//             16x256b gives each thread 2 tokens x NP/4 rows in the mma.sync fragment order, so
+//             stmatrix.trans writes P^T as the K-major swizzled B operand, 16 bytes per row.
+//             The window test keeps per row and split the max, min and a NaN marker of s, and
+//             classifies once per split (the rounding of s - phi is monotone in s, so this is
+//             exactly the per-score test). At a segment's end each thread reads one d of O^T
+//             and writes it for every row.
+// Rows recomputed with online softmax (fallback pieces, and every segment in forced-online mode)
+// are streamed twice: first for the rows' maxima M, then for the sums in the frame M (the
+// accumulator in tensor memory is never rescaled). The result is the online softmax's up to
+// rounding.
+// Every wait is bounded; a wait that runs out sets FDPP_ERRBIT_TIMEOUT, the CTA lets its
+// copies and MMAs land, frees its tensor memory and exits.
+#include "split_tc_common.cuh"
+#include "tcgen05.cuh"
+
+namespace fdpp {
+namespace {
+
+constexpr int UM_D = 128;                 // head dim of this kernel
+constexpr int UM_NSW = 8;                 // softmax warps: two per tensor-memory lane quadrant
+constexpr int UM_PROD_WARP = UM_NSW;      // then the producer
+constexpr int UM_MMA_WARP = UM_NSW + 1;   // and the MMA warp
+constexpr int UM_THREADS = (UM_NSW + 2) * 32;
+constexpr int UM_FSLOTS = 8;              // window decisions of split pieces in flight
+constexpr int UM_MAX_ROWS = 64;
+constexpr int UM_NBARS = 19;              // barriers besides the stage ring's
+
+// Shared-memory layout (byte offsets from a 1024-byte aligned base).
+//   stages   nstage x (K tile, V tile), each two [64 token][64 d] boxes of 128-byte rows
+//   qring    2 slots x two [NP row][64 d] halves (the B operand of S^T)
+//   pbuf     2 buffers x (hi, lo) [NP row][64 token] (the B operand of O^T), used in turn by the
+//            tiles that have a P.V
+//   qhdr     2 segment headers
+//   fsw/fcnt per split piece in flight: each lane quadrant's flag nibble of every row (the two
+//            warps of a quadrant hold different rows), arrival count
+//   taint    the rows with a score outside the window, per segment parity (64-bit)
+//   xl/xm    per lane quadrant and row: the l sum of a segment, the max of a max pass
+struct UmLayout {
+    static constexpr bool UM = true;
+    int stage_bytes, kv_bytes, qslot_bytes, qhalf_bytes, p_bytes;
+    int stages, qring, pbuf, qhdr, fsw, fcnt, taint, xl, xm, plan, bars, misc, tslot, total;
+
+    __host__ __device__ static constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+    __host__ __device__ UmLayout(int NP, int nstage, int B)
+        : stage_bytes(2 * TILE * UM_D * 2), kv_bytes(TILE * UM_D * 2), qslot_bytes(2 * NP * 128),
+          qhalf_bytes(NP * 128), p_bytes(NP * 128), stages(0), qring(0), pbuf(0), qhdr(0), fsw(0),
+          fcnt(0), taint(0), xl(0), xm(0), plan(0), bars(0), misc(0), tslot(0), total(0)
+    {
+        qring = stages + nstage * stage_bytes;
+        pbuf = qring + 2 * qslot_bytes;
+        qhdr = pbuf + 2 * 2 * p_bytes;
+        fsw = qhdr + 2 * QHDR_BYTES;
+        fcnt = fsw + UM_FSLOTS * 4 * UM_MAX_ROWS;
+        taint = fcnt + UM_FSLOTS * 4;
+        xl = taint + 2 * 8;
+        xm = xl + 4 * UM_MAX_ROWS * 4;
+        plan = xm + 4 * UM_MAX_ROWS * 4;
+        const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 2 * B + 1 : 0) + 1;
+        bars = round_up(plan + plan_ints * 4, 8);
+        misc = bars + (2 * nstage + UM_NBARS) * 8;
+        tslot = misc + 16;
+        total = tslot + 16;
+    }
+};
+
+// The barriers besides the producer's ring (shared addresses). Arrival counts: sfull, pfree,
+// ofull and drain one commit; sfree, pready, ofree and wsync the four softmax warps.
+struct UmBars {
+    uint32_t sfull, sfree;     // [2] S^T buffer written / read out (tile parity)
+    uint32_t pready, pfree;    // [2] P^T buffer written / consumed by its MMAs (parity of the
+                               //     tiles that have a P.V: max passes have none)
+    uint32_t ofull, ofree;     // [2] O^T buffer complete / read out (segment parity)
+    uint32_t drain;            // every MMA of the CTA has completed
+    uint32_t wsync;            // the softmax warps meet (a bounded barrier among them)
+};
+
+// hi = bf16(p0, p1) rounded to nearest, lo = bf16 of what hi leaves out (p ~ hi + lo to ~16 bits)
+__device__ __forceinline__ void split_bf16x2(float p0, float p1, uint32_t& hi, uint32_t& lo)
+{
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+    hi = *reinterpret_cast<const uint32_t*>(&h2);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(p0 - h0, p1 - h1);
+}
+
+// 2^x (ex2.approx, flushing results below 2^-126 to zero)
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// ------------------------------------------------------------------------------------------
+// MMA warp
+// ------------------------------------------------------------------------------------------
+template <int NP>
+__device__ __forceinline__ void mma_warp(const KernelArgs& a, const UmLayout& lay, const uint8_t* sm,
+                                         uint32_t sbase, const Ring& rg, const UmBars& ub, uint32_t tmem,
+                                         volatile int* misc)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t IDESC_S = umma_idesc_bf16(64, NP, false);
+    constexpr uint32_t IDESC_O = umma_idesc_bf16(128, NP, true);
+    uint32_t stage = 0, phase = 0, qiter = 0, it = 0, pit = 0, obn = 0;
+    // the tile whose P.V is still to issue (pd_pit: its P buffer use)
+    bool pd_on = false, pd_first = false, pd_last = false;
+    uint32_t pd_pit = 0, pd_stage = 0, pd_ob = 0;
+
+    auto issue_o = [&]() -> bool {
+        const uint32_t sb = pd_pit & 1u;
+        if (!ring_wait(ub.pready + 8 * sb, (pd_pit >> 1) & 1u, misc, a)) return false;
+        if (pd_first && !ring_wait(ub.ofree + 8 * (pd_ob & 1u), ((pd_ob >> 1) & 1u) ^ 1u, misc, a)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t vb = sbase + lay.stages + pd_stage * lay.stage_bytes + lay.kv_bytes;
+            const uint32_t pb = sbase + lay.pbuf + sb * 2 * lay.p_bytes;
+            const uint32_t od = tmem + 2 * NP + (pd_ob & 1u) * NP;
+#pragma unroll
+            for (int kt = 0; kt < TILE / 16; ++kt) {
+                // V^T: d on M (two 64-wide halves TILE * 128 bytes apart), 16 tokens per k-step
+                const uint64_t av = sw128_mnmajor_desc(vb + kt * 2048, TILE * 128, 1024);
+                umma_bf16(od, av, sw128_kmajor_desc(pb + kt * 32), IDESC_O, (pd_first && kt == 0) ? 0u : 1u);
+                umma_bf16(od, av, sw128_kmajor_desc(pb + lay.p_bytes + kt * 32), IDESC_O, 1u);
+            }
+            umma_commit(ub.pfree + 8 * sb);
+            umma_commit(rg.empty + 8 * pd_stage);
+            if (pd_last) umma_commit(ub.ofull + 8 * (pd_ob & 1u));
+        }
+        __syncwarp();
+        pd_on = false;
+        return true;
+    };
+
+    for (;;) {
+        const uint32_t qs = qiter & 1u;
+        if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) break;
+        const int* hdr = reinterpret_cast<const int*>(sm + lay.qhdr + qs * QHDR_BYTES);
+        const int kind = hdr[H_KIND];
+        if (kind == KIND_END) break;
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], S = hdr[H_S];
+        const bool maxpass = hdr[H_PASS] == PASS_MAX;
+        ++qiter;
+        const uint32_t qb = sbase + lay.qring + qs * lay.qslot_bytes;
+        int tt = t0, se = (t0 / S + 1) * S;
+        bool first = true;
+        bool ok = true;
+        while (tt < t1) {
+            const int tend = min(min(tt + TILE, se), t1);
+            const uint32_t sb = it & 1u;
+            if (!ring_wait(rg.full + 8 * stage, phase, misc, a) ||
+                !ring_wait(ub.sfree + 8 * sb, ((it >> 1) & 1u) ^ 1u, misc, a)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
+                const uint32_t sd = tmem + sb * NP;
+#pragma unroll
+                for (int ks = 0; ks < UM_D / 16; ++ks) {
+                    // K and Q^T: K-major, 32 bytes per 16 of d, the second half of d in its own box
+                    umma_bf16(sd, sw128_kmajor_desc(kb + (ks >> 2) * (TILE * 128) + (ks & 3) * 32),
+                              sw128_kmajor_desc(qb + (ks >> 2) * lay.qhalf_bytes + (ks & 3) * 32), IDESC_S,
+                              ks > 0 ? 1u : 0u);
+                }
+                umma_commit(ub.sfull + 8 * sb);
+                if (tend == t1) umma_commit(rg.qempty + 8 * qs);   // the segment's Q slot is read
+                if (maxpass) umma_commit(rg.empty + 8 * stage);
+            }
+            __syncwarp();
+            if (pd_on && !issue_o()) { ok = false; break; }
+            if (!maxpass) {
+                pd_on = true;
+                pd_pit = pit++;
+                pd_stage = stage;
+                pd_first = first;
+                pd_last = tend == t1;
+                pd_ob = obn;
+            }
+            first = false;
+            ++it;
+            if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
+            tt = tend;
+            if (tt == se) se += S;
+        }
+        // the segment's last P.V now: its partial must not wait for the next segment (the
+        // producer may wait for this one's fallback pushes before it emits another)
+        if (ok && pd_on && !issue_o()) ok = false;
+        if (!ok) break;
+        if (!maxpass) ++obn;
+    }
+    // every MMA this CTA issued has landed before the tensor memory and the stages are released
+    if (lane == 0) umma_commit(ub.drain);
+    __syncwarp();
+    if (!mbar_wait(ub.drain, 0u) && lane == 0) {
+        misc[0] = 1;
+        set_error(a, FDPP_ERRBIT_TIMEOUT);
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------------------------------
+// softmax warps
+// ------------------------------------------------------------------------------------------
+// Softmax warp w: tensor-memory quadrant w % 4 (tokens 16 (w % 4) .. + 15 of a tile), row half
+// w / 4 (rows NP/2 (w / 4) .. + NP/2 - 1). A thread holds NPC = NP / 8 rows of 2 tokens.
+template <int NP>
+__device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayout& lay, uint8_t* sm,
+                                              uint32_t sbase, const Ring& rg, const UmBars& ub,
+                                              uint32_t tmem, volatile int* misc)
+{
+    constexpr int NGW = NP / 16;         // 8-column groups of S^T per warp
+    constexpr int NV = 4 * NGW;          // S^T values per thread and tile
+    constexpr int NPC = 2 * NGW;         // rows (columns) per thread
+    constexpr float LOG2E = 1.4426950408889634f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qw = warp & 3, hw = warp >> 2;
+    const int q = lane & 3, a4 = lane >> 2;
+    const int tokA = qw * 16 + a4;       // this thread's tokens in a tile: tokA, tokA + 8
+    const int g0 = hw * NGW;             // first 8-column group of this warp
+    const uint32_t lane_base = (uint32_t)(32 * qw) << 16;
+    uint8_t* fsw = sm + lay.fsw;
+    int* fcnt = reinterpret_cast<int*>(sm + lay.fcnt);
+    unsigned long long* taint_s = reinterpret_cast<unsigned long long*>(sm + lay.taint);
+    float* xl_s = reinterpret_cast<float*>(sm + lay.xl);
+    float* xm_s = reinterpret_cast<float*>(sm + lay.xm);
+    uint32_t stage = 0, phase = 0, qiter = 0, it = 0, pit = 0, obn = 0, portion = 0, un = 0, nsync = 0;
+    const int R = a.R;
+    const float c_exp = a.scale * LOG2E;          // p = 2^(acc scale log2e - frame log2e)
+    // row n of column c of this thread
+    auto row_of = [&](int c) { return 8 * (g0 + (c >> 1)) + 2 * q + (c & 1); };
+    // the softmax warps meet (bounded: a warp that gave up lets the others time out)
+    auto warps_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ub.wsync);
+        const bool ok = ring_wait(ub.wsync, nsync & 1u, misc, a);
+        ++nsync;
+        return ok;
+    };
+
+    for (;;) {
+        // ---- next segment ----
+        const uint32_t qs = qiter & 1u;
+        if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) return;
+        const int* hdr = reinterpret_cast<const int*>(sm + lay.qhdr + qs * QHDR_BYTES);
+        const int kind = hdr[H_KIND];
+        if (kind == KIND_END) return;
+        const int b = hdr[H_B], g = hdr[H_G], j0 = hdr[H_J];
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], dest = hdr[H_DEST], L = hdr[H_L], S = hdr[H_S];
+        const bool maxpass = hdr[H_PASS] == PASS_MAX;
+        const unsigned long long redo_mask =
+            (unsigned long long)(unsigned)hdr[H_MASK] | ((unsigned long long)(unsigned)hdr[H_MASK_HI] << 32);
+        const unsigned long long onl_mask =
+            (unsigned long long)(unsigned)hdr[H_ONL] | ((unsigned long long)(unsigned)hdr[H_ONL_HI] << 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rg.qempty + 8 * qs);
+        ++qiter;
+        const bool redo = kind == KIND_REDO;
+        const bool force_online = a.mode == FDPP_MODE_FORCE_ONLINE;
+        const uint32_t upar = un & 1u;
+        // causal limit of the query token with the fewest keys (row 0): a tile wholly below it
+        // needs no per-row mask
+        const int lim0 = key_limit(a, L, 0);
+
+        // Per row of this thread: the frame of the sums (phi, or the max pass's M) times log2 e,
+        // the causal key limit (absolute token index), the window trackers on the raw q.k
+        // (scale > 0 and each rounding is monotone, so the max, min and NaN of q.k decide the
+        // test of every s - phi exactly), and the l sum.
+        float frl[NPC], amax[NPC], amin[NPC], anan[NPC], lsum[NPC];
+        int lim[NPC];
+#pragma unroll
+        for (int c = 0; c < NPC; ++c) {
+            const int n = row_of(c);
+            const bool live = n < R;
+            lim[c] = live ? key_limit(a, L, n / a.G) : 0;
+            const bool onl = !maxpass && ((redo && ((onl_mask >> n) & 1ull)) || (!redo && force_online));
+            float fr = live ? phi_of(a, g * a.G + n % a.G) : a.phi;
+            if (onl) {
+                fr = xm_s[n];
+#pragma unroll
+                for (int w = 1; w < 4; ++w) fr = fmaxf(fr, xm_s[w * UM_MAX_ROWS + n]);
+            }
+            frl[c] = fr * LOG2E;
+            amax[c] = -INFINITY;
+            amin[c] = INFINITY;
+            anan[c] = -INFINITY;
+            lsum[c] = 0.f;
+        }
+
+        // End of one split piece of an own segment: each row's window decision from the trackers,
+        // ORed over the warp's tokens, then over the eight warps by whichever arrives last, which
+        // writes the flag bytes (the split's own, or the run slot's edge byte for a first piece
+        // that starts inside a split) and marks the segment's taint.
+        auto finish_piece = [&](int jp, bool first_piece) {
+            unsigned nb = 0u;
+#pragma unroll
+            for (int c = 0; c < NPC; ++c) {
+                const int n = row_of(c);
+                const float ph = n < R ? phi_of(a, g * a.G + n % a.G) : a.phi;
+                unsigned f = 0u;
+                if (__fsub_rn(__fmul_rn(amax[c], a.scale), ph) > a.hi) f |= FDPP_FLAG_OUT | FDPP_FLAG_ABOVE;
+                if (__fsub_rn(__fmul_rn(amin[c], a.scale), ph) < a.lo) f |= FDPP_FLAG_OUT | FDPP_FLAG_BELOW;
+                if (anan[c] != anan[c]) f |= FDPP_FLAG_OUT | FDPP_FLAG_NAN;
+                nb |= f << (4 * c);
+                amax[c] = -INFINITY;
+                amin[c] = INFINITY;
+                anan[c] = -INFINITY;
+            }
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) nb |= __shfl_xor_sync(0xffffffffu, nb, sh);
+            const uint32_t ks = portion++ & (uint32_t)(UM_FSLOTS - 1);
+            uint8_t* mine = fsw + (ks * 4 + qw) * UM_MAX_ROWS;
+            if (lane < 4) {
+#pragma unroll
+                for (int c = 0; c < NPC; ++c) mine[row_of(c)] = (uint8_t)((nb >> (4 * c)) & 15u);
+            }
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&fcnt[ks], 1);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != UM_NSW - 1) return;
+            __threadfence_block();
+            const uint8_t* all = fsw + ks * 4 * UM_MAX_ROWS;
+            unsigned long long out_rows = 0ull;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int n = lane + 32 * hf;
+                bool out = false;
+                if (n < R && n < NP) {
+                    const unsigned f = all[n] | all[UM_MAX_ROWS + n] | all[2 * UM_MAX_ROWS + n] |
+                                       all[3 * UM_MAX_ROWS + n];
+                    out = (f & FDPP_FLAG_OUT) != 0u;
+                    const uint8_t fb = (uint8_t)(f | (force_online ? FDPP_FLAG_RECOMPUTED : 0u));
+                    if (first_piece && dest >= 0 && t0 != jp * S)
+                        a.xf[(long long)dest * R + n] = fb;
+                    else
+                        a.flags[unit_row_slot(a, b, g, n, jp)] = fb;
+                }
+                out_rows |= (unsigned long long)__ballot_sync(0xffffffffu, out) << (32 * hf);
+            }
+            if (lane == 0) {
+                fcnt[ks] = 0;
+                if (out_rows) atomicOr(&taint_s[upar], out_rows);
+            }
+        };
+
+        // ---- the segment's tiles ----
+        int tt = t0, se = (t0 / S + 1) * S, jp = j0;
+        bool first_piece = true;
+        while (tt < t1) {
+            const int tend = min(min(tt + TILE, se), t1);
+            const int nvalid = tend - tt;
+            const uint32_t sb = it & 1u;
+            if (!ring_wait(ub.sfull + 8 * sb, (it >> 1) & 1u, misc, a)) return;
+            tc_fence_after();
+            uint32_t v[NV];
+            tmem_ld_16x256b<NGW>(tmem + sb * NP + lane_base + 8 * g0, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ub.sfree + 8 * sb);
+            // every score of the tile counts: no ragged tail and every row sees every key
+            const bool whole = nvalid == TILE && tt + TILE <= lim0;
+            // element e: row column c = 2 (e / 4) + e % 2, token tokA + 8 ((e / 2) % 2)
+            auto valid_at = [&](int e) {
+                const int c = 2 * (e >> 2) + (e & 1);
+                const int tok = tokA + 8 * ((e >> 1) & 1);
+                return tok < nvalid && tt + tok < lim[c];
+            };
+            if (maxpass) {
+                if (whole) {
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int c = 2 * (e >> 2) + (e & 1);
+                        amax[c] = fmaxf(amax[c], __uint_as_float(v[e]));
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int c = 2 * (e >> 2) + (e & 1);
+                        amax[c] = fmaxf(amax[c], valid_at(e) ? __uint_as_float(v[e]) : -INFINITY);
+                    }
+                }
+            } else {
+                float p[NV];
+                if (whole) {
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int c = 2 * (e >> 2) + (e & 1);
+                        const float x = __uint_as_float(v[e]);
+                        amax[c] = fmaxf(amax[c], x);
+                        amin[c] = fminf(amin[c], x);
+                        anan[c] = max_nan(anan[c], x);
+                        p[e] = ex2_approx(fmaf(x, c_exp, -frl[c]));
+                        lsum[c] += p[e];
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < NV; ++e) {
+                        const int c = 2 * (e >> 2) + (e & 1);
+                        const float x = __uint_as_float(v[e]);
+                        const bool ok = valid_at(e);
+                        amax[c] = fmaxf(amax[c], ok ? x : -INFINITY);
+                        amin[c] = fminf(amin[c], ok ? x : INFINITY);
+                        anan[c] = max_nan(anan[c], ok ? x : -INFINITY);
+                        p[e] = ok ? ex2_approx(fmaf(x, c_exp, -frl[c])) : 0.f;
+                        lsum[c] += p[e];
+                    }
+                    // V rows past the valid tokens may hold anything (NaN included): zero them
+                    // before the tensor core reads the tile (the stage has landed: its barrier
+                    // is waited on); the first row half's warps take the quadrant's 16 rows
+                    if (nvalid < TILE && hw == 0) {
+                        if (!ring_wait(rg.full + 8 * stage, phase, misc, a)) return;
+                        const int tok = qw * 16 + (lane & 15);
+                        if (tok >= nvalid) {
+                            uint4* row = reinterpret_cast<uint4*>(sm + lay.stages + stage * lay.stage_bytes +
+                                                                  lay.kv_bytes + (lane >> 4) * TILE * 128 + tok * 128);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                // P^T (hi, lo) into the next P buffer, once the MMAs that last read it are done:
+                // stored row n holds the tile's 64 tokens (16-byte chunk k = tokens 8k .. 8k + 7
+                // at chunk k ^ (n % 8), 128-byte swizzle), 8-row groups 1024 bytes apart
+                const uint32_t pbi = pit & 1u;
+                if (!ring_wait(ub.pfree + 8 * pbi, ((pit >> 1) & 1u) ^ 1u, misc, a)) return;
+                const uint32_t pb = sbase + lay.pbuf + pbi * 2 * lay.p_bytes;
+                {
+                    const int jm = lane >> 3, r = lane & 7;
+                    if constexpr (NGW >= 2) {
+#pragma unroll
+                        for (int u = 0; u < NGW / 2; ++u) {
+                            const int gg = g0 + 2 * u + (jm >> 1), th = jm & 1;
+                            const uint32_t addr = pb + gg * 1024 + r * 128 + ((uint32_t)((2 * qw + th) ^ r) << 4);
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) split_bf16x2(p[8 * u + 2 * j], p[8 * u + 2 * j + 1], hi[j], lo[j]);
+                            stmatrix_x4_trans(addr, hi[0], hi[1], hi[2], hi[3]);
+                            stmatrix_x4_trans(addr + lay.p_bytes, lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    } else {
+                        // one group per warp: two matrices (the token halves), addresses from lanes 0-15
+                        const int th = jm & 1;
+                        const uint32_t addr = pb + g0 * 1024 + r * 128 + ((uint32_t)((2 * qw + th) ^ r) << 4);
+                        uint32_t hi[2], lo[2];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) split_bf16x2(p[2 * j], p[2 * j + 1], hi[j], lo[j]);
+                        stmatrix_x2_trans(addr, hi[0], hi[1]);
+                        stmatrix_x2_trans(addr + lay.p_bytes, lo[0], lo[1]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ub.pready + 8 * pbi);
+                ++pit;
+            }
+            ++it;
+            if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
+            tt = tend;
+            if (tt == se || tt == t1) {            // a split piece ends here
+                if (!maxpass && !redo) finish_piece(jp, first_piece);
+                first_piece = false;
+                ++jp;
+                se += S;
+            }
+        }
+
+        if (maxpass) {
+            // ---- the rows' maxima over the segment (scaled): per quadrant, read by every warp ----
+#pragma unroll
+            for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+                for (int sh = 4; sh < 32; sh <<= 1) amax[c] = fmaxf(amax[c], __shfl_xor_sync(0xffffffffu, amax[c], sh));
+            }
+            if (lane < 4) {
+#pragma unroll
+                for (int c = 0; c < NPC; ++c) xm_s[qw * UM_MAX_ROWS + row_of(c)] = __fmul_rn(amax[c], a.scale);
+            }
+            if (!warps_sync()) return;
+            continue;
+        }
+
+        // ---- epilogue: l of every row, then O^T out of tensor memory ----
+#pragma unroll
+        for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+            for (int sh = 4; sh < 32; sh <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], sh);
+        }
+        if (lane < 4) {
+#pragma unroll
+            for (int c = 0; c < NPC; ++c) xl_s[qw * UM_MAX_ROWS + row_of(c)] = lsum[c];
+        }
+        // every warp's l, and every piece's window decisions (the taint), are in
+        if (!warps_sync()) return;
+        const unsigned long long write_mask = redo ? redo_mask : ~0ull;
+        const unsigned long long taint = redo ? 0ull : taint_s[upar];
+        const bool refill = !redo && a.mode == FDPP_MODE_NORMAL;
+        const uint32_t ob = obn & 1u;
+        if (!ring_wait(ub.ofull + 8 * ob, (obn >> 1) & 1u, misc, a)) return;
+        ++obn;
+        tc_fence_after();
+        {
+            // d = 32 (w % 4) + lane; 16-column chunks alternate between the quadrant's two warps
+            // (NP = 16: the first warp's)
+            const int d = 32 * qw + lane;
+#pragma unroll
+            for (int ch = 0; ch < NP / 16; ++ch) {
+                if (NP > 16 ? (ch & 1) != hw : hw != 0) continue;
+                float o[16];
+                tmem_ld16(tmem + 2 * NP + ob * NP + lane_base + 16 * ch, o);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int n = 16 * ch + k;
+                    if (n >= R || !((write_mask >> n) & 1ull)) continue;
+                    const bool empty = refill && ((taint >> n) & 1ull);
+                    float* orow = dest >= 0 ? a.xo + ((long long)dest * R + n) * UM_D
+                                            : a.o_part + unit_row_slot(a, b, g, n, j0) * UM_D;
+                    orow[d] = empty ? 0.f : o[k];
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ub.ofree + 8 * ob);
+        if (warp == 0) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int n = lane + 32 * hf;
+                if (n >= R || n >= NP || !((write_mask >> n) & 1ull)) continue;
+                const float lam = ((xl_s[n] + xl_s[UM_MAX_ROWS + n]) + xl_s[2 * UM_MAX_ROWS + n]) +
+                                  xl_s[3 * UM_MAX_ROWS + n];
+                const bool onl = (redo && ((onl_mask >> n) & 1ull)) || (!redo && force_online);
+                float M = phi_of(a, g * a.G + n % a.G);
+                if (onl) {
+                    M = xm_s[n];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) M = fmaxf(M, xm_s[w * UM_MAX_ROWS + n]);
+                }
+                const long long rs = dest >= 0 ? (long long)dest * R + n : unit_row_slot(a, b, g, n, j0);
+                float* lp = dest < 0 ? a.l_part : a.xl;
+                float* mp = dest < 0 ? a.m_part : a.xm;
+                const bool empty = refill && ((taint >> n) & 1ull);
+                lp[rs] = empty ? 0.f : lam;
+                mp[rs] = empty ? -INFINITY : M;
+                if (redo) {
+                    // the piece's flag byte (written by the pushing CTA) gains its marks
+                    uint8_t* fp = dest < 0 ? a.flags + rs : a.xf + rs;
+                    const unsigned f0 = __ldcg(fp);
+                    const unsigned rc = onl ? FDPP_FLAG_RECOMPUTED : 0u;
+                    *fp = (uint8_t)(f0 | rc | (dest < 0 ? FDPP_FLAG_SLOT : 0u));
+                }
+            }
+        }
+        // every warp's stores are ordered before the fallback push (a release by warp 0), and
+        // xl/xm are read before the next segment writes them
+        if (!warps_sync()) return;
+        ++un;
+        if (warp == 0 && lane == 0) {
+            if (!redo) {
+                taint_s[upar] = 0ull;
+                if (taint != 0ull && a.mode == FDPP_MODE_NORMAL) {
+                    const int list = (int)(blockIdx.x % REDO_NLISTS);
+                    const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
+                    long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
+                    ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
+                    ent[2] = dest;
+                    ent[3] = (long long)taint;
+                    st_release_gpu(ent, ((long long)(g * a.max_splits + j0) << 32) | (long long)(unsigned)(b + 1));
+                }
+            }
+            if (kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// kernel
+// ------------------------------------------------------------------------------------------
+template <int NP, bool PAGED>
+__global__ void __launch_bounds__(UM_THREADS, 1)
+    split_um_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmQ, const KernelArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const UmLayout lay(NP, a.nstage, a.B);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* misc = reinterpret_cast<volatile int*>(sm + lay.misc);   // [0] abort
+    Ring rg{};
+    rg.nstage = a.nstage;
+    rg.full = sbase + lay.bars;
+    rg.empty = rg.full + 8 * a.nstage;
+    rg.qfull = rg.empty + 8 * a.nstage;
+    rg.qempty = rg.qfull + 16;
+    rg.own_done = rg.qempty + 16;
+    UmBars ub;
+    ub.sfull = rg.own_done + 8;
+    ub.sfree = ub.sfull + 16;
+    ub.pready = ub.sfree + 16;
+    ub.pfree = ub.pready + 16;
+    ub.ofull = ub.pfree + 16;
+    ub.ofree = ub.ofull + 16;
+    ub.drain = ub.ofree + 16;
+    ub.wsync = ub.drain + 8;
+    static_assert(UM_NBARS * 8 >= 16 + 16 + 8 + 6 * 16 + 8 + 8, "barrier region");
+    constexpr uint32_t NCOLS = 4 * NP;      // S^T x 2, O^T x 2
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + lay.tslot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.nstage; ++s) {
+            mbar_init(rg.full + 8 * s, 1);
+            mbar_init(rg.empty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(rg.qfull + 8 * s, 1);
+            mbar_init(rg.qempty + 8 * s, 1 + UM_NSW);
+            mbar_init(ub.sfull + 8 * s, 1);
+            mbar_init(ub.sfree + 8 * s, UM_NSW);
+            mbar_init(ub.pready + 8 * s, UM_NSW);
+            mbar_init(ub.pfree + 8 * s, 1);
+            mbar_init(ub.ofull + 8 * s, 1);
+            mbar_init(ub.ofree + 8 * s, UM_NSW);
+        }
+        mbar_init(rg.own_done, 1);
+        mbar_init(ub.drain, 1);
+        mbar_init(ub.wsync, UM_NSW);
+        misc[0] = 0;
+        misc[1] = 0;
+        int* fc = reinterpret_cast<int*>(sm + lay.fcnt);
+        for (int i = 0; i < UM_FSLOTS; ++i) fc[i] = 0;
+        unsigned long long* ts = reinterpret_cast<unsigned long long*>(sm + lay.taint);
+        ts[0] = ts[1] = 0ull;
+        fence_mbar_init();
+    }
+    if (warp == UM_MMA_WARP) tmem_alloc(smem_u32(tslot), NCOLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    // a programmatic dependent: the tiles this CTA streamed first in the last call go into L2
+    // while the previous kernel finishes (contiguous caches), then every warp waits for it
+    if (!PAGED && warp == UM_PROD_WARP && lane == 0 && blockIdx.x < TC_MAX_PARTS) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        prefetch_tensormap(&tmQ);
+        const volatile int* h = a.hint + (long long)blockIdx.x * HINT_WORDS;
+        const int n = min(max(h[0], 0), HINT_TILES);
+        for (int i = 0; i < n; ++i) {
+            const int x = h[1 + 3 * i], y = h[2 + 3 * i], z = h[3 + 3 * i];
+            if (x < 0 || (x & 63) != 0) continue;
+#pragma unroll
+            for (int hv = 0; hv < UM_D / 64; ++hv) {
+                tma_prefetch_3d(&tmK, x + 64 * hv, y, z);
+                tma_prefetch_3d(&tmV, x + 64 * hv, y, z);
+            }
+        }
+    }
+    grid_dependency_wait();
+
+    int* plan = reinterpret_cast<int*>(sm + lay.plan);
+    if (warp == UM_PROD_WARP) {
+        Producer<false, UmLayout> pr{&tmK, &tmV, &a, &lay, rg, sbase, sm, misc, plan, plan + (a.B + 1), &tmQ};
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+            prefetch_tensormap(&tmQ);
+        }
+        pr.template run<UM_D, PAGED>();
+        if (pr.bad_block && lane == 0) set_error(a, FDPP_ERRBIT_BLOCK_TABLE);
+        if (lane == 0 && misc[0] != 0) {
+            // aborted: let every copy this CTA issued land before it exits (bounded waits); the
+            // latest issue into stage s had phase `phase` when s < stage, else phase ^ 1
+            for (int s = 0; s < a.nstage; ++s) {
+                const uint32_t par = (uint32_t)s < pr.stage ? pr.phase : (pr.phase ^ 1u);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(rg.full + 8 * s, par) && global_ns() - t0 < 100000000ull) {
+                }
+            }
+            for (uint32_t k = 0; k < 2 && k < pr.qiter; ++k) {
+                const uint32_t itq = pr.qiter - 1 - k, qs = itq & 1u, par = (itq >> 1) & 1u;
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(rg.qfull + 8 * qs, par) && global_ns() - t0 < 100000000ull) {
+                }
+            }
+        }
+    } else if (warp == UM_MMA_WARP) {
+        mma_warp<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
+    } else {
+        softmax_warps<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == UM_MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, NCOLS);
+    }
+}
+
+template <int NP, bool PAGED>
+cudaError_t launch_np(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                      int grid, int smem, cudaStream_t s)
+{
+    auto kern = split_um_kernel<NP, PAGED>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(UM_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, tq, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int split_um_rows_padded(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+
+int split_um_smem_bytes(int R, int nstage, int batch)
+{
+    return UmLayout(split_um_rows_padded(R), nstage, batch).total + 1024;
+}
+
+cudaError_t launch_split_um(const KernelArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tq, int grid, int smem_bytes, cudaStream_t s)
+{
+    const bool paged = a.block_table != nullptr;
+    switch (split_um_rows_padded(a.R)) {
+    case 16: return paged ? launch_np<16, true>(a, tk, tv, tq, grid, smem_bytes, s)
+                          : launch_np<16, false>(a, tk, tv, tq, grid, smem_bytes, s);
+    case 32: return paged ? launch_np<32, true>(a, tk, tv, tq, grid, smem_bytes, s)
+                          : launch_np<32, false>(a, tk, tv, tq, grid, smem_bytes, s);
+    default: return paged ? launch_np<64, true>(a, tk, tv, tq, grid, smem_bytes, s)
+                          : launch_np<64, false>(a, tk, tv, tq, grid, smem_bytes, s);
+    }
+}
+
+}  // namespace fdpp

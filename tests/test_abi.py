@@ -86,23 +86,34 @@ def test_max_splits_and_workspace_size():
 
 
 def test_workspace_size_with_row_groups():
-    # 16 query tokens of 4 heads per kv head: R = 64 rows, 8 row groups of the tensor kernel.
-    # Partials per (query row, split); a run slot holds one run of one row group, so 8 rows, one
-    # per part plus one per (sequence, kv head, row group); the fallback lists hold an entry per
-    # (sequence, kv head, row group, split) and per part
+    # 16 query tokens of 4 heads per kv head: R = 64 rows. Partials per (query row, split). The
+    # run slots serve either build: the mma.sync build's hold one run of one row group of 8 rows
+    # (one per part plus one per (sequence, kv head, row group)), the tcgen05 build's one run of
+    # all R rows (one per part, at most FDPP_TC_UM_MAX_CTAS, plus one per (sequence, kv head));
+    # the larger count is reserved. The fallback lists hold an entry per (sequence, kv head, row
+    # group, split) and per part.
     p = _gqa_params(q_tokens=16)
     ws = F.fdpp_workspace_size(p)
-    slots = 8 * 16 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 8
+    runs = max((F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 8, (F.FDPP_TC_UM_MAX_CTAS + 8 * 8) * 64)
+    slots = 8 * 16 * 32 * 8 + runs
     lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws <= fixed + 64 * 1024
-    # 12 rows: two groups (8 + 4); run slots still 8 rows, lists twice the one-group count
+    # 12 rows: two groups (8 + 4), lists twice the one-group count
     p12 = _gqa_params(q_tokens=3)
     ws12 = F.fdpp_workspace_size(p12)
-    slots = 8 * 3 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 8
+    runs = max((F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 8, (F.FDPP_TC_UM_MAX_CTAS + 8 * 8) * 12)
+    slots = 8 * 3 * 32 * 8 + runs
     lists = 8 * (8 * 8 * 2 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8 * 2) * 32
     fixed = slots * (128 * 4 + 4 + 4 + 1) + lists
     assert fixed <= ws12 <= fixed + 64 * 1024
+    # head_dim 64 has no tcgen05 build: row-group run slots only
+    p64 = _gqa_params(q_tokens=16, head_dim=64)
+    ws64 = F.fdpp_workspace_size(p64)
+    slots = 8 * 16 * 32 * 8 + (F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 8
+    lists = 8 * (8 * 8 * 8 * 8 + F.FDPP_TC_MAX_PARTS + 8 * 8 * 8) * 32
+    fixed = slots * (64 * 4 + 4 + 4 + 1) + lists
+    assert fixed <= ws64 <= fixed + 64 * 1024
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -114,6 +125,8 @@ def test_workspace_size_with_row_groups():
     ("max_seq_len", 0, F.FDPP_ERR_INVALID_ARG),
     ("split_len", -1, F.FDPP_ERR_INVALID_ARG),
     ("scale", float("nan"), F.FDPP_ERR_INVALID_ARG),
+    ("scale", 0.0, F.FDPP_ERR_INVALID_ARG),
+    ("scale", -0.125, F.FDPP_ERR_INVALID_ARG),
     ("phi", float("inf"), F.FDPP_ERR_INVALID_ARG),
     ("lo", 20.0, F.FDPP_ERR_INVALID_ARG),               # lo > hi
     ("mode", 3, F.FDPP_ERR_INVALID_ARG),
@@ -122,6 +135,8 @@ def test_workspace_size_with_row_groups():
     ("tc_ctas_per_sm", 3, F.FDPP_ERR_INVALID_ARG),
     ("tc_prefetch", 33, F.FDPP_ERR_INVALID_ARG),
     ("tc_prefetch", -2, F.FDPP_ERR_INVALID_ARG),
+    ("tc_mma", 3, F.FDPP_ERR_INVALID_ARG),
+    ("tc_mma", -1, F.FDPP_ERR_INVALID_ARG),
 ])
 def test_bad_params_are_rejected_on_the_host(field, value, status):
     p = _gqa_params()
@@ -134,6 +149,19 @@ def test_bad_params_are_rejected_on_the_host(field, value, status):
     st = F.lib.fdpp_decode_attn(fake, fake, fake, None, fake, ctypes.byref(p), fake * 256,
                                 1 << 30, fake, None)
     assert st == status
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q_tokens=16, head_dim=64),                   # tcgen05 build: d = 128 only
+    dict(q_tokens=2),                                 # 8 rows per kv head: the mma.sync build's
+    dict(q_tokens=16, dtype=F.FDPP_F32),              # bf16 only
+    dict(q_tokens=16, tc_ctas_per_sm=2),              # one CTA per SM
+])
+def test_tcgen05_build_outside_its_shapes_is_unsupported(kw):
+    p = _gqa_params(kernel=F.FDPP_KERNEL_TENSOR, tc_mma=F.FDPP_TC_MMA_TCGEN05, **kw)
+    assert F.fdpp_workspace_size(p) > 0
+    assert _call(p) == F.FDPP_ERR_UNSUPPORTED
+    assert F.fdpp_last_error()
 
 
 def test_group_too_large_is_unsupported():

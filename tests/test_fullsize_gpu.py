@@ -1,6 +1,6 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (default
 kernel choice and pipeline geometry), including two query tokens per sequence (spec_decode_tq2)
-and a 16-token prefill chunk (prefill_chunk_tq16: 64 rows per kv head, eight row groups):
+and a 16-token prefill chunk (prefill_chunk_tq16: 64 rows per kv head, the tcgen05 build):
   * sampled output rows against the fp64 oracle (computed one row at a time);
   * every output finite; the split plan equal to the oracle's scheduler;
   * window decisions: none for the N(0,1) workloads; for the fallback-stress workload every
@@ -39,6 +39,8 @@ def test_full_size(wl):
     got, diag, flags, ns, _ = H.run(dinp)
     assert np.isfinite(got).all()
     assert diag["error_bits"] == 0
+    if wl.group * max(1, wl.q_tokens) > 8:
+        assert diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
     p = H.params_for(inp)
     o_ns, _, o_units = oracle.plan(inp.seq_lens, wl.num_kv_heads, p.max_seq_len, wl.split_len)
     np.testing.assert_array_equal(ns, o_ns)

@@ -59,7 +59,23 @@ SMALL = {
                          q_tokens=8, seq_len_range=(40, 1200), split_len=256), None),
     "tq4_paged": (_wl(W.PAGED, name="tq4_paged", batch=4, num_q_heads=4, num_kv_heads=2,
                       q_tokens=4, seq_len_range=(3, 700), split_len=128), None),
+    # the tcgen05 build's shapes (bf16, d = 128, 9..64 rows per kv head, padded to 16, 32 or 64):
+    # sequences shorter than the chunk (rows that see no key), splits that are no multiple of
+    # the 64-token tile (ragged tiles inside a sequence), 20 rows on a paged cache
+    "tq16_short": (_wl(W.GQA, name="tq16_short", batch=6, num_q_heads=8, num_kv_heads=2,
+                       q_tokens=16, split_len=64), [5, 16, 17, 64, 65, 200]),
+    "tq4_g4_s100": (_wl(W.GQA, name="tq4_g4_s100", batch=3, num_q_heads=8, num_kv_heads=2,
+                        q_tokens=4, split_len=100), [777, 100, 3]),
+    "tq8_g4": (_wl(W.GQA, name="tq8_g4", batch=2, num_q_heads=8, num_kv_heads=2, q_tokens=8,
+                   split_len=256), [1000, 257]),
+    "tq5_paged_g4": (_wl(W.PAGED, name="tq5_paged_g4", batch=4, num_q_heads=8, num_kv_heads=2,
+                         q_tokens=5, seq_len_range=(2, 1300), split_len=256), None),
 }
+
+# More than 8 query rows per kv head with bf16 K/V and d = 128: the tcgen05 build by default,
+# the mma.sync build (rows in groups of 8) when asked for.
+MANY_ROWS = ["tq16_g4", "tq3_g4", "g16", "tq8_paged_g2", "tq16_short", "tq4_g4_s100", "tq8_g4",
+             "tq5_paged_g4"]
 
 
 _cache = {}
@@ -102,7 +118,37 @@ def test_small_parity(name):
         assert diag["n_flagged_row_splits"] == 0 and (flags & F.FDPP_FLAG_OUT).sum() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny", "tq4_paged"])
+@pytest.mark.parametrize("name", MANY_ROWS)
+@pytest.mark.parametrize("build", ["tcgen05", "mma_sync"])
+def test_many_rows_on_both_tensor_builds(name, build):
+    inp, dinp = _inputs(name)
+    ref = H.oracle_out(inp)
+    tc = F.FDPP_TC_MMA_TCGEN05 if build == "tcgen05" else F.FDPP_TC_MMA_SYNC
+    got, diag, flags, ns, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=tc)
+    H.assert_parity(got, ref, f"{name} {build}")
+    assert diag["error_bits"] == 0
+    assert diag["kernel"] == F.FDPP_KERNEL_TENSOR and diag["tc_build"] == tc
+    o_ns, _, o_units = oracle.plan(inp.seq_lens, inp.wl.num_kv_heads, 1 << 30, inp.wl.split_len)
+    np.testing.assert_array_equal(ns, o_ns)
+    assert diag["n_units"] == o_units
+    assert diag["n_flagged_row_splits"] == 0 and (flags & F.FDPP_FLAG_OUT).sum() == 0
+
+
+def test_many_rows_default_to_the_tcgen05_build():
+    inp, dinp = _inputs("tq16_g4")
+    _, diag, _, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    assert diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
+    # two CTAs per SM asked for: only the mma.sync build runs that geometry
+    _, diag, _, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_ctas_per_sm=2)
+    assert diag["tc_build"] == F.FDPP_TC_MMA_SYNC
+    # head_dim 64 has no tcgen05 build
+    inp64, dinp64 = _inputs("tq8_mha")
+    _, diag, _, _, _ = H.run(dinp64, kernel=F.FDPP_KERNEL_TENSOR)
+    assert diag["tc_build"] == F.FDPP_TC_MMA_SYNC
+
+
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny", "tq4_paged", "tq16_short",
+                                  "tq5_paged_g4"])
 def test_nan_past_seq_len_is_never_read_into_results(name):
     inp, dinp = _inputs(name, poison=True)
     ref = H.oracle_out(inp)
@@ -203,25 +249,29 @@ def test_fallback_decisions_and_results(kernel):
     H.assert_parity(got, ref, f"stress {kernel}")
 
 
-def test_fallback_with_row_groups():
-    """Four query tokens of four heads per kv head: 16 rows, two row groups of the tensor kernel.
-    Hot keys send segments of either group to the fallback lists; decisions and results as for
-    one group."""
+@pytest.mark.parametrize("build", ["tcgen05", "mma_sync"])
+def test_fallback_with_many_rows(build):
+    """Four query tokens of four heads per kv head: 16 rows, one unit of the tcgen05 build or two
+    row groups of the mma.sync build. Hot keys send segments to the fallback lists; the tcgen05
+    build streams a recomputed piece twice (the rows' maxima, then the sums in that frame).
+    Decisions and results as for one query token."""
     inp, oflags = _stress_inputs(batch=4, seq_len=1024, split_len=256, frac=0.1, num_q_heads=16,
                                  num_kv_heads=4, q_tokens=4)
     dinp = H.DeviceInputs(inp)
-    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    tc = F.FDPP_TC_MMA_TCGEN05 if build == "tcgen05" else F.FDPP_TC_MMA_SYNC
+    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=tc)
+    assert diag["tc_build"] == tc
     np.testing.assert_array_equal(flags & 0x0F, oflags)
     hot_rows = (oflags & oracle.FLAG_OUT) != 0
     assert hot_rows.sum() >= len(inp.hot)
     np.testing.assert_array_equal((flags & F.FDPP_FLAG_RECOMPUTED) != 0, hot_rows)
     assert diag["error_bits"] == 0
-    H.assert_parity(got, H.oracle_out(inp), "stress, row groups")
+    H.assert_parity(got, H.oracle_out(inp), f"stress, many rows, {build}")
 
 
-def _check_fallback(inp, oflags, what):
+def _check_fallback(inp, oflags, what, **kw):
     dinp = H.DeviceInputs(inp)
-    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR)
+    got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, **kw)
     np.testing.assert_array_equal(flags & 0x0F, oflags)
     hot_rows = (oflags & oracle.FLAG_OUT) != 0
     assert hot_rows.sum() >= len(inp.hot)
@@ -243,6 +293,16 @@ def test_one_split_spread_over_many_parts():
     assert diag["n_units"] == 1
 
 
+def test_one_split_over_many_parts_with_many_rows():
+    """The same on the tcgen05 build: four query tokens of four heads (16 rows) per kv head, one
+    split of 64 tiles cut into one-tile parts, whose run slots hold all 16 rows."""
+    inp, oflags = _stress_inputs(batch=1, seq_len=4096, split_len=4096, frac=1.0,
+                                 num_q_heads=4, num_kv_heads=1, q_tokens=4)
+    diag = _check_fallback(inp, oflags, "one split over 64 parts, 16 rows",
+                           tc_mma=F.FDPP_TC_MMA_TCGEN05)
+    assert diag["n_units"] == 1 and diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
+
+
 def test_batch_beyond_the_shared_memory_plan():
     """Batches above 1024 sequences are dealt out to the CTAs as whole units (no extra slots);
     results, decisions and the fallback must be the same as for the part-balanced path."""
@@ -260,6 +320,15 @@ def test_batch_beyond_the_shared_memory_plan_with_row_groups():
                                  num_q_heads=8, num_kv_heads=2, head_dim=64, q_tokens=5)
     diag = _check_fallback(inp, oflags, "batch 1100, row groups")
     assert diag["n_units"] == 1100 * 2 * 2
+
+
+def test_batch_beyond_the_shared_memory_plan_with_many_rows():
+    """The whole-unit path of the tcgen05 build: 20 rows per kv head (padded to 32), d = 128,
+    units dealt out per (sequence, kv head, split), fallback pieces in their split slots."""
+    inp, oflags = _stress_inputs(batch=1100, seq_len=256, split_len=128, frac=0.01,
+                                 num_q_heads=8, num_kv_heads=2, q_tokens=5)
+    diag = _check_fallback(inp, oflags, "batch 1100, 20 rows", tc_mma=F.FDPP_TC_MMA_TCGEN05)
+    assert diag["n_units"] == 1100 * 2 * 2 and diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
 
 
 def test_many_rows_share_combine_blocks():
@@ -316,14 +385,15 @@ def test_force_fast_is_wrong_exactly_where_flagged(kernel):
     assert (flags & F.FDPP_FLAG_RECOMPUTED).sum() == 0
 
 
-@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny"])
+@pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16", "tiny", "tq16_short", "tq5_paged_g4"])
 def test_force_online_matches(name):
     inp, dinp = _inputs(name)
     ref = H.oracle_out(inp)
+    rows = inp.wl.group * max(1, inp.wl.q_tokens)
     for kernel in _kernels(inp):
         got, diag, flags, _, _ = H.run(dinp, kernel=kernel, mode=F.FDPP_MODE_FORCE_ONLINE)
         H.assert_parity(got, ref, f"{name} online kernel {kernel}")
-        assert diag["n_recomputed_row_splits"] == diag["n_units"] * inp.wl.group
+        assert diag["n_recomputed_row_splits"] == diag["n_units"] * rows
 
 
 @pytest.mark.parametrize("name", ["gqa_ragged", "paged_bs16"])

@@ -98,8 +98,8 @@ SHIFTED = Workload("gqa_head_levels", 8, 32, 8, 128, BF16, split_len=512, seq_le
 # positions, causal), 8 query rows per kv head.
 SPEC = Workload("spec_decode_tq2", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=2,
                 seed=0x5EED0006)
-# A 16-token prefill chunk against gqa_decode's caches: 64 query rows per kv head, which the
-# tensor kernel takes in 8 groups of 8.
+# A 16-token prefill chunk against gqa_decode's caches: 64 query rows per kv head, one unit of
+# the tensor kernel's tcgen05 build.
 CHUNK = Workload("prefill_chunk_tq16", 8, 32, 8, 128, BF16, split_len=512, seq_len=4096, q_tokens=16,
                  seed=0x5EED0007)
 ALL = {w.name: w for w in (TINY, GQA, LONG, PAGED, STRESS, SHIFTED, SPEC, CHUNK)}
