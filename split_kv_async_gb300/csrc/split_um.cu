@@ -16,28 +16,34 @@
 // (q.K^T, and P.V with P split into bf16 hi and lo parts): 0.64 PFLOP/s at the copy rate, beyond
 // what m16n8k16 mma.sync issue keeps up with, well inside the tcgen05 rate.
 //
-// How. One CTA per SM, six warps:
-//   warp 4    the producer of split_tc_common.cuh: split plan, tile-balanced parts, 64-token K/V
+// How. One CTA per SM, eleven warps:
+//   warp 8    the producer of split_tc_common.cuh: split plan, tile-balanced parts, 64-token K/V
 //             tiles by TMA into a ring of stages (128-byte swizzle), fallback-list drain. The
 //             unit's R query rows arrive by one 4-D TMA load per 64-wide half of d.
-//   warp 5    one thread issues the MMAs, the warp owns the tensor memory:
-//               S^T = K Q^T      M = 64 tokens, N = NP (R rounded up to 16, 32 or 64), K = d;
-//               O^T += V^T P^T   M = d = 128, N = NP, K = 64 tokens, P as bf16 hi and lo (two
-//                                MMAs per 16 tokens into one accumulator, ~16 mantissa bits);
-//             V^T is read MN-major straight from the TMA-landed V tile. S^T has two buffers in
-//             tensor memory (tile parity), O^T two (segment parity). tcgen05.commit arrives on
+//   warps 9, 10  one thread each issues MMAs (warp 9 also owns the tensor memory):
+//               warp 9:  S^T = K Q^T      M = 64 tokens, N = NP (R rounded up to 16, 32 or 64),
+//                                         K = d, for every tile;
+//               warp 10: O^T += V^T P^T   M = d = 128, N = 2 NP, K = 64 tokens: P's bf16 hi
+//                                         parts are rows 0 .. NP - 1 of the B operand and its lo
+//                                         parts (what hi leaves out, ~16 mantissa bits together)
+//                                         rows NP .. 2 NP - 1, so one MMA per 16 tokens reads
+//                                         V^T once for both;
+//             V^T is read MN-major straight from the TMA-landed V tile. S^T has UM_NSB buffers in
+//             tensor memory (used in turn by the tiles), O^T two (segment parity). Two issuing warps keep
+//             either's waits (a stage, an S^T buffer, a P buffer) from holding the other's MMAs
+//             back, and descriptors are built once and offset per MMA: the issuing threads'
+//             own work, not the tensor core, set the pace before. tcgen05.commit arrives on
 //             mbarriers that release the K/V stage, the P buffer and the Q slot and wake the
-//             softmax warps. Inside a segment the P.V of tile i is issued after the q.K^T of
-//             tile i + 1, so the tensor core works on the next tile while the softmax warps finish
-//             this one.
-//   warps 0-3 softmax: warp w holds tokens 16w .. 16w + 15 of a tile (the 64-row accumulator
-//             puts token t in tensor-memory lane (t mod 16) + 32 floor(t / 16)); tcgen05.ld
-//             16x256b gives each thread 2 tokens x NP/4 rows in the mma.sync fragment order, so
+//             softmax warps.
+//   warps 0-7 softmax, two warps per tensor-memory lane quadrant: warp w holds tokens
+//             16 (w % 4) .. + 15 of a tile (the 64-row accumulator puts token t in lane
+//             (t mod 16) + 32 floor(t / 16)) and rows NP/2 floor(w / 4) .. + NP/2 - 1; tcgen05.ld
+//             16x256b gives each thread 2 tokens x NP/8 rows in the mma.sync fragment order, so
 //             stmatrix.trans writes P^T as the K-major swizzled B operand, 16 bytes per row.
-//             The window test keeps per row and split the max, min and a NaN marker of s, and
-//             classifies once per split (the rounding of s - phi is monotone in s, so this is
-//             exactly the per-score test). At a segment's end each thread reads one d of O^T
-//             and writes it for every row.
+//             The window test keeps per row and split the max, min and a NaN marker of q.k, and
+//             classifies once per split (scale > 0 and the rounding of s = scale q.k and of
+//             s - phi are monotone, so this is exactly the per-score test). At a segment's end
+//             each thread reads one d of O^T (hi plus lo) and writes it for its warp's rows.
 // Rows recomputed with online softmax (fallback pieces, and every segment in forced-online mode)
 // are streamed twice: first for the rows' maxima M, then for the sums in the frame M (the
 // accumulator in tensor memory is never rescaled). The result is the online softmax's up to
@@ -53,17 +59,24 @@ namespace {
 constexpr int UM_D = 128;                 // head dim of this kernel
 constexpr int UM_NSW = 8;                 // softmax warps: two per tensor-memory lane quadrant
 constexpr int UM_PROD_WARP = UM_NSW;      // then the producer
-constexpr int UM_MMA_WARP = UM_NSW + 1;   // and the MMA warp
-constexpr int UM_THREADS = (UM_NSW + 2) * 32;
+constexpr int UM_MMA_WARP = UM_NSW + 1;   // the q.K^T warp (owns the tensor memory)
+constexpr int UM_PV_WARP = UM_NSW + 2;    // the P.V warp
+constexpr int UM_THREADS = (UM_NSW + 3) * 32;
 constexpr int UM_FSLOTS = 8;              // window decisions of split pieces in flight
 constexpr int UM_MAX_ROWS = 64;
-constexpr int UM_NBARS = 19;              // barriers besides the stage ring's
+constexpr int UM_NBARS = 23;              // barriers besides the stage ring's
+// P^T buffers. One: the softmax warps compute a tile's P while the P.V of the tile before runs and
+// wait only to store it; the shared memory of a second goes to another K/V stage instead.
+constexpr int UM_NPB = 1;
+// S^T buffers in tensor memory (q.K^T runs up to this many tiles ahead of the softmax), then the
+// two O^T buffers: UM_NSB NP + 4 NP columns.
+constexpr int UM_NSB = 3;
 
 // Shared-memory layout (byte offsets from a 1024-byte aligned base).
 //   stages   nstage x (K tile, V tile), each two [64 token][64 d] boxes of 128-byte rows
 //   qring    2 slots x two [NP row][64 d] halves (the B operand of S^T)
-//   pbuf     2 buffers x (hi, lo) [NP row][64 token] (the B operand of O^T), used in turn by the
-//            tiles that have a P.V
+//   pbuf     UM_NPB buffers x (hi, lo) [NP row][64 token] (the B operand of O^T), used in turn by
+//            the tiles that have a P.V
 //   qhdr     2 segment headers
 //   fsw/fcnt per split piece in flight: each lane quadrant's flag nibble of every row (the two
 //            warps of a quadrant hold different rows), arrival count
@@ -83,7 +96,7 @@ struct UmLayout {
     {
         qring = stages + nstage * stage_bytes;
         pbuf = qring + 2 * qslot_bytes;
-        qhdr = pbuf + 2 * 2 * p_bytes;
+        qhdr = pbuf + UM_NPB * 2 * p_bytes;
         fsw = qhdr + 2 * QHDR_BYTES;
         fcnt = fsw + UM_FSLOTS * 4 * UM_MAX_ROWS;
         taint = fcnt + UM_FSLOTS * 4;
@@ -98,12 +111,13 @@ struct UmLayout {
     }
 };
 
-// The barriers besides the producer's ring (shared addresses). Arrival counts: sfull, pfree,
-// ofull and drain one commit; sfree, pready, ofree and wsync the four softmax warps.
+// The barriers besides the producer's ring (shared addresses). Arrival counts: sfull, pfree and
+// ofull one commit, drain one commit from each MMA warp; sfree, pready, ofree and wsync the
+// softmax warps.
 struct UmBars {
-    uint32_t sfull, sfree;     // [2] S^T buffer written / read out (tile parity)
-    uint32_t pready, pfree;    // [2] P^T buffer written / consumed by its MMAs (parity of the
-                               //     tiles that have a P.V: max passes have none)
+    uint32_t sfull, sfree;     // [UM_NSB] S^T buffer written / read out (used in turn by the tiles)
+    uint32_t pready, pfree;    // [UM_NPB] P^T buffer written / consumed by its MMAs (used in
+                               //     turn by the tiles that have a P.V: max passes have none)
     uint32_t ofull, ofree;     // [2] O^T buffer complete / read out (segment parity)
     uint32_t drain;            // every MMA of the CTA has completed
     uint32_t wsync;            // the softmax warps meet (a bounded barrier among them)
@@ -126,6 +140,17 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Two ring waits whose barriers usually have completed already: both are tested at once (their
+// latencies overlap), and only a phase still open takes the bounded wait.
+__device__ __forceinline__ bool ring_wait2(uint32_t bar1, uint32_t par1, uint32_t bar2, uint32_t par2,
+                                           volatile int* misc, const KernelArgs& a)
+{
+    const bool d1 = mbar_try_wait(bar1, par1);
+    const bool d2 = mbar_try_wait(bar2, par2);
+    if (__all_sync(0xffffffffu, d1 && d2)) return true;
+    return ring_wait(bar1, par1, misc, a) && ring_wait(bar2, par2, misc, a);
+}
+
 __device__ __forceinline__ float max_nan(float a, float b)
 {
     float d;
@@ -134,46 +159,52 @@ __device__ __forceinline__ float max_nan(float a, float b)
 }
 
 // ------------------------------------------------------------------------------------------
-// MMA warp
+// MMA warps: one issues q.K^T for every tile, the other P.V for every tile that has one, so that
+// neither's waits hold the other's MMAs back
 // ------------------------------------------------------------------------------------------
+// Descriptors are built once per stage, Q slot and P buffer; an MMA adds a constant to the
+// start-address field (addr / 16 in its low 14 bits; shared addresses stay below 256 KB, so the
+// field never carries).
+struct UmDescs {
+    uint64_t k0, v0, q0, p0;
+    uint32_t stage16, qslot16, qhalf16, pbuf16;
+
+    __device__ __forceinline__ UmDescs(const UmLayout& lay, uint32_t sbase)
+        : k0(sw128_kmajor_desc(sbase + lay.stages)),
+          v0(sw128_mnmajor_desc(sbase + lay.stages + lay.kv_bytes, TILE * 128, 1024)),
+          q0(sw128_kmajor_desc(sbase + lay.qring)), p0(sw128_kmajor_desc(sbase + lay.pbuf)),
+          stage16((uint32_t)lay.stage_bytes >> 4), qslot16((uint32_t)lay.qslot_bytes >> 4),
+          qhalf16((uint32_t)lay.qhalf_bytes >> 4), pbuf16((uint32_t)(2 * lay.p_bytes) >> 4)
+    {
+    }
+};
+
+// Every MMA the calling thread issued has landed (before the tensor memory and the stages are
+// released); the drain barrier takes one commit from each MMA warp.
+__device__ __forceinline__ void mma_drain(const KernelArgs& a, const UmBars& ub, volatile int* misc)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) umma_commit(ub.drain);
+    __syncwarp();
+    if (!mbar_wait(ub.drain, 0u) && lane == 0) {
+        misc[0] = 1;
+        set_error(a, FDPP_ERRBIT_TIMEOUT);
+    }
+    __syncwarp();
+}
+
+// q.K^T of every tile: S^T = K Q^T, M = 64 tokens, N = NP rows, into the S^T buffer of the tile's
+// parity once the softmax warps have read the tile two before out of it. The stage goes back to
+// the producer here for a max pass (no P.V follows); the Q slot after a segment's last tile.
 template <int NP>
-__device__ __forceinline__ void mma_warp(const KernelArgs& a, const UmLayout& lay, const uint8_t* sm,
-                                         uint32_t sbase, const Ring& rg, const UmBars& ub, uint32_t tmem,
-                                         volatile int* misc)
+__device__ __forceinline__ void mma_s_warp(const KernelArgs& a, const UmLayout& lay, const uint8_t* sm,
+                                           uint32_t sbase, const Ring& rg, const UmBars& ub, uint32_t tmem,
+                                           volatile int* misc)
 {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t IDESC_S = umma_idesc_bf16(64, NP, false);
-    constexpr uint32_t IDESC_O = umma_idesc_bf16(128, NP, true);
-    uint32_t stage = 0, phase = 0, qiter = 0, it = 0, pit = 0, obn = 0;
-    // the tile whose P.V is still to issue (pd_pit: its P buffer use)
-    bool pd_on = false, pd_first = false, pd_last = false;
-    uint32_t pd_pit = 0, pd_stage = 0, pd_ob = 0;
-
-    auto issue_o = [&]() -> bool {
-        const uint32_t sb = pd_pit & 1u;
-        if (!ring_wait(ub.pready + 8 * sb, (pd_pit >> 1) & 1u, misc, a)) return false;
-        if (pd_first && !ring_wait(ub.ofree + 8 * (pd_ob & 1u), ((pd_ob >> 1) & 1u) ^ 1u, misc, a)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-            const uint32_t vb = sbase + lay.stages + pd_stage * lay.stage_bytes + lay.kv_bytes;
-            const uint32_t pb = sbase + lay.pbuf + sb * 2 * lay.p_bytes;
-            const uint32_t od = tmem + 2 * NP + (pd_ob & 1u) * NP;
-#pragma unroll
-            for (int kt = 0; kt < TILE / 16; ++kt) {
-                // V^T: d on M (two 64-wide halves TILE * 128 bytes apart), 16 tokens per k-step
-                const uint64_t av = sw128_mnmajor_desc(vb + kt * 2048, TILE * 128, 1024);
-                umma_bf16(od, av, sw128_kmajor_desc(pb + kt * 32), IDESC_O, (pd_first && kt == 0) ? 0u : 1u);
-                umma_bf16(od, av, sw128_kmajor_desc(pb + lay.p_bytes + kt * 32), IDESC_O, 1u);
-            }
-            umma_commit(ub.pfree + 8 * sb);
-            umma_commit(rg.empty + 8 * pd_stage);
-            if (pd_last) umma_commit(ub.ofull + 8 * (pd_ob & 1u));
-        }
-        __syncwarp();
-        pd_on = false;
-        return true;
-    };
-
+    const UmDescs ds(lay, sbase);
+    uint32_t stage = 0, phase = 0, qiter = 0, it = 0;
     for (;;) {
         const uint32_t qs = qiter & 1u;
         if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) break;
@@ -183,63 +214,105 @@ __device__ __forceinline__ void mma_warp(const KernelArgs& a, const UmLayout& la
         const int t0 = hdr[H_T0], t1 = hdr[H_T1], S = hdr[H_S];
         const bool maxpass = hdr[H_PASS] == PASS_MAX;
         ++qiter;
-        const uint32_t qb = sbase + lay.qring + qs * lay.qslot_bytes;
+        const uint64_t qd = ds.q0 + qs * ds.qslot16;
         int tt = t0, se = (t0 / S + 1) * S;
-        bool first = true;
         bool ok = true;
         while (tt < t1) {
             const int tend = min(min(tt + TILE, se), t1);
-            const uint32_t sb = it & 1u;
-            if (!ring_wait(rg.full + 8 * stage, phase, misc, a) ||
-                !ring_wait(ub.sfree + 8 * sb, ((it >> 1) & 1u) ^ 1u, misc, a)) {
+            const uint32_t sb = it % UM_NSB, suse = it / UM_NSB;
+            if (!ring_wait2(rg.full + 8 * stage, phase, ub.sfree + 8 * sb, (suse & 1u) ^ 1u, misc, a)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t kb = sbase + lay.stages + stage * lay.stage_bytes;
+                const uint64_t kd = ds.k0 + stage * ds.stage16;
                 const uint32_t sd = tmem + sb * NP;
 #pragma unroll
                 for (int ks = 0; ks < UM_D / 16; ++ks) {
                     // K and Q^T: K-major, 32 bytes per 16 of d, the second half of d in its own box
-                    umma_bf16(sd, sw128_kmajor_desc(kb + (ks >> 2) * (TILE * 128) + (ks & 3) * 32),
-                              sw128_kmajor_desc(qb + (ks >> 2) * lay.qhalf_bytes + (ks & 3) * 32), IDESC_S,
-                              ks > 0 ? 1u : 0u);
+                    umma_bf16(sd, kd + (ks >> 2) * ((TILE * 128) >> 4) + (ks & 3) * (32 >> 4),
+                              qd + (ks >> 2) * ds.qhalf16 + (ks & 3) * (32 >> 4), IDESC_S, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(ub.sfull + 8 * sb);
                 if (tend == t1) umma_commit(rg.qempty + 8 * qs);   // the segment's Q slot is read
                 if (maxpass) umma_commit(rg.empty + 8 * stage);
             }
             __syncwarp();
-            if (pd_on && !issue_o()) { ok = false; break; }
-            if (!maxpass) {
-                pd_on = true;
-                pd_pit = pit++;
-                pd_stage = stage;
-                pd_first = first;
-                pd_last = tend == t1;
-                pd_ob = obn;
-            }
-            first = false;
             ++it;
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
             tt = tend;
             if (tt == se) se += S;
         }
-        // the segment's last P.V now: its partial must not wait for the next segment (the
-        // producer may wait for this one's fallback pushes before it emits another)
-        if (ok && pd_on && !issue_o()) ok = false;
+        if (!ok) break;
+    }
+    mma_drain(a, ub, misc);
+}
+
+// P.V of every tile of a sums pass: O^T += V^T P^T, M = d, N = 2 NP (P's bf16 hi parts are the
+// B operand's rows 0 .. NP - 1, its lo parts rows NP .. 2 NP - 1, so one MMA per 16 tokens reads
+// V^T once for both), into the O^T buffer of the segment's parity. Commits release the P buffer
+// and the stage, and after a segment's last tile wake the epilogue.
+template <int NP>
+__device__ __forceinline__ void mma_o_warp(const KernelArgs& a, const UmLayout& lay, const uint8_t* sm,
+                                           uint32_t sbase, const Ring& rg, const UmBars& ub, uint32_t tmem,
+                                           volatile int* misc)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t IDESC_O = umma_idesc_bf16(128, 2 * NP, true);
+    const UmDescs ds(lay, sbase);
+    uint32_t stage = 0, qiter = 0, pit = 0, obn = 0;
+    for (;;) {
+        const uint32_t qs = qiter & 1u;
+        if (!ring_wait(rg.qfull + 8 * qs, (qiter >> 1) & 1u, misc, a)) break;
+        const int* hdr = reinterpret_cast<const int*>(sm + lay.qhdr + qs * QHDR_BYTES);
+        const int kind = hdr[H_KIND];
+        if (kind == KIND_END) break;
+        const int t0 = hdr[H_T0], t1 = hdr[H_T1], S = hdr[H_S];
+        const bool maxpass = hdr[H_PASS] == PASS_MAX;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rg.qempty + 8 * qs);    // header read
+        ++qiter;
+        int tt = t0, se = (t0 / S + 1) * S;
+        bool ok = true, first = true;
+        const uint32_t ob = obn & 1u;
+        while (tt < t1) {
+            const int tend = min(min(tt + TILE, se), t1);
+            if (!maxpass) {
+                const uint32_t pb = pit % UM_NPB, puse = pit / UM_NPB;
+                if (!ring_wait(ub.pready + 8 * pb, puse & 1u, misc, a) ||
+                    (first && !ring_wait(ub.ofree + 8 * ob, ((obn >> 1) & 1u) ^ 1u, misc, a))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t vd = ds.v0 + stage * ds.stage16;
+                    const uint64_t pd = ds.p0 + pb * ds.pbuf16;
+                    const uint32_t od = tmem + UM_NSB * NP + ob * (2 * NP);
+#pragma unroll
+                    for (int kt = 0; kt < TILE / 16; ++kt) {
+                        // V^T: d on M (two 64-wide halves TILE * 128 bytes apart), 16 tokens
+                        // (2048 bytes) per k-step; P^T: 32 bytes per 16 tokens
+                        umma_bf16(od, vd + kt * (2048 >> 4), pd + kt * (32 >> 4), IDESC_O,
+                                  (first && kt == 0) ? 0u : 1u);
+                    }
+                    umma_commit(ub.pfree + 8 * pb);
+                    umma_commit(rg.empty + 8 * stage);
+                    if (tend == t1) umma_commit(ub.ofull + 8 * ob);
+                }
+                __syncwarp();
+                ++pit;
+                first = false;
+            }
+            if (++stage == (uint32_t)rg.nstage) stage = 0;
+            tt = tend;
+            if (tt == se) se += S;
+        }
         if (!ok) break;
         if (!maxpass) ++obn;
     }
-    // every MMA this CTA issued has landed before the tensor memory and the stages are released
-    if (lane == 0) umma_commit(ub.drain);
-    __syncwarp();
-    if (!mbar_wait(ub.drain, 0u) && lane == 0) {
-        misc[0] = 1;
-        set_error(a, FDPP_ERRBIT_TIMEOUT);
-    }
-    __syncwarp();
+    mma_drain(a, ub, misc);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -396,8 +469,8 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
         while (tt < t1) {
             const int tend = min(min(tt + TILE, se), t1);
             const int nvalid = tend - tt;
-            const uint32_t sb = it & 1u;
-            if (!ring_wait(ub.sfull + 8 * sb, (it >> 1) & 1u, misc, a)) return;
+            const uint32_t sb = it % UM_NSB, suse = it / UM_NSB;
+            if (!ring_wait(ub.sfull + 8 * sb, suse & 1u, misc, a)) return;
             tc_fence_after();
             uint32_t v[NV];
             tmem_ld_16x256b<NGW>(tmem + sb * NP + lane_base + 8 * g0, v);
@@ -469,8 +542,8 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
                 // P^T (hi, lo) into the next P buffer, once the MMAs that last read it are done:
                 // stored row n holds the tile's 64 tokens (16-byte chunk k = tokens 8k .. 8k + 7
                 // at chunk k ^ (n % 8), 128-byte swizzle), 8-row groups 1024 bytes apart
-                const uint32_t pbi = pit & 1u;
-                if (!ring_wait(ub.pfree + 8 * pbi, ((pit >> 1) & 1u) ^ 1u, misc, a)) return;
+                const uint32_t pbi = pit % UM_NPB, puse = pit / UM_NPB;
+                if (!ring_wait(ub.pfree + 8 * pbi, (puse & 1u) ^ 1u, misc, a)) return;
                 const uint32_t pb = sbase + lay.pbuf + pbi * 2 * lay.p_bytes;
                 {
                     const int jm = lane >> 3, r = lane & 7;
@@ -553,8 +626,11 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
 #pragma unroll
             for (int ch = 0; ch < NP / 16; ++ch) {
                 if (NP > 16 ? (ch & 1) != hw : hw != 0) continue;
-                float o[16];
-                tmem_ld16(tmem + 2 * NP + ob * NP + lane_base + 16 * ch, o);
+                float o[16], ol[16];
+                tmem_ld16(tmem + UM_NSB * NP + ob * (2 * NP) + lane_base + 16 * ch, o);
+                tmem_ld16(tmem + UM_NSB * NP + ob * (2 * NP) + NP + lane_base + 16 * ch, ol);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o[k] += ol[k];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int n = 16 * ch + k;
@@ -643,15 +719,19 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
     rg.own_done = rg.qempty + 16;
     UmBars ub;
     ub.sfull = rg.own_done + 8;
-    ub.sfree = ub.sfull + 16;
-    ub.pready = ub.sfree + 16;
+    ub.sfree = ub.sfull + 8 * 4;
+    ub.pready = ub.sfree + 8 * 4;
     ub.pfree = ub.pready + 16;
     ub.ofull = ub.pfree + 16;
     ub.ofree = ub.ofull + 16;
     ub.drain = ub.ofree + 16;
     ub.wsync = ub.drain + 8;
-    static_assert(UM_NBARS * 8 >= 16 + 16 + 8 + 6 * 16 + 8 + 8, "barrier region");
-    constexpr uint32_t NCOLS = 4 * NP;      // S^T x 2, O^T x 2
+    static_assert(UM_NSB <= 4 && UM_NPB <= 2, "barrier slots");
+    static_assert(UM_NBARS * 8 >= 16 + 16 + 8 + 2 * 32 + 4 * 16 + 8 + 8, "barrier region");
+    // S^T x UM_NSB (NP each), O^T x 2 (2 NP each), rounded up to a power of two
+    constexpr uint32_t NCOLS_USED = (UM_NSB + 4) * NP;
+    constexpr uint32_t NCOLS = NCOLS_USED <= 64 ? 64 : NCOLS_USED <= 128 ? 128 : NCOLS_USED <= 256 ? 256 : 512;
+    static_assert(NCOLS_USED <= 512, "tensor memory holds 512 columns");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + lay.tslot);
 
     if (threadIdx.x == 0) {
@@ -659,18 +739,20 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
             mbar_init(rg.full + 8 * s, 1);
             mbar_init(rg.empty + 8 * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(rg.qfull + 8 * s, 1);
-            mbar_init(rg.qempty + 8 * s, 1 + UM_NSW);
+        for (int s = 0; s < UM_NSB; ++s) {
             mbar_init(ub.sfull + 8 * s, 1);
             mbar_init(ub.sfree + 8 * s, UM_NSW);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(rg.qfull + 8 * s, 1);
+            mbar_init(rg.qempty + 8 * s, 2 + UM_NSW);   // q.K^T commit, P.V warp, softmax warps
             mbar_init(ub.pready + 8 * s, UM_NSW);
             mbar_init(ub.pfree + 8 * s, 1);
             mbar_init(ub.ofull + 8 * s, 1);
             mbar_init(ub.ofree + 8 * s, UM_NSW);
         }
         mbar_init(rg.own_done, 1);
-        mbar_init(ub.drain, 1);
+        mbar_init(ub.drain, 2);
         mbar_init(ub.wsync, UM_NSW);
         misc[0] = 0;
         misc[1] = 0;
@@ -732,7 +814,9 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
             }
         }
     } else if (warp == UM_MMA_WARP) {
-        mma_warp<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
+        mma_s_warp<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
+    } else if (warp == UM_PV_WARP) {
+        mma_o_warp<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
     } else {
         softmax_warps<NP>(a, lay, sm, sbase, rg, ub, tmem, misc);
         tc_fence_before();
