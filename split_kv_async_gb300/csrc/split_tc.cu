@@ -84,7 +84,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
     uint32_t stage = 0, phase = 0, qiter = 0, un = 0;   // un: segments merged so far
     uint32_t portion = 0;                         // split pieces of own segments finished
     unsigned long long* fslot = reinterpret_cast<unsigned long long*>(sm + lay.fslot);
-    unsigned* taint_s = reinterpret_cast<unsigned*>(sm + lay.fslot + TC_FSLOTS * 8);
+    // per segment parity: a warp switched to the running max (the merge weighs the frames)
+    unsigned* mixed_s = reinterpret_cast<unsigned*>(sm + lay.fslot + TC_FSLOTS * 8);
 
     for (;;) {
         // ---- next segment from the producer ----
@@ -101,8 +102,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         const unsigned redo_mask = (unsigned)hdr[H_MASK];
         const unsigned onl_mask = (unsigned)hdr[H_ONL];
         const bool redo = kind == KIND_REDO;
-        // a redo piece keeps the phi frame for rows whose own split stayed in the window
-        const bool online = (redo && onl_mask != 0u) || (a.mode == FDPP_MODE_FORCE_ONLINE);
+        // a redo piece keeps the phi frame for rows whose own split stayed in the window; a
+        // segment switches to the running max at its first score outside the window (below)
+        bool online = (redo && onl_mask != 0u) || (a.mode == FDPP_MODE_FORCE_ONLINE);
         const uint32_t upar = un & 1u;
         // RG builds: virtual head g = kv head kvh, row group of rows rbase .. rbase + nrow() - 1
         // of the kv head (rows() = the unit's row stride in the run slots); else g is the kv
@@ -144,16 +146,17 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             kseg[1] = hv[1] ? key_limit(a, seq_len, (rbase + head0 + 1) / a.G) - t0 : 0;
         }
         // rows kept in the phi frame inside an online segment (a redo piece's clean rows)
-        const bool frz[2] = {redo && !((onl_mask >> head0) & 1u), redo && !((onl_mask >> (head0 + 1)) & 1u)};
+        bool frz[2] = {redo && !((onl_mask >> head0) & 1u), redo && !((onl_mask >> (head0 + 1)) & 1u)};
         float mrun[2] = {online && !frz[0] ? -INFINITY : phv[0], online && !frz[1] ? -INFINITY : phv[1]};
         unsigned fl[2] = {0u, 0u};
 
         // End of one split piece of an own segment: the four warps' window decisions for it,
         // combined by whichever warp arrives last (one atomic OR on a 64-bit shared word: 4 bits
         // per row, an arrival bit per warp), which writes the rows' flag bytes (the split's own,
-        // or the run slot's edge byte for a first piece that starts inside a split) and marks
-        // the rows with a score outside the window as the segment's taint. Pieces cycle through
-        // TC_FSLOTS words: no warp runs more than a ring's depth of tiles ahead of another.
+        // or the run slot's edge byte for a first piece that starts inside a split). In normal
+        // mode a row-split with a score outside the window was finished with the running max
+        // (the switch below) and is marked recomputed. Pieces cycle through TC_FSLOTS words: no
+        // warp runs more than a ring's depth of tiles ahead of another.
         auto finish_piece = [&](int jp, bool first_piece) {
             unsigned f0 = fl[0], f1 = fl[1];
 #pragma unroll
@@ -172,17 +175,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             old = __shfl_sync(0xffffffffu, old, 0);
             if ((((unsigned)(old >> 32)) | (1u << warp)) != (1u << NCW) - 1u) return;
             const unsigned full = (unsigned)old | word;
-            if (lane == 0) {
-                fslot[ks] = 0ull;
-                unsigned out_rows = 0u;
-#pragma unroll
-                for (int hh = 0; hh < TC_MAX_GROUP; ++hh)
-                    if ((full >> (4 * hh)) & FDPP_FLAG_OUT) out_rows |= 1u << hh;
-                if (out_rows) atomicOr(&taint_s[upar], out_rows);
-            }
+            if (lane == 0) fslot[ks] = 0ull;
             if (lane < nrow()) {
-                const uint8_t fb = (uint8_t)(((full >> (4 * lane)) & 15u) |
-                                             (a.mode == FDPP_MODE_FORCE_ONLINE ? FDPP_FLAG_RECOMPUTED : 0u));
+                const unsigned f = (full >> (4 * lane)) & 15u;
+                const bool rc = a.mode == FDPP_MODE_FORCE_ONLINE ||
+                                (a.mode == FDPP_MODE_NORMAL && (f & FDPP_FLAG_OUT));
+                const uint8_t fb = (uint8_t)(f | (rc ? FDPP_FLAG_RECOMPUTED : 0u));
                 if (first_piece && dest >= 0 && t0 != jp * S)
                     a.xf[(long long)dest * rows() + lane] = fb;
                 else
@@ -191,13 +189,13 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             }
         };
 
-        // The tile loop, built once for the phi frame and once for the running max (redo pieces
-        // and forced online mode), so the hot phi-frame loop stays compact. Tiles are 64 tokens
-        // and never cross a split boundary.
+        // The tile loop, built once for the phi frame and once for the running max (redo pieces,
+        // forced online mode, and a segment after its first score outside the window), so the
+        // hot phi-frame loop stays compact. Tiles are 64 tokens and never cross a split boundary.
+        int tt = t0, se = (t0 / S + 1) * S, jp = j0;
+        bool first_piece = true, to_online = false;
         auto run_tiles = [&](auto online_c) -> bool {
             constexpr bool ONLINE = decltype(online_c)::value;
-            int tt = t0, se = (t0 / S + 1) * S, jp = j0;
-            bool first_piece = true;
             while (tt < t1) {
                 const int tend = min(min(tt + TILE, se), t1);
                 const int nvalid = tend - tt;
@@ -227,6 +225,17 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                     else
                         valid[e] = hv[e & 1] && tok < nvalid;
                     if (valid[e]) fl[e & 1] |= classify(__fsub_rn(sv[e], phv[e & 1]), a.lo, a.hi);
+                }
+                // Normal mode, phi frame: a score of this warp outside the window ends the
+                // phi-frame loop before the tile is used; the running-max loop takes the segment
+                // on from this tile (the tiles before were inside the window, so their sums are
+                // those of the online softmax in the frame phi).
+                if constexpr (!ONLINE) {
+                    if (a.mode == FDPP_MODE_NORMAL &&
+                        __any_sync(0xffffffffu, ((fl[0] | fl[1]) & FDPP_FLAG_OUT) != 0u)) {
+                        to_online = true;
+                        return true;
+                    }
                 }
 
                 float p[4];
@@ -320,6 +329,22 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             return true;
         };
         if (!(online ? run_tiles(std::true_type{}) : run_tiles(std::false_type{}))) return;
+        if (to_online) {
+            // Each row of this warp continues with its running max: the frame phi if the warp
+            // already holds some of the row's sum, else none yet. The merge then weighs the
+            // four warps' frames (the segment's mixed-frame mark).
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float lw = lsum[c];
+#pragma unroll
+                for (int sh = 4; sh < 32; sh <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, sh);
+                mrun[c] = lw > 0.f ? phv[c] : -INFINITY;
+                frz[c] = false;
+            }
+            online = true;
+            if (lane == 0) mixed_s[upar] = 1u;
+            if (!run_tiles(std::true_type{})) return;
+        }
         // ---- this warp's partial: reduce over its 16 tokens (lanes r), fold in the lo part ----
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -338,7 +363,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         // the previous segment's), every warp its rows' l and m; warps 0 and 1 add the slot of
         // their partner, warp 1 hands its sum to warp 0 through slot 1, and warp 0 writes the
         // rows' partial. In the phi frame every warp's m is phi and each weight is exactly 1, so
-        // the sums need no exponentials.
+        // the sums need no exponentials; a segment in which some warp switched to the running
+        // max weighs each warp's sums into the rows' common frame.
         float4* xs = reinterpret_cast<float4*>(sm + lay.xchg);
         float* xl_s = reinterpret_cast<float*>(sm + lay.xrow) + upar * 3 * NCW * TC_MAX_GROUP;
         float* xm_s = xl_s + NCW * TC_MAX_GROUP;
@@ -361,11 +387,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         ++un;
         if (warp >= 2) continue;                   // warps 2 and 3 go on to the next segment
         if (!ring_wait(rg.cbar, upar, misc, a)) return;
+        const bool mix = online || mixed_s[upar] != 0u;
 
         // this warp and its partner (warp + 2), each weighted into the rows' common frame
         {
             float ws[2] = {1.f, 1.f}, wp[2] = {1.f, 1.f};
-            if (online) {
+            if (mix) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     if (!hv[c]) continue;
@@ -381,7 +408,7 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const float4 v = xslot[mt * 32 + lane];
-                if (!online) {
+                if (!mix) {
                     o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
                 } else {
                     o[mt][0] = fmaf(wp[0], v.x, ws[0] * o[mt][0]);
@@ -403,13 +430,10 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
         }
 
         // ---- warp 0: l and m of every row (lane hh for row hh) ----
-        // Rows whose scores left the window in some split of an own segment (its taint, complete
-        // once all four warps have merged) get an empty partial here in normal mode: the fallback
-        // recomputes them piece by piece. A redo piece rewrites its tainted rows only and writes
-        // their flag bytes.
+        // A redo piece (pushed by the tcgen05 build's protocol; this build finishes a row-split
+        // with the running max in place and pushes none) rewrites its tainted rows only and
+        // writes their flag bytes.
         const unsigned write_mask = redo ? redo_mask : 0xffffffffu;
-        const unsigned taint = redo ? 0u : taint_s[upar];
-        const bool refill = !redo && a.mode == FDPP_MODE_NORMAL;
         {
             const int hh = lane;
             float M = 0.f, lam = 0.f;
@@ -419,8 +443,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 for (int w = 1; w < NCW; ++w) M = fmaxf(M, xm_s[w * TC_MAX_GROUP + hh]);
 #pragma unroll
                 for (int w = 0; w < NCW; ++w)
-                    lam = online ? fmaf(frame_weight(xm_s[w * TC_MAX_GROUP + hh], M), xl_s[w * TC_MAX_GROUP + hh], lam)
-                                 : lam + xl_s[w * TC_MAX_GROUP + hh];
+                    lam = mix ? fmaf(frame_weight(xm_s[w * TC_MAX_GROUP + hh], M), xl_s[w * TC_MAX_GROUP + hh], lam)
+                              : lam + xl_s[w * TC_MAX_GROUP + hh];
             }
             if (hh < nrow() && ((write_mask >> hh) & 1u)) {
                 const long long rs = dest >= 0 ? (long long)dest * rows() + hh
@@ -428,9 +452,8 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                                           : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j0;
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
-                const bool empty = refill && ((taint >> hh) & 1u);
-                lp[rs] = empty ? 0.f : lam;
-                mp[rs] = empty ? -INFINITY : M;
+                lp[rs] = lam;
+                mp[rs] = M;
                 if (redo) {
                     const unsigned f0 = ((hh < 4 ? fw0 : fw1) >> ((hh & 3) * 8)) & 0xffu;
                     const unsigned rc = ((onl_mask >> hh) & 1u) ? FDPP_FLAG_RECOMPUTED : 0u;
@@ -439,15 +462,12 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 }
             }
         }
-        if (!redo && lane == 0) taint_s[upar] = 0u;   // ready for the segment after next
         // the partial rows of this lane: head0 and head0 + 1, the run slot or the split's own
         float* orow[2] = {nullptr, nullptr};
-        bool oempty[2] = {false, false};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int hh = head0 + c;
             if (!hv[c] || !((write_mask >> hh) & 1u)) continue;
-            oempty[c] = refill && ((taint >> hh) & 1u);
             orow[c] = dest >= 0 ? a.xo + ((long long)dest * rows() + hh) * D
                                 : a.o_part + (MQ ? unit_row_slot(a, b, kvh, rbase + hh, j0)
                                                  : ((long long)b * a.Hq + kvh * a.G + rbase + hh) * a.max_splits + j0) * D;
@@ -461,6 +481,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
                 o[mt][0] += v.x; o[mt][1] += v.y; o[mt][2] += v.z; o[mt][3] += v.w;
             }
         }
+        // warp 1 has read the mark (mhand): clear it for the segment after next before warps 2
+        // and 3 may go on to it
+        if (lane == 0) mixed_s[upar] = 0u;
         __syncwarp();
         if (lane == 0) mbar_arrive(rg.mdone);      // both slots read: warps 2 and 3 may refill them
 #pragma unroll
@@ -468,22 +491,9 @@ __device__ __forceinline__ void consume(const KernelArgs& a, const TcLayout& lay
             if (orow[c] == nullptr) continue;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
-                orow[c][16 * mt + r] = oempty[c] ? 0.f : o[mt][c];
-                orow[c][16 * mt + r + 8] = oempty[c] ? 0.f : o[mt][c + 2];
+                orow[c][16 * mt + r] = o[mt][c];
+                orow[c][16 * mt + r + 8] = o[mt][c + 2];
             }
-        }
-        // ---- a segment with rows outside the window goes on the device-wide fallback list ----
-        // (every flag byte of its pieces, and warp 0's stores, are ordered before the release
-        // store that publishes the entry)
-        __syncwarp();
-        if (!redo && taint != 0u && a.mode == FDPP_MODE_NORMAL && lane == 0) {
-            const int list = (int)(blockIdx.x % REDO_NLISTS);
-            const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
-            long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
-            ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
-            ent[2] = dest;
-            ent[3] = (long long)taint;
-            st_release_gpu(ent, ((long long)(g * a.max_splits + j0) << 32) | (long long)(unsigned)(b + 1));
         }
         if (lane == 0 && kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
     }
