@@ -69,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--tc-mma", type=int, default=0,
                     help="tensor kernel build for > 8 rows per kv head (0 auto, 1 mma.sync, 2 tcgen05)")
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
+    ap.add_argument("--stress-frac", type=float, default=-1.0,
+                    help="override the workload's fraction of units given a hot key (fallback rate)")
     ap.add_argument("--split-k", type=int, default=0, help="flat GEMM configs: split_k (0 = auto)")
     ap.add_argument("--noalloc", action="store_true",
                     help="time fdpp_decode_attn_noalloc (the library's static scratch) in the "
@@ -354,6 +356,8 @@ def run_fdpp(args, dist: Dist):
     dev = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(dev)
     wl = W.ALL[args.config]
+    if args.stress_frac >= 0:
+        wl = wl.replace(stress_frac=args.stress_frac)
     if dist.world > 1:
         wl = wl.replace(seed=wl.seed + 1000 * dist.rank)      # each rank its own batch
     # the heuristic dataflow's table, measured offline on this GPU model (attn_lut.py): kernel
@@ -593,6 +597,7 @@ def run_fdpp(args, dist: Dist):
                    "seq_len": wl.seq_len if wl.seq_len else list(wl.seq_len_range),
                    "paged": wl.paged, "block_size": wl.block_size if wl.paged else None,
                    "q_tokens": max(1, wl.q_tokens),
+                   "stress_frac": wl.stress_frac,
                    "split_len": diag["split_len"],
                    "split_len_from": ("lookup table" if lut_rows and split_len == 0 else
                                       "scheduler defaults" if split_len == 0 else "workload"),

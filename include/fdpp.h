@@ -12,7 +12,10 @@
  * S tokens. Every split works alone against a unified max phi fixed in advance: it forms
  * o_j = sum exp(s_t - phi) v_t and l_j = sum exp(s_t - phi), with no communication between
  * splits. A split in which some score leaves the safe window, i.e. NOT (lo <= s_t - phi <= hi),
- * is computed again with the ordinary online softmax (running max m_j). The final combine is
+ * gets the ordinary online softmax's partial (running max m_j): the tensor kernel's mma.sync build
+ * continues it with the running max from the first tile holding such a score (the tiles before
+ * were inside the window, so their phi-frame sums stand), its tcgen05 build and the SIMT kernel
+ * compute it again. The final combine is
  * out = sum_j exp(m_j - M) o_j / sum_j exp(m_j - M) l_j with M = max_j m_j, which is the plain
  * sum of the page whenever no split fell back (every m_j = phi).
  *
@@ -76,8 +79,9 @@ enum {
     FDPP_FLAG_BELOW = 4,         /* ... below phi + lo */
     FDPP_FLAG_NAN = 8,           /* ... was NaN */
     FDPP_FLAG_RECOMPUTED = 16,   /* the partial of this row-split came from online softmax */
-    FDPP_FLAG_SLOT = 32          /* tensor kernel: this row-split's own partial slot holds a
-                                    recomputed piece (its run's phi-frame partial left it out) */
+    FDPP_FLAG_SLOT = 32          /* tensor kernel (tcgen05 build): this row-split's own partial
+                                    slot holds a recomputed piece (its run's phi-frame partial
+                                    left it out) */
 };
 
 /* Sticky device error bits (cleared by fdpp_workspace_init). */

@@ -269,6 +269,22 @@ def test_fallback_with_many_rows(build):
     H.assert_parity(got, H.oracle_out(inp), f"stress, many rows, {build}")
 
 
+@pytest.mark.parametrize("q_tokens,build", [(1, "mma_sync"), (4, "mma_sync"), (4, "tcgen05")])
+def test_every_unit_falls_back(q_tokens, build):
+    """A hot key in every unit: the mma.sync build finishes every such row-split in place with the
+    running max (most warps switch mid-segment, and the merge weighs their frames); the tcgen05
+    build streams every tainted piece twice. Decisions, recompute marks and results as for the
+    oracle."""
+    inp, oflags = _stress_inputs(batch=4, seq_len=1024, split_len=256, frac=1.0, num_q_heads=16,
+                                 num_kv_heads=4, q_tokens=q_tokens)
+    tc = F.FDPP_TC_MMA_TCGEN05 if build == "tcgen05" else F.FDPP_TC_MMA_SYNC
+    diag = _check_fallback(inp, oflags, f"every unit falls back, {q_tokens} tokens, {build}", tc_mma=tc)
+    # (a hot key in a sequence's last positions is hidden from the chunk's first query tokens)
+    assert diag["n_flagged_units"] >= 0.8 * diag["n_units"]
+    if q_tokens > 1:
+        assert diag["tc_build"] == tc
+
+
 def _check_fallback(inp, oflags, what, **kw):
     dinp = H.DeviceInputs(inp)
     got, diag, flags, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, **kw)
