@@ -16,6 +16,8 @@ the passage of the pages it follows:
   section 3: a score past the phi criterion sends its block back to online softmax).
 * ``split_method``     -- the method's steps in fp64: phi-frame partials per split, detect,
   online recompute, max-rescaled (plain when nothing fell back) sum.
+* ``inplace_partial``  -- one row's partial when a block continues in place with the running max
+  from its first tile holding an out-of-window score (oracle.c, R11).
 * ``split_len`` / ``plan`` -- the split scheduler restated: n_b = ceil(L_b / S).
 * several query tokens per sequence (``make_problem(q_tokens=Tq)``): the last Tq positions,
   causal (oracle.c, R9); every function above then works on the B*Tq query rows.
@@ -112,6 +114,10 @@ def _load():
             lib.or_flat_gemm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          vp, vp, ip, ctypes.c_int, vp, ctypes.c_int]
             lib.or_flat_gemm.restype = ctypes.c_int
+            lib.or_inplace_partial.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                               vp, vp, vp]
+            lib.or_inplace_partial.restype = ctypes.c_int
             lib.or_default_threads.argtypes = []
             lib.or_default_threads.restype = ctypes.c_int
             _lib = lib
@@ -255,6 +261,22 @@ def split_method(prob, q, k, v, seq_lens, split_len, max_splits, mode=MODE_NORMA
                         _ptr(res.get("part_o")), _ptr(res.get("part_l")),
                         _ptr(res.get("part_m")), _ptr(res["flags"]), _ptr(ph), n_threads)
     return res
+
+
+def inplace_partial(s, v, tile, phi, lo, hi):
+    """One softmax row's partial by oracle.c R11 (the in-place finish of a block whose scores
+    leave the window). s: scaled scores [n], v: values [n][d]. Returns (o [d], l, m, switched)."""
+    lib = _load()
+    s = np.ascontiguousarray(s, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64).reshape(len(s), -1)
+    o = np.zeros(v.shape[1], dtype=np.float64)
+    l = np.zeros(1, dtype=np.float64)
+    m = np.zeros(1, dtype=np.float64)
+    sw = lib.or_inplace_partial(_ptr(s), _ptr(v), len(s), v.shape[1], int(tile), float(phi),
+                                float(lo), float(hi), _ptr(o), _ptr(l), _ptr(m))
+    if sw < 0:
+        raise ValueError("or_inplace_partial: bad arguments")
+    return o, float(l[0]), float(m[0]), bool(sw)
 
 
 def split_len(seq_lens, num_kv_heads, max_seq_len, split_len_req, num_sms, units_per_sm,

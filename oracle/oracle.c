@@ -47,6 +47,14 @@
  *       (N x K). Read as y = x W^T with x [M][K] and W [N][K] row-major (a linear layer's weight
  *       as stored), C[m][n] = sum_k x[m][k] W[n][k]. The pages give no layout or dtype; bf16 in,
  *       as for the cache.
+ *   R11 "The block stops and is recomputed with the ordinary online softmax" ([theory] s3) is read
+ *       as a statement about the block's result: its partial is the online softmax's. Taking the
+ *       block's tiles in order and testing each tile's scores before using them, the tiles before
+ *       the first one holding a score outside the window are all inside it, so their phi-frame
+ *       sums are the online softmax's sums in the frame phi (the two formulas of s3 agree for any
+ *       shift); from that tile on the block continues with the running max, starting from phi when
+ *       some sum is already held and from nothing otherwise. or_inplace_partial restates these
+ *       steps for one softmax row, so that the tests can hold them against the plain definition.
  *
  * Precision: every value is widened exactly to double (bf16 and fp32 both widen exactly);
  * all arithmetic is double. Threads: rows are independent, and are spread over pthreads.
@@ -512,6 +520,45 @@ int or_split_method(const or_problem* p, const void* q, const void* k, const voi
     or_split_ctx c = { p, q, k, v, block_table, seq_lens, rows, S, max_splits, mode,
                        out, part_o, part_l, part_m, flags, phi_heads };
     return or_parallel_rows(or_split_row, &c, n_rows, n_threads);
+}
+
+/* One softmax row's partial by R11: scores s[n] (already scaled), values v[n][d], tiles of `tile`
+ * tokens. Writes o[d], *l and *m (the frame: phi, or the last running max) and returns 1 if the row
+ * switched to the running max. */
+int or_inplace_partial(const double* s, const double* v, int n, int d, int tile, double phi,
+                       double lo, double hi, double* o, double* l, double* m)
+{
+    if (n < 0 || d < 1 || tile < 1) return -1;
+    for (int i = 0; i < d; ++i) o[i] = 0.0;
+    double ll = 0.0, mm = phi;
+    int online = 0;
+    for (int t0 = 0; t0 < n; t0 += tile) {
+        int t1 = t0 + tile < n ? t0 + tile : n;
+        if (!online) {
+            /* the tile's scores are tested before any of them is used */
+            int out = 0;
+            for (int t = t0; t < t1; ++t) out |= or_classify(s[t] - phi, lo, hi) & OR_FLAG_OUT;
+            if (out) {
+                online = 1;
+                if (!(ll > 0.0)) mm = -INFINITY;    /* nothing held yet: the plain online start */
+            }
+        }
+        for (int t = t0; t < t1; ++t) {
+            if (online) {
+                double mnew = s[t] > mm ? s[t] : mm;
+                double corr = mm == -INFINITY ? 0.0 : exp(mm - mnew);
+                ll *= corr;
+                for (int i = 0; i < d; ++i) o[i] *= corr;
+                mm = mnew;
+            }
+            double w = exp(s[t] - mm);
+            ll += w;
+            for (int i = 0; i < d; ++i) o[i] += w * v[(size_t)t * (size_t)d + (size_t)i];
+        }
+    }
+    *l = ll;
+    *m = mm;
+    return online;
 }
 
 /* ----------------------------------------------------------------------------------------- */

@@ -554,3 +554,42 @@ def test_query_tokens_split_method_and_decisions():
     # sequence 2 has 2 keys for 3 query tokens: its first query row sees none
     np.testing.assert_array_equal(exact.reshape(B, Tq, Hq, d)[2, 0], 0.0)
     assert np.abs(exact.reshape(B, Tq, Hq, d)[2, 1]).sum() > 0
+
+
+@pytest.mark.parametrize("tile", [1, 3, 16, 64])
+def test_inplace_finish_is_the_online_softmax(tile):
+    """oracle.c R11: a row that continues in place with the running max from its first tile holding
+    a score outside the window ends with the softmax of the plain definition (scipy's softmax
+    here, a library routine), whatever the tile size; a row whose scores all stay inside keeps the
+    phi frame (m = phi, l = sum exp(s - phi)); and the frame it ends in is the running max over
+    phi (when some sum was held before the switch) and the scores from the switching tile on."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(100 + tile)
+    phi, lo, hi = 0.0, -30.0, 10.0
+    switched = 0
+    for trial in range(240):
+        n, d = int(rng.integers(1, 200)), 4
+        s = rng.standard_normal(n) * 3.0
+        kind = trial % 4
+        if kind == 1:                                   # one score far above phi + hi
+            s[int(rng.integers(0, n))] += 40.0
+        elif kind == 2:                                 # every score far below phi + lo
+            s -= 45.0
+        elif kind == 3:                                 # a few scores far below phi + lo
+            s[rng.integers(0, n, size=3)] -= 60.0
+        v = rng.standard_normal((n, d))
+        o, l, m, sw = oracle.inplace_partial(s, v, tile, phi, lo, hi)
+        np.testing.assert_allclose(o / l, softmax(s) @ v, rtol=1e-10, atol=1e-12)
+        inside = (s - phi >= lo) & (s - phi <= hi)
+        assert sw == (not inside.all())
+        if not sw:
+            assert m == phi
+            np.testing.assert_allclose(l, math.fsum(np.exp(s - phi)), rtol=1e-13)
+        else:
+            switched += 1
+            first = int(np.argmin(inside)) // tile * tile        # the switching tile's first token
+            held = first > 0
+            expect_m = max(([phi] if held else []) + list(s[first:]))
+            assert m == expect_m
+            np.testing.assert_allclose(l, math.fsum(np.exp(s - m)), rtol=1e-12)
+    assert switched >= 120
