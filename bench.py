@@ -69,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--tc-mma", type=int, default=0,
                     help="tensor kernel build for > 8 rows per kv head (0 auto, 1 mma.sync, 2 tcgen05)")
     ap.add_argument("--split-len", type=int, default=-1, help="override split_len (0 = auto)")
+    ap.add_argument("--q-tokens", type=int, default=0,
+                    help="override the workload's query tokens per sequence (rows per kv head = q_tokens G)")
     ap.add_argument("--stress-frac", type=float, default=-1.0,
                     help="override the workload's fraction of units given a hot key (fallback rate)")
     ap.add_argument("--split-k", type=int, default=0, help="flat GEMM configs: split_k (0 = auto)")
@@ -358,6 +360,8 @@ def run_fdpp(args, dist: Dist):
     wl = W.ALL[args.config]
     if args.stress_frac >= 0:
         wl = wl.replace(stress_frac=args.stress_frac)
+    if args.q_tokens > 0:
+        wl = wl.replace(q_tokens=args.q_tokens)
     if dist.world > 1:
         wl = wl.replace(seed=wl.seed + 1000 * dist.rank)      # each rank its own batch
     # the heuristic dataflow's table, measured offline on this GPU model (attn_lut.py): kernel
