@@ -26,7 +26,7 @@ DEFAULT_TABLE = os.path.join(HERE, "attn_lut_gb300.json")
 HKV, HEAD_DIM = 8, 128
 BATCHES = (1, 8, 64)                  # range tops; the last range is open
 SEQ_LENS = (2048, 16384, 131072)
-ROWS = (4, 8, 16)                     # query rows per kv head (one query token: G)
+ROWS = (4, 8, 16, 64)                 # query rows per kv head (one query token: G; 64: a prefill chunk)
 UNITS = (1, 2, 4, 8, 16)
 MIN_SPLIT = 256
 MAX_TOKENS = 1 << 21                  # batch x length measured (larger shapes take their range)
