@@ -133,6 +133,17 @@ bool um_applies(const fdpp_params& p)
     return p.dtype == FDPP_BF16 && p.head_dim == 128 && R > TC_MAX_GROUP && R <= TC_MAX_ROWS;
 }
 
+// The tcgen05 build's ring depth for short parts (measured on a GB300: 4 stages beat 5 at 27
+// tiles per CTA, tie at 54, lose at 108).
+constexpr int UM_SHORT_STAGES = 4;
+constexpr int UM_SHORT_TILES = 48;
+
+// The tcgen05 build's cost of a run boundary inside a CTA's part (the epilogue of one run and the
+// start of the next, while its stream waits), in 64-token tiles at the copy rate: the partition
+// counts that many phantom tiles between units, so a part that holds a boundary takes fewer tiles.
+// Measured best on a GB300 over 134 MB caches at 16, 32 and 64 rows per kv head.
+int um_seg_tiles(int R) { return R > 32 ? 9 : 6; }
+
 // The tensor kernel of this call is the tcgen05 build (tc_mma, and the geometry asked for).
 bool um_selected(const fdpp_params& p)
 {
@@ -380,6 +391,7 @@ KernelArgs kernel_args(const fdpp_params& P, const WsLayout& w, void* workspace,
     const AutoChoice ch = auto_choice(*p);
     a.auto_units = ch.units;
     a.auto_min = ch.min_split;
+    a.seg_tiles = um ? um_seg_tiles(a.R) : 0;
     return a;
 }
 
@@ -546,9 +558,14 @@ fdpp_status fdpp_decode_attn_timed(const void* q, const void* k_cache, const voi
     if (ev_split_begin && (e = cudaEventRecord((cudaEvent_t)ev_split_begin, s)) != cudaSuccess)
         return fail(FDPP_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
     if (um) {
-        // tcgen05 build: one CTA per SM with the deepest ring that fits (or the one asked for)
+        // tcgen05 build: one CTA per SM with the deepest ring that fits (or the depth asked for),
+        // but UM_SHORT_STAGES when every CTA streams few tiles (at most UM_SHORT_TILES, counted at
+        // max_seq_len): at the start each CTA asks for its whole ring at once, and a shallower
+        // ring lands its first tile sooner, which only short parts do not win back.
         const int budget = std::min(dev.smem_per_block, dev.smem_per_sm - 1024);
-        int ns = p->tc_stages > 0 ? p->tc_stages : 8;
+        const long long tiles_max = (long long)((p->max_seq_len + 63) / 64) * p->batch * p->num_kv_heads;
+        const bool short_parts = tiles_max <= (long long)UM_SHORT_TILES * dev.sms;
+        int ns = p->tc_stages > 0 ? p->tc_stages : (short_parts ? UM_SHORT_STAGES : 8);
         while (ns >= 2 && split_um_smem_bytes(R, ns, p->batch) > budget) --ns;
         if (ns < 2 || (p->tc_stages > 0 && ns != p->tc_stages))
             return fail(FDPP_ERR_UNSUPPORTED, "no tcgen05 geometry fits (stages %d)", p->tc_stages);

@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(NWC * 32) combine_kernel(KernelArgs a)
     const long long fbase = (long long)row * a.max_splits;   // the row's flag bytes and split slots
 
     // Runs of the row's head u = (grp, b, kvh): it owns tiles [W, W + nt) of the split kernel's
-    // order (row group, b, kv head, j); part c = tiles [floor(c T / P), floor((c + 1) T / P)).
+    // order (row group, b, kv head, j), at [V, V + nt) in the cut stream that counts K phantom
+    // tiles between heads (V = W + K u); part c = [floor(c T / P), floor((c + 1) T / P)) of that
+    // stream (T with the phantoms).
     const int P = a.hdr[HDR_PARTS];
     long long W = 0, tiles = 1;
     int nt = 0, TS = 1, c_first = 0, n_r = 0, u = 0;
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(NWC * 32) combine_kernel(KernelArgs a)
         nt = a.tstart[b + 1] - a.tstart[b];
         W = (long long)grp * a.Hkv * a.tstart[a.B] + (long long)a.Hkv * a.tstart[b] + (long long)kvh * nt;
         u = (grp * a.B + b) * a.Hkv + kvh;
+        W += (long long)a.hdr[HDR_SEGK] * u;
         // the parts holding tiles W and W + nt - 1
         c_first = (int)(((W + 1) * P - 1) / tiles);
         n_r = (int)(((W + nt) * P - 1) / tiles) - c_first + 1;

@@ -24,8 +24,10 @@ enum {
                          //   from list i (read together as one 8-byte word), i < REDO_NLISTS;
                          //   zeroed by the combine kernel
     HDR_PARTS = 11,     // tensor kernel: parts P of the tile-balanced partition (0: none)
-    HDR_TILES = 12,     // tensor kernel: 64-token tiles T of all units together
+    HDR_TILES = 12,     // tensor kernel: 64-token tiles T of all units together, with phantoms
     HDR_TC_BUILD = 13,  // tensor kernel build that ran: 1 mma.sync, 2 tcgen05 (split_um.cu)
+    HDR_SEGK = 14,      // tensor kernel: phantom tiles between units in the partition (HDR_TILES
+                        //   counts them)
     HDR_WORDS = 64
 };
 
@@ -98,6 +100,9 @@ struct KernelArgs {
     int NRG, Rg, Hv;
     // split_len == 0: the split scheduler's units per SM and least split length (dataflow table)
     int auto_units, auto_min;
+    // Tensor kernel partition: phantom tiles counted between consecutive units (row group,
+    // sequence, kv head) of the tile order, the time a run boundary inside a part costs (0: none)
+    int seg_tiles;
 };
 
 // Query rows per kv head (R = Tq * G): the tensor kernel takes 8 rows per unit (the columns of one

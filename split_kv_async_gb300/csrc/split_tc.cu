@@ -550,25 +550,15 @@ __global__ void __launch_bounds__(NTHREADS, MINB)
     }
     __syncthreads();
     // Launched as a programmatic dependent: nothing is read into the CTA or written before the
-    // previous kernel on the stream has completed. Before that, while it finishes, the tiles this
-    // CTA streamed first in the last call (contiguous caches) are prefetched into L2: the split
-    // plan changes little from one decode step to the next. A stale hint costs a useless
-    // prefetch only (L2 is where the previous kernel's writes land).
-    if (!PAGED && warp == NCW && lane == 0 && blockIdx.x < TC_MAX_PARTS) {
+    // previous kernel on the stream has completed. Before that, consumer warp 0 (idle until the
+    // first tiles land) brings into L2 the sequence lengths the producer's plan starts from and
+    // the start-up hint's tiles.
+    if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
-        const volatile int* h = a.hint + (long long)blockIdx.x * HINT_WORDS;
-        const int n = min(max(h[0], 0), HINT_TILES);
-        for (int i = 0; i < n; ++i) {
-            const int x = h[1 + 3 * i], y = h[2 + 3 * i], z = h[3 + 3 * i];
-            if (x < 0 || (x & 63) != 0) continue;
-#pragma unroll
-            for (int hv = 0; hv < D / 64; ++hv) {
-                tma_prefetch_3d(&tmK, x + 64 * hv, y, z);
-                tma_prefetch_3d(&tmV, x + 64 * hv, y, z);
-            }
-        }
+        for (int b = 0; b < a.B && b < 32 * 8; b += 32) prefetch_l2(a.seq_lens + b);
     }
+    if (!PAGED && warp == 0 && blockIdx.x < TC_MAX_PARTS) prefetch_hint<D>(a, &tmK, &tmV);
     grid_dependency_wait();
 
     int* plan = reinterpret_cast<int*>(sm + lay.plan);

@@ -88,6 +88,31 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
+// The start-up hint, by one whole warp before the programmatic dependency wait: the K/V tiles this
+// CTA streamed first in the last call go into L2 (contiguous caches; the plan changes little from
+// one decode step to the next, and a stale hint costs a useless prefetch only). The hint's words
+// arrive in one read, and each lane prefetches one tile.
+template <int D>
+__device__ __forceinline__ void prefetch_hint(const KernelArgs& a, const CUtensorMap* tmK, const CUtensorMap* tmV)
+{
+    static_assert(HINT_WORDS <= 32 && 1 + 3 * HINT_TILES <= HINT_WORDS, "hint layout");
+    const int lane = threadIdx.x & 31;
+    const int* h = a.hint + (long long)blockIdx.x * HINT_WORDS;
+    const int w = lane < HINT_WORDS ? __ldcg(h + lane) : 0;
+    const int n = min(max(__shfl_sync(0xffffffffu, w, 0), 0), HINT_TILES);
+    const int i = min(lane, HINT_TILES - 1);
+    const int x = __shfl_sync(0xffffffffu, w, 1 + 3 * i);
+    const int y = __shfl_sync(0xffffffffu, w, 2 + 3 * i);
+    const int z = __shfl_sync(0xffffffffu, w, 3 + 3 * i);
+    if (lane < n && x >= 0 && (x & 63) == 0) {
+#pragma unroll
+        for (int hv = 0; hv < D / 64; ++hv) {
+            tma_prefetch_3d(tmK, x + 64 * hv, y, z);
+            tma_prefetch_3d(tmV, x + 64 * hv, y, z);
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // producer warp
 // ------------------------------------------------------------------------------------------
@@ -114,6 +139,7 @@ struct Producer {
     int* lplan;                //   clamped L_b [B] (n_b = min(ceil(L_b / S), max_splits))
     const CUtensorMap* tmQ = nullptr;   // Lay::UM: q as {d, Hq, Tq, B}, box {64, G, Tq, 1}
     int S = 0, TS = 0;         // split length, tiles of a full split
+    int K = 0;                 // phantom tiles after each unit in the cut of own work
     uint32_t stage = 0, phase = 0, qiter = 0;
     int hint_n = 0;            // tiles recorded in this CTA's start-up hint
     bool bad_block = false;
@@ -416,7 +442,10 @@ struct Producer {
     // runs, one per (sequence, virtual head) it touches; a run may cover several splits and
     // begin or end inside one. Each run leaves one phi-frame partial, in run slot c + u (u: the
     // index of the (row group, sequence, kv head) in tile order; the slots of all runs are
-    // distinct), and the flag bytes split by split.
+    // distinct), and the flag bytes split by split. With K > 0 the cut is made in a stream where
+    // K phantom tiles follow each unit (T counts them; unit u's tiles start at W_u + K u): a part
+    // that holds a run boundary, which costs the CTA about K tiles' time, takes K tiles fewer. A
+    // phantom position starts the next unit.
     // RG builds order the tiles group-major, (row group, b, kv head, j): the groups' ranges
     // have the same shape, so parts c, c + P / NRG, ... read the same K/V tiles at about the
     // same time and all but the first find them in L2.
@@ -432,47 +461,71 @@ struct Producer {
         const long long tb = (long long)c * q + (c * r) / P;
         const long long te = (long long)(c + 1) * q + ((c + 1) * r) / P;
         const int zero4[4] = {0, 0, 0, 0};
-        struct Seg { int b, g, j, t0, t1, L, ntile, dest; };
+        struct Seg { int b, g, kvh, j, t0, t1, L, ntile, dest; };
         const int nseq = A.B;
         int cb = 0, cgrp = 0;
-        auto seg_at = [&](long long t, Seg& s) {
-            long long tg = t;                        // tile index within the row group
-            int grp = 0;
-            if constexpr (RG) {
-                const long long TG = (long long)A.Hkv * tplan[A.B];
-                grp = (int)(t / TG);
-                tg = t - grp * TG;
-                if (grp != cgrp) { cgrp = grp; cb = 0; }
+        // The run at virtual tile v (moved past phantoms to the next unit's first tile); false
+        // once the part holds no more real tiles. (K is 0 outside the tcgen05 build.)
+        auto seg_at = [&](long long& v, Seg& s) -> bool {
+            const int K = Lay::UM ? this->K : 0;
+            for (;;) {
+                if (v >= te) return false;
+                long long vg = v;                    // virtual tile within the row group
+                int grp = 0;
+                if constexpr (RG) {
+                    const long long TG = (long long)A.Hkv * (tplan[A.B] + (long long)K * A.B);
+                    grp = (int)(v / TG);
+                    vg = v - grp * TG;
+                    if (grp != cgrp) { cgrp = grp; cb = 0; }
+                }
+                while ((long long)A.Hkv * (tplan[cb + 1] + (long long)K * (cb + 1)) <= vg) ++cb;
+                const int ntb = tplan[cb + 1] - tplan[cb];
+                const int r = (int)(vg - (long long)A.Hkv * (tplan[cb] + (long long)K * cb));
+                const int kvh = r / (ntb + K);
+                const int k = r - kvh * (ntb + K);   // tile of sequence cb, kv head kvh
+                if (Lay::UM && k >= ntb) {           // a phantom: the next unit's first tile
+                    v += ntb + K - k;
+                    continue;
+                }
+                s.b = cb;
+                s.g = RG ? kvh * A.NRG + grp : kvh;
+                s.kvh = kvh;
+                // the run: tiles k .. kend - 1 of the sequence's ntb (split j has tiles j TS .. j TS +
+                // TS - 1, the last split fewer), tokens t0 .. t1
+                const int kend = (int)min((long long)ntb, k + (te - v));
+                s.j = k / TS;
+                s.L = lplan[cb];
+                s.t0 = s.j * S + (k - s.j * TS) * TILE;
+                if (kend >= ntb) {
+                    s.t1 = s.L;
+                } else {
+                    const int je = kend / TS;
+                    s.t1 = je * S + (kend - je * TS) * TILE;
+                }
+                s.ntile = kend - k;
+                s.dest = c + (grp * nseq + cb) * A.Hkv + kvh;
+                return true;
             }
-            while ((long long)A.Hkv * tplan[cb + 1] <= tg) ++cb;
-            const int ntb = tplan[cb + 1] - tplan[cb];
-            const int r = (int)(tg - (long long)A.Hkv * tplan[cb]);
-            s.b = cb;
-            const int kvh = r / ntb;
-            s.g = RG ? kvh * A.NRG + grp : kvh;
-            const int k = r - kvh * ntb;             // tile of sequence cb, kv head kvh
-            // the run: tiles k .. kend - 1 of the sequence's ntb (split j has tiles j TS .. j TS +
-            // TS - 1, the last split fewer), tokens t0 .. t1
-            const int kend = (int)min((long long)ntb, k + (te - t));
-            s.j = k / TS;
-            s.L = lplan[cb];
-            s.t0 = s.j * S + (k - s.j * TS) * TILE;
-            if (kend >= ntb) {
-                s.t1 = s.L;
-            } else {
-                const int je = kend / TS;
-                s.t1 = je * S + (kend - je * TS) * TILE;
-            }
-            s.ntile = kend - k;
-            s.dest = c + (grp * nseq + cb) * A.Hkv + kvh;
         };
         Seg cur, nxt;
         long long t = tb;
-        seg_at(t, cur);
+        if (!seg_at(t, cur)) return true;            // phantoms only
         int cur_ent = PAGED ? window_entry(cur.b, cur.t0, cur.L) : -1;
         for (;;) {
-            const long long tn = t + cur.ntile;
-            const bool last = tn >= te;
+            long long tn = t + cur.ntile;
+            // Whether a real tile remains: a run that ends before te ends at its unit's last tile,
+            // and the next unit (past K phantoms) is the sequence's next kv head, which has tiles,
+            // or the next sequence's first, which may have none.
+            bool last = tn >= te;
+            if (Lay::UM && !last && K > 0) {
+                if (te <= tn + K) {
+                    last = true;
+                } else if (cur.kvh + 1 >= A.Hkv) {
+                    long long v = tn;
+                    Seg probe;
+                    last = !seg_at(v, probe);
+                }
+            }
             // The next segment is located after this one is issued (its block-table window is
             // loaded while the ring holds this segment's tiles), unless the L2 prefetch wants
             // its first tiles now.
@@ -545,23 +598,48 @@ struct Producer {
         long long T = 0;
         const int n_units = make_plan(T);
         const bool in_smem = A.B <= PLAN_SMEM_MAX_B;
-        const int P = (in_smem && T > 0 && T < (1ll << 31))
+        // The cut stream (tcgen05 build): the real tiles and K phantoms after each unit. None where
+        // the equal cut already ends parts at unit boundaries only (units of equal length, U
+        // dividing P). The mma.sync builds cut the real tiles (their run boundaries cost little).
+        const long long U = (long long)A.NRG * A.B * A.Hkv;      // units (runs' heads)
+        const int P = (in_smem && T > 0 && T + (Lay::UM ? (long long)A.seg_tiles * U : 0ll) < (1ll << 31))
                           ? (int)min(min((long long)gridDim.x, T), (long long)TC_MAX_PARTS) : 0;
+        if constexpr (Lay::UM) {
+            bool eq = true;
+            if (in_smem)
+                for (int b = lane; b < A.B; b += 32) eq = eq && tplan[b + 1] - tplan[b] == tplan[1] - tplan[0];
+            eq = __all_sync(0xffffffffu, eq);
+            K = (eq && P > 0 && P % (int)U == 0) ? 0 : A.seg_tiles;
+        }
+        const long long TV = T + (long long)K * U;
         if (blockIdx.x == 0 && lane == 0) {
             A.hdr[HDR_PARTS] = P;
-            A.hdr[HDR_TILES] = P > 0 ? (int)T : 0;
+            A.hdr[HDR_TILES] = P > 0 ? (int)TV : 0;
+            A.hdr[HDR_SEGK] = K;
         }
         bool had_own = false;
-        const bool ok = P > 0 ? run_parts<D, PAGED>(T, P, had_own) : run_units<D, PAGED>(n_units, had_own);
+        const bool ok = P > 0 ? run_parts<D, PAGED>(TV, P, had_own) : run_units<D, PAGED>(n_units, had_own);
         if (!ok) return;
 
-        if (A.mode == FDPP_MODE_NORMAL) {
-            // The consumers push this CTA's flagged segments before they report the own work done.
-            // The list is REDO_NLISTS lists, CTA c pushing to list c % REDO_NLISTS: a CTA drains
-            // its own list first, then the others in turn, so that few CTAs contend for one
-            // list's claim word.
+        // The fallback lists. Only the tcgen05 build pushes (the mma.sync builds finish an
+        // out-of-window row-split in place), and there every CTA that pushed drains the lists after
+        // its push, so no entry is left behind; a CTA that pushed nothing helps only if entries
+        // were waiting when its last own tiles had been issued (read now, while they stream).
+        // The consumers push this CTA's flagged segments (misc[1]) before they report the own
+        // work done. The list is REDO_NLISTS lists, CTA c pushing to list c % REDO_NLISTS: a CTA
+        // drains its own list first, then the others in turn, so that few CTAs contend for one
+        // list's claim word.
+        if (Lay::UM && A.mode == FDPP_MODE_NORMAL) {
+            bool help = false;
+            if (lane < REDO_NLISTS) {
+                const unsigned long long both = ld_relaxed_gpu_u64(
+                    reinterpret_cast<const unsigned long long*>(&A.hdr[HDR_REDO_LISTS + 2 * lane]));
+                help = (int)(unsigned)(both & 0xffffffffull) > (int)(unsigned)(both >> 32);
+            }
+            help = __any_sync(0xffffffffu, help);
             if (had_own && !ring_wait(rg.own_done, 0u, misc, A)) return;
-            for (;;) {
+            help = help || misc[1] != 0;
+            while (help) {
                 // every list's (count, taken) in one read, a lane per list starting at this CTA's
                 const int my = (int)((blockIdx.x + lane) % REDO_NLISTS);
                 bool pending = false;

@@ -81,18 +81,20 @@ constexpr int UM_NSB = 3;
 //   fsw/fcnt per split piece in flight: each lane quadrant's flag nibble of every row (the two
 //            warps of a quadrant hold different rows), arrival count
 //   taint    the rows with a score outside the window, per segment parity (64-bit)
-//   xl/xm    per lane quadrant and row: the l sum of a segment, the max of a max pass
+//   xl/xm    per lane quadrant and row: the l sum of a segment (per segment parity), the max of
+//            a max pass
+//   rowoff   per row n = i G + h: its offset (i Hq + h) max_splits in the split-slot order
 struct UmLayout {
     static constexpr bool UM = true;
     int stage_bytes, kv_bytes, qslot_bytes, qhalf_bytes, p_bytes;
-    int stages, qring, pbuf, qhdr, fsw, fcnt, taint, xl, xm, plan, bars, misc, tslot, total;
+    int stages, qring, pbuf, qhdr, fsw, fcnt, taint, xl, xm, rowoff, plan, bars, misc, tslot, total;
 
     __host__ __device__ static constexpr int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
     __host__ __device__ UmLayout(int NP, int nstage, int B)
         : stage_bytes(2 * TILE * UM_D * 2), kv_bytes(TILE * UM_D * 2), qslot_bytes(2 * NP * 128),
           qhalf_bytes(NP * 128), p_bytes(NP * 128), stages(0), qring(0), pbuf(0), qhdr(0), fsw(0),
-          fcnt(0), taint(0), xl(0), xm(0), plan(0), bars(0), misc(0), tslot(0), total(0)
+          fcnt(0), taint(0), xl(0), xm(0), rowoff(0), plan(0), bars(0), misc(0), tslot(0), total(0)
     {
         qring = stages + nstage * stage_bytes;
         pbuf = qring + 2 * qslot_bytes;
@@ -101,8 +103,9 @@ struct UmLayout {
         fcnt = fsw + UM_FSLOTS * 4 * UM_MAX_ROWS;
         taint = fcnt + UM_FSLOTS * 4;
         xl = taint + 2 * 8;
-        xm = xl + 4 * UM_MAX_ROWS * 4;
-        plan = xm + 4 * UM_MAX_ROWS * 4;
+        xm = xl + 2 * 4 * UM_MAX_ROWS * 4;
+        rowoff = xm + 4 * UM_MAX_ROWS * 4;
+        plan = rowoff + UM_MAX_ROWS * 8;
         const int plan_ints = (B <= PLAN_SMEM_MAX_B ? 2 * B + 1 : 0) + 1;
         bars = round_up(plan + plan_ints * 4, 8);
         misc = bars + (2 * nstage + UM_NBARS) * 8;
@@ -340,6 +343,7 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
     unsigned long long* taint_s = reinterpret_cast<unsigned long long*>(sm + lay.taint);
     float* xl_s = reinterpret_cast<float*>(sm + lay.xl);
     float* xm_s = reinterpret_cast<float*>(sm + lay.xm);
+    const long long* rowoff_s = reinterpret_cast<const long long*>(sm + lay.rowoff);
     uint32_t stage = 0, phase = 0, qiter = 0, it = 0, pit = 0, obn = 0, portion = 0, un = 0, nsync = 0;
     const int R = a.R;
     const float c_exp = a.scale * LOG2E;          // p = 2^(acc scale log2e - frame log2e)
@@ -377,6 +381,8 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
         // causal limit of the query token with the fewest keys (row 0): a tile wholly below it
         // needs no per-row mask
         const int lim0 = key_limit(a, L, 0);
+        // split j0's slot of row 0; row n of split j is at slot0 + (j - j0) + rowoff_s[n]
+        const long long slot0 = (((long long)b * a.Tq) * a.Hq + (long long)g * a.G) * a.max_splits + j0;
 
         // Per row of this thread: the frame of the sums (phi, or the max pass's M) times log2 e,
         // the causal key limit (absolute token index), the window trackers on the raw q.k
@@ -403,11 +409,10 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
             lsum[c] = 0.f;
         }
 
-        // End of one split piece of an own segment: each row's window decision from the trackers,
-        // ORed over the warp's tokens, then over the eight warps by whichever arrives last, which
-        // writes the flag bytes (the split's own, or the run slot's edge byte for a first piece
-        // that starts inside a split) and marks the segment's taint.
-        auto finish_piece = [&](int jp, bool first_piece) {
+        // Window decisions of split pieces. A piece's trackers give each row's nibble (ORed over
+        // the warp's tokens; the trackers restart), which the warp puts in the piece's slot for
+        // its quadrant; a row is out when any quadrant's nibble says so.
+        auto piece_nibbles = [&]() -> unsigned {
             unsigned nb = 0u;
 #pragma unroll
             for (int c = 0; c < NPC; ++c) {
@@ -424,21 +429,19 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
             }
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) nb |= __shfl_xor_sync(0xffffffffu, nb, sh);
-            const uint32_t ks = portion++ & (uint32_t)(UM_FSLOTS - 1);
+            return nb;
+        };
+        auto publish = [&](uint32_t ks, unsigned nb) {
             uint8_t* mine = fsw + (ks * 4 + qw) * UM_MAX_ROWS;
             if (lane < 4) {
 #pragma unroll
                 for (int c = 0; c < NPC; ++c) mine[row_of(c)] = (uint8_t)((nb >> (4 * c)) & 15u);
             }
-            __syncwarp();
-            int old = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                old = atomicAdd(&fcnt[ks], 1);
-            }
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old != UM_NSW - 1) return;
-            __threadfence_block();
+        };
+        // The out rows of slot ks once every quadrant's nibbles are in; `write`: this warp also
+        // writes the piece's flag bytes (split jp's own, or the run slot's edge byte for a first
+        // piece that starts inside a split).
+        auto piece_rows = [&](uint32_t ks, int jp, bool first_piece, bool write) -> unsigned long long {
             const uint8_t* all = fsw + ks * 4 * UM_MAX_ROWS;
             unsigned long long out_rows = 0ull;
 #pragma unroll
@@ -449,14 +452,35 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
                     const unsigned f = all[n] | all[UM_MAX_ROWS + n] | all[2 * UM_MAX_ROWS + n] |
                                        all[3 * UM_MAX_ROWS + n];
                     out = (f & FDPP_FLAG_OUT) != 0u;
-                    const uint8_t fb = (uint8_t)(f | (force_online ? FDPP_FLAG_RECOMPUTED : 0u));
-                    if (first_piece && dest >= 0 && t0 != jp * S)
-                        a.xf[(long long)dest * R + n] = fb;
-                    else
-                        a.flags[unit_row_slot(a, b, g, n, jp)] = fb;
+                    if (write) {
+                        const uint8_t fb = (uint8_t)(f | (force_online ? FDPP_FLAG_RECOMPUTED : 0u));
+                        if (first_piece && dest >= 0 && t0 != jp * S)
+                            a.xf[(long long)dest * R + n] = fb;
+                        else
+                            a.flags[slot0 + (jp - j0) + rowoff_s[n]] = fb;
+                    }
                 }
                 out_rows |= (unsigned long long)__ballot_sync(0xffffffffu, out) << (32 * hf);
             }
+            return out_rows;
+        };
+        // A piece that ends inside the segment: the warp that arrives last (a shared count) decides
+        // it and marks the segment's taint. The segment's last piece is decided by every warp after
+        // the epilogue's barrier instead.
+        auto finish_piece = [&](int jp, bool first_piece) {
+            const unsigned nb = piece_nibbles();
+            const uint32_t ks = portion++ & (uint32_t)(UM_FSLOTS - 1);
+            publish(ks, nb);
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                old = atomicAdd(&fcnt[ks], 1);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != UM_NSW - 1) return;
+            __threadfence_block();
+            const unsigned long long out_rows = piece_rows(ks, jp, first_piece, true);
             if (lane == 0) {
                 fcnt[ks] = 0;
                 if (out_rows) atomicOr(&taint_s[upar], out_rows);
@@ -464,8 +488,9 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
         };
 
         // ---- the segment's tiles ----
-        int tt = t0, se = (t0 / S + 1) * S, jp = j0;
-        bool first_piece = true;
+        int tt = t0, se = (t0 / S + 1) * S, jp = j0, last_jp = j0;
+        bool first_piece = true, last_first = false;
+        int last_ks = -1;
         while (tt < t1) {
             const int tend = min(min(tt + TILE, se), t1);
             const int nvalid = tend - tt;
@@ -578,7 +603,16 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
             if (++stage == (uint32_t)rg.nstage) { stage = 0; phase ^= 1u; }
             tt = tend;
             if (tt == se || tt == t1) {            // a split piece ends here
-                if (!maxpass && !redo) finish_piece(jp, first_piece);
+                if (!maxpass && !redo) {
+                    if (tt < t1) {
+                        finish_piece(jp, first_piece);
+                    } else {
+                        last_ks = (int)(portion++ & (uint32_t)(UM_FSLOTS - 1));
+                        publish((uint32_t)last_ks, piece_nibbles());
+                        last_jp = jp;
+                        last_first = first_piece;
+                    }
+                }
                 first_piece = false;
                 ++jp;
                 se += S;
@@ -606,52 +640,69 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
 #pragma unroll
             for (int sh = 4; sh < 32; sh <<= 1) lsum[c] += __shfl_xor_sync(0xffffffffu, lsum[c], sh);
         }
+        float* xl_p = xl_s + upar * 4 * UM_MAX_ROWS;     // by segment parity: no barrier before reuse
         if (lane < 4) {
 #pragma unroll
-            for (int c = 0; c < NPC; ++c) xl_s[qw * UM_MAX_ROWS + row_of(c)] = lsum[c];
+            for (int c = 0; c < NPC; ++c) xl_p[qw * UM_MAX_ROWS + row_of(c)] = lsum[c];
         }
-        // every warp's l, and every piece's window decisions (the taint), are in
+        // every warp's l, and every piece's window decisions, are in
         if (!warps_sync()) return;
+        // the taint: the rows out of the window in any piece (the last one decided here, its flag
+        // bytes written by the last warp). Every warp read the previous segment's taint word
+        // before this barrier: it is cleared for the segment after this one.
+        unsigned long long taint = 0ull;
+        if (!redo) {
+            taint = taint_s[upar];
+            if (last_ks >= 0) taint |= piece_rows((uint32_t)last_ks, last_jp, last_first, warp == UM_NSW - 1);
+        }
+        if (warp == 0 && lane == 0) taint_s[upar ^ 1u] = 0ull;
         const unsigned long long write_mask = redo ? redo_mask : ~0ull;
-        const unsigned long long taint = redo ? 0ull : taint_s[upar];
         const bool refill = !redo && a.mode == FDPP_MODE_NORMAL;
+        const unsigned long long zero_rows = refill ? taint : 0ull;
+        const bool push = refill && taint != 0ull;
         const uint32_t ob = obn & 1u;
         if (!ring_wait(ub.ofull + 8 * ob, (obn >> 1) & 1u, misc, a)) return;
         ++obn;
         tc_fence_after();
         {
-            // d = 32 (w % 4) + lane; 16-column chunks alternate between the quadrant's two warps
-            // (NP = 16: the first warp's)
-            const int d = 32 * qw + lane;
+            // d = 32 (w % 4) + lane; the quadrant's two warps take a half of the 16-column chunks
+            // each (NP = 16: the first warp the one chunk). All loads, then one wait.
+            constexpr int NCH = NP / 16, CPW = NCH >= 2 ? NCH / 2 : 1;
+            if (hw * CPW < NCH) {
+                const int d = 32 * qw + lane;
+                uint32_t oh[CPW][16], olo[CPW][16];
 #pragma unroll
-            for (int ch = 0; ch < NP / 16; ++ch) {
-                if (NP > 16 ? (ch & 1) != hw : hw != 0) continue;
-                float o[16], ol[16];
-                tmem_ld16(tmem + UM_NSB * NP + ob * (2 * NP) + lane_base + 16 * ch, o);
-                tmem_ld16(tmem + UM_NSB * NP + ob * (2 * NP) + NP + lane_base + 16 * ch, ol);
+                for (int u = 0; u < CPW; ++u) {
+                    const uint32_t col = UM_NSB * NP + ob * (2 * NP) + 16 * (hw * CPW + u);
+                    tmem_ld16_async(tmem + col + lane_base, oh[u]);
+                    tmem_ld16_async(tmem + col + NP + lane_base, olo[u]);
+                }
+                tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) o[k] += ol[k];
+                for (int u = 0; u < CPW; ++u) {
+                    reg_fence16(oh[u]);
+                    reg_fence16(olo[u]);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int n = 16 * ch + k;
-                    if (n >= R || !((write_mask >> n) & 1ull)) continue;
-                    const bool empty = refill && ((taint >> n) & 1ull);
-                    float* orow = dest >= 0 ? a.xo + ((long long)dest * R + n) * UM_D
-                                            : a.o_part + unit_row_slot(a, b, g, n, j0) * UM_D;
-                    orow[d] = empty ? 0.f : o[k];
+                    for (int k = 0; k < 16; ++k) {
+                        const int n = 16 * (hw * CPW + u) + k;
+                        if (n >= R || !((write_mask >> n) & 1ull)) continue;
+                        const float o = __uint_as_float(oh[u][k]) + __uint_as_float(olo[u][k]);
+                        float* orow = dest >= 0 ? a.xo + ((long long)dest * R + n) * UM_D
+                                                : a.o_part + (slot0 + rowoff_s[n]) * UM_D;
+                        orow[d] = ((zero_rows >> n) & 1ull) ? 0.f : o;
+                    }
                 }
             }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(ub.ofree + 8 * ob);
-        if (warp == 0) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int n = lane + 32 * hf;
-                if (n >= R || n >= NP || !((write_mask >> n) & 1ull)) continue;
-                const float lam = ((xl_s[n] + xl_s[UM_MAX_ROWS + n]) + xl_s[2 * UM_MAX_ROWS + n]) +
-                                  xl_s[3 * UM_MAX_ROWS + n];
+        // l and m: warp w writes rows 8 w .. 8 w + 7
+        if (lane < 8) {
+            const int n = 8 * warp + lane;
+            if (n < R && n < NP && ((write_mask >> n) & 1ull)) {
+                const float lam = ((xl_p[n] + xl_p[UM_MAX_ROWS + n]) + xl_p[2 * UM_MAX_ROWS + n]) +
+                                  xl_p[3 * UM_MAX_ROWS + n];
                 const bool onl = (redo && ((onl_mask >> n) & 1ull)) || (!redo && force_online);
                 float M = phi_of(a, g * a.G + n % a.G);
                 if (onl) {
@@ -659,10 +710,10 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
 #pragma unroll
                     for (int w = 1; w < 4; ++w) M = fmaxf(M, xm_s[w * UM_MAX_ROWS + n]);
                 }
-                const long long rs = dest >= 0 ? (long long)dest * R + n : unit_row_slot(a, b, g, n, j0);
+                const long long rs = dest >= 0 ? (long long)dest * R + n : slot0 + rowoff_s[n];
                 float* lp = dest < 0 ? a.l_part : a.xl;
                 float* mp = dest < 0 ? a.m_part : a.xm;
-                const bool empty = refill && ((taint >> n) & 1ull);
+                const bool empty = (zero_rows >> n) & 1ull;
                 lp[rs] = empty ? 0.f : lam;
                 mp[rs] = empty ? -INFINITY : M;
                 if (redo) {
@@ -674,22 +725,23 @@ __device__ __forceinline__ void softmax_warps(const KernelArgs& a, const UmLayou
                 }
             }
         }
-        // every warp's stores are ordered before the fallback push (a release by warp 0), and
-        // xl/xm are read before the next segment writes them
-        if (!warps_sync()) return;
+        // Only where needed, the warps meet again: every warp's stores before the fallback push (a
+        // release by warp 0), and a redo or forced-online segment's maxima read before the next
+        // max pass writes them.
+        if (push || redo || force_online) {
+            if (!warps_sync()) return;
+        }
         ++un;
         if (warp == 0 && lane == 0) {
-            if (!redo) {
-                taint_s[upar] = 0ull;
-                if (taint != 0ull && a.mode == FDPP_MODE_NORMAL) {
-                    const int list = (int)(blockIdx.x % REDO_NLISTS);
-                    const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
-                    long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
-                    ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
-                    ent[2] = dest;
-                    ent[3] = (long long)taint;
-                    st_release_gpu(ent, ((long long)(g * a.max_splits + j0) << 32) | (long long)(unsigned)(b + 1));
-                }
+            if (push) {
+                const int list = (int)(blockIdx.x % REDO_NLISTS);
+                const int k = atomicAdd(&a.hdr[HDR_REDO_LISTS + 2 * list], 1);
+                long long* ent = a.redo + ((long long)list * a.redo_cap + k) * REDO_WORDS;
+                ent[1] = (long long)(unsigned)t0 | ((long long)(unsigned)t1 << 32);
+                ent[2] = dest;
+                ent[3] = (long long)taint;
+                st_release_gpu(ent, ((long long)(g * a.max_splits + j0) << 32) | (long long)(unsigned)(b + 1));
+                misc[1] = 1;                        // the producer drains the lists after its own work
             }
             if (kind == KIND_LAST_OWN) mbar_arrive(rg.own_done);
         }
@@ -762,29 +814,26 @@ __global__ void __launch_bounds__(UM_THREADS, 1)
         ts[0] = ts[1] = 0ull;
         fence_mbar_init();
     }
+    if (threadIdx.x < UM_MAX_ROWS) {
+        const int n = (int)threadIdx.x;
+        reinterpret_cast<long long*>(sm + lay.rowoff)[n] =
+            ((long long)(n / a.G) * a.Hq + n % a.G) * a.max_splits;
+    }
     if (warp == UM_MMA_WARP) tmem_alloc(smem_u32(tslot), NCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    // a programmatic dependent: the tiles this CTA streamed first in the last call go into L2
-    // while the previous kernel finishes (contiguous caches), then every warp waits for it
-    if (!PAGED && warp == UM_PROD_WARP && lane == 0 && blockIdx.x < TC_MAX_PARTS) {
+    // a programmatic dependent: while the previous kernel finishes, the P.V warp (idle until the
+    // first tiles land) brings into L2 the sequence lengths the plan starts from and the tiles
+    // this CTA streamed first in the last call (contiguous caches), then every warp waits for it
+    if (warp == UM_PV_WARP && lane == 0) {
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
         prefetch_tensormap(&tmQ);
-        const volatile int* h = a.hint + (long long)blockIdx.x * HINT_WORDS;
-        const int n = min(max(h[0], 0), HINT_TILES);
-        for (int i = 0; i < n; ++i) {
-            const int x = h[1 + 3 * i], y = h[2 + 3 * i], z = h[3 + 3 * i];
-            if (x < 0 || (x & 63) != 0) continue;
-#pragma unroll
-            for (int hv = 0; hv < UM_D / 64; ++hv) {
-                tma_prefetch_3d(&tmK, x + 64 * hv, y, z);
-                tma_prefetch_3d(&tmV, x + 64 * hv, y, z);
-            }
-        }
+        for (int b = 0; b < a.B && b < 32 * 8; b += 32) prefetch_l2(a.seq_lens + b);
     }
+    if (!PAGED && warp == UM_PV_WARP && blockIdx.x < TC_MAX_PARTS) prefetch_hint<UM_D>(a, &tmK, &tmV);
     grid_dependency_wait();
 
     int* plan = reinterpret_cast<int*>(sm + lay.plan);
