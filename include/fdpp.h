@@ -176,6 +176,11 @@ typedef struct fdpp_diag {
     int32_t kernel;               /* fdpp_kernel that ran last (1 tensor, 2 SIMT) */
     int32_t tc_build;             /* tensor kernel: the build that ran (FDPP_TC_MMA_SYNC, or
                                      FDPP_TC_MMA_TCGEN05); 0 for the SIMT kernel */
+    int32_t tc_parts;             /* tensor kernel: parts P its tiles were cut into (one per CTA;
+                                     0: whole units, no run slots); 0 for the SIMT kernel */
+    int32_t tc_seg_tiles;         /* tensor kernel: phantom tiles counted after each (sequence,
+                                     kv head) unit in that cut (a part holding a run boundary
+                                     takes that many tiles fewer); 0 for the SIMT kernel */
 } fdpp_diag;
 
 /* Partial slots per (b, h) that a workspace for `p` holds: ceil(max_seq_len / S) for a fixed

@@ -74,7 +74,7 @@ class fdpp_diag(ctypes.Structure):
         ("n_units", ctypes.c_int64), ("n_flagged_row_splits", ctypes.c_int64),
         ("n_flagged_units", ctypes.c_int64), ("n_recomputed_row_splits", ctypes.c_int64),
         ("error_bits", ctypes.c_uint32), ("kernel", ctypes.c_int32),
-        ("tc_build", ctypes.c_int32),
+        ("tc_build", ctypes.c_int32), ("tc_parts", ctypes.c_int32), ("tc_seg_tiles", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

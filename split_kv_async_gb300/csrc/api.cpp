@@ -776,6 +776,8 @@ fdpp_status fdpp_read_diag(const void* workspace, size_t workspace_bytes, const 
     diag->error_bits = (uint32_t)hdr[HDR_ERR];
     diag->kernel = hdr[HDR_KERNEL];
     diag->tc_build = hdr[HDR_KERNEL] == FDPP_KERNEL_TENSOR ? hdr[HDR_TC_BUILD] : 0;
+    diag->tc_parts = hdr[HDR_KERNEL] == FDPP_KERNEL_TENSOR ? hdr[HDR_PARTS] : 0;
+    diag->tc_seg_tiles = hdr[HDR_KERNEL] == FDPP_KERNEL_TENSOR && hdr[HDR_PARTS] > 0 ? hdr[HDR_SEGK] : 0;
     const size_t G = Hq / (size_t)p->num_kv_heads;
     for (size_t b = 0; b < B; ++b) {
         const int n = ns[b] < 0 ? 0 : (ns[b] > (int)ms ? (int)ms : ns[b]);

@@ -319,6 +319,54 @@ def test_one_split_over_many_parts_with_many_rows():
     assert diag["n_units"] == 1 and diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
 
 
+# The tcgen05 build cuts its tiles in a stream that counts phantom tiles after every (sequence,
+# kv head) unit, so that a part holding a run boundary takes fewer tiles: empty sequences (units
+# of phantoms only) at the start, inside and at the end; many more tiles than CTAs (boundaries
+# inside parts); and units of equal length whose count divides the parts (no phantoms).
+PHANTOM_CASES = {
+    "empty_units": (_wl(W.GQA, name="ph_empty", batch=6, num_q_heads=8, num_kv_heads=2, q_tokens=16,
+                        split_len=128), [0, 300, 0, 0, 130, 0]),
+    "many_units": (_wl(W.GQA, name="ph_many", batch=12, num_q_heads=8, num_kv_heads=2, q_tokens=16,
+                       split_len=256),
+                   [2900, 150, 1777, 64, 3000, 999, 2048, 65, 1200, 2500, 333, 1800]),
+    "many_units_16_rows": (_wl(W.GQA, name="ph_many16", batch=12, num_q_heads=8, num_kv_heads=2,
+                               q_tokens=4, split_len=192),
+                           [2900, 150, 1777, 64, 3000, 999, 2048, 65, 1200, 2500, 333, 1800]),
+    "even_units": (_wl(W.GQA, name="ph_even", batch=1, num_q_heads=32, num_kv_heads=8, q_tokens=16,
+                       split_len=512), [2048]),
+}
+
+
+@pytest.mark.parametrize("name", list(PHANTOM_CASES))
+def test_tcgen05_partition_with_phantom_tiles(name):
+    wl, sl = PHANTOM_CASES[name]
+    inp = W.generate(wl, seq_lens=np.array(sl, np.int32))
+    dinp = H.DeviceInputs(inp)
+    ref = H.oracle_out(inp)
+    got, diag, flags, ns, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=F.FDPP_TC_MMA_TCGEN05)
+    H.assert_parity(got, ref, f"{name} tcgen05")
+    assert diag["error_bits"] == 0 and diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
+    o_ns, _, o_units = oracle.plan(inp.seq_lens, wl.num_kv_heads, 1 << 30, wl.split_len)
+    np.testing.assert_array_equal(ns, o_ns)
+    assert diag["n_units"] == o_units
+    # the cut: P parts, and phantoms unless units of equal length fall evenly on the parts
+    units = wl.batch * wl.num_kv_heads
+    tiles = wl.num_kv_heads * sum(-(-L // 64) for L in sl)     # splits are whole tiles here
+    rows = wl.q_tokens * wl.group
+    assert diag["tc_parts"] > 0
+    even = len(set(sl)) == 1 and diag["tc_parts"] % units == 0
+    assert diag["tc_seg_tiles"] == (0 if even else (9 if rows > 32 else 6))
+    assert diag["tc_parts"] <= tiles
+    g = got.reshape(wl.batch, wl.q_tokens, wl.num_q_heads, wl.head_dim)
+    for b, L in enumerate(sl):
+        if L == 0:
+            assert np.all(g[b] == 0.0)                        # no key: zero rows
+    # the mma.sync build cuts the same tiles without phantoms
+    got2, diag2, _, _, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=F.FDPP_TC_MMA_SYNC)
+    H.assert_parity(got2, ref, f"{name} mma.sync")
+    assert diag2["tc_build"] == F.FDPP_TC_MMA_SYNC and diag2["tc_seg_tiles"] == 0
+
+
 def test_batch_beyond_the_shared_memory_plan():
     """Batches above 1024 sequences are dealt out to the CTAs as whole units (no extra slots);
     results, decisions and the fallback must be the same as for the part-balanced path."""
