@@ -188,9 +188,12 @@ typedef struct fdpp_diag {
 int fdpp_max_splits(const fdpp_params* p);
 
 /* The tensor kernel cuts the 64-token tiles of all (b, g, j) units into at most this many
- * equal parts, one per CTA, so that every CTA streams the same number of bytes. A part's share
- * of one sequence's kv head is a run, which leaves one partial (in the phi frame, summed across
- * its splits) in a run slot of the workspace; window decisions stay per split. */
+ * equal parts, one per CTA, so that every CTA streams about the same number of bytes. A part's
+ * share of one sequence's kv head is a run, which leaves one partial (in the phi frame, summed
+ * across its splits) in a run slot of the workspace; window decisions stay per split. The
+ * tcgen05 build cuts a stream that counts a few phantom tiles after each (sequence, kv head), so
+ * that a part holding a run boundary, which costs time, takes fewer real tiles (fdpp_diag's
+ * tc_seg_tiles). */
 #define FDPP_TC_MAX_PARTS 512
 
 /* The tensor kernel's tcgen05 build (more than 8 query rows per kv head, bf16, d = 128) runs at
