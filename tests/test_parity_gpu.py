@@ -367,6 +367,50 @@ def test_tcgen05_partition_with_phantom_tiles(name):
     assert diag2["tc_build"] == F.FDPP_TC_MMA_SYNC and diag2["tc_seg_tiles"] == 0
 
 
+def _random_tc_case(i):
+    """A seeded random shape for the tcgen05 build: 1-4 kv heads, groups of 1-8, query tokens
+    so that 9..64 rows share a kv head, 1-6 sequences of 0..1199 keys (one no longer than the
+    chunk, often an empty one), split lengths that are and are not tile multiples, contiguous or
+    paged caches (blocks of 16, 32 or 64; the split a whole number of blocks), NaN past every
+    sequence's end."""
+    rng = np.random.default_rng([0x5EED1100, i])
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    tq = int(rng.integers(-(-9 // g), 64 // g + 1))
+    b = int(rng.integers(1, 7))
+    sl = rng.integers(0, 1200, b)
+    sl[int(rng.integers(0, b))] = int(rng.integers(0, tq + 1))
+    if b > 2:
+        sl[int(rng.integers(0, b))] = 0
+    split = int(rng.choice([64, 100, 128, 192, 256, 500, 512]))
+    paged = bool(rng.random() < 0.4)
+    kw = dict(name=f"rnd{i}", batch=b, num_q_heads=hkv * g, num_kv_heads=hkv, head_dim=128,
+              dtype=W.BF16, q_tokens=tq, split_len=split, seed=0x5EED1200 + i)
+    if paged:
+        bs = int(rng.choice([16, 32, 64]))
+        # a paged split is a whole number of blocks (the API's contract), still often no whole tile
+        kw.update(block_size=bs, seq_len_range=None, split_len=max(bs, split // bs * bs))
+    return _wl(W.PAGED if paged else W.GQA, **kw), sl.astype(np.int32)
+
+
+@pytest.mark.parametrize("i", range(16))
+@pytest.mark.parametrize("build", ["tcgen05", "mma_sync"])
+def test_many_rows_random_shapes(i, build):
+    wl, sl = _random_tc_case(i)
+    inp = W.generate(wl, seq_lens=sl, poison_tail=True)
+    dinp = H.DeviceInputs(inp)
+    ref = H.oracle_out(inp)
+    tc = F.FDPP_TC_MMA_TCGEN05 if build == "tcgen05" else F.FDPP_TC_MMA_SYNC
+    got, diag, flags, ns, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=tc)
+    what = (f"random case {i} ({build}): B {wl.batch}, Hkv {wl.num_kv_heads}, G {wl.group}, "
+            f"Tq {wl.q_tokens}, S {wl.split_len}, paged {wl.paged}, L {[int(x) for x in sl]}")
+    H.assert_parity(got, ref, what)
+    assert diag["error_bits"] == 0 and diag["tc_build"] == tc, what
+    o_ns, _, o_units = oracle.plan(inp.seq_lens, wl.num_kv_heads, 1 << 30, wl.split_len)
+    np.testing.assert_array_equal(ns, o_ns)
+    assert diag["n_units"] == o_units
+
+
 def test_batch_beyond_the_shared_memory_plan():
     """Batches above 1024 sequences are dealt out to the CTAs as whole units (no extra slots);
     results, decisions and the fallback must be the same as for the part-balanced path."""
