@@ -411,6 +411,51 @@ def test_many_rows_random_shapes(i, build):
     assert diag["n_units"] == o_units
 
 
+def _random_decode_case(i):
+    """A seeded random decode shape: 1-8 kv heads, groups of 1-16, one or two query tokens (at most
+    16 rows per kv head), d = 64 or 128, bf16 or fp32, 1-8 sequences of 0..2999 keys (often an
+    empty and a one-key one), splits of whole or partial tiles, contiguous or paged caches, NaN
+    past every sequence's end; every kernel that takes the shape runs it."""
+    rng = np.random.default_rng([0x5EED1300, i])
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    tq = int(rng.choice([1, 2])) if g <= 8 else 1
+    b = int(rng.integers(1, 9))
+    sl = rng.integers(0, 3000, b)
+    if b > 1:
+        sl[int(rng.integers(0, b))] = int(rng.integers(0, 2))
+    d = int(rng.choice([64, 128]))
+    dt = W.F32 if rng.random() < 0.25 else W.BF16
+    split = int(rng.choice([64, 96, 128, 200, 256, 512, 1000]))
+    paged = bool(rng.random() < 0.4)
+    kw = dict(name=f"drnd{i}", batch=b, num_q_heads=hkv * g, num_kv_heads=hkv, head_dim=d, dtype=dt,
+              q_tokens=tq, split_len=split, seed=0x5EED1400 + i)
+    if paged:
+        bs = int(rng.choice([16, 32, 64, 128]))
+        kw.update(block_size=bs, seq_len_range=None, split_len=max(bs, split // bs * bs))
+    return _wl(W.PAGED if paged else W.GQA, **kw), sl.astype(np.int32)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_decode_random_shapes(i):
+    wl, sl = _random_decode_case(i)
+    inp = W.generate(wl, seq_lens=sl, poison_tail=True)
+    dinp = H.DeviceInputs(inp)
+    ref = H.oracle_out(inp)
+    ks = _kernels(inp)
+    assert ks
+    for kernel in ks:
+        got, diag, flags, ns, _ = H.run(dinp, kernel=kernel)
+        what = (f"random decode case {i} (kernel {kernel}): B {wl.batch}, Hkv {wl.num_kv_heads}, "
+                f"G {wl.group}, Tq {wl.q_tokens}, d {wl.head_dim}, {wl.dtype}, S {wl.split_len}, "
+                f"paged {wl.paged}, L {[int(x) for x in sl]}")
+        H.assert_parity(got, ref, what)
+        assert diag["error_bits"] == 0 and diag["kernel"] == kernel, what
+        o_ns, _, o_units = oracle.plan(inp.seq_lens, wl.num_kv_heads, 1 << 30, wl.split_len)
+        np.testing.assert_array_equal(ns, o_ns)
+        assert diag["n_units"] == o_units
+
+
 def test_batch_beyond_the_shared_memory_plan():
     """Batches above 1024 sequences are dealt out to the CTAs as whole units (no extra slots);
     results, decisions and the fallback must be the same as for the part-balanced path."""
