@@ -297,6 +297,34 @@ def _check_fallback(inp, oflags, what, **kw):
     return diag
 
 
+def _random_fallback_case(i):
+    """A seeded random hot-key shape for the tensor kernel: 1-12 sequences of 200..3000 keys, 1-4
+    kv heads, groups of 1-8, query tokens so that 9..64 rows share a kv head, a split length of
+    64..1000, 5-100 % of units with a hot key."""
+    rng = np.random.default_rng([0x5EED1500, i])
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    tq = int(rng.integers(-(-9 // g), 64 // g + 1))
+    kw = dict(batch=int(rng.integers(1, 13)), seq_len=int(rng.integers(200, 3001)),
+              split_len=int(rng.choice([64, 128, 192, 256, 500, 1000])),
+              frac=float(rng.choice([0.05, 0.2, 0.5, 1.0])), num_q_heads=hkv * g, num_kv_heads=hkv,
+              q_tokens=tq, seed_offset=50 + 17 * i)
+    return kw
+
+
+@pytest.mark.parametrize("i", range(6))
+@pytest.mark.parametrize("build", ["tcgen05", "mma_sync"])
+def test_fallback_random_shapes_with_many_rows(i, build):
+    """Decisions, recompute marks and results of seeded random hot-key shapes on both tensor
+    builds: the tcgen05 build's pushed runs and redo pieces over its phantom-tile partition, the
+    mma.sync row groups' in-place finish."""
+    kw = _random_fallback_case(i)
+    inp, oflags = _stress_inputs(**kw)
+    tc = F.FDPP_TC_MMA_TCGEN05 if build == "tcgen05" else F.FDPP_TC_MMA_SYNC
+    diag = _check_fallback(inp, oflags, f"random fallback case {i} ({build}): {kw}", tc_mma=tc)
+    assert diag["tc_build"] == tc
+
+
 def test_one_split_spread_over_many_parts():
     """The tensor kernel cuts the tiles of all units into equal parts, one per CTA. One split of
     64 tiles becomes 64 one-tile parts: 63 of them leave their share in an extra slot that the
