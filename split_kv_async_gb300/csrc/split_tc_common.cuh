@@ -515,15 +515,19 @@ struct Producer {
             long long tn = t + cur.ntile;
             // Whether a real tile remains: a run that ends before te ends at its unit's last tile,
             // and the next unit (past K phantoms) is the sequence's next kv head, which has tiles,
-            // or the next sequence's first, which may have none.
+            // or the next sequence's first, which may have none. The look ahead leaves the
+            // sequence cursor where it was: the walk from tn starts inside this sequence.
             bool last = tn >= te;
             if (Lay::UM && !last && K > 0) {
                 if (te <= tn + K) {
                     last = true;
                 } else if (cur.kvh + 1 >= A.Hkv) {
+                    const int cb_keep = cb, cgrp_keep = cgrp;
                     long long v = tn;
                     Seg probe;
                     last = !seg_at(v, probe);
+                    cb = cb_keep;
+                    cgrp = cgrp_keep;
                 }
             }
             // The next segment is located after this one is issued (its block-table window is

@@ -395,6 +395,31 @@ def test_tcgen05_partition_with_phantom_tiles(name):
     assert diag2["tc_build"] == F.FDPP_TC_MMA_SYNC and diag2["tc_seg_tiles"] == 0
 
 
+# Parts that run on past a sequence's last kv head into the next sequence, many times over: 48
+# sequences of 0..3499 keys, 2 kv heads, parts of ~10 tiles. (The look ahead that decides whether a
+# part holds another run must leave the walk's sequence cursor where it was.)
+SEQ_CROSS_LENS = np.random.default_rng([0x5EED1700, 44]).integers(0, 3500, 48).astype(np.int32)
+
+
+@pytest.mark.parametrize("tq,split,paged", [(4, 256, False), (16, 512, False), (4, 256, True)])
+def test_tcgen05_parts_across_sequences(tq, split, paged):
+    kw = dict(name=f"seqx{tq}", batch=48, num_q_heads=8, num_kv_heads=2, head_dim=128, dtype=W.BF16,
+              q_tokens=tq, split_len=split, seed=0x5EED1701)
+    if paged:
+        kw.update(block_size=32, seq_len_range=None)
+    wl = _wl(W.PAGED if paged else W.GQA, **kw)
+    inp = W.generate(wl, seq_lens=SEQ_CROSS_LENS)
+    dinp = H.DeviceInputs(inp)
+    ref = H.oracle_out(inp)
+    got, diag, flags, ns, _ = H.run(dinp, kernel=F.FDPP_KERNEL_TENSOR, tc_mma=F.FDPP_TC_MMA_TCGEN05)
+    assert diag["error_bits"] == 0 and diag["tc_build"] == F.FDPP_TC_MMA_TCGEN05
+    assert diag["tc_seg_tiles"] == (9 if tq * wl.group > 32 else 6)
+    H.assert_parity(got, ref, f"parts across sequences, Tq {tq}, S {split}, paged {paged}")
+    o_ns, _, o_units = oracle.plan(inp.seq_lens, wl.num_kv_heads, 1 << 30, wl.split_len)
+    np.testing.assert_array_equal(ns, o_ns)
+    assert (flags & F.FDPP_FLAG_OUT).sum() == 0
+
+
 def _random_tc_case(i):
     """A seeded random shape for the tcgen05 build: 1-4 kv heads, groups of 1-8, query tokens
     so that 9..64 rows share a kv head, 1-6 sequences of 0..1199 keys (one no longer than the
