@@ -1,6 +1,7 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py times (default
 kernel choice and pipeline geometry), including two query tokens per sequence (spec_decode_tq2)
-and a 16-token prefill chunk (prefill_chunk_tq16: 64 rows per kv head, the tcgen05 build):
+a 16-token prefill chunk (prefill_chunk_tq16: 64 rows per kv head, the tcgen05 build) and the paged
+batch's caches with 4 and 8 query tokens (the tcgen05 build on 64 ragged sequences):
   * sampled output rows against the fp64 oracle (computed one row at a time);
   * every output finite; the split plan equal to the oracle's scheduler;
   * window decisions: none for the N(0,1) workloads; for the fallback-stress workload every
@@ -30,7 +31,13 @@ def _sample_rows(inp, n, seed):
     return rows
 
 
-@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS, W.SPEC, W.CHUNK],
+# The paged batch's caches with 4 and 8 query tokens per sequence (32 and 64 rows per kv head): the
+# tcgen05 build on 64 ragged sequences, whose parts run on past sequences' ends into the next ones.
+PAGED_TQ4 = W.PAGED.replace(name="paged_batch_tq4", q_tokens=4)
+PAGED_TQ8 = W.PAGED.replace(name="paged_batch_tq8", q_tokens=8)
+
+
+@pytest.mark.parametrize("wl", [W.TINY, W.GQA, W.LONG, W.PAGED, W.STRESS, W.SPEC, W.CHUNK, PAGED_TQ4, PAGED_TQ8],
                          ids=lambda w: w.name)
 def test_full_size(wl):
     import split_kv_async_gb300 as F
