@@ -608,6 +608,8 @@ def run_fdpp(args, dist: Dist):
                    "phi": wl.phi, "window": [wl.lo, wl.hi],
                    "kv_bytes_per_step": kv_bytes, "kernel": kernel_name,
                    "tensor_build": {0: None, 1: "mma.sync", 2: "tcgen05"}.get(diag.get("tc_build", 0)),
+                   "tensor_parts": diag.get("tc_parts", 0) or None,
+                   "tensor_phantom_tiles": diag.get("tc_seg_tiles", 0) if diag.get("tc_parts", 0) else None,
                    "l2_policy": f"rotate {R} K/V copies ({R * kv_pool_bytes / 2**20:.0f} MiB >= "
                                 f"4x L2 {l2 / 2**20:.0f} MiB); no flush",
                    "parallelism": f"replicas{dist.world}" if dist.world > 1 else "single",
